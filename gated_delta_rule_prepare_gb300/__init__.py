@@ -1,0 +1,223 @@
+"""Python binding of libkda, the GB300 (sm_103a) KDA core library.
+
+Argument marshalling only: every function here checks tensor dtypes, shapes
+and devices, then calls the C ABI declared in ``include/kda.h`` with raw
+device pointers and the current CUDA stream.  All arithmetic runs in the
+library's CUDA kernels; there is no fallback.  Importing this package on a
+machine without the built library raises immediately.
+
+Entry points (same names as the C ABI): ``kda_decode``, ``kda_decode_k``,
+``kda_prefill``, ``kda_conv_silu_l2``, ``kda_prefill_workspace_size``,
+``kda_sync_status``.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+HEAD_DIM = 128
+Q_SCALE = 0.08838834764831845
+MAX_K = 8
+F32, BF16 = 0, 1
+
+_c = ctypes
+_vp, _i, _u64, _i64, _f, _sz = _c.c_void_p, _c.c_int, _c.c_uint64, _c.c_int64, _c.c_float, _c.c_size_t
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__("kda status %d: %s" % (status, message))
+        self.status = status
+
+
+def _load():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError("libkda.so is not built (%s); run __graft_entry__.build() first" % path)
+    lib = _c.CDLL(path)
+    sig = {
+        "kda_decode": [_vp] * 7 + [_i] * 3 + [_u64],
+        "kda_decode_k": [_vp] * 7 + [_i] * 4 + [_vp, _i, _u64],
+        "kda_prefill": [_vp] * 7 + [_i, _i, _i, _f, _i, _i, _i, _i64, _vp, _i, _vp, _sz, _u64],
+        "kda_conv_silu_l2": [_vp] * 4 + [_i, _i, _vp, _i, _f, _i, _i, _u64],
+        "kda_sync_status": [_u64],
+    }
+    for name, args in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = _i
+    lib.kda_prefill_workspace_size.argtypes = [_i] * 5
+    lib.kda_prefill_workspace_size.restype = _sz
+    lib.kda_last_error.argtypes = []
+    lib.kda_last_error.restype = _c.c_char_p
+    lib.kda_version.argtypes = []
+    lib.kda_version.restype = _c.c_char_p
+    return lib
+
+
+LIB = _load()
+
+
+def _check(status: int):
+    if status != 0:
+        raise KdaError(status, LIB.kda_last_error().decode())
+
+
+def _stream(t: torch.Tensor) -> int:
+    return torch.cuda.current_stream(t.device).cuda_stream
+
+
+def _ptr(t, dtype=None, name="tensor"):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t.data_ptr()
+
+
+def _contig(t, name):
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def version() -> str:
+    return LIB.kda_version().decode()
+
+
+def kda_decode(state, q, k, v, g, beta, o):
+    """One token per sequence: state [N,H,128,128] FP32 in place; q, k, v, g, o
+    [N,H,128] FP32; beta [N,H] FP32."""
+    N, H = state.shape[0], state.shape[1]
+    for n_, t in (("state", state), ("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta),
+                  ("o", o)):
+        _contig(t, n_)
+    if q.shape != (N, H, HEAD_DIM) or beta.shape != (N, H):
+        raise ValueError("kda_decode: shape mismatch")
+    f = torch.float32
+    _check(LIB.kda_decode(_ptr(state, f, "state"), _ptr(q, f, "q"), _ptr(k, f, "k"),
+                          _ptr(v, f, "v"), _ptr(g, f, "g"), _ptr(beta, f, "beta"),
+                          _ptr(o, f, "o"), N, H, state.shape[-1], _stream(state)))
+
+
+def kda_decode_k(state, q, k, v, g, beta, o, snapshots=()):
+    """k rows per sequence walked in order: q, k, v, g, o [N,k,H,128]; beta
+    [N,k,H]; snapshots: up to k tensors [N,H,128,128], snapshots[t] = state
+    after row t."""
+    N, krows, H = q.shape[0], q.shape[1], q.shape[2]
+    for n_, t in (("state", state), ("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta),
+                  ("o", o)):
+        _contig(t, n_)
+    if beta.shape != (N, krows, H) or state.shape[:2] != (N, H):
+        raise ValueError("kda_decode_k: shape mismatch")
+    f = torch.float32
+    snaps = list(snapshots)
+    for s in snaps:
+        _contig(s, "snapshot")
+        if s.shape != state.shape or s.dtype != f:
+            raise ValueError("kda_decode_k: snapshot shape/dtype mismatch")
+    arr = (_c.c_void_p * max(1, len(snaps)))(*[s.data_ptr() for s in snaps])
+    _check(LIB.kda_decode_k(_ptr(state, f, "state"), _ptr(q, f, "q"), _ptr(k, f, "k"),
+                            _ptr(v, f, "v"), _ptr(g, f, "g"), _ptr(beta, f, "beta"),
+                            _ptr(o, f, "o"), N, krows, H, state.shape[-1],
+                            _c.cast(arr, _c.c_void_p) if snaps else None, len(snaps),
+                            _stream(state)))
+
+
+def kda_prefill_workspace_size(max_tokens, n_seqs, chunk, heads):
+    return int(LIB.kda_prefill_workspace_size(max_tokens, n_seqs, chunk, heads, HEAD_DIM))
+
+
+def kda_prefill(state, q, k, v, g, beta, o, t, chunk, pad_fill=0.0, cu_seqlens=None,
+                workspace=None):
+    """Chunked prefill.  Without cu_seqlens: q, k, v, g [N, T_pad, H, 128]
+    (or [T_pad, H, 128] for one sequence), beta [N, T_pad, H], t valid tokens
+    per sequence; rows [t, T_pad) are overwritten with pad_fill.  With
+    cu_seqlens (device int32 [N+1]): packed rows [T, H, 128] and t = T.
+    q, k and v may be strided views whose token rows are ``q.stride(-3)``
+    elements apart (e.g. slices of one [T, 3*H*128] buffer)."""
+    dt = q.dtype
+    if dt not in (torch.float32, torch.bfloat16):
+        raise TypeError("kda_prefill: inputs must be float32 or bfloat16")
+    in_dtype = BF16 if dt == torch.bfloat16 else F32
+    H = q.shape[-2]
+    if q.shape[-1] != HEAD_DIM:
+        raise ValueError("kda_prefill: head_dim must be 128")
+    for n_, t_ in (("q", q), ("k", k), ("v", v)):
+        if t_.dtype != dt or t_.stride(-1) != 1 or t_.stride(-2) != HEAD_DIM:
+            raise ValueError("kda_prefill: %s must have unit channel stride and heads packed" % n_)
+    stride = q.stride(-3)
+    if k.stride(-3) != stride or v.stride(-3) != stride:
+        raise ValueError("kda_prefill: q, k, v must share one token-row stride")
+    for n_, t_ in (("g", g), ("beta", beta), ("o", o), ("state", state)):
+        _contig(t_, n_)
+    if g.dtype != dt or beta.dtype != dt:
+        raise TypeError("kda_prefill: g and beta must have the inputs' dtype")
+    if cu_seqlens is not None:
+        n_seqs = cu_seqlens.numel() - 1
+        t_pad = t
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise TypeError("kda_prefill: cu_seqlens must be a CUDA int32 tensor")
+        rows = q.shape[0]
+    else:
+        if q.dim() == 3:
+            n_seqs, t_pad = 1, q.shape[0]
+        else:
+            n_seqs, t_pad = q.shape[0], q.shape[1]
+            if q.dim() == 4 and q.stride(0) != t_pad * stride:
+                raise ValueError("kda_prefill: sequences must be consecutive row blocks")
+        rows = n_seqs * t_pad
+    if g.numel() != rows * H * HEAD_DIM or beta.numel() != rows * H or o.numel() != rows * H * HEAD_DIM:
+        raise ValueError("kda_prefill: g/beta/o sizes do not match the token rows")
+    if state.numel() != n_seqs * H * HEAD_DIM * HEAD_DIM or state.dtype != torch.float32:
+        raise ValueError("kda_prefill: state must be FP32 [N, H, 128, 128]")
+    ws_need = kda_prefill_workspace_size(rows, n_seqs, chunk, H)
+    if ws_need and workspace is None:
+        raise ValueError("kda_prefill: a workspace of %d bytes is required" % ws_need)
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(LIB.kda_prefill(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                           _ptr(o, torch.float32, "o"), int(t), int(t_pad), int(chunk),
+                           float(pad_fill), H, HEAD_DIM, in_dtype, int(stride),
+                           _ptr(cu_seqlens), n_seqs, ws_ptr, ws_bytes, _stream(state)))
+
+
+def kda_conv_silu_l2(conv_state, x, w, out, cu_seqlens=None, n_seqs=None, l2_eps=1e-6):
+    """Depthwise causal conv + SiLU + L2(q, k).  x, out BF16 [tokens, 3*H*128];
+    w BF16 [3*H*128, K]; conv_state FP32 [N, 3*H*128, K] in place.  Without
+    cu_seqlens x holds N sequences of tokens/N tokens each."""
+    for n_, t_ in (("conv_state", conv_state), ("x", x), ("w", w), ("out", out)):
+        _contig(t_, n_)
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise TypeError("kda_conv_silu_l2: x, w, out must be bfloat16")
+    conv_dim = x.shape[-1]
+    if conv_dim % (3 * HEAD_DIM):
+        raise ValueError("kda_conv_silu_l2: channels must be 3 * heads * 128")
+    H = conv_dim // (3 * HEAD_DIM)
+    K = w.shape[1]
+    tokens = x.numel() // conv_dim
+    if cu_seqlens is not None:
+        N = cu_seqlens.numel() - 1
+        t = tokens
+    else:
+        N = conv_state.shape[0] if n_seqs is None else n_seqs
+        if tokens % N:
+            raise ValueError("kda_conv_silu_l2: tokens not divisible by n_seqs")
+        t = tokens // N
+    if conv_state.shape != (N, conv_dim, K):
+        raise ValueError("kda_conv_silu_l2: conv_state must be [N, conv_dim, K]")
+    _check(LIB.kda_conv_silu_l2(_ptr(conv_state, torch.float32, "conv_state"), _ptr(x), _ptr(w),
+                                _ptr(out), t, N, _ptr(cu_seqlens), K, float(l2_eps), H,
+                                HEAD_DIM, _stream(x)))
+
+
+def kda_sync_status(device=None):
+    """Synchronise the current stream and raise if a device-side check failed."""
+    s = torch.cuda.current_stream(device).cuda_stream
+    _check(LIB.kda_sync_status(s))

@@ -1,0 +1,218 @@
+// Front end of the KDA block: depthwise causal conv1d + SiLU, then L2 over the
+// q and k channels (block pipeline "conv1d + SiLU -> L2(q,k only)"; fused at
+// decode as causal_conv1d_update_l2norm, split at prefill into conv_prefill
+// and l2_norm_bf16; config.rs: conv state of conv_kernel slots, L2 applied as
+// 1/sqrt(sum + eps)).
+//
+// Kernel 1 (conv_silu_l2_kernel): one CTA per (head-sized group of 128
+// channels, block of 32 tokens); a thread owns one channel.  History before a
+// sequence's first token comes from the conv state, which this kernel only
+// reads.  The L2 sum over a q/k head's 128 channels is a warp shuffle
+// reduction plus a 4-warp smem reduction per token.
+// Kernel 2 (conv_state_kernel): after kernel 1, each thread rewrites one
+// (sequence, channel) state row to hold that sequence's last conv_kernel
+// inputs, reading the old row first; separating it from kernel 1 keeps any
+// CTA from reading a state row another CTA has already replaced.
+#include <cuda_bf16.h>
+
+#include "kda_common.h"
+
+namespace kda {
+namespace {
+
+__device__ unsigned g_conv_status = 0;
+
+constexpr int kTok = 32;  // tokens per CTA
+constexpr int kThreads = D;
+
+__device__ __forceinline__ float bf16_to_f32(uint16_t b) {
+    return __uint_as_float(static_cast<uint32_t>(b) << 16);
+}
+
+__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// Sequence holding packed token tau: largest n with cu[n] <= tau.  Returns
+// false when the offsets do not bracket tau (malformed cu_seqlens).
+__device__ __forceinline__ bool find_seq(const int* __restrict__ cu, int n_seqs, int tau,
+                                         int& n, int& start) {
+    int lo = 0, hi = n_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu + mid) <= tau) lo = mid;
+        else hi = mid - 1;
+    }
+    n = lo;
+    start = __ldg(cu + lo);
+    const int end = __ldg(cu + lo + 1);
+    return start >= 0 && start <= tau && tau < end;
+}
+
+template <int K>
+__global__ void __launch_bounds__(kThreads)
+conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __restrict__ x,
+                    const uint16_t* __restrict__ w, uint16_t* __restrict__ out, int total,
+                    int t_per_seq, const int* __restrict__ cu, int n_seqs, int heads,
+                    float l2_eps) {
+    __shared__ float red[kThreads / 32][kTok];
+    const int grp = blockIdx.x;
+    const int c = grp * D + threadIdx.x;
+    const size_t conv_dim = (size_t)3 * heads * D;
+    const bool normalise = grp < 2 * heads;
+    float wj[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) wj[j] = bf16_to_f32(__ldg(w + (size_t)c * K + j));
+
+    const int tok0 = blockIdx.y * kTok;
+    float y[kTok];
+#pragma unroll
+    for (int m = 0; m < kTok; ++m) {
+        const int tau = tok0 + m;
+        y[m] = 0.f;
+        if (tau >= total) continue;
+        int n, start;
+        if (cu) {
+            if (!find_seq(cu, n_seqs, tau, n, start)) {
+                if (threadIdx.x == 0) atomicOr(&g_conv_status, STATUS_BAD_CU_SEQLENS);
+                continue;
+            }
+        } else {
+            n = tau / t_per_seq;
+            start = n * t_per_seq;
+        }
+        const float* hist = conv_state + ((size_t)n * conv_dim + c) * K;
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int src = tau - (K - 1) + j;
+            const float xv = (src >= start) ? bf16_to_f32(__ldg(x + (size_t)src * conv_dim + c))
+                                            : __ldg(hist + K + (src - start));
+            acc = __fmaf_rn(wj[j], xv, acc);
+        }
+        y[m] = acc / (1.0f + expf(-acc));
+    }
+
+    if (normalise) {  // uniform per CTA: the whole block takes this branch or none
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+        for (int m = 0; m < kTok; ++m) {
+            float p = y[m] * y[m];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
+            if (lane == 0) red[warp][m] = p;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < kTok; ++m) {
+            const float ss = (red[0][m] + red[1][m]) + (red[2][m] + red[3][m]);
+            y[m] = y[m] * (1.0f / sqrtf(ss + l2_eps));
+        }
+    }
+#pragma unroll
+    for (int m = 0; m < kTok; ++m) {
+        const int tau = tok0 + m;
+        if (tau < total) out[(size_t)tau * conv_dim + c] = f32_to_bf16(y[m]);
+    }
+}
+
+template <int K>
+__global__ void conv_state_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
+                                  int total, int t_per_seq, const int* __restrict__ cu,
+                                  int n_seqs, int heads) {
+    const size_t conv_dim = (size_t)3 * heads * D;
+    const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= (size_t)n_seqs * conv_dim) return;
+    const int n = (int)(idx / conv_dim);
+    const size_t c = idx % conv_dim;
+    int start, end;
+    if (cu) {
+        start = __ldg(cu + n);
+        end = __ldg(cu + n + 1);
+        bool ok = start >= 0 && start <= end && end <= total;
+        if (n == 0) ok = ok && start == 0;
+        if (n == n_seqs - 1) ok = ok && end == total;
+        if (!ok) {
+            atomicOr(&g_conv_status, STATUS_BAD_CU_SEQLENS);
+            return;
+        }
+    } else {
+        start = n * t_per_seq;
+        end = start + t_per_seq;
+    }
+    const int len = end - start;
+    float* st = conv_state + idx * K;
+    float old[K], nw[K];
+#pragma unroll
+    for (int j = 0; j < K; ++j) old[j] = st[j];
+#pragma unroll
+    for (int j = 0; j < K; ++j) {
+        const int rel = len - K + j;  // position relative to the sequence start
+        nw[j] = (rel >= 0) ? bf16_to_f32(__ldg(x + (size_t)(start + rel) * conv_dim + c))
+                           : old[(j + len < K) ? j + len : K - 1];
+    }
+#pragma unroll
+    for (int j = 0; j < K; ++j) st[j] = nw[j];
+}
+
+template <int K>
+kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint16_t* out,
+                  int total, int t_per_seq, const int* cu, int n_seqs, int heads, float eps,
+                  cudaStream_t s) {
+    dim3 grid(3 * heads, (total + kTok - 1) / kTok);
+    conv_silu_l2_kernel<K><<<grid, kThreads, 0, s>>>(conv_state, x, w, out, total, t_per_seq,
+                                                      cu, n_seqs, heads, eps);
+    kda_status st = launch_result("kda_conv_silu_l2 (conv)");
+    if (st != KDA_OK) return st;
+    const size_t rows = (size_t)n_seqs * 3 * heads * D;
+    conv_state_kernel<K><<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(conv_state, x, total,
+                                                                        t_per_seq, cu, n_seqs,
+                                                                        heads);
+    return launch_result("kda_conv_silu_l2 (state)");
+}
+
+}  // namespace
+
+cudaError_t read_and_clear_status_conv(unsigned* out) {
+    unsigned zero = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(out, g_conv_status, sizeof(unsigned));
+    if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_conv_status, &zero, sizeof(unsigned));
+    return e;
+}
+
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, const uint16_t* w,
+                                       uint16_t* out, int t, int n_seqs, const int* cu_seqlens,
+                                       int conv_kernel, float l2_eps, int heads, int head_dim,
+                                       uint64_t stream) {
+    KDA_REQUIRE(conv_state && x && w && out, KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2: null pointer argument");
+    KDA_REQUIRE(aligned16(conv_state) && aligned16(x) && aligned16(out), KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2: conv_state, x and out must be 16-byte aligned");
+    KDA_REQUIRE(head_dim == D, KDA_ERR_UNSUPPORTED,
+                "kda_conv_silu_l2: head_dim %d unsupported (only 128)", head_dim);
+    KDA_REQUIRE(heads >= 1 && n_seqs >= 1 && t >= 1, KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2: heads (%d), n_seqs (%d) and t (%d) must be >= 1", heads,
+                n_seqs, t);
+    KDA_REQUIRE(conv_kernel >= 1 && conv_kernel <= KDA_MAX_CONV_KERNEL, KDA_ERR_UNSUPPORTED,
+                "kda_conv_silu_l2: conv_kernel %d outside [1, %d]", conv_kernel,
+                KDA_MAX_CONV_KERNEL);
+    KDA_REQUIRE(l2_eps >= 0.f, KDA_ERR_INVALID_ARG, "kda_conv_silu_l2: l2_eps must be >= 0");
+    const long long total = cu_seqlens ? (long long)t : (long long)t * n_seqs;
+    KDA_REQUIRE(total <= 0x7fffffffLL && (long long)3 * heads * D * total < (1LL << 46),
+                KDA_ERR_INVALID_ARG, "kda_conv_silu_l2: problem too large");
+    KDA_REQUIRE((total + kTok - 1) / kTok <= 65535, KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2: more than %d tokens in one call", 65535 * kTok);
+    KDA_REQUIRE(!fault_injected(), KDA_ERR_CUDA, "kda_conv_silu_l2: injected launch failure");
+    cudaStream_t s = as_stream(stream);
+    const int tps = cu_seqlens ? 0 : t;
+    switch (conv_kernel) {
+        case 1: return launch<1>(conv_state, x, w, out, (int)total, tps, cu_seqlens, n_seqs, heads, l2_eps, s);
+        case 2: return launch<2>(conv_state, x, w, out, (int)total, tps, cu_seqlens, n_seqs, heads, l2_eps, s);
+        case 3: return launch<3>(conv_state, x, w, out, (int)total, tps, cu_seqlens, n_seqs, heads, l2_eps, s);
+        default: return launch<4>(conv_state, x, w, out, (int)total, tps, cu_seqlens, n_seqs, heads, l2_eps, s);
+    }
+}

@@ -1,0 +1,231 @@
+// Single-token decode and the decode_k row walk of the KDA core.
+//
+// Glm5NextKdaLayer::decode / decode_k and Glm5NextKdaKernels::recurrent_smem:
+// the per-head gated delta-rule step, streaming the FP32 [128 x 128] state of
+// each (sequence, head) once in and once out (1R + 1W).
+//
+// Mapping: one CTA of 256 threads per (sequence, head).  Warp w owns key rows
+// [16w, 16w + 16); lane l owns value columns [4l, 4l + 4) as one float4, so
+// each warp-wide load or store is one contiguous 512-byte state row.  A thread
+// keeps its 16 x 4 block of the state in registers for the whole step (and,
+// in decode_k, for all k rows).  The two reductions over the key index
+// (S^T k and S^T q) sum 16 rows inside each thread, then the 8 warp partials
+// through shared memory in a fixed order.
+//
+// Bit-identity of decode_k with k serial decodes: both run the very same
+// token_step() with explicit round-to-nearest intrinsics (no contraction
+// choices left to the compiler), the same thread mapping and the same
+// reduction order; an FP32 state written to memory and read back is exact.
+#include "kda_common.h"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRows = D / kWarps;  // key rows per warp
+
+struct TokenSmem {
+    float dec[D];  // exp(g_i)
+    float kk[D];   // k_i
+    float bk[D];   // beta * k_i
+    float qs[D];   // KDA_Q_SCALE * q_i
+    float v[D];
+    float u[D];    // v - S^T k (decayed S)
+    float red[kWarps][D];
+};
+
+// Stage one token of one head: threads 0..127 take one channel each.
+__device__ __forceinline__ void stage_token(TokenSmem& sm, const float* __restrict__ q,
+                                            const float* __restrict__ k,
+                                            const float* __restrict__ v,
+                                            const float* __restrict__ g, float beta) {
+    const int c = threadIdx.x;
+    if (c < D) {
+        const float kc = __ldg(k + c);
+        sm.dec[c] = expf(__ldg(g + c));
+        sm.kk[c] = kc;
+        sm.bk[c] = __fmul_rn(beta, kc);
+        sm.qs[c] = __fmul_rn(KDA_Q_SCALE, __ldg(q + c));
+        sm.v[c] = __ldg(v + c);
+    }
+}
+
+__device__ __forceinline__ void scale4(float4& s, float a) {
+    s.x = __fmul_rn(s.x, a);
+    s.y = __fmul_rn(s.y, a);
+    s.z = __fmul_rn(s.z, a);
+    s.w = __fmul_rn(s.w, a);
+}
+
+__device__ __forceinline__ void fma4(float4& acc, const float4& s, float a) {
+    acc.x = __fmaf_rn(s.x, a, acc.x);
+    acc.y = __fmaf_rn(s.y, a, acc.y);
+    acc.z = __fmaf_rn(s.z, a, acc.z);
+    acc.w = __fmaf_rn(s.w, a, acc.w);
+}
+
+// Sum the 8 warp partials of column j in warp order.
+__device__ __forceinline__ float reduce_col(const TokenSmem& sm, int j) {
+    float t = sm.red[0][j];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) t = __fadd_rn(t, sm.red[w][j]);
+    return t;
+}
+
+// One token step on the register-resident state block `s` (inputs staged and
+// visible).  Writes o[j] for j < 128.  Ends with every thread past its last
+// read of the staged inputs, so the caller may stage the next token.
+__device__ __forceinline__ void token_step(float4 (&s)[kRows], TokenSmem& sm,
+                                           float* __restrict__ o) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int i0 = warp * kRows;
+
+    // decay rows, then partial S^T k over this warp's rows
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        scale4(s[r], sm.dec[i0 + r]);
+        fma4(acc, s[r], sm.kk[i0 + r]);
+    }
+    reinterpret_cast<float4*>(sm.red[warp])[lane] = acc;
+    __syncthreads();
+    if (threadIdx.x < D) {
+        const int j = threadIdx.x;
+        sm.u[j] = __fsub_rn(sm.v[j], reduce_col(sm, j));
+    }
+    __syncthreads();
+
+    // rank-1 update, then partial S^T (scale q) over this warp's rows
+    const float4 u = reinterpret_cast<const float4*>(sm.u)[lane];
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int r = 0; r < kRows; ++r) {
+        const float b = sm.bk[i0 + r];
+        s[r].x = __fmaf_rn(b, u.x, s[r].x);
+        s[r].y = __fmaf_rn(b, u.y, s[r].y);
+        s[r].z = __fmaf_rn(b, u.z, s[r].z);
+        s[r].w = __fmaf_rn(b, u.w, s[r].w);
+        fma4(acc, s[r], sm.qs[i0 + r]);
+    }
+    reinterpret_cast<float4*>(sm.red[warp])[lane] = acc;
+    __syncthreads();
+    if (threadIdx.x < D) {
+        const int j = threadIdx.x;
+        o[j] = reduce_col(sm, j);
+    }
+}
+
+__device__ __forceinline__ void load_state(float4 (&s)[kRows], const float* __restrict__ S) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+        s[r] = __ldcs(reinterpret_cast<const float4*>(S + (size_t)(warp * kRows + r) * D) + lane);
+}
+
+__device__ __forceinline__ void store_state(const float4 (&s)[kRows], float* __restrict__ S) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+        __stcs(reinterpret_cast<float4*>(S + (size_t)(warp * kRows + r) * D) + lane, s[r]);
+}
+
+__global__ void __launch_bounds__(kThreads, 2)
+decode_kernel(float* __restrict__ state, const float* __restrict__ q,
+              const float* __restrict__ k, const float* __restrict__ v,
+              const float* __restrict__ g, const float* __restrict__ beta,
+              float* __restrict__ o) {
+    __shared__ TokenSmem sm;
+    const size_t nh = blockIdx.x;  // n * heads + h
+    float* S = state + nh * (size_t)(D * D);
+    float4 s[kRows];
+    load_state(s, S);
+    stage_token(sm, q + nh * D, k + nh * D, v + nh * D, g + nh * D, __ldg(beta + nh));
+    __syncthreads();
+    token_step(s, sm, o + nh * D);
+    store_state(s, S);
+}
+
+struct SnapList {
+    float* p[KDA_MAX_K];
+};
+
+__global__ void __launch_bounds__(kThreads, 2)
+decode_k_kernel(float* __restrict__ state, const float* __restrict__ q,
+                const float* __restrict__ k, const float* __restrict__ v,
+                const float* __restrict__ g, const float* __restrict__ beta,
+                float* __restrict__ o, int heads, int krows, SnapList snaps, int n_snap) {
+    __shared__ TokenSmem sm;
+    const size_t nh = blockIdx.x;
+    const size_t n = nh / heads, h = nh % heads;
+    float* S = state + nh * (size_t)(D * D);
+    float4 s[kRows];
+    load_state(s, S);
+    for (int t = 0; t < krows; ++t) {
+        const size_t row = (n * krows + t) * heads + h;
+        stage_token(sm, q + row * D, k + row * D, v + row * D, g + row * D, __ldg(beta + row));
+        __syncthreads();
+        token_step(s, sm, o + row * D);
+        if (t < n_snap) store_state(s, snaps.p[t] + nh * (size_t)(D * D));
+    }
+    store_state(s, S);
+}
+
+kda_status check_common(const char* fn, float* state, const float* q, const float* k,
+                        const float* v, const float* g, const float* beta, float* o,
+                        int n_seqs, int heads, int head_dim) {
+    KDA_REQUIRE(state && q && k && v && g && beta && o, KDA_ERR_INVALID_ARG,
+                "%s: null pointer argument", fn);
+    KDA_REQUIRE(aligned16(state) && aligned16(q) && aligned16(k) && aligned16(v) &&
+                    aligned16(g) && aligned16(o),
+                KDA_ERR_INVALID_ARG, "%s: state, q, k, v, g and o must be 16-byte aligned", fn);
+    KDA_REQUIRE(head_dim == D, KDA_ERR_UNSUPPORTED, "%s: head_dim %d unsupported (only 128)", fn,
+                head_dim);
+    KDA_REQUIRE(n_seqs >= 1 && heads >= 1, KDA_ERR_INVALID_ARG,
+                "%s: n_seqs (%d) and heads (%d) must be >= 1", fn, n_seqs, heads);
+    KDA_REQUIRE((long long)n_seqs * heads <= 0x7fffffffLL, KDA_ERR_INVALID_ARG,
+                "%s: n_seqs * heads too large", fn);
+    KDA_REQUIRE(!fault_injected(), KDA_ERR_CUDA, "%s: injected launch failure", fn);
+    return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" kda_status kda_decode(float* state, const float* q, const float* k, const float* v,
+                                 const float* g, const float* beta, float* o, int n_seqs,
+                                 int heads, int head_dim, uint64_t stream) {
+    kda_status st = check_common("kda_decode", state, q, k, v, g, beta, o, n_seqs, heads,
+                                 head_dim);
+    if (st != KDA_OK) return st;
+    decode_kernel<<<n_seqs * heads, kThreads, 0, as_stream(stream)>>>(state, q, k, v, g, beta, o);
+    return launch_result("kda_decode");
+}
+
+extern "C" kda_status kda_decode_k(float* state, const float* q, const float* k, const float* v,
+                                   const float* g, const float* beta, float* o, int n_seqs,
+                                   int krows, int heads, int head_dim, float* const* snapshots,
+                                   int n_snap, uint64_t stream) {
+    kda_status st = check_common("kda_decode_k", state, q, k, v, g, beta, o, n_seqs, heads,
+                                 head_dim);
+    if (st != KDA_OK) return st;
+    KDA_REQUIRE(krows >= 1 && krows <= KDA_MAX_K, KDA_ERR_INVALID_ARG,
+                "kda_decode_k: k = %d outside [1, %d]", krows, KDA_MAX_K);
+    KDA_REQUIRE(n_snap >= 0 && n_snap <= krows, KDA_ERR_INVALID_ARG,
+                "kda_decode_k: n_snap = %d outside [0, k = %d]", n_snap, krows);
+    KDA_REQUIRE(n_snap == 0 || snapshots, KDA_ERR_INVALID_ARG,
+                "kda_decode_k: snapshots is NULL with n_snap = %d", n_snap);
+    SnapList sl = {};
+    for (int t = 0; t < n_snap; ++t) {
+        KDA_REQUIRE(snapshots[t] && aligned16(snapshots[t]), KDA_ERR_INVALID_ARG,
+                    "kda_decode_k: snapshot %d is NULL or not 16-byte aligned", t);
+        KDA_REQUIRE(snapshots[t] != state, KDA_ERR_INVALID_ARG,
+                    "kda_decode_k: snapshot %d aliases the state", t);
+        sl.p[t] = snapshots[t];
+    }
+    decode_k_kernel<<<n_seqs * heads, kThreads, 0, as_stream(stream)>>>(
+        state, q, k, v, g, beta, o, heads, krows, sl, n_snap);
+    return launch_result("kda_decode_k");
+}

@@ -1,0 +1,58 @@
+// Internal helpers shared by the libkda translation units: error reporting,
+// argument checks, the fault-injection hook and the device status words.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+
+#include "kda.h"
+
+namespace kda {
+
+constexpr int D = KDA_HEAD_DIM;
+
+// Thread-local last-error text (kda_last_error).
+void set_error(const char* fmt, ...);
+
+// Returns true when KDA_FAULT_INJECT=launch is set: the API then reports a
+// launch failure without enqueuing anything (host-side failure testing).
+bool fault_injected();
+
+inline cudaStream_t as_stream(uint64_t s) { return reinterpret_cast<cudaStream_t>(s); }
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Bits of the device status words (one per translation unit that checks).
+enum : unsigned {
+    STATUS_BAD_CU_SEQLENS = 1u << 0,
+};
+
+// Each checking unit exposes a reader that returns and clears its word on the
+// current device (synchronous; called from kda_sync_status only).
+cudaError_t read_and_clear_status_prefill(unsigned* out);
+cudaError_t read_and_clear_status_conv(unsigned* out);
+
+#define KDA_REQUIRE(cond, code, ...)      \
+    do {                                  \
+        if (!(cond)) {                    \
+            ::kda::set_error(__VA_ARGS__); \
+            return (code);                \
+        }                                 \
+    } while (0)
+
+// Check a launch; on failure record the CUDA error text.
+inline kda_status launch_result(const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) {
+        set_error("%s: launch failed: %s", what, cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+}  // namespace kda

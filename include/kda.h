@@ -1,0 +1,189 @@
+/*
+ * kda.h -- C ABI of libkda: the KDA (Kimi-style delta attention) core of the
+ * GLM-5.3-Flash attention block on one GB300 (sm_103a).
+ *
+ * The method (rustdoc pages of the "glm5next_kda" module: the block pipeline
+ * in the module index, Glm5NextKdaLayer's decode / decode_k / prefill /
+ * prefill_with_pad_fill, Glm5NextKdaKernels' chunk_prepare / chunk_scan /
+ * recurrent, and config.rs): per head, an FP32 state S[i][j] of
+ * KDA_HEAD_DIM x KDA_HEAD_DIM, i = key channel (outer, "K-major"),
+ * j = value channel.  For each token t with inputs q_t, k_t, v_t, g_t (one
+ * value per key channel) and beta_t (one per head):
+ *
+ *     S[i][j] <- exp(g_t[i]) * S[i][j]
+ *     u[j]     = v_t[j] - sum_i S[i][j] * k_t[i]
+ *     S[i][j] += beta_t * k_t[i] * u[j]
+ *     o_t[j]   = sum_i S[i][j] * (KDA_Q_SCALE * q_t[i])
+ *
+ * q and k arrive L2-normalised (kda_conv_silu_l2 produces them that way);
+ * the core itself does not normalise.
+ *
+ * Conventions for every call:
+ *  - Pointers are device pointers unless stated; buffers are caller-owned,
+ *    contiguous in the stated layout and 16-byte aligned.  The library never
+ *    allocates, frees or keeps a pointer after the call returns.
+ *  - `stream` is a cudaStream_t cast to uint64_t (0 = legacy default stream).
+ *    Work is enqueued and the call returns without synchronising.
+ *  - Arguments are validated before anything is enqueued; on any error the
+ *    call returns a non-zero kda_status, launches nothing, and
+ *    kda_last_error() describes the problem.
+ *  - Faults the host cannot see (malformed device-side cu_seqlens) are
+ *    recorded in a device status word and reported by kda_sync_status().
+ *  - Calls on one stream are ordered; calls that touch the same state buffer
+ *    from different streams must be ordered by the caller.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Fixed geometry: head_dim is 128 (config.rs validate refuses any other). */
+#define KDA_HEAD_DIM 128
+/* The query scale 1/sqrt(KDA_HEAD_DIM), applied as q_hat = KDA_Q_SCALE * q in
+ * FP32 before any use of q.  The pages print no scale; this is the library's
+ * fixed reading (the conventional attention scale). */
+#define KDA_Q_SCALE 0.08838834764831845f
+/* decode_k row limit: Glm5NextKdaKernels::gemv_batchm serves 2..=8 rows. */
+#define KDA_MAX_K 8
+/* Depthwise conv taps: the conv kernels keep the window in 4 registers
+ * (config.rs validate). */
+#define KDA_MAX_CONV_KERNEL 4
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size or count    */
+    KDA_ERR_UNSUPPORTED = 2, /* valid in principle, not built (head_dim, chunk) */
+    KDA_ERR_WORKSPACE = 3,   /* workspace smaller than kda_prefill_workspace_size */
+    KDA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed            */
+    KDA_ERR_DEVICE = 5       /* device-side check failed (kda_sync_status)     */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/*
+ * kda_decode -- one token for each of n_seqs independent sequences
+ * (Glm5NextKdaLayer::decode; Glm5NextKdaKernels::recurrent_smem, the 1R+1W
+ * single-token recurrence).  Reads and writes the state exactly once.
+ *
+ *   state : FP32 [n_seqs][heads][128][128], updated in place
+ *   q,k,v,g : FP32 [n_seqs][heads][128]      beta : FP32 [n_seqs][heads]
+ *   o     : FP32 [n_seqs][heads][128], written
+ *   heads >= 1, head_dim == 128, n_seqs >= 1.
+ * The result is deterministic: the same inputs give the same bits.
+ */
+kda_status kda_decode(float* state, const float* q, const float* k, const float* v,
+                      const float* g, const float* beta, float* o, int n_seqs, int heads,
+                      int head_dim, uint64_t stream);
+
+/*
+ * kda_decode_k -- krows tokens of each of n_seqs sequences, walked in row
+ * order with the state held on chip (Glm5NextKdaLayer::decode_k: the
+ * speculative-verify row walk).  The output is bit-identical to krows serial
+ * kda_decode calls on the same rows.
+ *
+ *   state : FP32 [n_seqs][heads][128][128], updated in place to the state
+ *           after the last row
+ *   q,k,v,g : FP32 [n_seqs][krows][heads][128]   beta : FP32 [n_seqs][krows][heads]
+ *   o     : FP32 [n_seqs][krows][heads][128]
+ *   snapshots : HOST array of n_snap device pointers; snapshots[t] (FP32
+ *           [n_seqs][heads][128][128]) receives the state after row t.  Rows
+ *           t >= n_snap take no snapshot ("rows past snapshots.len() take no
+ *           snapshot").  May be NULL when n_snap == 0.
+ *   Refused: krows < 1 or krows > KDA_MAX_K ("refuses k == 0 or k above the
+ *   workspace"), n_snap < 0 or n_snap > krows, a null snapshot pointer.
+ */
+kda_status kda_decode_k(float* state, const float* q, const float* k, const float* v,
+                        const float* g, const float* beta, float* o, int n_seqs, int krows,
+                        int heads, int head_dim, float* const* snapshots, int n_snap,
+                        uint64_t stream);
+
+/*
+ * kda_prefill -- chunked prefill from the carried state
+ * (Glm5NextKdaLayer::prefill_with_pad_fill; Glm5NextKdaKernels::chunk_prepare
+ * for the intra-chunk solve and cumulative decay, chunk_scan for the
+ * inter-chunk state carry).
+ *
+ * Two batch forms:
+ *  - cu_seqlens == NULL: n_seqs sequences of t valid tokens each, stored as
+ *    [n_seqs][t_pad] token rows (t <= t_pad).  Before the core runs, rows
+ *    [t, t_pad) of q, k, v, g and beta are overwritten with pad_fill in the
+ *    input dtype (the pages' padded tails); the core never reads them into
+ *    arithmetic, so o and the final state do not depend on pad_fill.
+ *  - cu_seqlens != NULL: DEVICE int32 [n_seqs + 1] offsets of n_seqs packed
+ *    sequences; t is the total token count (== cu_seqlens[n_seqs]); t_pad
+ *    must equal t and no fill happens.  Offsets are checked on the device
+ *    (non-decreasing, cu_seqlens[0] == 0, last == t); a violation makes the
+ *    kernel skip that sequence and sets KDA_ERR_DEVICE for kda_sync_status.
+ *
+ *   state : FP32 [n_seqs][heads][128][128], in place (state after the last
+ *           valid token of each sequence)
+ *   q,k,v : in_dtype, token row r of head h at ptr + r*qkv_row_stride + h*128
+ *           (qkv_row_stride >= heads*128, in elements; lets q/k/v be views of
+ *           one [T][3*heads*128] buffer such as kda_conv_silu_l2's output)
+ *   g     : in_dtype [rows][heads][128]   beta : in_dtype [rows][heads]
+ *   o     : FP32 [rows][heads][128]; rows of padding are not written
+ *   chunk : 16, 32, 64 or 128 (the chunk width C)
+ *   in_dtype : KDA_F32 or KDA_BF16 (applies to q, k, v, g, beta)
+ *   workspace : device scratch of at least kda_prefill_workspace_size(...)
+ *           bytes (may be NULL when that size is 0)
+ */
+kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* beta, float* o,
+                       int t, int t_pad, int chunk, float pad_fill, int heads, int head_dim,
+                       int in_dtype, int64_t qkv_row_stride, const int* cu_seqlens, int n_seqs,
+                       void* workspace, size_t workspace_bytes, uint64_t stream);
+
+/* Bytes of device workspace kda_prefill needs for at most max_tokens token
+ * rows in total over n_seqs sequences.  Returns 0 when none is needed. */
+size_t kda_prefill_workspace_size(int max_tokens, int n_seqs, int chunk, int heads,
+                                  int head_dim);
+
+/*
+ * kda_conv_silu_l2 -- depthwise causal conv1d + SiLU, then L2 over the q and k
+ * channels (block pipeline "conv1d + SiLU -> L2(q,k only)";
+ * causal_conv1d_update_l2norm at decode, conv_prefill + l2_norm_bf16 at
+ * prefill; config.rs: the L2 epsilon is applied as 1/sqrt(sum + eps)).
+ *
+ * Channels: conv_dim = 3*heads*128, laid out q | k | v.  Per sequence and
+ * channel the conv state holds conv_kernel slots, slot conv_kernel-1 the
+ * newest input; each token shifts it left, inserts x, and convolves:
+ * y = sum_j w[c][j] * state[c][j]; y <- y * sigmoid(y).  Each q and k head is
+ * then scaled by 1/sqrt(sum y^2 + l2_eps); v channels are not normalised.
+ *
+ *   conv_state : FP32 [n_seqs][conv_dim][conv_kernel], in place
+ *   x          : BF16 [tokens][conv_dim]     out : BF16 [tokens][conv_dim]
+ *   w          : BF16 [conv_dim][conv_kernel]
+ *   cu_seqlens == NULL: n_seqs sequences of t tokens each, packed
+ *       ([n_seqs][t][conv_dim]); decode is t == 1.
+ *   cu_seqlens != NULL: DEVICE int32 [n_seqs + 1] offsets, t = total tokens;
+ *       checked on the device like kda_prefill's.
+ *   1 <= conv_kernel <= KDA_MAX_CONV_KERNEL; (2*heads*128) % 256 == 0.
+ * Two kernels are enqueued: the conv (reads the old state) and the state
+ * update (writes the last conv_kernel inputs of each sequence).
+ */
+kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, const uint16_t* w,
+                            uint16_t* out, int t, int n_seqs, const int* cu_seqlens,
+                            int conv_kernel, float l2_eps, int heads, int head_dim,
+                            uint64_t stream);
+
+/* Synchronises `stream`, then reads and clears the device status words of the
+ * calling thread's current device.  Returns KDA_OK, KDA_ERR_DEVICE (a
+ * device-side check failed since the last call; kda_last_error says which),
+ * or KDA_ERR_CUDA (the stream reported an error). */
+kda_status kda_sync_status(uint64_t stream);
+
+/* Thread-local description of the last error returned on this thread. */
+const char* kda_last_error(void);
+
+/* Library version string. */
+const char* kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

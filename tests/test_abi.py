@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library loads, exports every entry point
+include/kda.h declares, and refuses bad arguments before touching the device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__
+    path = __graft_entry__._library_builder().build()
+    L = ctypes.CDLL(path)
+    L.kda_last_error.restype = ctypes.c_char_p
+    return L
+
+
+def test_header_declares_the_four_calls_and_helpers():
+    fns = declared_functions()
+    for name in ("kda_prefill", "kda_decode", "kda_decode_k", "kda_conv_silu_l2",
+                 "kda_prefill_workspace_size", "kda_sync_status", "kda_last_error"):
+        assert name in fns
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_every_declaration_is_documented():
+    text = open(HEADER).read()
+    for name in declared_functions():
+        m = re.search(r"\n([a-z][a-z_0-9 ]*\**\s*)" + name + r"\(", text)
+        assert m, name
+        prev = text[:m.start()].rstrip()
+        assert prev.endswith("*/"), "%s has no comment block above it" % name
+
+
+V, I, F, U64, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_uint64, ctypes.c_size_t
+BUF = ctypes.create_string_buffer(64)
+P = ctypes.cast(ctypes.addressof(BUF) + (16 - ctypes.addressof(BUF) % 16) % 16, V)
+
+
+def test_decode_refuses_bad_arguments(lib):
+    f = lib.kda_decode
+    f.argtypes = [V] * 7 + [I] * 3 + [U64]
+    assert f(None, P, P, P, P, P, P, 1, 1, 128, 0) == 1
+    assert b"null" in lib.kda_last_error()
+    assert f(P, P, P, P, P, P, P, 1, 1, 64, 0) == 2
+    assert f(P, P, P, P, P, P, P, 0, 1, 128, 0) == 1
+    mis = ctypes.cast(P.value + 4, V)
+    assert f(mis, P, P, P, P, P, P, 1, 1, 128, 0) == 1
+    assert b"aligned" in lib.kda_last_error()
+
+
+def test_decode_k_refuses_k_zero_and_k_above_limit(lib):
+    f = lib.kda_decode_k
+    f.argtypes = [V] * 7 + [I] * 4 + [V, I, U64]
+    assert f(P, P, P, P, P, P, P, 1, 0, 1, 128, None, 0, 0) == 1
+    assert b"k = 0" in lib.kda_last_error()
+    assert f(P, P, P, P, P, P, P, 1, 9, 1, 128, None, 0, 0) == 1
+    assert f(P, P, P, P, P, P, P, 1, 4, 1, 128, None, 5, 0) == 1   # n_snap > k
+    assert f(P, P, P, P, P, P, P, 1, 4, 1, 128, None, 2, 0) == 1   # NULL snapshot list
+    arr = (V * 1)(P.value)
+    assert f(P, P, P, P, P, P, P, 1, 4, 1, 128, ctypes.cast(arr, V), 1, 0) == 1  # aliases state
+
+
+def test_prefill_refuses_bad_arguments(lib):
+    f = lib.kda_prefill
+    f.argtypes = [V] * 7 + [I, I, I, F, I, I, I, ctypes.c_int64, V, I, V, SZ, U64]
+    ok = dict(t=100, t_pad=128, chunk=64, heads=2, hd=128, dt=1, stride=256)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return f(P, P, P, P, P, P, P, a["t"], a["t_pad"], a["chunk"], 0.0, a["heads"], a["hd"],
+                 a["dt"], a["stride"], None, 1, None, 0, 0)
+    assert call(chunk=48) == 2
+    assert call(hd=64) == 2
+    assert call(t=0) == 1
+    assert call(t=200) == 1            # t > t_pad
+    assert call(dt=7) == 1
+    assert call(stride=100) == 1       # stride < heads * 128
+    assert call(stride=260) == 1       # stride not a multiple of 16 bytes
+    # packed sequences take no padding
+    assert f(P, P, P, P, P, P, P, 100, 128, 64, 0.0, 2, 128, 1, 256, P, 1, None, 0, 0) == 1
+
+
+def test_conv_refuses_bad_arguments(lib):
+    f = lib.kda_conv_silu_l2
+    f.argtypes = [V] * 4 + [I, I, V, I, F, I, I, U64]
+    assert f(P, P, P, P, 4, 1, None, 5, 1e-6, 1, 128, 0) == 2      # conv_kernel > 4
+    assert f(P, P, P, P, 4, 1, None, 0, 1e-6, 1, 128, 0) == 2
+    assert f(P, P, P, P, 0, 1, None, 4, 1e-6, 1, 128, 0) == 1      # no tokens
+    assert f(P, P, P, P, 4, 1, None, 4, -1.0, 1, 128, 0) == 1      # negative eps
+    assert f(None, P, P, P, 4, 1, None, 4, 1e-6, 1, 128, 0) == 1
+
+
+def test_fault_injection_hook_reports_launch_failure(lib, monkeypatch):
+    """KDA_FAULT_INJECT=launch makes a valid call fail as a launch would,
+    before anything reaches the device."""
+    f = lib.kda_decode
+    f.argtypes = [V] * 7 + [I] * 3 + [U64]
+    monkeypatch.setenv("KDA_FAULT_INJECT", "launch")
+    assert f(P, P, P, P, P, P, P, 1, 1, 128, 0) == 4
+    assert b"injected" in lib.kda_last_error()
+
+
+def test_workspace_size_is_queryable(lib):
+    lib.kda_prefill_workspace_size.restype = SZ
+    lib.kda_prefill_workspace_size.argtypes = [I] * 5
+    assert lib.kda_prefill_workspace_size(8192, 1, 64, 32, 128) >= 0
