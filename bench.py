@@ -1,0 +1,461 @@
+"""Benchmark of the KDA core on one GB300 (or N independent replicas).
+
+One step = one kda_prefill of the chunked-prefill workload: 1 sequence of
+8192 tokens, 32 heads, head_dim 128, chunk 64, BF16 q/k/v/g/beta, FP32 state
+and output, inputs resident in HBM (400 MB per step, larger than the 129 MB
+L2, so no flush is needed between steps).  The state carries from step to
+step, as one long prefill would.  The same run also times the decode
+workload (64 sequences x 32 heads, 100 chained steps) and the decode_k
+workload (128 sequences x k=4 rows, 4 snapshots) and reports their state
+GB/s against the HBM peak.
+
+Prints ONE JSON line on rank 0.  `--impl reference` times the FP64 CPU oracle
+instead (a bounded sample of the same workload per step).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+import kda_workloads as wl  # noqa: E402
+
+METRIC = "KDA prefill tokens/s and decode state GB/s (% of HBM peak), 1xGB300"
+T_PREFILL, H, D, CHUNK = 8192, 32, 128, 64
+# Algorithmic bytes of one prefill launch: q, k, v, g BF16 [8192, 32, 128],
+# beta BF16 [8192, 32], o FP32 [8192, 32, 128], state FP32 read + write.
+PREFILL_BYTES = 4 * T_PREFILL * H * D * 2 + T_PREFILL * H * 2 + T_PREFILL * H * D * 4 \
+    + 2 * H * D * D * 4
+# Multiply-adds x 2 of the chunked form per token-head: 6 D^2 + 5 C D + C^2 / 3.
+PREFILL_FLOPS = T_PREFILL * H * (6 * D * D + 5 * CHUNK * D + CHUNK * CHUNK / 3)
+DECODE_N, DECODE_STEPS = 64, 100
+DECODE_BYTES = 2 * DECODE_N * H * D * D * 4 + 4 * DECODE_N * H * D * 4 + DECODE_N * H * 4
+DK_N, DK_K = 128, 4
+DK_BYTES = (2 + DK_K) * DK_N * H * D * D * 4 + 4 * DK_N * DK_K * H * D * 4 + DK_N * DK_K * H * 4
+TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor ratio of the part
+
+
+def peaks():
+    p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+         "source": "fallback"}
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        m = json.load(open(path))
+        p.update({k: float(m[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")
+                  if k in m})
+        p["source"] = "measured"
+    return p
+
+
+def kernel_source_sha() -> str:
+    path = os.path.join(ROOT, "gated_delta_rule_prepare_gb300", "csrc", "prefill.cu")
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_from_profile():
+    """Per-launch DRAM bytes of the prefill kernel from the committed ncu
+    summary, valid only while the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", "prefill_traffic.json")
+    if not os.path.exists(path):
+        return None
+    rec = json.load(open(path))
+    if rec.get("source_sha") != kernel_source_sha():
+        return None
+    return rec.get("traffic_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,utilization.gpu,"
+              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                rows.append({"sm": float(f[1]), "max": float(f[2]), "util": float(f[4]),
+                             "hw": f[6], "hwt": f[7], "swt": f[8], "pcap": f[9]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        load = [r for r in rows if r["util"] > 0] or rows
+        reasons = set()
+        for r in load:
+            for key, name in (("hw", "hw_slowdown"), ("hwt", "hw_thermal_slowdown"),
+                              ("swt", "sw_thermal_slowdown"), ("pcap", "sw_power_cap")):
+                if r[key].lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load),
+                "sm_max_mhz": max(r["max"] for r in rows), "reasons": sorted(reasons),
+                "samples_under_load": len(load)}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------- GPU arm
+
+def time_launches(fn, n: int, stream):
+    """Runs fn() n times with an event pair around each call on `stream`;
+    returns (list of per-call ms, total ms from the first to the last event)."""
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    per = [a.elapsed_time(b) for a, b in evs]
+    return per, evs[0][0].elapsed_time(evs[-1][1])
+
+
+def run_gpu(args):
+    import gated_delta_rule_prepare_gb300 as K
+
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pk = peaks()
+    stream = torch.cuda.current_stream(dev)
+
+    # ---------------- prefill workload (the step)
+    d = wl.prefill()
+    q, k, v, g, beta = (d[n].to(dev) for n in ("q", "k", "v", "g", "beta"))
+    S = d["state"].to(dev)
+    o = torch.empty((T_PREFILL, H, D), device=dev)
+
+    def prefill():
+        K.kda_prefill(S, q, k, v, g, beta, o, T_PREFILL, CHUNK)
+
+    for _ in range(args.warmup):
+        prefill()
+    K.kda_sync_status()
+
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        per, total_ms = time_launches(prefill, args.steps, stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - t0
+        K.kda_sync_status()
+        ms_step = max_over_ranks(total_ms / args.steps, world, dev)
+
+        # ---------------- decode workload: 100 chained steps
+        dd = wl.decode_steps()
+        dS = dd["state"].to(dev)
+        dq, dk, dv, dg, db = (dd[n].to(dev) for n in ("q", "k", "v", "g", "beta"))
+        do = torch.empty((DECODE_N, H, D), device=dev)
+        step = [0]
+
+        def decode():
+            t = step[0] % DECODE_STEPS
+            K.kda_decode(dS, dq[t], dk[t], dv[t], dg[t], db[t], do)
+            step[0] += 1
+
+        for _ in range(5):
+            decode()
+        dec_per, _ = time_launches(decode, DECODE_STEPS, stream)
+        del dq, dk, dv, dg, db, dS
+
+        # ---------------- decode_k workload
+        kd = wl.decode_k()
+        kS = kd["state"].to(dev)
+        kin = {n: kd[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+        ko = torch.empty((DK_N, DK_K, H, D), device=dev)
+        snaps = [torch.empty_like(kS) for _ in range(DK_K)]
+
+        def decode_k():
+            K.kda_decode_k(kS, kin["q"], kin["k"], kin["v"], kin["g"], kin["beta"], ko, snaps)
+
+        for _ in range(3):
+            decode_k()
+        dk_per, _ = time_launches(decode_k, 20, stream)
+        del kS, snaps, kin
+    clocks = clk.summary()
+
+    # ---------------- end to end through the public API, host buffers
+    host = {n: d[n].pin_memory() for n in ("q", "k", "v", "g", "beta")}
+    o_host = torch.empty((T_PREFILL, H, D), dtype=torch.float32).pin_memory()
+    S_host = torch.empty_like(S, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = o_host.numel() * 4 + S_host.numel() * 4
+
+    def e2e_step():
+        for n_, t_ in zip(("q", "k", "v", "g", "beta"), (q, k, v, g, beta)):
+            t_.copy_(host[n_], non_blocking=True)
+        prefill()
+        o_host.copy_(o, non_blocking=True)
+        S_host.copy_(S, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, min(args.steps, 20))
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_wall = max_over_ranks(time.perf_counter() - t0, world, dev)
+
+    # ---------------- report
+    avg_launch_s = statistics.mean(per) / 1e3
+    achieved = PREFILL_BYTES / avg_launch_s / 1e9
+    tf32_peak = pk["bf16_tflops"] * TF32_OVER_BF16
+    t_bytes = PREFILL_BYTES / (pk["hbm_gbs"] * 1e9)
+    t_flops = PREFILL_FLOPS / (tf32_peak * 1e12)
+    bound = "hbm" if t_bytes >= t_flops else "tensor"
+    dec_s = statistics.mean(dec_per) / 1e3
+    dk_s = statistics.mean(dk_per) / 1e3
+    value = world * T_PREFILL / (ms_step / 1e3)
+    out = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": wl.PREFILL.name,
+            "description": wl.PREFILL.description,
+            "seq_len": T_PREFILL, "heads": H, "head_dim": D, "chunk": CHUNK,
+            "global_batch": world, "in_dtype": "bf16",
+            "l2": "inputs larger than L2 (400 MB per step), no flush",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+        },
+        "roofline": {
+            "bound": bound,
+            "achieved": achieved if bound == "hbm" else PREFILL_FLOPS / avg_launch_s / 1e12,
+            "peak": pk["hbm_gbs"] if bound == "hbm" else tf32_peak,
+            "unit": "GB/s" if bound == "hbm" else "TFLOP/s",
+            "frac": (achieved / pk["hbm_gbs"]) if bound == "hbm"
+            else (PREFILL_FLOPS / avg_launch_s / 1e12) / tf32_peak,
+            "traffic": traffic_from_profile(),
+            "kernel": "prefill (kda_prefill)",
+            "algorithmic_bytes": PREFILL_BYTES, "algorithmic_flops": PREFILL_FLOPS,
+            "avg_launch_us": avg_launch_s * 1e6,
+            "peak_source": pk["source"] + " (hbm_gbs)",
+            "time_floor_us": {"bytes": t_bytes * 1e6, "tf32_flops": t_flops * 1e6},
+        },
+        "e2e": {
+            "value": world * T_PREFILL * e_steps / e_wall, "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "path": "pinned host q/k/v/g/beta -> kda_prefill -> o and state to host",
+        },
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+        "decode": {
+            "workload": wl.DECODE.name, "value": DECODE_BYTES / dec_s / 1e9, "unit": "GB/s",
+            "frac_of_hbm_peak": DECODE_BYTES / dec_s / 1e9 / pk["hbm_gbs"],
+            "us_per_step": dec_s * 1e6, "algorithmic_bytes": DECODE_BYTES,
+            "steps": DECODE_STEPS,
+        },
+        "decode_k": {
+            "workload": wl.DECODE_K.name, "value": DK_BYTES / dk_s / 1e9, "unit": "GB/s",
+            "frac_of_hbm_peak": DK_BYTES / dk_s / 1e9 / pk["hbm_gbs"],
+            "us_per_call": dk_s * 1e6, "algorithmic_bytes": DK_BYTES,
+        },
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline_prefill(seconds=args.cpu_seconds)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+# ------------------------------------------------------------ oracle (CPU)
+
+def _oracle_prefill_sample(d, tokens):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.prefill(d["q"][:tokens], d["k"][:tokens], d["v"][:tokens], d["g"][:tokens],
+                   d["beta"][:tokens], d["state"][0])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_prefill(seconds: float = 15.0):
+    """The FP64 oracle on the host cores, on a bounded sample of the prefill
+    workload: the first `tokens` tokens of the sequence, all 32 heads."""
+    import oracle
+    d = wl.prefill()
+    tokens = 64
+    dt = _oracle_prefill_sample(d, tokens)
+    tokens = int(min(T_PREFILL, max(64, tokens * seconds / max(dt, 1e-3) / 2)))
+    dt = _oracle_prefill_sample(d, tokens)
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": oracle.threads(),
+            "kind": "oracle",
+            "sample": "first %d tokens of the 8192-token sequence, all 32 heads, FP64, %.1f s"
+                      % (tokens, dt)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    d = wl.prefill()
+    tokens = 64   # one chunk of the sequence, all heads, per step
+    for _ in range(args.warmup):
+        _oracle_prefill_sample(d, tokens)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_prefill_sample(d, tokens)
+    wall = time.perf_counter() - t0
+    value = tokens * args.steps / wall
+    sample = "per step: the first %d tokens of the 8192-token prefill workload, all 32 heads, " \
+             "FP64 oracle on the host cores" % tokens
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": wall / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.PREFILL.name, "description": wl.PREFILL.description,
+                   "seq_len": T_PREFILL, "heads": H, "head_dim": D, "chunk": CHUNK},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }))
+
+
+def run_case(args):
+    """One kernel alone on a chosen size, for ncu captures: W + K launches."""
+    import gated_delta_rule_prepare_gb300 as K
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    if args.case == "prefill":
+        d = wl.prefill(t=args.seq_len)
+        q, k, v, g, beta = (d[n].to(dev) for n in ("q", "k", "v", "g", "beta"))
+        S = d["state"].to(dev)
+        o = torch.empty((args.seq_len, H, D), device=dev)
+        fn = lambda: K.kda_prefill(S, q, k, v, g, beta, o, args.seq_len, CHUNK)
+        nbytes = 4 * args.seq_len * H * D * 2 + args.seq_len * H * 2 + args.seq_len * H * D * 4 \
+            + 2 * H * D * D * 4
+    elif args.case == "decode":
+        dd = wl.decode_steps(steps=1)
+        S = dd["state"].to(dev)
+        ins = [dd[n][0].to(dev) for n in ("q", "k", "v", "g", "beta")]
+        o = torch.empty((DECODE_N, H, D), device=dev)
+        fn = lambda: K.kda_decode(S, *ins, o)
+        nbytes = DECODE_BYTES
+    else:
+        kd = wl.decode_k()
+        S = kd["state"].to(dev)
+        ins = [kd[n].to(dev) for n in ("q", "k", "v", "g", "beta")]
+        o = torch.empty((DK_N, DK_K, H, D), device=dev)
+        snaps = [torch.empty_like(S) for _ in range(DK_K)]
+        fn = lambda: K.kda_decode_k(S, *ins, o, snaps)
+        nbytes = DK_BYTES
+    for _ in range(args.warmup):
+        fn()
+    per, _ = time_launches(fn, args.steps, stream)
+    K.kda_sync_status()
+    us = statistics.mean(per) * 1e3
+    print(json.dumps({"case": args.case, "seq_len": args.seq_len, "launches": args.steps,
+                      "avg_launch_us": us, "algorithmic_bytes": nbytes,
+                      "GBps": nbytes / us / 1e3}))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, choices=["prefill", "decode", "decode_k"],
+                    help="time one kernel alone (for profiler captures)")
+    ap.add_argument("--seq-len", type=int, default=T_PREFILL)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.case:
+        run_case(args)
+    elif args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()
