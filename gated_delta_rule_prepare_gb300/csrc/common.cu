@@ -29,18 +29,21 @@ extern "C" kda_status kda_sync_status(uint64_t stream) {
         kda::set_error("kda_sync_status: stream error: %s", cudaGetErrorString(e));
         return KDA_ERR_CUDA;
     }
-    unsigned a = 0, b = 0;
+    unsigned a = 0, b = 0, c = 0;
     e = kda::read_and_clear_status_prefill(&a);
     if (e == cudaSuccess) e = kda::read_and_clear_status_conv(&b);
+    if (e == cudaSuccess) e = kda::read_and_clear_status_prefill_tc(&c);
+    a |= c;
     if (e != cudaSuccess) {
         kda::set_error("kda_sync_status: reading the status word failed: %s",
                        cudaGetErrorString(e));
         return KDA_ERR_CUDA;
     }
     if (a | b) {
-        kda::set_error("kda_sync_status: device-side check failed (prefill 0x%x, conv 0x%x): "
-                       "malformed cu_seqlens",
-                       a, b);
+        kda::set_error("kda_sync_status: device-side check failed (prefill 0x%x, conv 0x%x): %s",
+                       a, b,
+                       ((a | b) & kda::STATUS_TIMEOUT) ? "a bounded wait timed out"
+                                                       : "malformed cu_seqlens");
         return KDA_ERR_DEVICE;
     }
     return KDA_OK;

@@ -30,12 +30,21 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // Bits of the device status words (one per translation unit that checks).
 enum : unsigned {
     STATUS_BAD_CU_SEQLENS = 1u << 0,
+    STATUS_TIMEOUT = 1u << 1,  // a bounded wait on a copy or an MMA gave up
 };
 
 // Each checking unit exposes a reader that returns and clears its word on the
 // current device (synchronous; called from kda_sync_status only).
 cudaError_t read_and_clear_status_prefill(unsigned* out);
 cudaError_t read_and_clear_status_conv(unsigned* out);
+cudaError_t read_and_clear_status_prefill_tc(unsigned* out);
+
+// Tensor-core prefill for BF16 inputs and chunk 64 (prefill_tc.cu); the
+// arguments have been validated by kda_prefill.
+kda_status launch_prefill_tc(float* state, const void* q, const void* k, const void* v,
+                             const void* g, const void* beta, float* o, int t, int t_pad,
+                             int heads, long long stride, const int* cu, int n_seqs,
+                             cudaStream_t s);
 
 #define KDA_REQUIRE(cond, code, ...)      \
     do {                                  \

@@ -245,6 +245,14 @@ kda_status launch(float* state, void* q, void* k, void* v, void* g, void* beta, 
         kda_status st = launch_result("kda_prefill (pad fill)");
         if (st != KDA_OK) return st;
     }
+    if constexpr (sizeof(TIn) == 2) {
+        // BF16 inputs with chunk 64 take the tensor-core kernel unless the
+        // caller pins the SIMT kernel (KDA_PREFILL_IMPL=simt, for comparisons).
+        const char* impl = getenv("KDA_PREFILL_IMPL");
+        if (chunk == 64 && !(impl && strcmp(impl, "simt") == 0))
+            return launch_prefill_tc(state, q, k, v, g, beta, o, t, t_pad, heads, stride, cu,
+                                     n_seqs, s);
+    }
     const size_t smem = sizeof(ChunkSmem);
     cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<TIn>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -171,3 +171,34 @@ def test_chained_prefills_equal_one_prefill():
     o2, S2, _ = run_prefill(K, second, 100, 64)
     assert rel_err(torch.cat([o1, o2]), o_all.cpu().double().numpy()) < 1e-5
     assert rel_err(S2, S_all.cpu().double().numpy()) < 1e-5
+
+
+def test_tensor_core_and_simt_kernels_agree(orc, monkeypatch):
+    """BF16 inputs with chunk 64 run on the tensor-core kernel; the FP32 SIMT
+    kernel (pinned with KDA_PREFILL_IMPL=simt) computes the same method; both
+    stay within the prefill tolerance of the oracle and of each other."""
+    K = kda()
+    d = wl.prefill(seed=21, t=300, heads=4, chunk=64, dtype=torch.bfloat16)
+    o_tc, S_tc, _ = run_prefill(K, d, 300, 64)
+    monkeypatch.setenv("KDA_PREFILL_IMPL", "simt")
+    o_si, S_si, _ = run_prefill(K, d, 300, 64)
+    o_ref, S_ref = orc.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"][0])
+    assert rel_err(o_si, o_ref) < 1e-5 and rel_err(S_si[0], S_ref) < 1e-5
+    assert rel_err(o_tc, o_ref) < TOL_PREFILL and rel_err(S_tc[0], S_ref) < TOL_PREFILL
+    assert rel_err(o_tc, o_si.double().cpu().numpy()) < TOL_PREFILL
+
+
+@pytest.mark.parametrize("g_low", [-0.05, -10.0])
+def test_prefill_long_memory_and_strong_decay(orc, g_low):
+    """Slow decay (g in [-0.05, 0]: the state carries across all 16 chunks, so
+    rounding in the carried state accumulates) and the steepest supported
+    decay (g in [-10, 0])."""
+    K = kda()
+    gen = torch.Generator().manual_seed(31)
+    T, H = 1024, 2
+    d = wl.core_inputs(gen, (T,), H, torch.bfloat16, g_low=g_low)
+    d["state"] = wl.state(gen, (1,), H, 0.02)
+    o, S, _ = run_prefill(K, d, T, 64)
+    o_ref, S_ref = orc.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"][0])
+    assert rel_err(o, o_ref) < TOL_PREFILL
+    assert rel_err(S[0], S_ref) < TOL_PREFILL
