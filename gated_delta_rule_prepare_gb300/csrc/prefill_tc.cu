@@ -11,7 +11,7 @@
 //   P_rs     = beta_s sum_i qh_ri k_si e^(Gamma_ri-Gamma_si), s <= r
 //   T        = (I + A)^-1                    (blocked forward substitution)
 //   X        = V - Ktil S,   Ktil = e^Gamma (.) k,  Qtil = e^Gamma (.) qh
-//   U        = T X,   O = Qtil S + (P T) X
+//   U        = T X,   O = Qtil S + P U
 //   S       <- diag(e^Gamma_{L-1}) S + Khat^T U,
 //              Khat_s = beta_s e^(Gamma_{L-1}-Gamma_s) (.) k_s
 // A and P are formed on the tensor cores one 16-column block b at a time:
@@ -23,10 +23,10 @@
 //
 // Tensor-core products (tcgen05.mma kind::tf32, FP32 accumulate in TMEM):
 //   [X_b; QX_b] (128x128) . Y_b^T     -> A, P column block b   (x4)
-//   [T; P] (128x64) . T               -> P T
 //   [Ktil; Qtil] (128x128) . S        -> Ktil S, Qtil S
-//   [T; P T] (128x64) . X             -> U, P T X
+//   [T; P] (128x64) . X               -> U = T X (rows 0..63)
 //   Khat^T (128x64) . U               -> state increment
+//   [T; P] (128x64) . U               -> P U (rows 64..127)
 // Raw q, k, g and the value slice arrive by TMA (cp.async.bulk.tensor).
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
@@ -65,8 +65,7 @@ struct Op {
 using OpX = Op<128, 0>;   // A: [Xb; QXb] then [Ktil; Qtil], K = 128 channels
 using OpY = Op<16, 0>;    // B: Y_b, 16 rows, K = 128 channels
 using OpKH = Op<128, 0>;  // A: Khat^T, rows = key channel, K = 64 tokens
-using OpTP = Op<128, 0>;  // A: [T; P] then [T; P T], K = 64 tokens
-using OpTT = Op<64, 0>;   // B: T^T, rows = column of T, K = 64
+using OpTP = Op<128, 0>;  // A: [T; P], K = 64 tokens
 using OpXV = Op<32, 16>;  // B: X^T and U^T, rows = value column, K = 64 tokens
 using OpS = Op<32, 16>;   // B: S^T, rows = value column, K = 128 key channels
 
@@ -81,8 +80,7 @@ constexpr uint32_t SM_STAGE_END = SM_GAM + 64 * KP * 4;
 constexpr uint32_t SM_AM = SM_KF;                    // FP32 A [64][AP]
 constexpr uint32_t SM_TM = SM_AM + 64 * AP * 4;      // FP32 T [64][AP]
 constexpr uint32_t SM_TP = (SM_TM + 64 * AP * 4 + 15) & ~15u;
-constexpr uint32_t SM_TT = SM_TP + OpTP::bytes(64);
-constexpr uint32_t SM_XV = SM_TT + OpTT::bytes(64);
+constexpr uint32_t SM_XV = SM_TP + OpTP::bytes(64);
 constexpr uint32_t SM_ZS = SM_XV + OpXV::bytes(64);  // solve scratch [3][16][17]
 constexpr uint32_t SM_OPKH = SM_STAGE_END;
 constexpr uint32_t SM_OPY = SM_OPKH + OpKH::bytes(64);  // Y_b, later U^T
@@ -100,7 +98,7 @@ static_assert(OpY::bytes(128) <= OpXV::bytes(64), "Y_b does not fit its slot");
 static_assert(SM_TOTAL <= 232448, "shared memory budget exceeded");
 
 // TMEM columns (256 allocated)
-constexpr uint32_t TC_AP = 0, TC_PT = 64, TC_Y = 128, TC_U = 160, TC_E = 192;
+constexpr uint32_t TC_AP = 0, TC_PU = 64, TC_Y = 128, TC_U = 160, TC_E = 192;
 
 __device__ __forceinline__ float bf(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -155,7 +153,7 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
     const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + SM_RAWV);
     const uint32_t s_opx = tc::smem_u32(sm + SM_OPX), s_opy = tc::smem_u32(sm + SM_OPY),
                    s_opkh = tc::smem_u32(sm + SM_OPKH), s_tp = tc::smem_u32(sm + SM_TP),
-                   s_tt = tc::smem_u32(sm + SM_TT), s_xv = tc::smem_u32(sm + SM_XV),
+                   s_xv = tc::smem_u32(sm + SM_XV),
                    s_ops = tc::smem_u32(sm + SM_OPS);
 
     int start, end;
@@ -420,34 +418,13 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
             }
             __syncthreads();
         }
-        {   // T into [T; P] rows 0..63 and T^T into the B operand
+        {   // T into rows 0..63 of [T; P]
             const int r = tid & 63, qg = tid >> 6;
             for (int jj = 0; jj < 4; ++jj) {
                 const int j = qg + 4 * jj;
                 const float* tr = TM + r * AP + 4 * j;
                 st4(sm + SM_TP, OpTP::off(r, 4 * j), tr[0], tr[1], tr[2], tr[3]);
-                st4(sm + SM_TT, OpTT::off(r, 4 * j), TM[(4 * j) * AP + r], TM[(4 * j + 1) * AP + r],
-                    TM[(4 * j + 2) * AP + r], TM[(4 * j + 3) * AP + r]);
             }
-        }
-        sync_for_mma();
-        if (tid == 0) {
-            tc::tc_fence_after();
-            issue_mma<OpTP, OpTT>(tmem + TC_PT, s_tp, s_tt, 8, tc::idesc_tf32(128, 64));
-            tc::mma_commit(bar_mma);
-        }
-        wait_mma();
-        if (ln >= 64) {  // P T replaces P in the lower half of [T; P]
-            float v[32];
-            tc::tmem_ld16(tmem + lane_base + TC_PT + 32 * ch, *reinterpret_cast<float(*)[16]>(v));
-            tc::tmem_ld16(tmem + lane_base + TC_PT + 32 * ch + 16,
-                          *reinterpret_cast<float(*)[16]>(v + 16));
-            tc::tmem_ld_wait();
-            const int r = ln - 64;
-#pragma unroll
-            for (int c4 = 0; c4 < 8; ++c4)
-                st4(sm + SM_TP, OpTP::off(64 + r, 32 * ch + 4 * c4), v[4 * c4], v[4 * c4 + 1],
-                    v[4 * c4 + 2], v[4 * c4 + 3]);
         }
         sync_for_mma();
 
@@ -482,36 +459,39 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
             tc::mma_commit(bar_mma);
         }
         wait_mma();
-        {
+        if (ln < 64) {
             float v[16];
             tc::tmem_ld16(tmem + lane_base + TC_U + 16 * ch, v);
             tc::tmem_ld_wait();
-            if (ln < 64) {
-                const int r = ln;
+            const int r = ln;
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
-                    const float u = (r < L) ? v[jj] : 0.f;
-                    *reinterpret_cast<float*>(sm + SM_OPY + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(u);
-                }
-            } else {
-                const int r = ln - 64;
-                if (r < L) {
-                    float* orow = o + ((size_t)(c0 + r) * heads + h) * D + slice * DV + 16 * ch;
-#pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4)
-                        *reinterpret_cast<float4*>(orow + 4 * q4) =
-                            make_float4(qs[4 * q4] + v[4 * q4], qs[4 * q4 + 1] + v[4 * q4 + 1],
-                                        qs[4 * q4 + 2] + v[4 * q4 + 2], qs[4 * q4 + 3] + v[4 * q4 + 3]);
-                }
+            for (int jj = 0; jj < 16; ++jj) {
+                const float u = (r < L) ? v[jj] : 0.f;
+                *reinterpret_cast<float*>(sm + SM_OPY + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(u);
             }
         }
         sync_for_mma();
         if (tid == 0) {
             tc::tc_fence_after();
             issue_mma<OpKH, OpXV>(tmem + TC_E, s_opkh, s_opy, 8, tc::idesc_tf32(128, DV));
+            issue_mma<OpTP, OpXV>(tmem + TC_PU, s_tp, s_opy, 8, tc::idesc_tf32(128, DV));
             tc::mma_commit(bar_mma);
         }
         wait_mma();
+        if (ln >= 64) {  // O = Qtil S + P U for the chunk's rows
+            float v[16];
+            tc::tmem_ld16(tmem + lane_base + TC_PU + 16 * ch, v);
+            tc::tmem_ld_wait();
+            const int r = ln - 64;
+            if (r < L) {
+                float* orow = o + ((size_t)(c0 + r) * heads + h) * D + slice * DV + 16 * ch;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<float4*>(orow + 4 * q4) =
+                        make_float4(qs[4 * q4] + v[4 * q4], qs[4 * q4 + 1] + v[4 * q4 + 1],
+                                    qs[4 * q4 + 2] + v[4 * q4 + 2], qs[4 * q4 + 3] + v[4 * q4 + 3]);
+            }
+        }
         {
             float v[16];
             tc::tmem_ld16(tmem + lane_base + TC_E + 16 * ch, v);
