@@ -43,6 +43,7 @@ PREFILL_FLOPS = T_PREFILL * H * (6 * D * D + 5 * CHUNK * D + CHUNK * CHUNK / 3)
 DECODE_N, DECODE_STEPS = 64, 100
 DECODE_BYTES = 2 * DECODE_N * H * D * D * 4 + 4 * DECODE_N * H * D * 4 + DECODE_N * H * 4
 DK_N, DK_K = 128, 4
+CONV_K = 4
 DK_BYTES = (2 + DK_K) * DK_N * H * D * D * 4 + 4 * DK_N * DK_K * H * D * 4 + DK_N * DK_K * H * 4
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor ratio of the part
 
@@ -240,6 +241,36 @@ def run_gpu(args):
             decode_k()
         dk_per, _ = time_launches(decode_k, 20, stream)
         del kS, snaps, kin
+
+        # ---------------- front end + core: 16 packed sequences, conv then prefill
+        fe = wl.frontend()
+        cu = fe["cu_seqlens"].to(dev)
+        tot = int(fe["cu_seqlens"][-1])
+        x = fe["x"].to(dev)
+        wconv = fe["w"].to(dev)
+        cst = fe["conv_state"].to(dev)
+        xo = torch.empty_like(x)
+        fg, fb = fe["g"].to(dev), fe["beta"].to(dev)
+        fS = fe["state"].to(dev)
+        fo = torch.empty((tot, H, D), device=dev)
+        hd = H * D
+
+        def conv():
+            K.kda_conv_silu_l2(cst, x, wconv, xo, cu_seqlens=cu)
+
+        def core():
+            K.kda_prefill(fS, xo[:, :hd].view(tot, H, D), xo[:, hd:2 * hd].view(tot, H, D),
+                          xo[:, 2 * hd:].view(tot, H, D), fg, fb, fo, tot, CHUNK, cu_seqlens=cu)
+
+        for _ in range(3):
+            conv()
+            core()
+        conv_per, _ = time_launches(conv, 10, stream)
+        core_per, _ = time_launches(core, 3, stream)
+        K.kda_sync_status()
+        n_fe = len(fe["lengths"])
+        conv_bytes = tot * 3 * hd * 2 * 2 + 3 * hd * CONV_K * 2 + 2 * n_fe * 3 * hd * CONV_K * 4
+        del x, xo, fg, fb, fS, fo, cst
     clocks = clk.summary()
 
     # ---------------- end to end through the public API, host buffers
@@ -329,6 +360,20 @@ def run_gpu(args):
             "workload": wl.DECODE_K.name, "value": DK_BYTES / dk_s / 1e9, "unit": "GB/s",
             "frac_of_hbm_peak": DK_BYTES / dk_s / 1e9 / pk["hbm_gbs"],
             "us_per_call": dk_s * 1e6, "algorithmic_bytes": DK_BYTES,
+        },
+        "conv": {
+            "workload": wl.FRONTEND.name + " (conv + SiLU + L2 stage)",
+            "value": conv_bytes / (statistics.mean(conv_per) / 1e3) / 1e9, "unit": "GB/s",
+            "frac_of_hbm_peak": conv_bytes / (statistics.mean(conv_per) / 1e3) / 1e9
+            / pk["hbm_gbs"],
+            "us_per_call": statistics.mean(conv_per) * 1e3, "algorithmic_bytes": conv_bytes,
+            "tokens": tot, "gpu_launches_per_call": 2,
+        },
+        "frontend": {
+            "workload": wl.FRONTEND.name, "lengths": fe["lengths"],
+            "value": tot / ((statistics.mean(conv_per) + statistics.mean(core_per)) / 1e3),
+            "unit": "tokens/s", "conv_us": statistics.mean(conv_per) * 1e3,
+            "core_us": statistics.mean(core_per) * 1e3,
         },
         "wall_s_timed_region": wall,
     }

@@ -5,10 +5,11 @@
 // 1/sqrt(sum + eps)).
 //
 // Kernel 1 (conv_silu_l2_kernel): one CTA per (head-sized group of 128
-// channels, block of 32 tokens); a thread owns one channel.  History before a
-// sequence's first token comes from the conv state, which this kernel only
-// reads.  The L2 sum over a q/k head's 128 channels is a warp shuffle
-// reduction plus a 4-warp smem reduction per token.
+// channels, block of 32 consecutive tokens); a thread owns one channel and
+// slides a register window of the last conv_kernel - 1 inputs along the
+// tokens.  History before a sequence's first token comes from the conv
+// state, which this kernel only reads.  The L2 sum over a q/k head's 128
+// channels is a warp shuffle reduction plus a 4-warp smem reduction per token.
 // Kernel 2 (conv_state_kernel): after kernel 1, each thread rewrites one
 // (sequence, channel) state row to hold that sequence's last conv_kernel
 // inputs, reading the old row first; separating it from kernel 1 keeps any
@@ -65,33 +66,72 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
     for (int j = 0; j < K; ++j) wj[j] = bf16_to_f32(__ldg(w + (size_t)c * K + j));
 
     const int tok0 = blockIdx.y * kTok;
+    const int tok_end = min(total, tok0 + kTok);
+    // The block's tokens are consecutive: find the first one's sequence once,
+    // then step to the next sequence whenever a token reaches its end.
+    int n, start, end;
+    bool ok = true;
+    if (cu) {
+        ok = find_seq(cu, n_seqs, tok0, n, start);
+        end = ok ? __ldg(cu + n + 1) : tok0;
+    } else {
+        n = tok0 / t_per_seq;
+        start = n * t_per_seq;
+        end = start + t_per_seq;
+    }
+    // All of the block's inputs first, as independent loads.
+    float xs[kTok];
+#pragma unroll
+    for (int m = 0; m < kTok; ++m) {
+        const int tau = tok0 + m;
+        xs[m] = (tau < tok_end) ? bf16_to_f32(__ldg(x + (size_t)tau * conv_dim + c)) : 0.f;
+    }
+    // hist[j] holds the input at token tau - (K - 1) + j for the current tau.
+    float hist[K > 1 ? K - 1 : 1];
+    if (ok) {  // history of the first token: earlier inputs of its sequence, else its state
+        const float* st = conv_state + ((size_t)n * conv_dim + c) * K;
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+            const int src = tok0 - (K - 1) + j;
+            hist[j] = (src >= start) ? bf16_to_f32(__ldg(x + (size_t)src * conv_dim + c))
+                                     : __ldg(st + K + (src - start));
+        }
+    }
     float y[kTok];
 #pragma unroll
     for (int m = 0; m < kTok; ++m) {
         const int tau = tok0 + m;
         y[m] = 0.f;
-        if (tau >= total) continue;
-        int n, start;
-        if (cu) {
-            if (!find_seq(cu, n_seqs, tau, n, start)) {
-                if (threadIdx.x == 0) atomicOr(&g_conv_status, STATUS_BAD_CU_SEQLENS);
-                continue;
+        if (!ok || tau >= tok_end) continue;
+        if (tau >= end) {  // a new sequence starts at tau (skipping empty ones)
+            if (cu) {
+                while (n + 1 < n_seqs && __ldg(cu + n + 1) <= tau) ++n;
+                start = __ldg(cu + n);
+                end = __ldg(cu + n + 1);
+                if (!(start == tau && tau < end)) {
+                    ok = false;
+                    continue;
+                }
+            } else {
+                ++n;
+                start = n * t_per_seq;
+                end = start + t_per_seq;
             }
-        } else {
-            n = tau / t_per_seq;
-            start = n * t_per_seq;
+            const float* st = conv_state + ((size_t)n * conv_dim + c) * K;
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j) hist[j] = __ldg(st + j + 1);
         }
-        const float* hist = conv_state + ((size_t)n * conv_dim + c) * K;
+        const float xv = xs[m];
         float acc = 0.f;
 #pragma unroll
-        for (int j = 0; j < K; ++j) {
-            const int src = tau - (K - 1) + j;
-            const float xv = (src >= start) ? bf16_to_f32(__ldg(x + (size_t)src * conv_dim + c))
-                                            : __ldg(hist + K + (src - start));
-            acc = __fmaf_rn(wj[j], xv, acc);
-        }
-        y[m] = acc / (1.0f + expf(-acc));
+        for (int j = 0; j < K - 1; ++j) acc = __fmaf_rn(wj[j], hist[j], acc);
+        acc = __fmaf_rn(wj[K - 1], xv, acc);
+#pragma unroll
+        for (int j = 0; j + 1 < K - 1; ++j) hist[j] = hist[j + 1];
+        if constexpr (K > 1) hist[K - 2] = xv;
+        y[m] = __fdividef(acc, 1.0f + __expf(-acc));  // SiLU; rounded to BF16 below
     }
+    if (!ok && threadIdx.x == 0) atomicOr(&g_conv_status, STATUS_BAD_CU_SEQLENS);
 
     if (normalise) {  // uniform per CTA: the whole block takes this branch or none
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -112,7 +152,7 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
 #pragma unroll
     for (int m = 0; m < kTok; ++m) {
         const int tau = tok0 + m;
-        if (tau < total) out[(size_t)tau * conv_dim + c] = f32_to_bf16(y[m]);
+        if (tau < tok_end) out[(size_t)tau * conv_dim + c] = f32_to_bf16(y[m]);
     }
 }
 

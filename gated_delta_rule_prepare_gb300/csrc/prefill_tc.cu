@@ -241,6 +241,7 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
         {
             const int i = tid & 127, hf = tid >> 7;
             float acc = 0.f;
+#pragma unroll
             for (int rr = 0; rr < 32; ++rr) {
                 const int r = 32 * hf + rr;
                 float gv = 0.f, kv = 0.f, qv = 0.f;
@@ -266,6 +267,7 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
         if (tid >= 128) {
             const int i = tid & 127;
             const float base = GH[i];
+#pragma unroll
             for (int rr = 0; rr < 32; ++rr) GAM[(32 + rr) * KP + i] += base;
         }
         __syncthreads();

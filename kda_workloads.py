@@ -147,10 +147,11 @@ def frontend(seed: int = 0, n_seqs: int = 16, lo: int = 512, hi: int = 8192,
     n_seqs = len(lengths)
     total = int(sum(lengths))
     ch = 3 * heads * HEAD_DIM
-    x = torch.randn((total, ch), generator=gen, dtype=torch.float64).to(torch.bfloat16)
+    # x is the largest draw (sum T x 12288 values): FP32 draws, rounded to BF16.
+    x = torch.randn((total, ch), generator=gen, dtype=torch.float32).to(torch.bfloat16)
     w = (torch.randn((ch, conv_kernel), generator=gen, dtype=torch.float64) * 0.5
          ).to(torch.bfloat16)
-    g = (torch.rand((total, heads, HEAD_DIM), generator=gen, dtype=torch.float64) * 5.0
+    g = (torch.rand((total, heads, HEAD_DIM), generator=gen, dtype=torch.float32) * 5.0
          - 5.0).to(torch.bfloat16)
     beta = torch.sigmoid(torch.randn((total, heads), generator=gen, dtype=torch.float64)
                          ).to(torch.bfloat16)
