@@ -61,8 +61,12 @@ def peaks():
 
 
 def kernel_source_sha() -> str:
-    path = os.path.join(ROOT, "gated_delta_rule_prepare_gb300", "csrc", "prefill.cu")
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    """Hash of the sources the prefill kernels are built from."""
+    h = hashlib.sha256()
+    for name in ("prefill_tc.cu", "prefill.cu", "sm103_tc.h", "kda_common.h"):
+        h.update(open(os.path.join(ROOT, "gated_delta_rule_prepare_gb300", "csrc", name),
+                      "rb").read())
+    return h.hexdigest()[:16]
 
 
 def traffic_from_profile():
@@ -462,6 +466,15 @@ def run_case(args):
         o = torch.empty((DECODE_N, H, D), device=dev)
         fn = lambda: K.kda_decode(S, *ins, o)
         nbytes = DECODE_BYTES
+    elif args.case == "conv":
+        fe = wl.frontend(lengths=[args.seq_len])
+        cu = fe["cu_seqlens"].to(dev)
+        x = fe["x"].to(dev)
+        wconv = fe["w"].to(dev)
+        cst = fe["conv_state"].to(dev)
+        xo = torch.empty_like(x)
+        fn = lambda: K.kda_conv_silu_l2(cst, x, wconv, xo, cu_seqlens=cu)
+        nbytes = args.seq_len * 3 * H * D * 2 * 2 + 3 * H * D * CONV_K * 2 + 2 * 3 * H * D * CONV_K * 4
     else:
         kd = wl.decode_k()
         S = kd["state"].to(dev)
@@ -488,7 +501,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default=None, choices=["prefill", "decode", "decode_k"],
+    ap.add_argument("--case", default=None, choices=["prefill", "decode", "decode_k", "conv"],
                     help="time one kernel alone (for profiler captures)")
     ap.add_argument("--seq-len", type=int, default=T_PREFILL)
     args = ap.parse_args()

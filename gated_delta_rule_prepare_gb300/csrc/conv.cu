@@ -23,8 +23,8 @@ namespace {
 
 __device__ unsigned g_conv_status = 0;
 
-constexpr int kTok = 32;  // tokens per CTA
-constexpr int kThreads = D;
+constexpr int kTok = 32;        // tokens per CTA
+constexpr int kThreads = D;     // two heads of 128 channels, two channels per thread
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -32,6 +32,14 @@ __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
 
 __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
     return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+__device__ __forceinline__ float2 bf16x2_to_f32(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint32_t f32x2_to_bf16x2(float a, float b) {
+    return (uint32_t)f32_to_bf16(a) | ((uint32_t)f32_to_bf16(b) << 16);
 }
 
 // Sequence holding packed token tau: largest n with cu[n] <= tau.  Returns
@@ -50,6 +58,10 @@ __device__ __forceinline__ bool find_seq(const int* __restrict__ cu, int n_seqs,
     return start >= 0 && start <= tau && tau < end;
 }
 
+__device__ __forceinline__ float silu(float a) {
+    return __fdividef(a, 1.0f + __expf(-a));  // rounded to BF16 by the caller
+}
+
 template <int K>
 __global__ void __launch_bounds__(kThreads)
 conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __restrict__ x,
@@ -57,13 +69,19 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
                     int t_per_seq, const int* __restrict__ cu, int n_seqs, int heads,
                     float l2_eps) {
     __shared__ float red[kThreads / 32][kTok];
-    const int grp = blockIdx.x;
-    const int c = grp * D + threadIdx.x;
+    const int pair = blockIdx.x;  // head groups 2 pair and 2 pair + 1 of the 3H groups
+    const int c = pair * 2 * D + 2 * threadIdx.x;  // first of this thread's two channels
     const size_t conv_dim = (size_t)3 * heads * D;
-    const bool normalise = grp < 2 * heads;
-    float wj[K];
+    // The first 2H groups (q and k) always pair up fully; with an odd head count the
+    // last v pair has only one group, and its second half of threads stays idle.
+    if ((size_t)c >= conv_dim) return;
+    const bool normalise = pair < heads;
+    float w0[K], w1[K];
 #pragma unroll
-    for (int j = 0; j < K; ++j) wj[j] = bf16_to_f32(__ldg(w + (size_t)c * K + j));
+    for (int j = 0; j < K; ++j) {
+        w0[j] = bf16_to_f32(__ldg(w + (size_t)c * K + j));
+        w1[j] = bf16_to_f32(__ldg(w + (size_t)(c + 1) * K + j));
+    }
 
     const int tok0 = blockIdx.y * kTok;
     const int tok_end = min(total, tok0 + kTok);
@@ -80,28 +98,43 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
         end = start + t_per_seq;
     }
     // All of the block's inputs first, as independent loads.
-    float xs[kTok];
+    const uint32_t* xp = reinterpret_cast<const uint32_t*>(x + (size_t)tok0 * conv_dim + c);
+    const size_t step = conv_dim / 2;  // one token row, in channel pairs
+    float2 xs[kTok];
 #pragma unroll
-    for (int m = 0; m < kTok; ++m) {
-        const int tau = tok0 + m;
-        xs[m] = (tau < tok_end) ? bf16_to_f32(__ldg(x + (size_t)tau * conv_dim + c)) : 0.f;
-    }
-    // hist[j] holds the input at token tau - (K - 1) + j for the current tau.
-    float hist[K > 1 ? K - 1 : 1];
-    if (ok) {  // history of the first token: earlier inputs of its sequence, else its state
+    for (int m = 0; m < kTok; ++m)
+        xs[m] = (tok0 + m < tok_end) ? bf16x2_to_f32(__ldg(xp + m * step)) : make_float2(0.f, 0.f);
+    // h0[j], h1[j]: the two channels' inputs at token tau - (K - 1) + j.
+    float h0[K > 1 ? K - 1 : 1], h1[K > 1 ? K - 1 : 1];
+    auto state_history = [&]() {  // a sequence's first token: history from its state
+        const float* st = conv_state + ((size_t)n * conv_dim + c) * K;
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j) {
+            h0[j] = __ldg(st + j + 1);
+            h1[j] = __ldg(st + K + j + 1);
+        }
+    };
+    if (ok) {
         const float* st = conv_state + ((size_t)n * conv_dim + c) * K;
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) {
             const int src = tok0 - (K - 1) + j;
-            hist[j] = (src >= start) ? bf16_to_f32(__ldg(x + (size_t)src * conv_dim + c))
-                                     : __ldg(st + K + (src - start));
+            if (src >= start) {
+                const float2 v = bf16x2_to_f32(__ldg(reinterpret_cast<const uint32_t*>(
+                    x + (size_t)src * conv_dim + c)));
+                h0[j] = v.x;
+                h1[j] = v.y;
+            } else {
+                h0[j] = __ldg(st + K + (src - start));
+                h1[j] = __ldg(st + K + K + (src - start));
+            }
         }
     }
-    float y[kTok];
+    float2 y[kTok];
 #pragma unroll
     for (int m = 0; m < kTok; ++m) {
         const int tau = tok0 + m;
-        y[m] = 0.f;
+        y[m] = make_float2(0.f, 0.f);
         if (!ok || tau >= tok_end) continue;
         if (tau >= end) {  // a new sequence starts at tau (skipping empty ones)
             if (cu) {
@@ -117,43 +150,51 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
                 start = n * t_per_seq;
                 end = start + t_per_seq;
             }
-            const float* st = conv_state + ((size_t)n * conv_dim + c) * K;
-#pragma unroll
-            for (int j = 0; j < K - 1; ++j) hist[j] = __ldg(st + j + 1);
+            state_history();
         }
-        const float xv = xs[m];
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < K - 1; ++j) acc = __fmaf_rn(wj[j], hist[j], acc);
-        acc = __fmaf_rn(wj[K - 1], xv, acc);
+        for (int j = 0; j < K - 1; ++j) {
+            a0 = __fmaf_rn(w0[j], h0[j], a0);
+            a1 = __fmaf_rn(w1[j], h1[j], a1);
+        }
+        a0 = __fmaf_rn(w0[K - 1], xs[m].x, a0);
+        a1 = __fmaf_rn(w1[K - 1], xs[m].y, a1);
 #pragma unroll
-        for (int j = 0; j + 1 < K - 1; ++j) hist[j] = hist[j + 1];
-        if constexpr (K > 1) hist[K - 2] = xv;
-        y[m] = __fdividef(acc, 1.0f + __expf(-acc));  // SiLU; rounded to BF16 below
+        for (int j = 0; j + 1 < K - 1; ++j) {
+            h0[j] = h0[j + 1];
+            h1[j] = h1[j + 1];
+        }
+        if constexpr (K > 1) {
+            h0[K - 2] = xs[m].x;
+            h1[K - 2] = xs[m].y;
+        }
+        y[m] = make_float2(silu(a0), silu(a1));
     }
     if (!ok && threadIdx.x == 0) atomicOr(&g_conv_status, STATUS_BAD_CU_SEQLENS);
 
-    if (normalise) {  // uniform per CTA: the whole block takes this branch or none
+    if (normalise) {  // uniform per CTA: both heads are q/k heads or neither is
         const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
         for (int m = 0; m < kTok; ++m) {
-            float p = y[m] * y[m];
+            float p = y[m].x * y[m].x + y[m].y * y[m].y;
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
             if (lane == 0) red[warp][m] = p;
         }
         __syncthreads();
+        const int hw = warp & ~1;  // the two warps of this thread's head
 #pragma unroll
         for (int m = 0; m < kTok; ++m) {
-            const float ss = (red[0][m] + red[1][m]) + (red[2][m] + red[3][m]);
-            y[m] = y[m] * (1.0f / sqrtf(ss + l2_eps));
+            const float inv = rsqrtf(red[hw][m] + red[hw + 1][m] + l2_eps);
+            y[m].x *= inv;
+            y[m].y *= inv;
         }
     }
+    uint32_t* op = reinterpret_cast<uint32_t*>(out + (size_t)tok0 * conv_dim + c);
 #pragma unroll
-    for (int m = 0; m < kTok; ++m) {
-        const int tau = tok0 + m;
-        if (tau < tok_end) out[(size_t)tau * conv_dim + c] = f32_to_bf16(y[m]);
-    }
+    for (int m = 0; m < kTok; ++m)
+        if (tok0 + m < tok_end) op[m * step] = f32x2_to_bf16x2(y[m].x, y[m].y);
 }
 
 template <int K>
@@ -199,7 +240,7 @@ template <int K>
 kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint16_t* out,
                   int total, int t_per_seq, const int* cu, int n_seqs, int heads, float eps,
                   cudaStream_t s) {
-    dim3 grid(3 * heads, (total + kTok - 1) / kTok);
+    dim3 grid((3 * heads + 1) / 2, (total + kTok - 1) / kTok);
     conv_silu_l2_kernel<K><<<grid, kThreads, 0, s>>>(conv_state, x, w, out, total, t_per_seq,
                                                       cu, n_seqs, heads, eps);
     kda_status st = launch_result("kda_conv_silu_l2 (conv)");

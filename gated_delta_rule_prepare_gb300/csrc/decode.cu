@@ -4,13 +4,13 @@
 // the per-head gated delta-rule step, streaming the FP32 [128 x 128] state of
 // each (sequence, head) once in and once out (1R + 1W).
 //
-// Mapping: one CTA of 256 threads per (sequence, head).  Warp w owns key rows
-// [16w, 16w + 16); lane l owns value columns [4l, 4l + 4) as one float4, so
-// each warp-wide load or store is one contiguous 512-byte state row.  A thread
-// keeps its 16 x 4 block of the state in registers for the whole step (and,
-// in decode_k, for all k rows).  The two reductions over the key index
-// (S^T k and S^T q) sum 16 rows inside each thread, then the 8 warp partials
-// through shared memory in a fixed order.
+// Mapping: one CTA of 512 threads per (sequence, head).  Warp w owns key rows
+// [8w, 8w + 8); lane l owns value columns [4l, 4l + 4) as one float4, so each
+// warp-wide load or store is one contiguous 512-byte state row.  A thread
+// keeps its 8 x 4 block of the state in registers for the whole step (and, in
+// decode_k, for all k rows).  The two reductions over the key index (S^T k
+// and S^T q) sum 8 rows inside each thread, then the 16 warp partials through
+// shared memory in a fixed order.
 //
 // Bit-identity of decode_k with k serial decodes: both run the very same
 // token_step() with explicit round-to-nearest intrinsics (no contraction
@@ -21,7 +21,7 @@
 namespace kda {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRows = D / kWarps;  // key rows per warp
 
