@@ -195,9 +195,11 @@ def run_gpu(args):
     q, k, v, g, beta = (d[n].to(dev) for n in ("q", "k", "v", "g", "beta"))
     S = d["state"].to(dev)
     o = torch.empty((T_PREFILL, H, D), device=dev)
+    ws = torch.empty(K.kda_prefill_workspace_size(T_PREFILL, 1, CHUNK, H), dtype=torch.uint8,
+                     device=dev)
 
     def prefill():
-        K.kda_prefill(S, q, k, v, g, beta, o, T_PREFILL, CHUNK)
+        K.kda_prefill(S, q, k, v, g, beta, o, T_PREFILL, CHUNK, workspace=ws)
 
     for _ in range(args.warmup):
         prefill()
@@ -257,6 +259,8 @@ def run_gpu(args):
         fg, fb = fe["g"].to(dev), fe["beta"].to(dev)
         fS = fe["state"].to(dev)
         fo = torch.empty((tot, H, D), device=dev)
+        fws = torch.empty(K.kda_prefill_workspace_size(tot, len(fe["lengths"]), CHUNK, H),
+                          dtype=torch.uint8, device=dev)
         hd = H * D
 
         def conv():
@@ -264,7 +268,8 @@ def run_gpu(args):
 
         def core():
             K.kda_prefill(fS, xo[:, :hd].view(tot, H, D), xo[:, hd:2 * hd].view(tot, H, D),
-                          xo[:, 2 * hd:].view(tot, H, D), fg, fb, fo, tot, CHUNK, cu_seqlens=cu)
+                          xo[:, 2 * hd:].view(tot, H, D), fg, fb, fo, tot, CHUNK, cu_seqlens=cu,
+                          workspace=fws)
 
         for _ in range(3):
             conv()
@@ -274,7 +279,7 @@ def run_gpu(args):
         K.kda_sync_status()
         n_fe = len(fe["lengths"])
         conv_bytes = tot * 3 * hd * 2 * 2 + 3 * hd * CONV_K * 2 + 2 * n_fe * 3 * hd * CONV_K * 4
-        del x, xo, fg, fb, fS, fo, cst
+        del x, xo, fg, fb, fS, fo, cst, fws
     clocks = clk.summary()
 
     # ---------------- end to end through the public API, host buffers
@@ -352,7 +357,7 @@ def run_gpu(args):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "path": "pinned host q/k/v/g/beta -> kda_prefill -> o and state to host",
         },
-        "gpu_launches": args.steps,
+        "gpu_launches": 3 * args.steps,
         "clocks": clocks,
         "decode": {
             "workload": wl.DECODE.name, "value": DECODE_BYTES / dec_s / 1e9, "unit": "GB/s",
@@ -456,7 +461,9 @@ def run_case(args):
         q, k, v, g, beta = (d[n].to(dev) for n in ("q", "k", "v", "g", "beta"))
         S = d["state"].to(dev)
         o = torch.empty((args.seq_len, H, D), device=dev)
-        fn = lambda: K.kda_prefill(S, q, k, v, g, beta, o, args.seq_len, CHUNK)
+        ws = torch.empty(K.kda_prefill_workspace_size(args.seq_len, 1, CHUNK, H),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: K.kda_prefill(S, q, k, v, g, beta, o, args.seq_len, CHUNK, workspace=ws)
         nbytes = 4 * args.seq_len * H * D * 2 + args.seq_len * H * 2 + args.seq_len * H * D * 4 \
             + 2 * H * D * D * 4
     elif args.case == "decode":

@@ -51,7 +51,7 @@ def _load():
         fn = getattr(lib, name)
         fn.argtypes = args
         fn.restype = _i
-    lib.kda_prefill_workspace_size.argtypes = [_i] * 5
+    lib.kda_prefill_workspace_size.argtypes = [_i64, _i, _i, _i, _i, _i]
     lib.kda_prefill_workspace_size.restype = _sz
     lib.kda_last_error.argtypes = []
     lib.kda_last_error.restype = _c.c_char_p
@@ -130,8 +130,10 @@ def kda_decode_k(state, q, k, v, g, beta, o, snapshots=()):
                             _stream(state)))
 
 
-def kda_prefill_workspace_size(max_tokens, n_seqs, chunk, heads):
-    return int(LIB.kda_prefill_workspace_size(max_tokens, n_seqs, chunk, heads, HEAD_DIM))
+def kda_prefill_workspace_size(rows, n_seqs, chunk, heads, dtype=torch.bfloat16):
+    """Workspace bytes kda_prefill needs for `rows` token rows in total."""
+    in_dtype = BF16 if dtype == torch.bfloat16 else F32
+    return int(LIB.kda_prefill_workspace_size(int(rows), n_seqs, chunk, heads, HEAD_DIM, in_dtype))
 
 
 def kda_prefill(state, q, k, v, g, beta, o, t, chunk, pad_fill=0.0, cu_seqlens=None,
@@ -177,9 +179,11 @@ def kda_prefill(state, q, k, v, g, beta, o, t, chunk, pad_fill=0.0, cu_seqlens=N
         raise ValueError("kda_prefill: g/beta/o sizes do not match the token rows")
     if state.numel() != n_seqs * H * HEAD_DIM * HEAD_DIM or state.dtype != torch.float32:
         raise ValueError("kda_prefill: state must be FP32 [N, H, 128, 128]")
-    ws_need = kda_prefill_workspace_size(rows, n_seqs, chunk, H)
+    ws_need = kda_prefill_workspace_size(rows, n_seqs, chunk, H, dt)
     if ws_need and workspace is None:
-        raise ValueError("kda_prefill: a workspace of %d bytes is required" % ws_need)
+        # The caller gave none: allocate one here, outside the library (which
+        # never allocates).  Timed callers pass a preallocated buffer.
+        workspace = torch.empty(ws_need, dtype=torch.uint8, device=q.device)
     ws_ptr = workspace.data_ptr() if workspace is not None else None
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(LIB.kda_prefill(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),

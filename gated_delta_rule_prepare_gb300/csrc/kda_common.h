@@ -39,12 +39,14 @@ cudaError_t read_and_clear_status_prefill(unsigned* out);
 cudaError_t read_and_clear_status_conv(unsigned* out);
 cudaError_t read_and_clear_status_prefill_tc(unsigned* out);
 
-// Tensor-core prefill for BF16 inputs and chunk 64 (prefill_tc.cu); the
-// arguments have been validated by kda_prefill.
+// Tensor-core prefill for BF16 inputs and chunk 64 (prefill_tc.cu): its
+// workspace size for `rows` token rows, and the launch (arguments validated by
+// kda_prefill).
+size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads);
 kda_status launch_prefill_tc(float* state, const void* q, const void* k, const void* v,
                              const void* g, const void* beta, float* o, int t, int t_pad,
                              int heads, long long stride, const int* cu, int n_seqs,
-                             cudaStream_t s);
+                             void* workspace, cudaStream_t s);
 
 #define KDA_REQUIRE(cond, code, ...)      \
     do {                                  \

@@ -228,10 +228,17 @@ __global__ void pad_fill_kernel(TIn* q, TIn* k, TIn* v, TIn* g, TIn* beta, int t
     }
 }
 
+// True when this call runs on the tensor-core kernels (which need a workspace).
+bool uses_tensor_cores(int chunk, int in_dtype) {
+    if (in_dtype != KDA_BF16 || chunk != 64) return false;
+    const char* impl = getenv("KDA_PREFILL_IMPL");
+    return !(impl && strcmp(impl, "simt") == 0);
+}
+
 template <typename TIn>
 kda_status launch(float* state, void* q, void* k, void* v, void* g, void* beta, float* o, int t,
                   int t_pad, int chunk, float pad_fill, int heads, long long stride,
-                  const int* cu, int n_seqs, cudaStream_t s) {
+                  const int* cu, int n_seqs, void* workspace, cudaStream_t s) {
     if (!cu && t_pad > t) {
         TIn fill;
         if constexpr (sizeof(TIn) == 2) fill = __bfloat16_as_ushort(__float2bfloat16_rn(pad_fill));
@@ -245,14 +252,11 @@ kda_status launch(float* state, void* q, void* k, void* v, void* g, void* beta, 
         kda_status st = launch_result("kda_prefill (pad fill)");
         if (st != KDA_OK) return st;
     }
-    if constexpr (sizeof(TIn) == 2) {
-        // BF16 inputs with chunk 64 take the tensor-core kernel unless the
-        // caller pins the SIMT kernel (KDA_PREFILL_IMPL=simt, for comparisons).
-        const char* impl = getenv("KDA_PREFILL_IMPL");
-        if (chunk == 64 && !(impl && strcmp(impl, "simt") == 0))
-            return launch_prefill_tc(state, q, k, v, g, beta, o, t, t_pad, heads, stride, cu,
-                                     n_seqs, s);
-    }
+    // BF16 inputs with chunk 64 take the tensor-core kernels unless the caller
+    // pins the SIMT kernel (KDA_PREFILL_IMPL=simt, for comparisons).
+    if (uses_tensor_cores(chunk, sizeof(TIn) == 2 ? KDA_BF16 : KDA_F32))
+        return launch_prefill_tc(state, q, k, v, g, beta, o, t, t_pad, heads, stride, cu, n_seqs,
+                                 workspace, s);
     const size_t smem = sizeof(ChunkSmem);
     cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<TIn>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -281,14 +285,11 @@ cudaError_t read_and_clear_status_prefill(unsigned* out) {
 
 using namespace kda;
 
-extern "C" size_t kda_prefill_workspace_size(int max_tokens, int n_seqs, int chunk, int heads,
-                                             int head_dim) {
-    (void)max_tokens;
-    (void)n_seqs;
-    (void)chunk;
-    (void)heads;
-    (void)head_dim;
-    return 0;
+extern "C" size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads,
+                                             int head_dim, int in_dtype) {
+    if (rows < 0 || n_seqs < 1 || heads < 1 || head_dim != D) return 0;
+    if (!uses_tensor_cores(chunk, in_dtype)) return 0;
+    return prefill_tc_workspace_bytes(rows, n_seqs, heads);
 }
 
 extern "C" kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* beta,
@@ -322,15 +323,16 @@ extern "C" kda_status kda_prefill(float* state, void* q, void* k, void* v, void*
                 "kda_prefill: qkv_row_stride must be a multiple of 16 bytes");
     const long long rows = cu_seqlens ? (long long)t : (long long)t_pad * n_seqs;
     KDA_REQUIRE(rows <= 0x7fffffffLL, KDA_ERR_INVALID_ARG, "kda_prefill: too many token rows");
-    const size_t need = kda_prefill_workspace_size((int)rows, n_seqs, chunk, heads, head_dim);
+    const size_t need = kda_prefill_workspace_size(rows, n_seqs, chunk, heads, head_dim, in_dtype);
     KDA_REQUIRE(workspace_bytes >= need && (need == 0 || workspace), KDA_ERR_WORKSPACE,
                 "kda_prefill: workspace of %zu B given, %zu B needed", workspace_bytes, need);
+    KDA_REQUIRE(need == 0 || aligned16(workspace), KDA_ERR_INVALID_ARG,
+                "kda_prefill: workspace must be 16-byte aligned");
     KDA_REQUIRE(!fault_injected(), KDA_ERR_CUDA, "kda_prefill: injected launch failure");
-    (void)workspace;
     cudaStream_t s = as_stream(stream);
     if (in_dtype == KDA_BF16)
         return launch<uint16_t>(state, q, k, v, g, beta, o, t, t_pad, chunk, pad_fill, heads,
-                                qkv_row_stride, cu_seqlens, n_seqs, s);
+                                qkv_row_stride, cu_seqlens, n_seqs, workspace, s);
     return launch<float>(state, q, k, v, g, beta, o, t, t_pad, chunk, pad_fill, heads,
-                         qkv_row_stride, cu_seqlens, n_seqs, s);
+                         qkv_row_stride, cu_seqlens, n_seqs, workspace, s);
 }

@@ -1,33 +1,29 @@
-// Tensor-core chunked prefill of the KDA core for BF16 inputs and chunk 64
-// (Glm5NextKdaKernels::chunk_prepare + chunk_scan fused in one kernel).
+// Tensor-core chunked prefill of the KDA core for BF16 inputs and chunk 64:
+// Glm5NextKdaKernels::chunk_prepare and chunk_scan as two kernels around a
+// caller-owned workspace.
 //
-// One CTA of 256 threads per (sequence, head, 32-column value slice); it walks
-// the sequence's chunks in order, keeping its 128 x 32 slice of the FP32
-// state in registers (and a TF32 copy in shared memory as an MMA operand).
+// For a chunk of L <= 64 tokens (rows r, s; key channels i; value columns j)
+// of one head, with Gamma_r = sum_{u<=r} g_u and qh = KDA_Q_SCALE q:
+//   A_rs   = beta_s sum_i k_ri k_si e^(Gamma_ri-Gamma_si), s < r
+//   P_rs   = beta_s sum_i qh_ri k_si e^(Gamma_ri-Gamma_si), s <= r
+//   T      = (I + A)^-1                    (blocked forward substitution)
+//   Ktil   = e^Gamma (.) k,  Qtil = e^Gamma (.) qh,
+//   Khat_s = beta_s e^(Gamma_{L-1}-Gamma_s) (.) k_s,   dec = e^Gamma_{L-1}
+// prepare_kernel, one CTA per (chunk, head), fully parallel: everything above
+// that does not depend on the carried state.  It writes [Ktil; Qtil],
+// [T; P], Khat^T (as TF32 tensor-core operands, already in the layout the
+// scan consumes) and dec to the workspace: 131,584 bytes per chunk and head.
+// scan_kernel, one CTA per (sequence, head, 32-column value slice), carries
+// the FP32 state across the sequence's chunks in order:
+//   X = V - Ktil S;  U = T X;  O = Qtil S + P U;  S <- dec (.) S + Khat^T U
+// as three tensor-core round trips per chunk; the chunk's operands arrive by
+// bulk copy from the workspace and the value slice by TMA.
 //
-// Per chunk of L <= 64 tokens (rows r, s; key channels i; value columns j):
-//   Gamma_r  = sum_{u<=r} g_u                                  (FP32, SIMT)
-//   A_rs     = beta_s sum_i k_ri k_si e^(Gamma_ri-Gamma_si), s < r
-//   P_rs     = beta_s sum_i qh_ri k_si e^(Gamma_ri-Gamma_si), s <= r
-//   T        = (I + A)^-1                    (blocked forward substitution)
-//   X        = V - Ktil S,   Ktil = e^Gamma (.) k,  Qtil = e^Gamma (.) qh
-//   U        = T X,   O = Qtil S + P U
-//   S       <- diag(e^Gamma_{L-1}) S + Khat^T U,
-//              Khat_s = beta_s e^(Gamma_{L-1}-Gamma_s) (.) k_s
-// A and P are formed on the tensor cores one 16-column block b at a time:
-// with m_b = 16b + 8, e^(Gamma_r-Gamma_s) = e^(Gamma_r-Gamma_mb) e^(Gamma_mb-Gamma_s),
-// and for every (r >= 16b, s in block b) both factors stay within
-// e^(+-8 |g|_max), so FP32 neither overflows nor loses the product for
-// g >= -10; rows above the block (where the first factor would overflow) are
-// never formed into results.
-//
-// Tensor-core products (tcgen05.mma kind::tf32, FP32 accumulate in TMEM):
-//   [X_b; QX_b] (128x128) . Y_b^T     -> A, P column block b   (x4)
-//   [Ktil; Qtil] (128x128) . S        -> Ktil S, Qtil S
-//   [T; P] (128x64) . X               -> U = T X (rows 0..63)
-//   Khat^T (128x64) . U               -> state increment
-//   [T; P] (128x64) . U               -> P U (rows 64..127)
-// Raw q, k, g and the value slice arrive by TMA (cp.async.bulk.tensor).
+// A and P come from four tensor-core products, one per 16-column block b with
+// reference token m_b = 16b + 8: e^(Gamma_r-Gamma_s) = e^(Gamma_r-Gamma_mb)
+// e^(Gamma_mb-Gamma_s) with both factors within e^(+-8 |g|max) for every
+// (r >= 16b, s in block b), so FP32 neither overflows nor loses the product
+// for g >= -10; rows above the block are never formed into results.
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -62,16 +58,33 @@ struct Op {
     }
     static constexpr uint32_t bytes(int K) { return (uint32_t)(K / 4) * LBO; }
 };
-using OpX = Op<128, 0>;   // A: [Xb; QXb] then [Ktil; Qtil], K = 128 channels
+using OpX = Op<128, 0>;   // A: [X_b; QX_b] then [Ktil; Qtil], K = 128 channels
 using OpY = Op<16, 0>;    // B: Y_b, 16 rows, K = 128 channels
 using OpKH = Op<128, 0>;  // A: Khat^T, rows = key channel, K = 64 tokens
 using OpTP = Op<128, 0>;  // A: [T; P], K = 64 tokens
 using OpXV = Op<32, 16>;  // B: X^T and U^T, rows = value column, K = 64 tokens
 using OpS = Op<32, 16>;   // B: S^T, rows = value column, K = 128 key channels
 
-// ------------------------------------------------------------ smem layout
+// ------------------------------------------------------------ workspace
+// [chunk_off: (n_seqs + 1) int32, padded to 256 B][blob (g, h) for every
+// chunk g and head h].  A blob is the byte image of the scan's operands.
+constexpr uint32_t BLOB_OPX = 0;
+constexpr uint32_t BLOB_TP = BLOB_OPX + OpX::bytes(128);
+constexpr uint32_t BLOB_KH = BLOB_TP + OpTP::bytes(64);
+constexpr uint32_t BLOB_DEC = BLOB_KH + OpKH::bytes(64);
+constexpr uint32_t BLOB_BYTES = BLOB_DEC + 128 * 4;
+static_assert(BLOB_BYTES % 128 == 0, "blobs must stay 128-byte aligned");
+
+__host__ __device__ inline size_t header_bytes(int n_seqs) {
+    return ((size_t)(n_seqs + 1) * 4 + 255) & ~(size_t)255;
+}
+__host__ __device__ inline size_t blob_offset(int n_seqs, long long g, int h, int heads) {
+    return header_bytes(n_seqs) + ((size_t)g * heads + h) * BLOB_BYTES;
+}
+
+// ------------------------------------------------------------ prepare smem
 constexpr uint32_t SM_OPX = 0;                       // 65536 (raw TMA tiles alias it)
-constexpr uint32_t SM_RAWQ = 0, SM_RAWK = 16384, SM_RAWG = 32768, SM_RAWV = 49152;
+constexpr uint32_t SM_RAWQ = 0, SM_RAWK = 16384, SM_RAWG = 32768;
 constexpr uint32_t SM_KF = 65536;                    // FP32 k       [64][KP]
 constexpr uint32_t SM_QF = SM_KF + 64 * KP * 4;      // FP32 qh      [64][KP]
 constexpr uint32_t SM_GAM = SM_QF + 64 * KP * 4;     // FP32 Gamma   [64][KP]
@@ -80,25 +93,34 @@ constexpr uint32_t SM_STAGE_END = SM_GAM + 64 * KP * 4;
 constexpr uint32_t SM_AM = SM_KF;                    // FP32 A [64][AP]
 constexpr uint32_t SM_TM = SM_AM + 64 * AP * 4;      // FP32 T [64][AP]
 constexpr uint32_t SM_TP = (SM_TM + 64 * AP * 4 + 15) & ~15u;
-constexpr uint32_t SM_XV = SM_TP + OpTP::bytes(64);
-constexpr uint32_t SM_ZS = SM_XV + OpXV::bytes(64);  // solve scratch [3][16][17]
+constexpr uint32_t SM_ZS = SM_TP + OpTP::bytes(64);  // solve scratch [3][16][17]
 constexpr uint32_t SM_OPKH = SM_STAGE_END;
-constexpr uint32_t SM_OPY = SM_OPKH + OpKH::bytes(64);  // Y_b, later U^T
-constexpr uint32_t SM_OPS = SM_OPY + OpXV::bytes(64);
-constexpr uint32_t SM_BETA = SM_OPS + OpS::bytes(128);
+constexpr uint32_t SM_OPY = SM_OPKH + OpKH::bytes(64);
+constexpr uint32_t SM_BETA = SM_OPY + OpY::bytes(128);
 constexpr uint32_t SM_GH = SM_BETA + 64 * 4;
 constexpr uint32_t SM_GMID = SM_GH + 128 * 4;
 constexpr uint32_t SM_GLAST = SM_GMID + 4 * 128 * 4;
 constexpr uint32_t SM_DEC = SM_GLAST + 128 * 4;
 constexpr uint32_t SM_BAR = SM_DEC + 128 * 4;        // 2 mbarriers + TMEM base + flag
-constexpr uint32_t SM_TOTAL = SM_BAR + 64;
-
+constexpr uint32_t SM_PREP_TOTAL = SM_BAR + 64;
 static_assert(SM_ZS + 3 * 16 * 17 * 4 <= SM_STAGE_END, "solve scratch overlaps");
-static_assert(OpY::bytes(128) <= OpXV::bytes(64), "Y_b does not fit its slot");
-static_assert(SM_TOTAL <= 232448, "shared memory budget exceeded");
+static_assert(SM_PREP_TOTAL <= 232448, "shared memory budget exceeded");
 
-// TMEM columns (256 allocated)
-constexpr uint32_t TC_AP = 0, TC_PU = 64, TC_Y = 128, TC_U = 160, TC_E = 192;
+// ------------------------------------------------------------ scan smem
+constexpr uint32_t SS_BLOB = 0;                      // blob image: OPX | TP | KH | DEC
+constexpr uint32_t SS_OPX = SS_BLOB + BLOB_OPX, SS_TP = SS_BLOB + BLOB_TP,
+                   SS_KH = SS_BLOB + BLOB_KH, SS_DEC = SS_BLOB + BLOB_DEC;
+constexpr uint32_t SS_XV = SS_BLOB + BLOB_BYTES;
+constexpr uint32_t SS_U = SS_XV + OpXV::bytes(64);
+constexpr uint32_t SS_OPS = SS_U + OpXV::bytes(64);
+constexpr uint32_t SS_RAWV = (SS_OPS + OpS::bytes(128) + 127) & ~127u;
+constexpr uint32_t SS_BAR = SS_RAWV + 64 * DV * 2;
+constexpr uint32_t SS_TOTAL = SS_BAR + 64;
+static_assert(SS_TOTAL <= 232448, "shared memory budget exceeded");
+
+// TMEM columns: prepare 64 (A and P), scan 128
+constexpr uint32_t TC_AP = 0;
+constexpr uint32_t TC_PU = 0, TC_Y = 32, TC_U = 64, TC_E = 96;
 
 __device__ __forceinline__ float bf(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -110,8 +132,8 @@ __device__ __forceinline__ void st4(unsigned char* base, uint32_t off, float a, 
         make_float4(tc::to_tf32(a), tc::to_tf32(b), tc::to_tf32(c), tc::to_tf32(d));
 }
 
-struct TmaMaps {
-    CUtensorMap q, k, g, v;
+struct PrepMaps {
+    CUtensorMap q, k, g;
 };
 
 // D = A . B^T over `ksteps` K-steps of 8, issued by the calling thread.
@@ -122,15 +144,91 @@ __device__ __forceinline__ void issue_mma(uint32_t d, uint32_t a, uint32_t b, in
         tc::mma_tf32(d, OA::desc(a, ks), OB::desc(b, ks), idesc, ks > 0);
 }
 
+// Token range [start, end) of sequence n; false when cu_seqlens is malformed.
+__device__ __forceinline__ bool seq_range(const int* __restrict__ cu, int n, int n_seqs, int t,
+                                          int t_pad, int& start, int& end) {
+    if (!cu) {
+        start = n * t_pad;
+        end = start + t;
+        return true;
+    }
+    start = __ldg(cu + n);
+    end = __ldg(cu + n + 1);
+    bool ok = start >= 0 && start <= end && end <= t;
+    if (n == 0) ok = ok && start == 0;
+    if (n == n_seqs - 1) ok = ok && end == t;
+    return ok;
+}
+
+// chunk_off[n] = number of chunks of all sequences before n (one CTA).
+constexpr int MAP_THREADS = 1024;
+__global__ void __launch_bounds__(MAP_THREADS)
+chunk_map_kernel(const int* __restrict__ cu, int n_seqs, int t, int* __restrict__ chunk_off) {
+    __shared__ int part[MAP_THREADS];
+    const int per = (n_seqs + MAP_THREADS - 1) / MAP_THREADS;
+    const int lo = threadIdx.x * per, hi = min(n_seqs, lo + per);
+    int sum = 0;
+    for (int n = lo; n < hi; ++n) {
+        int len = t;
+        if (cu) {
+            len = __ldg(cu + n + 1) - __ldg(cu + n);
+            if (len < 0) {
+                atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
+                len = 0;
+            }
+        }
+        sum += (len + C - 1) / C;
+    }
+    part[threadIdx.x] = sum;
+    __syncthreads();
+    for (int off = 1; off < MAP_THREADS; off <<= 1) {  // inclusive scan of the partial sums
+        const int v = (threadIdx.x >= off) ? part[threadIdx.x - off] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int run = (threadIdx.x == 0) ? 0 : part[threadIdx.x - 1];
+    for (int n = lo; n < hi; ++n) {
+        chunk_off[n] = run;
+        int len = t;
+        if (cu) len = max(0, __ldg(cu + n + 1) - __ldg(cu + n));
+        run += (len + C - 1) / C;
+    }
+    if (threadIdx.x == MAP_THREADS - 1) chunk_off[n_seqs] = part[MAP_THREADS - 1];
+}
+
 __global__ void __launch_bounds__(NT, 1)
-prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ state,
-                  const uint16_t* __restrict__ beta, float* __restrict__ o, int t, int t_pad,
-                  int heads, const int* __restrict__ cu, int n_seqs) {
+prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict__ beta, int t,
+               int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
+               unsigned char* __restrict__ ws) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int h = blockIdx.y;
+    const long long g = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column half
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+    const int* chunk_off = reinterpret_cast<const int*>(ws);
+    const int total = __ldg(chunk_off + n_seqs);
+    if (g >= total) return;
+    int n = 0;
+    {   // the sequence holding chunk g: largest n with chunk_off[n] <= g
+        int lo = 0, hi = n_seqs - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (__ldg(chunk_off + mid) <= g) lo = mid;
+            else hi = mid - 1;
+        }
+        n = lo;
+    }
+    int start, end;
+    if (!seq_range(cu, n, n_seqs, t, t_pad, start, end)) {
+        if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
+        return;
+    }
+    const int c0 = start + (int)(g - __ldg(chunk_off + n)) * C;
+    if (c0 >= end) return;
+    const int L = min(C, end - c0);
 
     float* KF = reinterpret_cast<float*>(sm + SM_KF);
     float* QF = reinterpret_cast<float*>(sm + SM_QF);
@@ -146,31 +244,10 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 16);
-    int* abort_flag = reinterpret_cast<int*>(sm + SM_BAR + 20);
     const uint16_t* RAWQ = reinterpret_cast<const uint16_t*>(sm + SM_RAWQ);
     const uint16_t* RAWK = reinterpret_cast<const uint16_t*>(sm + SM_RAWK);
     const uint16_t* RAWG = reinterpret_cast<const uint16_t*>(sm + SM_RAWG);
-    const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + SM_RAWV);
-    const uint32_t s_opx = tc::smem_u32(sm + SM_OPX), s_opy = tc::smem_u32(sm + SM_OPY),
-                   s_opkh = tc::smem_u32(sm + SM_OPKH), s_tp = tc::smem_u32(sm + SM_TP),
-                   s_xv = tc::smem_u32(sm + SM_XV),
-                   s_ops = tc::smem_u32(sm + SM_OPS);
-
-    int start, end;
-    if (!cu) {
-        start = n * t_pad;
-        end = start + t;
-    } else {
-        start = __ldg(cu + n);
-        end = __ldg(cu + n + 1);
-        bool ok = start >= 0 && start <= end && end <= t;
-        if (n == 0) ok = ok && start == 0;
-        if (n == n_seqs - 1) ok = ok && end == t;
-        if (!ok) {
-            if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
-            return;
-        }
-    }
+    const uint32_t s_opx = tc::smem_u32(sm + SM_OPX), s_opy = tc::smem_u32(sm + SM_OPY);
 
     if (tid == 0) {
         tc::mbar_init(bar_tma, 1);
@@ -179,35 +256,19 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
         tc::prefetch_tmap(&maps.q);
         tc::prefetch_tmap(&maps.k);
         tc::prefetch_tmap(&maps.g);
-        tc::prefetch_tmap(&maps.v);
-        *abort_flag = 0;
     }
-    if (warp == 0) tc::tmem_alloc(tmem_slot, 256);
+    if (warp == 0) tc::tmem_alloc(tmem_slot, 64);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t ph_tma = 0, ph_mma = 0;
-
-    // state slice: thread (key ln, half ch) owns S[ln][16 ch .. 16 ch + 15]
-    float* Sg = state + ((size_t)n * heads + h) * D * D + (size_t)ln * D + slice * DV + ch * 16;
-    float sreg[16];
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(Sg + 4 * q4);
-        sreg[4 * q4] = v4.x;
-        sreg[4 * q4 + 1] = v4.y;
-        sreg[4 * q4 + 2] = v4.z;
-        sreg[4 * q4 + 3] = v4.w;
-    }
-#pragma unroll
-    for (int jj = 0; jj < 16; ++jj)
-        *reinterpret_cast<float*>(sm + SM_OPS + OpS::off(ch * 16 + jj, ln)) = tc::to_tf32(sreg[jj]);
+    uint32_t ph_mma = 0;
+    bool failed = false;
 
     auto wait_mma = [&]() {
         if (!tc::mbar_wait(bar_mma, ph_mma)) {
             atomicOr(&g_tc_status, STATUS_TIMEOUT);
-            *abort_flag = 1;
+            failed = true;
         }
         ph_mma ^= 1;
         tc::tc_fence_after();
@@ -218,24 +279,18 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
         __syncthreads();
     };
 
-    for (int c0 = start; c0 < end; c0 += C) {
-        const int L = min(C, end - c0);
-        // ---------------------------------------------------------- P0 loads
-        sync_for_mma();
-        if (*abort_flag) break;
-        if (tid == 0) {
-            tc::mbar_arrive_expect_tx(bar_tma, 3 * 16384 + 64 * DV * 2);
-            tc::tma_load_2d(sm + SM_RAWQ, &maps.q, bar_tma, h * D, c0);
-            tc::tma_load_2d(sm + SM_RAWK, &maps.k, bar_tma, h * D, c0);
-            tc::tma_load_2d(sm + SM_RAWG, &maps.g, bar_tma, h * D, c0);
-            tc::tma_load_2d(sm + SM_RAWV, &maps.v, bar_tma, h * D + slice * DV, c0);
-        }
-        if (tid < C) BETA[tid] = (tid < L) ? bf(__ldg(beta + (size_t)(c0 + tid) * heads + h)) : 0.f;
-        if (!tc::mbar_wait(bar_tma, ph_tma)) {
-            atomicOr(&g_tc_status, STATUS_TIMEOUT);
-            *abort_flag = 1;
-        }
-        ph_tma ^= 1;
+    // ---------------------------------------------------------- P0 loads
+    if (tid == 0) {
+        tc::mbar_arrive_expect_tx(bar_tma, 3 * 16384);
+        tc::tma_load_2d(sm + SM_RAWQ, &maps.q, bar_tma, h * D, c0);
+        tc::tma_load_2d(sm + SM_RAWK, &maps.k, bar_tma, h * D, c0);
+        tc::tma_load_2d(sm + SM_RAWG, &maps.g, bar_tma, h * D, c0);
+    }
+    if (tid < C) BETA[tid] = (tid < L) ? bf(__ldg(beta + (size_t)(c0 + tid) * heads + h)) : 0.f;
+    if (!tc::mbar_wait(bar_tma, 0)) {
+        atomicOr(&g_tc_status, STATUS_TIMEOUT);
+        failed = true;
+    }
 
         // ---------------------------------------------------------- P1 Gamma, staging
         {
@@ -256,12 +311,6 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
                 QF[r * KP + i] = qv;
             }
             if (hf == 0) GH[i] = acc;
-        }
-        float vreg[16];
-        if (ln < C) {
-#pragma unroll
-            for (int jj = 0; jj < 16; ++jj)
-                vreg[jj] = (ln < L) ? bf(RAWV[ln * DV + ch * 16 + jj]) : 0.f;
         }
         __syncthreads();
         if (tid >= 128) {
@@ -428,7 +477,115 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
                 st4(sm + SM_TP, OpTP::off(r, 4 * j), tr[0], tr[1], tr[2], tr[3]);
             }
         }
+        // ---------------------------------------------------------- write the blob
+        tc::fence_async_smem();
+        __syncthreads();
+        if (tid == 0 && !failed) {
+            unsigned char* blob = ws + blob_offset(n_seqs, g, h, heads);
+            tc::bulk_store(blob + BLOB_OPX, sm + SM_OPX, OpX::bytes(128));
+            tc::bulk_store(blob + BLOB_TP, sm + SM_TP, OpTP::bytes(64));
+            tc::bulk_store(blob + BLOB_KH, sm + SM_OPKH, OpKH::bytes(64));
+            tc::bulk_store(blob + BLOB_DEC, sm + SM_DEC, 128 * 4);
+            tc::bulk_commit();
+            tc::bulk_wait_all();
+        }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 64);
+    }
+}
+
+__global__ void __launch_bounds__(NT, 1)
+scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
+            float* __restrict__ o, int t, int t_pad, int heads, const int* __restrict__ cu,
+            int n_seqs, const unsigned char* __restrict__ ws) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column half
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+
+    int start, end;
+    if (!seq_range(cu, n, n_seqs, t, t_pad, start, end)) {
+        if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
+        return;
+    }
+    const long long g0 = __ldg(reinterpret_cast<const int*>(ws) + n);
+
+    float* DEC = reinterpret_cast<float*>(sm + SS_DEC);
+    const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + SS_RAWV);
+    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + SS_BAR);
+    uint64_t* bar_mma = bar_ld + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SS_BAR + 16);
+    int* abort_flag = reinterpret_cast<int*>(sm + SS_BAR + 20);
+    const uint32_t s_opx = tc::smem_u32(sm + SS_OPX), s_tp = tc::smem_u32(sm + SS_TP),
+                   s_opkh = tc::smem_u32(sm + SS_KH), s_xv = tc::smem_u32(sm + SS_XV),
+                   s_opy = tc::smem_u32(sm + SS_U), s_ops = tc::smem_u32(sm + SS_OPS);
+
+    if (tid == 0) {
+        tc::mbar_init(bar_ld, 1);
+        tc::mbar_init(bar_mma, 1);
+        tc::fence_mbar_init();
+        tc::prefetch_tmap(&vmap);
+        *abort_flag = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_slot, 128);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    uint32_t ph_ld = 0, ph_mma = 0;
+
+    // state slice: thread (key ln, half ch) owns S[ln][16 ch .. 16 ch + 15]
+    float* Sg = state + ((size_t)n * heads + h) * D * D + (size_t)ln * D + slice * DV + ch * 16;
+    float sreg[16];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 v4 = *reinterpret_cast<const float4*>(Sg + 4 * q4);
+        sreg[4 * q4] = v4.x;
+        sreg[4 * q4 + 1] = v4.y;
+        sreg[4 * q4 + 2] = v4.z;
+        sreg[4 * q4 + 3] = v4.w;
+    }
+#pragma unroll
+    for (int jj = 0; jj < 16; ++jj)
+        *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(ch * 16 + jj, ln)) = tc::to_tf32(sreg[jj]);
+
+    auto wait_mma = [&]() {
+        if (!tc::mbar_wait(bar_mma, ph_mma)) {
+            atomicOr(&g_tc_status, STATUS_TIMEOUT);
+            *abort_flag = 1;
+        }
+        ph_mma ^= 1;
+        tc::tc_fence_after();
+    };
+    auto sync_for_mma = [&]() {  // generic smem writes and TMEM reads before an MMA
+        tc::fence_async_smem();
+        tc::tc_fence_before();
+        __syncthreads();
+    };
+
+    long long g = g0;
+    for (int c0 = start; c0 < end; c0 += C, ++g) {
+        const int L = min(C, end - c0);
         sync_for_mma();
+        if (*abort_flag) break;
+        if (tid == 0) {
+            const unsigned char* blob = ws + blob_offset(n_seqs, g, h, heads);
+            tc::mbar_arrive_expect_tx(bar_ld, BLOB_BYTES + 64 * DV * 2);
+            tc::bulk_load(sm + SS_OPX, blob + BLOB_OPX, OpX::bytes(128), bar_ld);
+            tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTP::bytes(64), bar_ld);
+            tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKH::bytes(64), bar_ld);
+            tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_ld);
+            tc::tma_load_2d(sm + SS_RAWV, &vmap, bar_ld, h * D + slice * DV, c0);
+        }
+        if (!tc::mbar_wait(bar_ld, ph_ld)) {
+            atomicOr(&g_tc_status, STATUS_TIMEOUT);
+            *abort_flag = 1;
+        }
+        ph_ld ^= 1;
 
         // ---------------------------------------------------------- P6 state scan
         if (tid == 0) {
@@ -446,8 +603,8 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
                 const int r = ln;
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
-                    const float x = (r < L) ? vreg[jj] - v[jj] : 0.f;
-                    *reinterpret_cast<float*>(sm + SM_XV + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(x);
+                    const float x = (r < L) ? bf(RAWV[r * DV + 16 * ch + jj]) - v[jj] : 0.f;
+                    *reinterpret_cast<float*>(sm + SS_XV + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(x);
                 }
             } else {
 #pragma unroll
@@ -469,7 +626,7 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 const float u = (r < L) ? v[jj] : 0.f;
-                *reinterpret_cast<float*>(sm + SM_OPY + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(u);
+                *reinterpret_cast<float*>(sm + SS_U + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(u);
             }
         }
         sync_for_mma();
@@ -502,7 +659,7 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 sreg[jj] = __fmaf_rn(dk, sreg[jj], v[jj]);
-                *reinterpret_cast<float*>(sm + SM_OPS + OpS::off(16 * ch + jj, ln)) = tc::to_tf32(sreg[jj]);
+                *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(16 * ch + jj, ln)) = tc::to_tf32(sreg[jj]);
             }
         }
     }
@@ -517,7 +674,7 @@ prefill_tc_kernel(const __grid_constant__ TmaMaps maps, float* __restrict__ stat
     __syncthreads();
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 256);
+        tc::tmem_dealloc(tmem, 128);
     }
 }
 
@@ -548,35 +705,53 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+
 }  // namespace
 
-// Launches the tensor-core prefill (BF16 inputs, chunk 64); arguments are
-// validated by kda_prefill.
+size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads) {
+    const long long chunks = (rows + C - 1) / C + n_seqs;
+    return header_bytes(n_seqs) + (size_t)chunks * heads * BLOB_BYTES;
+}
+
+// Launches the tensor-core prefill (BF16 inputs, chunk 64); arguments,
+// including the workspace size, are validated by kda_prefill.
 kda_status launch_prefill_tc(float* state, const void* q, const void* k, const void* v,
                              const void* g, const void* beta, float* o, int t, int t_pad,
                              int heads, long long stride, const int* cu, int n_seqs,
-                             cudaStream_t s) {
+                             void* workspace, cudaStream_t s) {
     const uint64_t rows = cu ? (uint64_t)t : (uint64_t)t_pad * n_seqs;
-    TmaMaps maps;
+    PrepMaps maps;
+    CUtensorMap vmap;
     const uint64_t hd = (uint64_t)heads * D;
     if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, D) ||
         !make_map(&maps.k, k, hd, rows, (uint64_t)stride, D) ||
         !make_map(&maps.g, g, hd, rows, hd, D) ||
-        !make_map(&maps.v, v, hd, rows, (uint64_t)stride, DV)) {
+        !make_map(&vmap, v, hd, rows, (uint64_t)stride, DV)) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
-    cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SM_TOTAL);
+    cudaError_t e = cudaFuncSetAttribute(prepare_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)SM_PREP_TOTAL);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)SS_TOTAL);
     if (e != cudaSuccess) {
-        set_error("kda_prefill: cannot reserve %u B of shared memory: %s", SM_TOTAL,
-                  cudaGetErrorString(e));
+        set_error("kda_prefill: cannot reserve shared memory: %s", cudaGetErrorString(e));
         return KDA_ERR_CUDA;
     }
-    dim3 grid(D / DV, heads, n_seqs);
-    prefill_tc_kernel<<<grid, NT, SM_TOTAL, s>>>(maps, state, (const uint16_t*)beta, o, t, t_pad,
-                                                 heads, cu, n_seqs);
-    return launch_result("kda_prefill (tensor cores)");
+    unsigned char* ws = static_cast<unsigned char*>(workspace);
+    chunk_map_kernel<<<1, MAP_THREADS, 0, s>>>(cu, n_seqs, cu ? 0 : t, reinterpret_cast<int*>(ws));
+    kda_status st = launch_result("kda_prefill (chunk map)");
+    if (st != KDA_OK) return st;
+    const long long chunks = ((long long)rows + C - 1) / C + n_seqs;
+    prepare_kernel<<<dim3((unsigned)chunks, heads), NT, SM_PREP_TOTAL, s>>>(
+        maps, (const uint16_t*)beta, t, t_pad, heads, cu, n_seqs, ws);
+    st = launch_result("kda_prefill (prepare)");
+    if (st != KDA_OK) return st;
+    scan_kernel<<<dim3(D / DV, heads, n_seqs), NT, SS_TOTAL, s>>>(vmap, state, o, t, t_pad, heads,
+                                                                  cu, n_seqs, ws);
+    return launch_result("kda_prefill (scan)");
 }
 
 cudaError_t read_and_clear_status_prefill_tc(unsigned* out) {

@@ -127,20 +127,27 @@ kda_status kda_decode_k(float* state, const float* q, const float* k, const floa
  *           one [T][3*heads*128] buffer such as kda_conv_silu_l2's output)
  *   g     : in_dtype [rows][heads][128]   beta : in_dtype [rows][heads]
  *   o     : FP32 [rows][heads][128]; rows of padding are not written
- *   chunk : 16, 32, 64 or 128 (the chunk width C)
+ *   chunk : 16, 32 or 64 (the chunk width C; 128 is refused as unsupported)
  *   in_dtype : KDA_F32 or KDA_BF16 (applies to q, k, v, g, beta)
- *   workspace : device scratch of at least kda_prefill_workspace_size(...)
- *           bytes (may be NULL when that size is 0)
+ *   workspace : device scratch, 16-byte aligned, of at least
+ *           kda_prefill_workspace_size(...) bytes (may be NULL when that
+ *           size is 0).  Its contents on entry do not matter; calls that
+ *           share one workspace must be ordered on the GPU.
  */
 kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* beta, float* o,
                        int t, int t_pad, int chunk, float pad_fill, int heads, int head_dim,
                        int in_dtype, int64_t qkv_row_stride, const int* cu_seqlens, int n_seqs,
                        void* workspace, size_t workspace_bytes, uint64_t stream);
 
-/* Bytes of device workspace kda_prefill needs for at most max_tokens token
- * rows in total over n_seqs sequences.  Returns 0 when none is needed. */
-size_t kda_prefill_workspace_size(int max_tokens, int n_seqs, int chunk, int heads,
-                                  int head_dim);
+/* Bytes of device workspace kda_prefill needs for `rows` token rows in total
+ * (n_seqs * t_pad in the uniform form, t in the packed form) over n_seqs
+ * sequences with the given chunk width and input dtype.  Returns 0 when the
+ * call needs none (FP32 inputs or chunk != 64 run without one) or when an
+ * argument is invalid.  The BF16, chunk-64 tensor-core path stores the
+ * state-independent operands of every (chunk, head) there: about 128.5 KiB
+ * per chunk of 64 tokens and head, plus (n_seqs + 1) * 4 bytes. */
+size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads, int head_dim,
+                                  int in_dtype);
 
 /*
  * kda_conv_silu_l2 -- depthwise causal conv1d + SiLU, then L2 over the q and k

@@ -117,6 +117,18 @@ def test_fault_injection_hook_reports_launch_failure(lib, monkeypatch):
 
 
 def test_workspace_size_is_queryable(lib):
-    lib.kda_prefill_workspace_size.restype = SZ
-    lib.kda_prefill_workspace_size.argtypes = [I] * 5
-    assert lib.kda_prefill_workspace_size(8192, 1, 64, 32, 128) >= 0
+    f = lib.kda_prefill_workspace_size
+    f.restype = SZ
+    f.argtypes = [ctypes.c_int64, I, I, I, I, I]
+    big = f(8192, 1, 64, 32, 128, 1)          # BF16, chunk 64: tensor-core path
+    assert big >= (8192 // 64) * 32 * 131584
+    assert f(8192, 1, 64, 32, 128, 0) == 0    # FP32 inputs need none
+    assert f(8192, 1, 32, 32, 128, 1) == 0    # other chunk widths need none
+    assert f(8192, 1, 64, 32, 64, 1) == 0     # invalid head_dim
+
+
+def test_prefill_refuses_a_small_workspace(lib):
+    f = lib.kda_prefill
+    f.argtypes = [V] * 7 + [I, I, I, F, I, I, I, ctypes.c_int64, V, I, V, SZ, U64]
+    assert f(P, P, P, P, P, P, P, 128, 128, 64, 0.0, 2, 128, 1, 256, None, 1, P, 64, 0) == 3
+    assert b"workspace" in lib.kda_last_error()
