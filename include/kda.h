@@ -177,6 +177,36 @@ kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, const uint16_t
                             int conv_kernel, float l2_eps, int heads, int head_dim,
                             uint64_t stream);
 
+/* Size of the library-owned device array kda_prefill_static_ws uses as its
+ * workspace: 64 MiB on every GPU that loads the library, held until exit. */
+#define KDA_STATIC_WORKSPACE_BYTES (64u << 20)
+
+/*
+ * kda_prefill_static_ws -- kda_prefill without a caller workspace: the
+ * workspace is a fixed array of KDA_STATIC_WORKSPACE_BYTES that the library
+ * owns, so the call allocates nothing and the caller passes only inputs and
+ * outputs.  The source pages have no counterpart; it serves callers that
+ * cannot allocate device memory themselves, such as a plugin that receives
+ * only input and output pointers from its host application, or a serving
+ * loop that forbids cudaMalloc because it can synchronise the device.
+ *
+ *   Arguments, layouts and results are those of kda_prefill.
+ *   Refused with KDA_ERR_WORKSPACE when kda_prefill_workspace_size(...) for
+ *   the call exceeds KDA_STATIC_WORKSPACE_BYTES: at 32 heads that is about 15
+ *   chunks of 64 tokens in total; fewer heads allow proportionally more.
+ *   The first call on a device resolves the array's device address for that
+ *   device (cudaGetSymbolAddress, with the device current); make that first
+ *   call before any stream capture.
+ *   All calls on a device share the one array and it keeps the last call's
+ *   contents; nothing in it needs to start at zero (each call rewrites what it
+ *   reads).  Calls that overlap on the GPU (other streams, other threads)
+ *   race on it: order them.
+ */
+kda_status kda_prefill_static_ws(float* state, void* q, void* k, void* v, void* g, void* beta,
+                                 float* o, int t, int t_pad, int chunk, float pad_fill, int heads,
+                                 int head_dim, int in_dtype, int64_t qkv_row_stride,
+                                 const int* cu_seqlens, int n_seqs, uint64_t stream);
+
 /* Synchronises `stream`, then reads and clears the device status words of the
  * calling thread's current device.  Returns KDA_OK, KDA_ERR_DEVICE (a
  * device-side check failed since the last call; kda_last_error says which),
