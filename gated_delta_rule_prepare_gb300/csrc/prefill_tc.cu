@@ -40,8 +40,9 @@ __device__ unsigned g_tc_status = 0;
 constexpr int C = 64;
 constexpr int DV = 32;
 constexpr int NT = 256;
-constexpr int KP = 129;  // pitch (floats) of FP32 [64][128] staging arrays
-constexpr int AP = 65;   // pitch (floats) of FP32 [64][64] arrays
+constexpr int KP = 132;  // pitch (floats) of FP32 [64][128] staging arrays (16-B rows)
+constexpr int AP = 65;   // pitch (floats) of the FP32 [64][64] A / W array
+constexpr int TPP = 68;  // pitch (floats) of the FP32 [64][64] T array (16-B rows)
 
 // K-major operand of R rows in the "K-outer" core-matrix layout: the core
 // matrices of one K group of 4 columns are stacked over all rows (128 B per 8
@@ -56,7 +57,7 @@ struct Op {
     static __device__ __forceinline__ uint64_t desc(uint32_t base, int ks) {
         return tc::make_desc(base + (uint32_t)ks * 2u * LBO, LBO, 128u);
     }
-    static constexpr uint32_t bytes(int K) { return (uint32_t)(K / 4) * LBO; }
+    static __host__ __device__ constexpr uint32_t bytes(int K) { return (uint32_t)(K / 4) * LBO; }
 };
 using OpX = Op<128, 0>;   // A: [X_b; QX_b] then [Ktil; Qtil], K = 128 channels
 using OpY = Op<16, 0>;    // B: Y_b, 16 rows, K = 128 channels
@@ -90,20 +91,20 @@ constexpr uint32_t SM_QF = SM_KF + 64 * KP * 4;      // FP32 qh      [64][KP]
 constexpr uint32_t SM_GAM = SM_QF + 64 * KP * 4;     // FP32 Gamma   [64][KP]
 constexpr uint32_t SM_STAGE_END = SM_GAM + 64 * KP * 4;
 // reused after the prepare operands are built
-constexpr uint32_t SM_AM = SM_KF;                    // FP32 A [64][AP]
-constexpr uint32_t SM_TM = SM_AM + 64 * AP * 4;      // FP32 T [64][AP]
-constexpr uint32_t SM_TP = (SM_TM + 64 * AP * 4 + 15) & ~15u;
-constexpr uint32_t SM_ZS = SM_TP + OpTP::bytes(64);  // solve scratch [3][16][17]
+constexpr uint32_t SM_AM = SM_KF;                    // FP32 A, then W blocks [64][AP]
+constexpr uint32_t SM_TM = (SM_AM + 64 * AP * 4 + 15) & ~15u;  // FP32 T [64][TPP]
+constexpr uint32_t SM_TP = SM_TM + 64 * TPP * 4;
+// Khat^T; during the A/P products it holds the four Y_b operands instead
 constexpr uint32_t SM_OPKH = SM_STAGE_END;
-constexpr uint32_t SM_OPY = SM_OPKH + OpKH::bytes(64);
-constexpr uint32_t SM_BETA = SM_OPY + OpY::bytes(128);
+constexpr uint32_t SM_BETA = SM_OPKH + OpKH::bytes(64);
 constexpr uint32_t SM_GH = SM_BETA + 64 * 4;
 constexpr uint32_t SM_GMID = SM_GH + 128 * 4;
 constexpr uint32_t SM_GLAST = SM_GMID + 4 * 128 * 4;
 constexpr uint32_t SM_DEC = SM_GLAST + 128 * 4;
 constexpr uint32_t SM_BAR = SM_DEC + 128 * 4;        // 2 mbarriers + TMEM base + flag
 constexpr uint32_t SM_PREP_TOTAL = SM_BAR + 64;
-static_assert(SM_ZS + 3 * 16 * 17 * 4 <= SM_STAGE_END, "solve scratch overlaps");
+static_assert(SM_TP + OpTP::bytes(64) <= SM_STAGE_END, "solve arrays overlap");
+static_assert(4 * OpY::bytes(128) <= OpKH::bytes(64), "Y_b operands do not fit");
 static_assert(SM_PREP_TOTAL <= 232448, "shared memory budget exceeded");
 
 // ------------------------------------------------------------ scan smem
@@ -235,7 +236,6 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
     float* GAM = reinterpret_cast<float*>(sm + SM_GAM);
     float* AM = reinterpret_cast<float*>(sm + SM_AM);
     float* TM = reinterpret_cast<float*>(sm + SM_TM);
-    float* ZS = reinterpret_cast<float*>(sm + SM_ZS);
     float* BETA = reinterpret_cast<float*>(sm + SM_BETA);
     float* GH = reinterpret_cast<float*>(sm + SM_GH);
     float* GMID = reinterpret_cast<float*>(sm + SM_GMID);
@@ -247,7 +247,7 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
     const uint16_t* RAWQ = reinterpret_cast<const uint16_t*>(sm + SM_RAWQ);
     const uint16_t* RAWK = reinterpret_cast<const uint16_t*>(sm + SM_RAWK);
     const uint16_t* RAWG = reinterpret_cast<const uint16_t*>(sm + SM_RAWG);
-    const uint32_t s_opx = tc::smem_u32(sm + SM_OPX), s_opy = tc::smem_u32(sm + SM_OPY);
+    const uint32_t s_opx = tc::smem_u32(sm + SM_OPX), s_opkh = tc::smem_u32(sm + SM_OPKH);
 
     if (tid == 0) {
         tc::mbar_init(bar_tma, 1);
@@ -329,38 +329,43 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
         __syncthreads();
 
         // ---------------------------------------------------------- P2 A and P blocks
+        // Y_b for all four blocks first: row s of block b = s / 16 is
+        // k_s e^(Gamma_mb - Gamma_s); they live in the Khat^T slot until P3.
+        for (int e = tid; e < 64 * 32; e += NT) {
+            const int s = e & 63, j = e >> 6, b = s >> 4;
+            const float4 gm = *reinterpret_cast<const float4*>(GMID + b * 128 + 4 * j);
+            const float4 ga = *reinterpret_cast<const float4*>(GAM + s * KP + 4 * j);
+            const float4 kf = *reinterpret_cast<const float4*>(KF + s * KP + 4 * j);
+            st4(sm + SM_OPKH + b * OpY::bytes(128), OpY::off(s & 15, 4 * j),
+                kf.x * __expf(gm.x - ga.x), kf.y * __expf(gm.y - ga.y),
+                kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
+        }
         for (int b = 0; b < 4; ++b) {
-            {
+            {   // rows r >= 16 b: k_r and qh_r times e^(Gamma_r - Gamma_mb)
                 const int r = tid & 63, qg = tid >> 6;
                 if (r >= 16 * b) {
-                    const float* gm = GMID + b * 128;
+                    const float* gmb = GMID + b * 128;
+#pragma unroll 4
                     for (int jj = 0; jj < 8; ++jj) {
                         const int j = qg + 4 * jj;
-                        float f[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) f[e] = __expf(GAM[r * KP + 4 * j + e] - gm[4 * j + e]);
-                        const float* kr = KF + r * KP + 4 * j;
-                        const float* qr = QF + r * KP + 4 * j;
-                        st4(sm + SM_OPX, OpX::off(r, 4 * j), kr[0] * f[0], kr[1] * f[1],
-                            kr[2] * f[2], kr[3] * f[3]);
-                        st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qr[0] * f[0], qr[1] * f[1],
-                            qr[2] * f[2], qr[3] * f[3]);
+                        const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
+                        const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
+                        const float4 kf = *reinterpret_cast<const float4*>(KF + r * KP + 4 * j);
+                        const float4 qf = *reinterpret_cast<const float4*>(QF + r * KP + 4 * j);
+                        const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
+                                    f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
+                        st4(sm + SM_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
+                            kf.w * f3);
+                        st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1,
+                            qf.z * f2, qf.w * f3);
                     }
-                }
-                const float* gm = GMID + b * 128;
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    const int sr = tid & 15, j = (tid >> 4) + 16 * q2, s = 16 * b + sr;
-                    float y[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        y[e] = KF[s * KP + 4 * j + e] * __expf(gm[4 * j + e] - GAM[s * KP + 4 * j + e]);
-                    st4(sm + SM_OPY, OpY::off(sr, 4 * j), y[0], y[1], y[2], y[3]);
                 }
             }
             sync_for_mma();
             if (tid == 0) {
                 tc::tc_fence_after();
-                issue_mma<OpX, OpY>(tmem + TC_AP + 16 * b, s_opx, s_opy, 16, tc::idesc_tf32(128, 16));
+                issue_mma<OpX, OpY>(tmem + TC_AP + 16 * b, s_opx,
+                                    s_opkh + b * OpY::bytes(128), 16, tc::idesc_tf32(128, 16));
                 tc::mma_commit(bar_mma);
             }
             wait_mma();
@@ -369,17 +374,17 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
         // ---------------------------------------------------------- P3 Ktil/Qtil, Khat^T
         {
             const int r = tid & 63, qg = tid >> 6;
+#pragma unroll 4
             for (int jj = 0; jj < 8; ++jj) {
                 const int j = qg + 4 * jj;
-                float f[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) f[e] = __expf(GAM[r * KP + 4 * j + e]);
-                const float* kr = KF + r * KP + 4 * j;
-                const float* qr = QF + r * KP + 4 * j;
-                st4(sm + SM_OPX, OpX::off(r, 4 * j), kr[0] * f[0], kr[1] * f[1], kr[2] * f[2],
-                    kr[3] * f[3]);
-                st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qr[0] * f[0], qr[1] * f[1],
-                    qr[2] * f[2], qr[3] * f[3]);
+                const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
+                const float4 kf = *reinterpret_cast<const float4*>(KF + r * KP + 4 * j);
+                const float4 qf = *reinterpret_cast<const float4*>(QF + r * KP + 4 * j);
+                const float f0 = __expf(ga.x), f1 = __expf(ga.y), f2 = __expf(ga.z),
+                            f3 = __expf(ga.w);
+                st4(sm + SM_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2, kf.w * f3);
+                st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1, qf.z * f2,
+                    qf.w * f3);
             }
             const int i = tid & 127, hq = tid >> 7;
             const float gl = GLAST[i];
@@ -394,7 +399,15 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                 st4(sm + SM_OPKH, OpKH::off(i, 4 * q4), kh[0], kh[1], kh[2], kh[3]);
             }
         }
+        tc::fence_async_smem();
         __syncthreads();  // staging arrays are dead from here on
+        unsigned char* blob = ws + blob_offset(n_seqs, g, h, heads);
+        if (tid == 0 && !failed) {  // these three parts of the blob are final
+            tc::bulk_store(blob + BLOB_OPX, sm + SM_OPX, OpX::bytes(128));
+            tc::bulk_store(blob + BLOB_KH, sm + SM_OPKH, OpKH::bytes(64));
+            tc::bulk_store(blob + BLOB_DEC, sm + SM_DEC, 128 * 4);
+            tc::bulk_commit();
+        }
 
         // ---------------------------------------------------------- P4 read A, P
         {
@@ -424,12 +437,12 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                 }
             }
         }
-        for (int e = tid; e < 64 * 64; e += NT) TM[(e >> 6) * AP + (e & 63)] = 0.f;
+        for (int e = tid; e < 64 * 64; e += NT) TM[(e >> 6) * TPP + (e & 63)] = 0.f;
         tc::tc_fence_before();
         __syncthreads();
 
         // ---------------------------------------------------------- P5 T = (I + A)^-1
-        if (tid < 64) {  // diagonal 16 x 16 blocks: one column per thread
+        if (tid < 64) {  // diagonal 16 x 16 blocks T_aa = (I + A_aa)^-1, one column per thread
             const int a = tid >> 4, cc = tid & 15, o0 = 16 * a;
             float col[16];
 #pragma unroll
@@ -441,53 +454,93 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                 col[rr] = (rr < cc) ? 0.f : x;
             }
 #pragma unroll
-            for (int rr = 0; rr < 16; ++rr) TM[(o0 + rr) * AP + o0 + cc] = col[rr];
+            for (int rr = 0; rr < 16; ++rr) TM[(o0 + rr) * TPP + o0 + cc] = col[rr];
         }
         __syncthreads();
-        for (int d = 1; d < 4; ++d) {  // block sub-diagonal d: T_ab = -T_aa sum_c A_ac T_cb
-            const int np = 4 - d;
-            for (int e = tid; e < np * 256; e += NT) {
-                const int pb = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                const int b = pb, a = pb + d;
-                float z = 0.f;
-                for (int c = b; c < a; ++c)
+        // Below the diagonal, with W_ac = T_aa A_ac:  T_ab = -sum_{c=b}^{a-1} W_ac T_cb.
+        // Work in 1 x 4 tiles (one row, four consecutive columns) per thread.
+        {
+            float4 w[2];
 #pragma unroll
-                    for (int kk = 0; kk < 16; ++kk)
-                        z = __fmaf_rn(AM[(16 * a + rr) * AP + 16 * c + kk],
-                                      TM[(16 * c + kk) * AP + 16 * b + cc], z);
-                ZS[(pb * 16 + rr) * 17 + cc] = z;
+            for (int m = 0; m < 2; ++m) {
+                const int e = tid + NT * m;
+                w[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (e < 6 * 64) {
+                    const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
+                    const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
+                    const int c = (pb == 0) ? 0 : (pb < 3) ? pb - 1 : pb - 3;
+                    const float* arow = AM + 16 * c + 4 * cq;
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const float t = TM[(16 * a + rr) * TPP + 16 * a + kk];
+                        const float* ak = arow + (16 * a + kk) * AP;
+                        w[m].x = __fmaf_rn(t, ak[0], w[m].x);
+                        w[m].y = __fmaf_rn(t, ak[1], w[m].y);
+                        w[m].z = __fmaf_rn(t, ak[2], w[m].z);
+                        w[m].w = __fmaf_rn(t, ak[3], w[m].w);
+                    }
+                }
             }
             __syncthreads();
-            for (int e = tid; e < np * 256; e += NT) {
-                const int pb = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
-                const int b = pb, a = pb + d;
-                float x = 0.f;
 #pragma unroll
-                for (int kk = 0; kk < 16; ++kk)
-                    x = __fmaf_rn(TM[(16 * a + rr) * AP + 16 * a + kk], ZS[(pb * 16 + kk) * 17 + cc], x);
-                TM[(16 * a + rr) * AP + 16 * b + cc] = -x;
+            for (int m = 0; m < 2; ++m) {
+                const int e = tid + NT * m;
+                if (e < 6 * 64) {
+                    const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
+                    const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
+                    const int c = (pb == 0) ? 0 : (pb < 3) ? pb - 1 : pb - 3;
+                    float* dst = AM + (16 * a + rr) * AP + 16 * c + 4 * cq;
+                    dst[0] = w[m].x;
+                    dst[1] = w[m].y;
+                    dst[2] = w[m].z;
+                    dst[3] = w[m].w;
+                }
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int d = 1; d < 4; ++d) {
+            if (tid < (4 - d) * 64) {
+                const int b = tid >> 6, a = b + d, rr = (tid >> 2) & 15, cq = tid & 3;
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int cd = 0; cd < d; ++cd) {
+                    const int c = b + cd;
+#pragma unroll
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const float wv = AM[(16 * a + rr) * AP + 16 * c + kk];
+                        const float4 t4 =
+                            *reinterpret_cast<const float4*>(TM + (16 * c + kk) * TPP + 16 * b + 4 * cq);
+                        x.x = __fmaf_rn(wv, t4.x, x.x);
+                        x.y = __fmaf_rn(wv, t4.y, x.y);
+                        x.z = __fmaf_rn(wv, t4.z, x.z);
+                        x.w = __fmaf_rn(wv, t4.w, x.w);
+                    }
+                }
+                *reinterpret_cast<float4*>(TM + (16 * a + rr) * TPP + 16 * b + 4 * cq) =
+                    make_float4(-x.x, -x.y, -x.z, -x.w);
             }
             __syncthreads();
         }
         {   // T into rows 0..63 of [T; P]
             const int r = tid & 63, qg = tid >> 6;
+#pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
                 const int j = qg + 4 * jj;
-                const float* tr = TM + r * AP + 4 * j;
-                st4(sm + SM_TP, OpTP::off(r, 4 * j), tr[0], tr[1], tr[2], tr[3]);
+                const float4 tr = *reinterpret_cast<const float4*>(TM + r * TPP + 4 * j);
+                st4(sm + SM_TP, OpTP::off(r, 4 * j), tr.x, tr.y, tr.z, tr.w);
             }
         }
+
         // ---------------------------------------------------------- write the blob
         tc::fence_async_smem();
         __syncthreads();
-        if (tid == 0 && !failed) {
-            unsigned char* blob = ws + blob_offset(n_seqs, g, h, heads);
-            tc::bulk_store(blob + BLOB_OPX, sm + SM_OPX, OpX::bytes(128));
-            tc::bulk_store(blob + BLOB_TP, sm + SM_TP, OpTP::bytes(64));
-            tc::bulk_store(blob + BLOB_KH, sm + SM_OPKH, OpKH::bytes(64));
-            tc::bulk_store(blob + BLOB_DEC, sm + SM_DEC, 128 * 4);
-            tc::bulk_commit();
-            tc::bulk_wait_all();
+        if (tid == 0) {
+            if (!failed) {
+                tc::bulk_store(blob + BLOB_TP, sm + SM_TP, OpTP::bytes(64));
+                tc::bulk_commit();
+            }
+            tc::bulk_wait_read_all();  // shared memory stays valid until read
         }
     tc::tc_fence_before();
     __syncthreads();
@@ -516,16 +569,18 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
 
     float* DEC = reinterpret_cast<float*>(sm + SS_DEC);
     const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + SS_RAWV);
-    uint64_t* bar_ld = reinterpret_cast<uint64_t*>(sm + SS_BAR);
-    uint64_t* bar_mma = bar_ld + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SS_BAR + 16);
-    int* abort_flag = reinterpret_cast<int*>(sm + SS_BAR + 20);
+    uint64_t* bar_a = reinterpret_cast<uint64_t*>(sm + SS_BAR);
+    uint64_t* bar_b = bar_a + 1;
+    uint64_t* bar_mma = bar_a + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SS_BAR + 24);
+    int* abort_flag = reinterpret_cast<int*>(sm + SS_BAR + 28);
     const uint32_t s_opx = tc::smem_u32(sm + SS_OPX), s_tp = tc::smem_u32(sm + SS_TP),
                    s_opkh = tc::smem_u32(sm + SS_KH), s_xv = tc::smem_u32(sm + SS_XV),
                    s_opy = tc::smem_u32(sm + SS_U), s_ops = tc::smem_u32(sm + SS_OPS);
 
     if (tid == 0) {
-        tc::mbar_init(bar_ld, 1);
+        tc::mbar_init(bar_a, 1);
+        tc::mbar_init(bar_b, 1);
         tc::mbar_init(bar_mma, 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&vmap);
@@ -536,7 +591,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t ph_ld = 0, ph_mma = 0;
+    uint32_t ph_mma = 0;
 
     // state slice: thread (key ln, half ch) owns S[ln][16 ch .. 16 ch + 15]
     float* Sg = state + ((size_t)n * heads + h) * D * D + (size_t)ln * D + slice * DV + ch * 16;
@@ -567,34 +622,75 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         __syncthreads();
     };
 
-    long long g = g0;
-    for (int c0 = start; c0 < end; c0 += C, ++g) {
-        const int L = min(C, end - c0);
-        sync_for_mma();
-        if (*abort_flag) break;
-        if (tid == 0) {
-            const unsigned char* blob = ws + blob_offset(n_seqs, g, h, heads);
-            tc::mbar_arrive_expect_tx(bar_ld, BLOB_BYTES + 64 * DV * 2);
-            tc::bulk_load(sm + SS_OPX, blob + BLOB_OPX, OpX::bytes(128), bar_ld);
-            tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTP::bytes(64), bar_ld);
-            tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKH::bytes(64), bar_ld);
-            tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_ld);
-            tc::tma_load_2d(sm + SS_RAWV, &vmap, bar_ld, h * D + slice * DV, c0);
-        }
-        if (!tc::mbar_wait(bar_ld, ph_ld)) {
+    // Operands arrive in two groups so the next chunk's copies overlap this
+    // chunk's products: group A ([Ktil; Qtil] and the value tile) is consumed
+    // by the first product, group B ([T; P], Khat^T, dec) by the last two.
+    auto load_a = [&](long long gg, int cc0) {
+        const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
+        tc::mbar_arrive_expect_tx(bar_a, OpX::bytes(128) + 64 * DV * 2);
+        tc::bulk_load(sm + SS_OPX, blob + BLOB_OPX, OpX::bytes(128), bar_a);
+        tc::tma_load_2d(sm + SS_RAWV, &vmap, bar_a, h * D + slice * DV, cc0);
+    };
+    auto load_b = [&](long long gg) {
+        const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
+        tc::mbar_arrive_expect_tx(bar_b, OpTP::bytes(64) + OpKH::bytes(64) + 128 * 4);
+        tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTP::bytes(64), bar_b);
+        tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKH::bytes(64), bar_b);
+        tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_b);
+    };
+    auto wait_load = [&](uint64_t* bar, uint32_t& ph) {
+        if (!tc::mbar_wait(bar, ph)) {
             atomicOr(&g_tc_status, STATUS_TIMEOUT);
             *abort_flag = 1;
         }
-        ph_ld ^= 1;
+        ph ^= 1;
+    };
+    uint32_t ph_a = 0, ph_b = 0;
+    int pending = 0;  // groups in flight (thread 0's view), drained before exit
+    if (tid == 0 && start < end) {
+        load_a(g0, start);
+        load_b(g0);
+        pending = 2;
+    }
 
-        // ---------------------------------------------------------- P6 state scan
+    // O = Qtil S + P U of a chunk is written while the next chunk's first
+    // product runs: it is off the state's dependency chain.
+    float qs[16];
+    int o_c0 = -1, o_L = 0;  // the chunk whose O is still to be written
+    auto write_o = [&]() {
+        if (ln >= 64) {
+            float v[16];
+            tc::tmem_ld16(tmem + lane_base + TC_PU + 16 * ch, v);
+            tc::tmem_ld_wait();
+            const int r = ln - 64;
+            if (r < o_L) {
+                float* orow = o + ((size_t)(o_c0 + r) * heads + h) * D + slice * DV + 16 * ch;
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    *reinterpret_cast<float4*>(orow + 4 * q4) =
+                        make_float4(qs[4 * q4] + v[4 * q4], qs[4 * q4 + 1] + v[4 * q4 + 1],
+                                    qs[4 * q4 + 2] + v[4 * q4 + 2], qs[4 * q4 + 3] + v[4 * q4 + 3]);
+            }
+        }
+    };
+
+    long long g = g0;
+    for (int c0 = start; c0 < end; c0 += C, ++g) {
+        const int L = min(C, end - c0);
+        const bool more = c0 + C < end;
+        sync_for_mma();  // the previous chunk's state operand is written
+        if (*abort_flag) break;
+        wait_load(bar_a, ph_a);
+        if (tid == 0) --pending;
+
+        // ---------------------------------------------------------- X = V - Ktil S
         if (tid == 0) {
             tc::tc_fence_after();
             issue_mma<OpX, OpS>(tmem + TC_Y, s_opx, s_ops, 16, tc::idesc_tf32(128, DV));
             tc::mma_commit(bar_mma);
         }
+        if (o_c0 >= 0) write_o();  // the previous chunk's output
         wait_mma();
-        float qs[16];
         {
             float v[16];
             tc::tmem_ld16(tmem + lane_base + TC_Y + 16 * ch, v);
@@ -612,6 +708,15 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
             }
         }
         sync_for_mma();
+        if (tid == 0 && more) {  // [Ktil; Qtil] and the value tile are consumed
+            load_a(g + 1, c0 + C);
+            ++pending;
+        }
+        wait_load(bar_b, ph_b);
+        if (tid == 0) --pending;
+        const float dk = DEC[ln];
+
+        // ---------------------------------------------------------- U = T X
         if (tid == 0) {
             tc::tc_fence_after();
             issue_mma<OpTP, OpXV>(tmem + TC_U, s_tp, s_xv, 8, tc::idesc_tf32(128, DV));
@@ -630,6 +735,8 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
             }
         }
         sync_for_mma();
+
+        // ---------------------------------------------------------- Khat^T U and P U
         if (tid == 0) {
             tc::tc_fence_after();
             issue_mma<OpKH, OpXV>(tmem + TC_E, s_opkh, s_opy, 8, tc::idesc_tf32(128, DV));
@@ -637,31 +744,29 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
             tc::mma_commit(bar_mma);
         }
         wait_mma();
-        if (ln >= 64) {  // O = Qtil S + P U for the chunk's rows
-            float v[16];
-            tc::tmem_ld16(tmem + lane_base + TC_PU + 16 * ch, v);
-            tc::tmem_ld_wait();
-            const int r = ln - 64;
-            if (r < L) {
-                float* orow = o + ((size_t)(c0 + r) * heads + h) * D + slice * DV + 16 * ch;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<float4*>(orow + 4 * q4) =
-                        make_float4(qs[4 * q4] + v[4 * q4], qs[4 * q4 + 1] + v[4 * q4 + 1],
-                                    qs[4 * q4 + 2] + v[4 * q4 + 2], qs[4 * q4 + 3] + v[4 * q4 + 3]);
-            }
+        if (tid == 0 && more) {  // [T; P], Khat^T and dec are consumed
+            load_b(g + 1);
+            ++pending;
         }
-        {
+        {   // S <- dec (.) S + Khat^T U
             float v[16];
             tc::tmem_ld16(tmem + lane_base + TC_E + 16 * ch, v);
             tc::tmem_ld_wait();
-            const float dk = DEC[ln];
 #pragma unroll
             for (int jj = 0; jj < 16; ++jj) {
                 sreg[jj] = __fmaf_rn(dk, sreg[jj], v[jj]);
                 *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(16 * ch + jj, ln)) = tc::to_tf32(sreg[jj]);
             }
         }
+        o_c0 = c0;
+        o_L = L;
+    }
+    if (o_c0 >= 0 && !*abort_flag) write_o();  // the last chunk's output
+    // An early exit can leave copies in flight: let them land before the
+    // shared memory is released (bounded waits).
+    if (tid == 0 && pending > 0) {
+        tc::mbar_wait(bar_a, ph_a, 1u << 20);
+        tc::mbar_wait(bar_b, ph_b, 1u << 20);
     }
 
     if (!*abort_flag) {
