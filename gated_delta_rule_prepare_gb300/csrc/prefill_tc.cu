@@ -60,7 +60,8 @@ struct Op {
     static __host__ __device__ constexpr uint32_t bytes(int K) { return (uint32_t)(K / 4) * LBO; }
 };
 using OpX = Op<128, 0>;   // A: [X_b; QX_b] then [Ktil; Qtil], K = 128 channels
-using OpY = Op<16, 0>;    // B: Y_b, 16 rows, K = 128 channels
+using OpY = Op<16, 0>;    // B: Y_b of a 16-token block, K = 128 channels
+using OpY32 = Op<32, 0>;  // B: Y_b of a 32-token block, K = 128 channels
 using OpKH = Op<128, 0>;  // A: Khat^T, rows = key channel, K = 64 tokens
 using OpTP = Op<128, 0>;  // A: [T; P], K = 64 tokens
 using OpXV = Op<32, 16>;  // B: X^T and U^T, rows = value column, K = 64 tokens
@@ -99,12 +100,19 @@ constexpr uint32_t SM_OPKH = SM_STAGE_END;
 constexpr uint32_t SM_BETA = SM_OPKH + OpKH::bytes(64);
 constexpr uint32_t SM_GH = SM_BETA + 64 * 4;
 constexpr uint32_t SM_GMID = SM_GH + 128 * 4;
-constexpr uint32_t SM_GLAST = SM_GMID + 4 * 128 * 4;
+constexpr uint32_t SM_GLAST = SM_GMID + 6 * 128 * 4;  // GMID: 4 + 2 reference rows
 constexpr uint32_t SM_DEC = SM_GLAST + 128 * 4;
 constexpr uint32_t SM_BAR = SM_DEC + 128 * 4;        // 2 mbarriers + TMEM base + flag
 constexpr uint32_t SM_PREP_TOTAL = SM_BAR + 64;
 static_assert(SM_TP + OpTP::bytes(64) <= SM_STAGE_END, "solve arrays overlap");
 static_assert(4 * OpY::bytes(128) <= OpKH::bytes(64), "Y_b operands do not fit");
+static_assert(2 * OpY32::bytes(128) <= OpKH::bytes(64), "Y_b operands do not fit");
+
+// A chunk whose decays all satisfy g >= -kWideGMin takes 32-token column
+// blocks with reference token 32 b + 17: the A-side factor stays below
+// e^(17 |g|) < FLT_MAX, the B-side factor above e^(-17 |g|) (a normal
+// number), and a flushed A-side factor loses under 1.2e-38 e^(14 |g|) < 2e-7.
+constexpr float kWideGMin = 5.1f;
 static_assert(SM_PREP_TOTAL <= 232448, "shared memory budget exceeded");
 
 // ------------------------------------------------------------ scan smem
@@ -244,6 +252,7 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + SM_BAR);
     uint64_t* bar_mma = bar_tma + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 16);
+    int* wide_ok = reinterpret_cast<int*>(sm + SM_BAR + 20);
     const uint16_t* RAWQ = reinterpret_cast<const uint16_t*>(sm + SM_RAWQ);
     const uint16_t* RAWK = reinterpret_cast<const uint16_t*>(sm + SM_RAWK);
     const uint16_t* RAWG = reinterpret_cast<const uint16_t*>(sm + SM_RAWG);
@@ -256,6 +265,7 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
         tc::prefetch_tmap(&maps.q);
         tc::prefetch_tmap(&maps.k);
         tc::prefetch_tmap(&maps.g);
+        *wide_ok = 1;
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, 64);
     tc::tc_fence_before();
@@ -295,7 +305,7 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
         // ---------------------------------------------------------- P1 Gamma, staging
         {
             const int i = tid & 127, hf = tid >> 7;
-            float acc = 0.f;
+            float acc = 0.f, gmin = 0.f;
 #pragma unroll
             for (int rr = 0; rr < 32; ++rr) {
                 const int r = 32 * hf + rr;
@@ -305,12 +315,14 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                     kv = bf(RAWK[r * D + i]);
                     qv = __fmul_rn(KDA_Q_SCALE, bf(RAWQ[r * D + i]));
                 }
+                gmin = fminf(gmin, gv);
                 acc = __fadd_rn(acc, gv);
                 GAM[r * KP + i] = acc;
                 KF[r * KP + i] = kv;
                 QF[r * KP + i] = qv;
             }
             if (hf == 0) GH[i] = acc;
+            if (!(gmin >= -kWideGMin)) *wide_ok = 0;  // also catches NaN
         }
         __syncthreads();
         if (tid >= 128) {
@@ -323,52 +335,99 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
         if (tid < 128) {
 #pragma unroll
             for (int a = 0; a < 4; ++a) GMID[a * 128 + tid] = GAM[(16 * a + 8) * KP + tid];
+            GMID[4 * 128 + tid] = GAM[17 * KP + tid];
+            GMID[5 * 128 + tid] = GAM[49 * KP + tid];
             GLAST[tid] = GAM[63 * KP + tid];
             DEC[tid] = __expf(GAM[63 * KP + tid]);
         }
         __syncthreads();
 
         // ---------------------------------------------------------- P2 A and P blocks
-        // Y_b for all four blocks first: row s of block b = s / 16 is
-        // k_s e^(Gamma_mb - Gamma_s); they live in the Khat^T slot until P3.
-        for (int e = tid; e < 64 * 32; e += NT) {
-            const int s = e & 63, j = e >> 6, b = s >> 4;
-            const float4 gm = *reinterpret_cast<const float4*>(GMID + b * 128 + 4 * j);
-            const float4 ga = *reinterpret_cast<const float4*>(GAM + s * KP + 4 * j);
-            const float4 kf = *reinterpret_cast<const float4*>(KF + s * KP + 4 * j);
-            st4(sm + SM_OPKH + b * OpY::bytes(128), OpY::off(s & 15, 4 * j),
-                kf.x * __expf(gm.x - ga.x), kf.y * __expf(gm.y - ga.y),
-                kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
-        }
-        for (int b = 0; b < 4; ++b) {
-            {   // rows r >= 16 b: k_r and qh_r times e^(Gamma_r - Gamma_mb)
-                const int r = tid & 63, qg = tid >> 6;
-                if (r >= 16 * b) {
-                    const float* gmb = GMID + b * 128;
+        if (*wide_ok) {
+            // Two 32-token column blocks (every g of the chunk is >= -kWideGMin).
+            for (int e = tid; e < 64 * 32; e += NT) {
+                const int s = e & 63, j = e >> 6, b = s >> 5;
+                const float4 gm = *reinterpret_cast<const float4*>(GMID + (4 + b) * 128 + 4 * j);
+                const float4 ga = *reinterpret_cast<const float4*>(GAM + s * KP + 4 * j);
+                const float4 kf = *reinterpret_cast<const float4*>(KF + s * KP + 4 * j);
+                st4(sm + SM_OPKH + b * OpY32::bytes(128), OpY32::off(s & 31, 4 * j),
+                    kf.x * __expf(gm.x - ga.x), kf.y * __expf(gm.y - ga.y),
+                    kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
+            }
+            for (int b = 0; b < 2; ++b) {
+                {
+                    const int r = tid & 63, qg = tid >> 6;
+                    if (r >= 32 * b) {
+                        const float* gmb = GMID + (4 + b) * 128;
 #pragma unroll 4
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int j = qg + 4 * jj;
-                        const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
-                        const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
-                        const float4 kf = *reinterpret_cast<const float4*>(KF + r * KP + 4 * j);
-                        const float4 qf = *reinterpret_cast<const float4*>(QF + r * KP + 4 * j);
-                        const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
-                                    f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
-                        st4(sm + SM_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
-                            kf.w * f3);
-                        st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1,
-                            qf.z * f2, qf.w * f3);
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int j = qg + 4 * jj;
+                            const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
+                            const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
+                            const float4 kf = *reinterpret_cast<const float4*>(KF + r * KP + 4 * j);
+                            const float4 qf = *reinterpret_cast<const float4*>(QF + r * KP + 4 * j);
+                            const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
+                                        f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
+                            st4(sm + SM_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
+                                kf.w * f3);
+                            st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1,
+                                qf.z * f2, qf.w * f3);
+                        }
                     }
                 }
+                sync_for_mma();
+                if (tid == 0) {
+                    tc::tc_fence_after();
+                    issue_mma<OpX, OpY32>(tmem + TC_AP + 32 * b, s_opx,
+                                          s_opkh + b * OpY32::bytes(128), 16,
+                                          tc::idesc_tf32(128, 32));
+                    tc::mma_commit(bar_mma);
+                }
+                wait_mma();
             }
-            sync_for_mma();
-            if (tid == 0) {
-                tc::tc_fence_after();
-                issue_mma<OpX, OpY>(tmem + TC_AP + 16 * b, s_opx,
-                                    s_opkh + b * OpY::bytes(128), 16, tc::idesc_tf32(128, 16));
-                tc::mma_commit(bar_mma);
+        } else {
+            // Four 16-token column blocks with reference token 16 b + 8.
+            // Y_b for all four blocks first: row s of block b = s / 16 is
+            // k_s e^(Gamma_mb - Gamma_s); they live in the Khat^T slot until P3.
+            for (int e = tid; e < 64 * 32; e += NT) {
+                const int s = e & 63, j = e >> 6, b = s >> 4;
+                const float4 gm = *reinterpret_cast<const float4*>(GMID + b * 128 + 4 * j);
+                const float4 ga = *reinterpret_cast<const float4*>(GAM + s * KP + 4 * j);
+                const float4 kf = *reinterpret_cast<const float4*>(KF + s * KP + 4 * j);
+                st4(sm + SM_OPKH + b * OpY::bytes(128), OpY::off(s & 15, 4 * j),
+                    kf.x * __expf(gm.x - ga.x), kf.y * __expf(gm.y - ga.y),
+                    kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
             }
-            wait_mma();
+            for (int b = 0; b < 4; ++b) {
+                {   // rows r >= 16 b: k_r and qh_r times e^(Gamma_r - Gamma_mb)
+                    const int r = tid & 63, qg = tid >> 6;
+                    if (r >= 16 * b) {
+                        const float* gmb = GMID + b * 128;
+    #pragma unroll 4
+                        for (int jj = 0; jj < 8; ++jj) {
+                            const int j = qg + 4 * jj;
+                            const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
+                            const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
+                            const float4 kf = *reinterpret_cast<const float4*>(KF + r * KP + 4 * j);
+                            const float4 qf = *reinterpret_cast<const float4*>(QF + r * KP + 4 * j);
+                            const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
+                                        f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
+                            st4(sm + SM_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
+                                kf.w * f3);
+                            st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1,
+                                qf.z * f2, qf.w * f3);
+                        }
+                    }
+                }
+                sync_for_mma();
+                if (tid == 0) {
+                    tc::tc_fence_after();
+                    issue_mma<OpX, OpY>(tmem + TC_AP + 16 * b, s_opx,
+                                        s_opkh + b * OpY::bytes(128), 16, tc::idesc_tf32(128, 16));
+                    tc::mma_commit(bar_mma);
+                }
+                wait_mma();
+            }
         }
 
         // ---------------------------------------------------------- P3 Ktil/Qtil, Khat^T

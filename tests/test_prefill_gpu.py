@@ -202,3 +202,21 @@ def test_prefill_long_memory_and_strong_decay(orc, g_low):
     o_ref, S_ref = orc.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"][0])
     assert rel_err(o, o_ref) < TOL_PREFILL
     assert rel_err(S[0], S_ref) < TOL_PREFILL
+
+
+def test_prefill_mixes_wide_and_narrow_decay_blocks(orc):
+    """Chunks whose decays all stay above -5.1 take 32-token A/P blocks, the
+    others 16-token blocks; one sequence with both kinds of chunk (single
+    steep decays of -9 and -5.5 in two of its chunks) matches the oracle."""
+    K = kda()
+    gen = torch.Generator().manual_seed(41)
+    T, H = 320, 2
+    d = wl.core_inputs(gen, (T,), H, torch.bfloat16)
+    d["g"][70, 0, 5] = -9.0
+    d["g"][200, 1, 100] = -5.5
+    d["g"][260, 0, 7] = -5.1
+    d["state"] = wl.state(gen, (1,), H, 0.02)
+    o, S, _ = run_prefill(K, d, T, 64)
+    o_ref, S_ref = orc.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"][0])
+    assert rel_err(o, o_ref) < TOL_PREFILL
+    assert rel_err(S[0], S_ref) < TOL_PREFILL
