@@ -42,8 +42,9 @@ extern "C" kda_status kda_sync_status(uint64_t stream) {
     if (a | b) {
         kda::set_error("kda_sync_status: device-side check failed (prefill 0x%x, conv 0x%x): %s",
                        a, b,
-                       ((a | b) & kda::STATUS_TIMEOUT) ? "a bounded wait timed out"
-                                                       : "malformed cu_seqlens");
+                       ((a | b) & kda::STATUS_TIMEOUT)      ? "a bounded wait timed out"
+                       : ((a | b) & kda::STATUS_SMEM_ALIGN) ? "shared memory misaligned"
+                                                            : "malformed cu_seqlens");
         return KDA_ERR_DEVICE;
     }
     return KDA_OK;

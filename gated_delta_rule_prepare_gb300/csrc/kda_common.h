@@ -31,6 +31,7 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 enum : unsigned {
     STATUS_BAD_CU_SEQLENS = 1u << 0,
     STATUS_TIMEOUT = 1u << 1,  // a bounded wait on a copy or an MMA gave up
+    STATUS_SMEM_ALIGN = 1u << 2,  // dynamic shared memory not 1024-byte aligned
 };
 
 // Each checking unit exposes a reader that returns and clears its word on the

@@ -85,35 +85,39 @@ __host__ __device__ inline size_t blob_offset(int n_seqs, long long g, int h, in
 }
 
 // ------------------------------------------------------------ prepare smem
-constexpr uint32_t SM_OPX = 0;                       // 65536 (raw TMA tiles alias it)
-constexpr uint32_t SM_RAWQ = 0, SM_RAWK = 16384, SM_RAWG = 32768;
-constexpr uint32_t SM_KF = 65536;                    // FP32 k       [64][KP]
-constexpr uint32_t SM_QF = SM_KF + 64 * KP * 4;      // FP32 qh      [64][KP]
-constexpr uint32_t SM_GAM = SM_QF + 64 * KP * 4;     // FP32 Gamma   [64][KP]
-constexpr uint32_t SM_STAGE_END = SM_GAM + 64 * KP * 4;
-// reused after the prepare operands are built
-constexpr uint32_t SM_AM = SM_KF;                    // FP32 A, then W blocks [64][AP]
-constexpr uint32_t SM_TM = (SM_AM + 64 * AP * 4 + 15) & ~15u;  // FP32 T [64][TPP]
-constexpr uint32_t SM_TP = SM_TM + 64 * TPP * 4;
-// Khat^T; during the A/P products it holds the four Y_b operands instead
-constexpr uint32_t SM_OPKH = SM_STAGE_END;
-constexpr uint32_t SM_BETA = SM_OPKH + OpKH::bytes(64);
-constexpr uint32_t SM_GH = SM_BETA + 64 * 4;
-constexpr uint32_t SM_GMID = SM_GH + 128 * 4;
-constexpr uint32_t SM_GLAST = SM_GMID + 6 * 128 * 4;  // GMID: 4 + 2 reference rows
-constexpr uint32_t SM_DEC = SM_GLAST + 128 * 4;
-constexpr uint32_t SM_BAR = SM_DEC + 128 * 4;        // 2 mbarriers + TMEM base + flag
-constexpr uint32_t SM_PREP_TOTAL = SM_BAR + 64;
-static_assert(SM_TP + OpTP::bytes(64) <= SM_STAGE_END, "solve arrays overlap");
-static_assert(4 * OpY::bytes(128) <= OpKH::bytes(64), "Y_b operands do not fit");
-static_assert(2 * OpY32::bytes(128) <= OpKH::bytes(64), "Y_b operands do not fit");
+// prepare_kernel is persistent: each CTA walks (chunk, head) items with the
+// next item's raw tiles loading into the other of two buffers.  A raw buffer
+// holds the BF16 q, k and g tiles [64 tokens][128 channels], each as two TMA
+// boxes of 64 channels with the 128-byte swizzle (row r, 16-byte chunk c
+// stored at chunk c ^ (r & 7)).
+constexpr uint32_t RAW_TILE = 16384;
+constexpr uint32_t RAW_BUF = 3 * RAW_TILE;
+constexpr uint32_t RAW_Q = 0, RAW_K = RAW_TILE, RAW_G = 2 * RAW_TILE;
+// inside the current buffer, once Gamma is formed: reference rows and
+// Gamma_{L-1} at the end of the g tile; once the operands are out: the solve
+constexpr uint32_t RB_GMID = RAW_G + RAW_TILE - 7 * 128 * 4;  // 6 x 128: 4 + 2 reference rows
+constexpr uint32_t RB_GLAST = RB_GMID + 6 * 128 * 4;
+constexpr uint32_t RB_AM = 0;                                 // FP32 A, then W blocks [64][AP]
+constexpr uint32_t RB_TM = (RB_AM + 64 * AP * 4 + 15) & ~15u;  // FP32 T [64][TPP]
+constexpr uint32_t PS_GAM = 2 * RAW_BUF;                     // FP32 Gamma [64][KP]
+constexpr uint32_t PS_OPX = PS_GAM + 64 * KP * 4;            // A operand of the A/P products
+constexpr uint32_t PS_Y = PS_OPX + OpX::bytes(128);          // B operands Y_b
+constexpr uint32_t PS_BETA = PS_Y + 4 * OpY::bytes(128);
+constexpr uint32_t PS_GH = PS_BETA + 64 * 4;
+constexpr uint32_t PS_BAR = PS_GH + 128 * 4;  // bar_tma[2], bar_mma, TMEM base
+constexpr uint32_t PS_TOTAL = PS_BAR + 64;
+static_assert(RB_TM + 64 * TPP * 4 <= RB_GMID, "solve arrays overlap the reference rows");
+static_assert(RB_GLAST + 128 * 4 == RAW_G + RAW_TILE, "reference rows must end the g tile");
+static_assert(2 * OpY32::bytes(128) <= 4 * OpY::bytes(128), "Y_b operands do not fit");
+static_assert(OpKH::bytes(64) <= 4 * OpY::bytes(128), "Khat^T staging does not fit");
+static_assert(PS_OPX % 1024 == 0 && PS_Y % 16 == 0, "operand alignment");
 
 // A chunk whose decays all satisfy g >= -kWideGMin takes 32-token column
 // blocks with reference token 32 b + 17: the A-side factor stays below
 // e^(17 |g|) < FLT_MAX, the B-side factor above e^(-17 |g|) (a normal
 // number), and a flushed A-side factor loses under 1.2e-38 e^(14 |g|) < 2e-7.
 constexpr float kWideGMin = 5.1f;
-static_assert(SM_PREP_TOTAL <= 232448, "shared memory budget exceeded");
+static_assert(PS_TOTAL <= 232448, "shared memory budget exceeded");
 
 // ------------------------------------------------------------ scan smem
 constexpr uint32_t SS_BLOB = 0;                      // blob image: OPX | TP | KH | DEC
@@ -206,73 +210,93 @@ chunk_map_kernel(const int* __restrict__ cu, int n_seqs, int t, int* __restrict_
     if (threadIdx.x == MAP_THREADS - 1) chunk_off[n_seqs] = part[MAP_THREADS - 1];
 }
 
+// Byte offset of channel c of row r inside a raw tile (see above).
+__device__ __forceinline__ uint32_t raw_off(int r, int c) {
+    return (uint32_t)((c >> 6) * 8192 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+__device__ __forceinline__ float raw1(const unsigned char* tile, int r, int c) {
+    return bf(*reinterpret_cast<const uint16_t*>(tile + raw_off(r, c)));
+}
+// Channels c .. c + 3 (c a multiple of 4) of row r.
+__device__ __forceinline__ float4 raw4(const unsigned char* tile, int r, int c) {
+    const uint2 u = *reinterpret_cast<const uint2*>(tile + raw_off(r, c));
+    return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                       __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+}
+
+// Four values rounded to TF32, stored as one 16-byte global write.
+__device__ __forceinline__ void stg4(unsigned char* p, float a, float b, float c, float d) {
+    *reinterpret_cast<float4*>(p) =
+        make_float4(tc::to_tf32(a), tc::to_tf32(b), tc::to_tf32(c), tc::to_tf32(d));
+}
+
+// A (chunk, head) item of the prepare walk: item = g * heads + h.
+struct PrepItem {
+    long long g;
+    int h, c0, L;
+    bool valid;
+};
+
+__device__ __forceinline__ PrepItem prep_item(long long item, int heads, const int* __restrict__ cu,
+                                              const int* __restrict__ chunk_off, int n_seqs, int t,
+                                              int t_pad) {
+    PrepItem it;
+    it.g = item / heads;
+    it.h = (int)(item - it.g * heads);
+    int lo = 0, hi = n_seqs - 1;  // the sequence holding chunk g: largest n with chunk_off[n] <= g
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (__ldg(chunk_off + mid) <= it.g) lo = mid;
+        else hi = mid - 1;
+    }
+    int start, end;
+    it.valid = seq_range(cu, lo, n_seqs, t, t_pad, start, end);
+    it.c0 = start + (int)(it.g - __ldg(chunk_off + lo)) * C;
+    it.valid = it.valid && it.c0 < end;
+    it.L = it.valid ? min(C, end - it.c0) : 0;
+    return it;
+}
+
 __global__ void __launch_bounds__(NT, 1)
 prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict__ beta, int t,
                int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
                unsigned char* __restrict__ ws) {
     extern __shared__ __align__(1024) unsigned char sm[];
-    const int h = blockIdx.y;
-    const long long g = blockIdx.x;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column half
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     const int* chunk_off = reinterpret_cast<const int*>(ws);
-    const int total = __ldg(chunk_off + n_seqs);
-    if (g >= total) return;
-    int n = 0;
-    {   // the sequence holding chunk g: largest n with chunk_off[n] <= g
-        int lo = 0, hi = n_seqs - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (__ldg(chunk_off + mid) <= g) lo = mid;
-            else hi = mid - 1;
-        }
-        n = lo;
-    }
-    int start, end;
-    if (!seq_range(cu, n, n_seqs, t, t_pad, start, end)) {
-        if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
+    const long long items = (long long)__ldg(chunk_off + n_seqs) * heads;
+    if ((long long)blockIdx.x >= items) return;
+    if (tc::smem_u32(sm) & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
+        if (tid == 0) atomicOr(&g_tc_status, STATUS_SMEM_ALIGN);
         return;
     }
-    const int c0 = start + (int)(g - __ldg(chunk_off + n)) * C;
-    if (c0 >= end) return;
-    const int L = min(C, end - c0);
 
-    float* KF = reinterpret_cast<float*>(sm + SM_KF);
-    float* QF = reinterpret_cast<float*>(sm + SM_QF);
-    float* GAM = reinterpret_cast<float*>(sm + SM_GAM);
-    float* AM = reinterpret_cast<float*>(sm + SM_AM);
-    float* TM = reinterpret_cast<float*>(sm + SM_TM);
-    float* BETA = reinterpret_cast<float*>(sm + SM_BETA);
-    float* GH = reinterpret_cast<float*>(sm + SM_GH);
-    float* GMID = reinterpret_cast<float*>(sm + SM_GMID);
-    float* GLAST = reinterpret_cast<float*>(sm + SM_GLAST);
-    float* DEC = reinterpret_cast<float*>(sm + SM_DEC);
-    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + SM_BAR);
-    uint64_t* bar_mma = bar_tma + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SM_BAR + 16);
-    int* wide_ok = reinterpret_cast<int*>(sm + SM_BAR + 20);
-    const uint16_t* RAWQ = reinterpret_cast<const uint16_t*>(sm + SM_RAWQ);
-    const uint16_t* RAWK = reinterpret_cast<const uint16_t*>(sm + SM_RAWK);
-    const uint16_t* RAWG = reinterpret_cast<const uint16_t*>(sm + SM_RAWG);
-    const uint32_t s_opx = tc::smem_u32(sm + SM_OPX), s_opkh = tc::smem_u32(sm + SM_OPKH);
+    float* GAM = reinterpret_cast<float*>(sm + PS_GAM);
+    float* BETA = reinterpret_cast<float*>(sm + PS_BETA);
+    float* GH = reinterpret_cast<float*>(sm + PS_GH);
+    uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + PS_BAR);  // one per raw buffer
+    uint64_t* bar_mma = bar_tma + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PS_BAR + 24);
+    const uint32_t s_opx = tc::smem_u32(sm + PS_OPX), s_y = tc::smem_u32(sm + PS_Y);
 
     if (tid == 0) {
         tc::mbar_init(bar_tma, 1);
+        tc::mbar_init(bar_tma + 1, 1);
         tc::mbar_init(bar_mma, 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&maps.q);
         tc::prefetch_tmap(&maps.k);
         tc::prefetch_tmap(&maps.g);
-        *wide_ok = 1;
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, 64);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t ph_mma = 0;
+    uint32_t ph_mma = 0, ph_tma[2] = {0, 0};
     bool failed = false;
 
     auto wait_mma = [&]() {
@@ -288,319 +312,348 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
         tc::tc_fence_before();
         __syncthreads();
     };
-
-    // ---------------------------------------------------------- P0 loads
-    if (tid == 0) {
-        tc::mbar_arrive_expect_tx(bar_tma, 3 * 16384);
-        tc::tma_load_2d(sm + SM_RAWQ, &maps.q, bar_tma, h * D, c0);
-        tc::tma_load_2d(sm + SM_RAWK, &maps.k, bar_tma, h * D, c0);
-        tc::tma_load_2d(sm + SM_RAWG, &maps.g, bar_tma, h * D, c0);
-    }
-    if (tid < C) BETA[tid] = (tid < L) ? bf(__ldg(beta + (size_t)(c0 + tid) * heads + h)) : 0.f;
-    if (!tc::mbar_wait(bar_tma, 0)) {
-        atomicOr(&g_tc_status, STATUS_TIMEOUT);
-        failed = true;
-    }
-
-        // ---------------------------------------------------------- P1 Gamma, staging
-        {
-            const int i = tid & 127, hf = tid >> 7;
-            float acc = 0.f, gmin = 0.f;
+    // Raw tiles of item `it` into buffer b (thread 0), and its beta (threads
+    // 0..63, returned in a register).
+    auto load_raw = [&](const PrepItem& it, int b) {
+        if (tid == 0 && it.valid) {
+            unsigned char* dst = sm + b * RAW_BUF;
+            tc::fence_async_smem();  // the buffer's previous generic-proxy contents are dead
+            tc::mbar_arrive_expect_tx(bar_tma + b, RAW_BUF);
+            const CUtensorMap* mp[3] = {&maps.q, &maps.k, &maps.g};
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr) {
-                const int r = 32 * hf + rr;
-                float gv = 0.f, kv = 0.f, qv = 0.f;
-                if (r < L) {
-                    gv = bf(RAWG[r * D + i]);
-                    kv = bf(RAWK[r * D + i]);
-                    qv = __fmul_rn(KDA_Q_SCALE, bf(RAWQ[r * D + i]));
-                }
-                gmin = fminf(gmin, gv);
-                acc = __fadd_rn(acc, gv);
-                GAM[r * KP + i] = acc;
-                KF[r * KP + i] = kv;
-                QF[r * KP + i] = qv;
-            }
-            if (hf == 0) GH[i] = acc;
-            if (!(gmin >= -kWideGMin)) *wide_ok = 0;  // also catches NaN
-        }
-        __syncthreads();
-        if (tid >= 128) {
-            const int i = tid & 127;
-            const float base = GH[i];
+            for (int a = 0; a < 3; ++a)
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr) GAM[(32 + rr) * KP + i] += base;
+                for (int half = 0; half < 2; ++half)
+                    tc::tma_load_2d(dst + a * RAW_TILE + half * (RAW_TILE / 2), mp[a], bar_tma + b,
+                                    it.h * D + 64 * half, it.c0);
         }
-        __syncthreads();
-        if (tid < 128) {
-#pragma unroll
-            for (int a = 0; a < 4; ++a) GMID[a * 128 + tid] = GAM[(16 * a + 8) * KP + tid];
-            GMID[4 * 128 + tid] = GAM[17 * KP + tid];
-            GMID[5 * 128 + tid] = GAM[49 * KP + tid];
-            GLAST[tid] = GAM[63 * KP + tid];
-            DEC[tid] = __expf(GAM[63 * KP + tid]);
-        }
-        __syncthreads();
+    };
+    auto load_beta = [&](const PrepItem& it) {
+        return (tid < C && it.valid && tid < it.L)
+                   ? bf(__ldg(beta + (size_t)(it.c0 + tid) * heads + it.h))
+                   : 0.f;
+    };
 
-        // ---------------------------------------------------------- P2 A and P blocks
-        if (*wide_ok) {
-            // Two 32-token column blocks (every g of the chunk is >= -kWideGMin).
-            for (int e = tid; e < 64 * 32; e += NT) {
-                const int s = e & 63, j = e >> 6, b = s >> 5;
-                const float4 gm = *reinterpret_cast<const float4*>(GMID + (4 + b) * 128 + 4 * j);
-                const float4 ga = *reinterpret_cast<const float4*>(GAM + s * KP + 4 * j);
-                const float4 kf = *reinterpret_cast<const float4*>(KF + s * KP + 4 * j);
-                st4(sm + SM_OPKH + b * OpY32::bytes(128), OpY32::off(s & 31, 4 * j),
-                    kf.x * __expf(gm.x - ga.x), kf.y * __expf(gm.y - ga.y),
-                    kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
-            }
-            for (int b = 0; b < 2; ++b) {
-                {
-                    const int r = tid & 63, qg = tid >> 6;
-                    if (r >= 32 * b) {
-                        const float* gmb = GMID + (4 + b) * 128;
-#pragma unroll 4
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const int j = qg + 4 * jj;
-                            const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
-                            const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
-                            const float4 kf = *reinterpret_cast<const float4*>(KF + r * KP + 4 * j);
-                            const float4 qf = *reinterpret_cast<const float4*>(QF + r * KP + 4 * j);
-                            const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
-                                        f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
-                            st4(sm + SM_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
-                                kf.w * f3);
-                            st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1,
-                                qf.z * f2, qf.w * f3);
-                        }
-                    }
-                }
-                sync_for_mma();
-                if (tid == 0) {
-                    tc::tc_fence_after();
-                    issue_mma<OpX, OpY32>(tmem + TC_AP + 32 * b, s_opx,
-                                          s_opkh + b * OpY32::bytes(128), 16,
-                                          tc::idesc_tf32(128, 32));
-                    tc::mma_commit(bar_mma);
-                }
-                wait_mma();
-            }
+    long long item = blockIdx.x;
+    PrepItem cur = prep_item(item, heads, cu, chunk_off, n_seqs, t, t_pad);
+    load_raw(cur, 0);
+    float beta_cur = load_beta(cur);
+
+    for (int iter = 0; item < items; ++iter) {
+        const int b = iter & 1;
+        const long long nitem = item + gridDim.x;
+        PrepItem nxt = {};
+        nxt.valid = false;
+        float beta_nxt = 0.f;
+        // The next item is resolved (global loads) while the first A/P product
+        // runs, and its raw tiles go to the other buffer, which the previous
+        // iteration's closing barrier released.
+        auto fetch_next = [&]() {
+            if (nitem < items) nxt = prep_item(nitem, heads, cu, chunk_off, n_seqs, t, t_pad);
+            load_raw(nxt, b ^ 1);
+            beta_nxt = load_beta(nxt);
+        };
+
+        if (!cur.valid) {
+            if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
+            fetch_next();
         } else {
-            // Four 16-token column blocks with reference token 16 b + 8.
-            // Y_b for all four blocks first: row s of block b = s / 16 is
-            // k_s e^(Gamma_mb - Gamma_s); they live in the Khat^T slot until P3.
-            for (int e = tid; e < 64 * 32; e += NT) {
-                const int s = e & 63, j = e >> 6, b = s >> 4;
-                const float4 gm = *reinterpret_cast<const float4*>(GMID + b * 128 + 4 * j);
-                const float4 ga = *reinterpret_cast<const float4*>(GAM + s * KP + 4 * j);
-                const float4 kf = *reinterpret_cast<const float4*>(KF + s * KP + 4 * j);
-                st4(sm + SM_OPKH + b * OpY::bytes(128), OpY::off(s & 15, 4 * j),
-                    kf.x * __expf(gm.x - ga.x), kf.y * __expf(gm.y - ga.y),
-                    kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
+            const int L = cur.L, h = cur.h;
+            const unsigned char* RAWQ = sm + b * RAW_BUF + RAW_Q;
+            const unsigned char* RAWK = sm + b * RAW_BUF + RAW_K;
+            const unsigned char* RAWG = sm + b * RAW_BUF + RAW_G;
+            float* GMID = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_GMID);
+            float* GLAST = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_GLAST);
+            float* AM = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_AM);
+            float* TM = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_TM);
+            unsigned char* blob = ws + blob_offset(n_seqs, cur.g, h, heads);
+
+            if (tid < C) BETA[tid] = beta_cur;
+            if (!tc::mbar_wait(bar_tma + b, ph_tma[b])) {
+                atomicOr(&g_tc_status, STATUS_TIMEOUT);
+                failed = true;
             }
-            for (int b = 0; b < 4; ++b) {
-                {   // rows r >= 16 b: k_r and qh_r times e^(Gamma_r - Gamma_mb)
-                    const int r = tid & 63, qg = tid >> 6;
-                    if (r >= 16 * b) {
-                        const float* gmb = GMID + b * 128;
-    #pragma unroll 4
-                        for (int jj = 0; jj < 8; ++jj) {
-                            const int j = qg + 4 * jj;
-                            const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
-                            const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
-                            const float4 kf = *reinterpret_cast<const float4*>(KF + r * KP + 4 * j);
-                            const float4 qf = *reinterpret_cast<const float4*>(QF + r * KP + 4 * j);
-                            const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
-                                        f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
-                            st4(sm + SM_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
-                                kf.w * f3);
-                            st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1,
-                                qf.z * f2, qf.w * f3);
-                        }
+            ph_tma[b] ^= 1;
+
+            // ------------------------------------------------------ P1 Gamma
+            bool wide;
+            {
+                const int i = tid & 127, hf = tid >> 7;
+                float acc = 0.f, gmin = 0.f;
+#pragma unroll 8
+                for (int rr = 0; rr < 32; ++rr) {
+                    const int r = 32 * hf + rr;
+                    const float gv = (r < L) ? raw1(RAWG, r, i) : 0.f;
+                    gmin = fminf(gmin, gv);
+                    acc = __fadd_rn(acc, gv);
+                    GAM[r * KP + i] = acc;
+                }
+                if (hf == 0) GH[i] = acc;
+                wide = __syncthreads_and(gmin >= -kWideGMin);  // false on NaN too
+            }
+            if (tid >= 128) {
+                const int i = tid & 127;
+                const float base = GH[i];
+#pragma unroll 8
+                for (int rr = 0; rr < 32; ++rr) GAM[(32 + rr) * KP + i] += base;
+            }
+            if (tid == 0) tc::bulk_wait_read_all();  // the last item's operands left OPX and Y
+            __syncthreads();  // the g tile is dead from here on
+            if (tid < 128) {
+#pragma unroll
+                for (int a = 0; a < 4; ++a) GMID[a * 128 + tid] = GAM[(16 * a + 8) * KP + tid];
+                GMID[4 * 128 + tid] = GAM[17 * KP + tid];
+                GMID[5 * 128 + tid] = GAM[49 * KP + tid];
+                const float gl = GAM[63 * KP + tid];
+                GLAST[tid] = gl;
+                if (!failed) reinterpret_cast<float*>(blob + BLOB_DEC)[tid] = __expf(gl);
+            }
+            __syncthreads();
+
+            // ------------------------------------------------------ P2 A and P blocks
+            // X_b rows r >= r0: k_r and qh_r times e^(Gamma_r - Gamma_mb).
+            auto build_x = [&](int r0, const float* gmb) {
+                const int r = tid & 63, qg = tid >> 6;
+                if (r >= r0) {
+                    const bool live = r < L;
+#pragma unroll 4
+                    for (int jj = 0; jj < 8; ++jj) {
+                        const int j = qg + 4 * jj;
+                        const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
+                        const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
+                        float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
+                        if (!live) kf = qf = make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
+                                    f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
+                        st4(sm + PS_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
+                            kf.w * f3);
+                        st4(sm + PS_OPX, OpX::off(64 + r, 4 * j), KDA_Q_SCALE * qf.x * f0,
+                            KDA_Q_SCALE * qf.y * f1, KDA_Q_SCALE * qf.z * f2,
+                            KDA_Q_SCALE * qf.w * f3);
                     }
                 }
-                sync_for_mma();
-                if (tid == 0) {
-                    tc::tc_fence_after();
-                    issue_mma<OpX, OpY>(tmem + TC_AP + 16 * b, s_opx,
-                                        s_opkh + b * OpY::bytes(128), 16, tc::idesc_tf32(128, 16));
-                    tc::mma_commit(bar_mma);
+            };
+            // Y_b row s of block b = s >> bshift: k_s e^(Gamma_mb - Gamma_s).
+            auto build_y = [&](int bshift, int gm_row0, uint32_t ybytes, auto op) {
+                for (int e = tid; e < 64 * 32; e += NT) {
+                    const int s = e & 63, j = e >> 6, bb = s >> bshift;
+                    const float4 gm =
+                        *reinterpret_cast<const float4*>(GMID + (gm_row0 + bb) * 128 + 4 * j);
+                    const float4 ga = *reinterpret_cast<const float4*>(GAM + s * KP + 4 * j);
+                    float4 kf = raw4(RAWK, s, 4 * j);
+                    if (s >= L) kf = make_float4(0.f, 0.f, 0.f, 0.f);
+                    st4(sm + PS_Y + bb * ybytes, decltype(op)::off(s & ((1 << bshift) - 1), 4 * j),
+                        kf.x * __expf(gm.x - ga.x), kf.y * __expf(gm.y - ga.y),
+                        kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
                 }
-                wait_mma();
-            }
-        }
-
-        // ---------------------------------------------------------- P3 Ktil/Qtil, Khat^T
-        {
-            const int r = tid & 63, qg = tid >> 6;
-#pragma unroll 4
-            for (int jj = 0; jj < 8; ++jj) {
-                const int j = qg + 4 * jj;
-                const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
-                const float4 kf = *reinterpret_cast<const float4*>(KF + r * KP + 4 * j);
-                const float4 qf = *reinterpret_cast<const float4*>(QF + r * KP + 4 * j);
-                const float f0 = __expf(ga.x), f1 = __expf(ga.y), f2 = __expf(ga.z),
-                            f3 = __expf(ga.w);
-                st4(sm + SM_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2, kf.w * f3);
-                st4(sm + SM_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1, qf.z * f2,
-                    qf.w * f3);
-            }
-            const int i = tid & 127, hq = tid >> 7;
-            const float gl = GLAST[i];
-            for (int qq = 0; qq < 8; ++qq) {
-                const int q4 = 2 * qq + hq;  // token quad
-                float kh[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int s = 4 * q4 + e;
-                    kh[e] = BETA[s] * KF[s * KP + i] * __expf(gl - GAM[s * KP + i]);
-                }
-                st4(sm + SM_OPKH, OpKH::off(i, 4 * q4), kh[0], kh[1], kh[2], kh[3]);
-            }
-        }
-        tc::fence_async_smem();
-        __syncthreads();  // staging arrays are dead from here on
-        unsigned char* blob = ws + blob_offset(n_seqs, g, h, heads);
-        if (tid == 0 && !failed) {  // these three parts of the blob are final
-            tc::bulk_store(blob + BLOB_OPX, sm + SM_OPX, OpX::bytes(128));
-            tc::bulk_store(blob + BLOB_KH, sm + SM_OPKH, OpKH::bytes(64));
-            tc::bulk_store(blob + BLOB_DEC, sm + SM_DEC, 128 * 4);
-            tc::bulk_commit();
-        }
-
-        // ---------------------------------------------------------- P4 read A, P
-        {
-            float v[32];
-            tc::tmem_ld16(tmem + lane_base + TC_AP + 32 * ch, *reinterpret_cast<float(*)[16]>(v));
-            tc::tmem_ld16(tmem + lane_base + TC_AP + 32 * ch + 16,
-                          *reinterpret_cast<float(*)[16]>(v + 16));
-            tc::tmem_ld_wait();
-            if (ln < 64) {
-                const int r = ln;
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    const int s = 32 * ch + c;
-                    AM[r * AP + s] = (s < r) ? v[c] * BETA[s] : 0.f;
+            };
+            if (wide) {
+                // Two 32-token column blocks (every g of the chunk is >= -kWideGMin).
+                build_y(5, 4, OpY32::bytes(128), OpY32{});
+                for (int bb = 0; bb < 2; ++bb) {
+                    build_x(32 * bb, GMID + (4 + bb) * 128);
+                    sync_for_mma();
+                    if (tid == 0) {
+                        tc::tc_fence_after();
+                        issue_mma<OpX, OpY32>(tmem + TC_AP + 32 * bb, s_opx,
+                                              s_y + bb * OpY32::bytes(128), 16,
+                                              tc::idesc_tf32(128, 32));
+                        tc::mma_commit(bar_mma);
+                    }
+                    if (bb == 0) fetch_next();
+                    wait_mma();
                 }
             } else {
-                const int r = ln - 64;
-#pragma unroll
-                for (int c4 = 0; c4 < 8; ++c4) {
-                    float p[4];
+                // Four 16-token column blocks with reference token 16 b + 8.
+                build_y(4, 0, OpY::bytes(128), OpY{});
+                for (int bb = 0; bb < 4; ++bb) {
+                    build_x(16 * bb, GMID + bb * 128);
+                    sync_for_mma();
+                    if (tid == 0) {
+                        tc::tc_fence_after();
+                        issue_mma<OpX, OpY>(tmem + TC_AP + 16 * bb, s_opx,
+                                            s_y + bb * OpY::bytes(128), 16,
+                                            tc::idesc_tf32(128, 16));
+                        tc::mma_commit(bar_mma);
+                    }
+                    if (bb == 0) fetch_next();
+                    wait_mma();
+                }
+            }
+
+            // ------------------------------------------------------ P3 [Ktil; Qtil], Khat^T
+            // Built in the A/P operand buffers (both products are complete) and
+            // sent to the workspace by bulk copies that drain during P4 and P5.
+            {
+                const int r = tid & 63, qg = tid >> 6;
+                const bool live = r < L;
+#pragma unroll 4
+                for (int jj = 0; jj < 8; ++jj) {
+                    const int j = qg + 4 * jj;
+                    const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
+                    float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
+                    if (!live) kf = qf = make_float4(0.f, 0.f, 0.f, 0.f);
+                    const float f0 = __expf(ga.x), f1 = __expf(ga.y), f2 = __expf(ga.z),
+                                f3 = __expf(ga.w);
+                    st4(sm + PS_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
+                        kf.w * f3);
+                    st4(sm + PS_OPX, OpX::off(64 + r, 4 * j), KDA_Q_SCALE * qf.x * f0,
+                        KDA_Q_SCALE * qf.y * f1, KDA_Q_SCALE * qf.z * f2, KDA_Q_SCALE * qf.w * f3);
+                }
+                const int i = tid & 127, hq = tid >> 7;
+                const float gl = GLAST[i];
+#pragma unroll 2
+                for (int qq = 0; qq < 8; ++qq) {
+                    const int q4 = 2 * qq + hq;  // token quad
+                    float kh[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int s = 32 * ch + 4 * c4 + e;
-                        p[e] = (s <= r) ? v[4 * c4 + e] * BETA[s] : 0.f;
+                        const int s = 4 * q4 + e;
+                        kh[e] = (s < L) ? BETA[s] * raw1(RAWK, s, i) * __expf(gl - GAM[s * KP + i])
+                                        : 0.f;
                     }
-                    st4(sm + SM_TP, OpTP::off(64 + r, 32 * ch + 4 * c4), p[0], p[1], p[2], p[3]);
+                    st4(sm + PS_Y, OpKH::off(i, 4 * q4), kh[0], kh[1], kh[2], kh[3]);
                 }
             }
-        }
-        for (int e = tid; e < 64 * 64; e += NT) TM[(e >> 6) * TPP + (e & 63)] = 0.f;
-        tc::tc_fence_before();
-        __syncthreads();
-
-        // ---------------------------------------------------------- P5 T = (I + A)^-1
-        if (tid < 64) {  // diagonal 16 x 16 blocks T_aa = (I + A_aa)^-1, one column per thread
-            const int a = tid >> 4, cc = tid & 15, o0 = 16 * a;
-            float col[16];
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) {
-                float x = (rr == cc) ? 1.f : 0.f;
-#pragma unroll
-                for (int ss = 0; ss < rr; ++ss)
-                    x = __fmaf_rn(-AM[(o0 + rr) * AP + o0 + ss], col[ss], x);
-                col[rr] = (rr < cc) ? 0.f : x;
-            }
-#pragma unroll
-            for (int rr = 0; rr < 16; ++rr) TM[(o0 + rr) * TPP + o0 + cc] = col[rr];
-        }
-        __syncthreads();
-        // Below the diagonal, with W_ac = T_aa A_ac:  T_ab = -sum_{c=b}^{a-1} W_ac T_cb.
-        // Work in 1 x 4 tiles (one row, four consecutive columns) per thread.
-        {
-            float4 w[2];
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int e = tid + NT * m;
-                w[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (e < 6 * 64) {
-                    const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
-                    const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
-                    const int c = (pb == 0) ? 0 : (pb < 3) ? pb - 1 : pb - 3;
-                    const float* arow = AM + 16 * c + 4 * cq;
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const float t = TM[(16 * a + rr) * TPP + 16 * a + kk];
-                        const float* ak = arow + (16 * a + kk) * AP;
-                        w[m].x = __fmaf_rn(t, ak[0], w[m].x);
-                        w[m].y = __fmaf_rn(t, ak[1], w[m].y);
-                        w[m].z = __fmaf_rn(t, ak[2], w[m].z);
-                        w[m].w = __fmaf_rn(t, ak[3], w[m].w);
-                    }
-                }
-            }
-            __syncthreads();
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-                const int e = tid + NT * m;
-                if (e < 6 * 64) {
-                    const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
-                    const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
-                    const int c = (pb == 0) ? 0 : (pb < 3) ? pb - 1 : pb - 3;
-                    float* dst = AM + (16 * a + rr) * AP + 16 * c + 4 * cq;
-                    dst[0] = w[m].x;
-                    dst[1] = w[m].y;
-                    dst[2] = w[m].z;
-                    dst[3] = w[m].w;
-                }
-            }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int d = 1; d < 4; ++d) {
-            if (tid < (4 - d) * 64) {
-                const int b = tid >> 6, a = b + d, rr = (tid >> 2) & 15, cq = tid & 3;
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int cd = 0; cd < d; ++cd) {
-                    const int c = b + cd;
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const float wv = AM[(16 * a + rr) * AP + 16 * c + kk];
-                        const float4 t4 =
-                            *reinterpret_cast<const float4*>(TM + (16 * c + kk) * TPP + 16 * b + 4 * cq);
-                        x.x = __fmaf_rn(wv, t4.x, x.x);
-                        x.y = __fmaf_rn(wv, t4.y, x.y);
-                        x.z = __fmaf_rn(wv, t4.z, x.z);
-                        x.w = __fmaf_rn(wv, t4.w, x.w);
-                    }
-                }
-                *reinterpret_cast<float4*>(TM + (16 * a + rr) * TPP + 16 * b + 4 * cq) =
-                    make_float4(-x.x, -x.y, -x.z, -x.w);
-            }
-            __syncthreads();
-        }
-        {   // T into rows 0..63 of [T; P]
-            const int r = tid & 63, qg = tid >> 6;
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const int j = qg + 4 * jj;
-                const float4 tr = *reinterpret_cast<const float4*>(TM + r * TPP + 4 * j);
-                st4(sm + SM_TP, OpTP::off(r, 4 * j), tr.x, tr.y, tr.z, tr.w);
-            }
-        }
-
-        // ---------------------------------------------------------- write the blob
-        tc::fence_async_smem();
-        __syncthreads();
-        if (tid == 0) {
-            if (!failed) {
-                tc::bulk_store(blob + BLOB_TP, sm + SM_TP, OpTP::bytes(64));
+            tc::fence_async_smem();
+            __syncthreads();  // the raw tiles and reference rows are dead from here on
+            if (tid == 0 && !failed) {
+                tc::bulk_store(blob + BLOB_OPX, sm + PS_OPX, OpX::bytes(128));
+                tc::bulk_store(blob + BLOB_KH, sm + PS_Y, OpKH::bytes(64));
                 tc::bulk_commit();
             }
-            tc::bulk_wait_read_all();  // shared memory stays valid until read
+
+            // ------------------------------------------------------ P4 read A, P
+            {
+                float v[32];
+                tc::tmem_ld16(tmem + lane_base + TC_AP + 32 * ch, *reinterpret_cast<float(*)[16]>(v));
+                tc::tmem_ld16(tmem + lane_base + TC_AP + 32 * ch + 16,
+                              *reinterpret_cast<float(*)[16]>(v + 16));
+                tc::tmem_ld_wait();
+                if (ln < 64) {
+                    const int r = ln;
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        const int s = 32 * ch + c;
+                        AM[r * AP + s] = (s < r) ? v[c] * BETA[s] : 0.f;
+                    }
+                } else if (!failed) {
+                    const int r = ln - 64;
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        float p[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int s = 32 * ch + 4 * c4 + e;
+                            p[e] = (s <= r) ? v[4 * c4 + e] * BETA[s] : 0.f;
+                        }
+                        stg4(blob + BLOB_TP + OpTP::off(64 + r, 32 * ch + 4 * c4), p[0], p[1], p[2],
+                             p[3]);
+                    }
+                }
+            }
+            for (int e = tid; e < 64 * 64; e += NT) TM[(e >> 6) * TPP + (e & 63)] = 0.f;
+            tc::tc_fence_before();
+            __syncthreads();
+
+            // ------------------------------------------------------ P5 T = (I + A)^-1
+            if (tid < 64) {  // diagonal 16 x 16 blocks T_aa = (I + A_aa)^-1, one column per thread
+                const int a = tid >> 4, cc = tid & 15, o0 = 16 * a;
+                float col[16];
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
+                    float x = (rr == cc) ? 1.f : 0.f;
+#pragma unroll
+                    for (int ss = 0; ss < rr; ++ss)
+                        x = __fmaf_rn(-AM[(o0 + rr) * AP + o0 + ss], col[ss], x);
+                    col[rr] = (rr < cc) ? 0.f : x;
+                }
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) TM[(o0 + rr) * TPP + o0 + cc] = col[rr];
+            }
+            __syncthreads();
+            // Below the diagonal, with W_ac = T_aa A_ac:  T_ab = -sum_{c=b}^{a-1} W_ac T_cb.
+            // Work in 1 x 4 tiles (one row, four consecutive columns) per thread.
+            {
+                float4 w[2];
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int e = tid + NT * m;
+                    w[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (e < 6 * 64) {
+                        const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
+                        const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
+                        const int c = (pb == 0) ? 0 : (pb < 3) ? pb - 1 : pb - 3;
+                        const float* arow = AM + 16 * c + 4 * cq;
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk) {
+                            const float tv = TM[(16 * a + rr) * TPP + 16 * a + kk];
+                            const float* ak = arow + (16 * a + kk) * AP;
+                            w[m].x = __fmaf_rn(tv, ak[0], w[m].x);
+                            w[m].y = __fmaf_rn(tv, ak[1], w[m].y);
+                            w[m].z = __fmaf_rn(tv, ak[2], w[m].z);
+                            w[m].w = __fmaf_rn(tv, ak[3], w[m].w);
+                        }
+                    }
+                }
+                __syncthreads();
+#pragma unroll
+                for (int m = 0; m < 2; ++m) {
+                    const int e = tid + NT * m;
+                    if (e < 6 * 64) {
+                        const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
+                        const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
+                        const int c = (pb == 0) ? 0 : (pb < 3) ? pb - 1 : pb - 3;
+                        float* dst = AM + (16 * a + rr) * AP + 16 * c + 4 * cq;
+                        dst[0] = w[m].x;
+                        dst[1] = w[m].y;
+                        dst[2] = w[m].z;
+                        dst[3] = w[m].w;
+                    }
+                }
+            }
+            __syncthreads();
+#pragma unroll
+            for (int d = 1; d < 4; ++d) {
+                if (tid < (4 - d) * 64) {
+                    const int bq = tid >> 6, a = bq + d, rr = (tid >> 2) & 15, cq = tid & 3;
+                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                    for (int cd = 0; cd < d; ++cd) {
+                        const int c = bq + cd;
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk) {
+                            const float wv = AM[(16 * a + rr) * AP + 16 * c + kk];
+                            const float4 t4 = *reinterpret_cast<const float4*>(
+                                TM + (16 * c + kk) * TPP + 16 * bq + 4 * cq);
+                            x.x = __fmaf_rn(wv, t4.x, x.x);
+                            x.y = __fmaf_rn(wv, t4.y, x.y);
+                            x.z = __fmaf_rn(wv, t4.z, x.z);
+                            x.w = __fmaf_rn(wv, t4.w, x.w);
+                        }
+                    }
+                    *reinterpret_cast<float4*>(TM + (16 * a + rr) * TPP + 16 * bq + 4 * cq) =
+                        make_float4(-x.x, -x.y, -x.z, -x.w);
+                }
+                __syncthreads();
+            }
+            if (!failed) {  // T into rows 0..63 of [T; P]
+                const int r = tid & 63, qg = tid >> 6;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const int j = qg + 4 * jj;
+                    const float4 tr = *reinterpret_cast<const float4*>(TM + r * TPP + 4 * j);
+                    stg4(blob + BLOB_TP + OpTP::off(r, 4 * j), tr.x, tr.y, tr.z, tr.w);
+                }
+            }
+            tc::tc_fence_before();
+            __syncthreads();  // buffer b is free for the item after next
         }
+        item = nitem;
+        cur = nxt;
+        beta_cur = beta_nxt;
+    }
+    if (tid == 0) tc::bulk_wait_all();
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -856,8 +909,10 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+// BF16 [rows][cols] with a row pitch of `pitch_elems`; boxes of `box_cols`
+// channels x 64 tokens, optionally with the 128-byte swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
-              uint32_t box_cols) {
+              uint32_t box_cols, bool swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t gdim[2] = {cols, rows};
@@ -865,10 +920,22 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
     cuuint32_t box[2] = {box_cols, (cuuint32_t)C};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!counts[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
 
 }  // namespace
 
@@ -887,16 +954,16 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     PrepMaps maps;
     CUtensorMap vmap;
     const uint64_t hd = (uint64_t)heads * D;
-    if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, D) ||
-        !make_map(&maps.k, k, hd, rows, (uint64_t)stride, D) ||
-        !make_map(&maps.g, g, hd, rows, hd, D) ||
-        !make_map(&vmap, v, hd, rows, (uint64_t)stride, DV)) {
+    if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, true) ||
+        !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, true) ||
+        !make_map(&maps.g, g, hd, rows, hd, 64, true) ||
+        !make_map(&vmap, v, hd, rows, (uint64_t)stride, DV, false)) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
     cudaError_t e = cudaFuncSetAttribute(prepare_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)SM_PREP_TOTAL);
+                                         (int)PS_TOTAL);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)SS_TOTAL);
@@ -908,8 +975,16 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     chunk_map_kernel<<<1, MAP_THREADS, 0, s>>>(cu, n_seqs, cu ? 0 : t, reinterpret_cast<int*>(ws));
     kda_status st = launch_result("kda_prefill (chunk map)");
     if (st != KDA_OK) return st;
-    const long long chunks = ((long long)rows + C - 1) / C + n_seqs;
-    prepare_kernel<<<dim3((unsigned)chunks, heads), NT, SM_PREP_TOTAL, s>>>(
+    // Persistent prepare: one CTA per SM (shared memory allows no more),
+    // never more CTAs than (chunk, head) items.
+    const long long items = (((long long)rows + C - 1) / C + n_seqs) * heads;
+    const int sms = sm_count();
+    if (sms <= 0) {
+        set_error("kda_prefill: cannot query the multiprocessor count");
+        return KDA_ERR_CUDA;
+    }
+    const unsigned grid = (unsigned)(items < sms ? items : sms);
+    prepare_kernel<<<grid, NT, PS_TOTAL, s>>>(
         maps, (const uint16_t*)beta, t, t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;

@@ -49,10 +49,15 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
+// Round an FP32 value to TF32 (10 explicit mantissa bits), to nearest with
+// ties away from zero: add half of the dropped 13-bit field to the magnitude
+// bits, then clear the field.  A carry out of the mantissa bumps the exponent
+// (the correct rounded value); infinities and the NaNs arithmetic produces
+// keep their class (a NaN whose payload lies only in the 13 dropped bits
+// would become an infinity; BF16-derived and computed NaNs never do).  Two
+// full-rate integer operations instead of a conversion instruction.
 __device__ __forceinline__ float to_tf32(float x) {
-    uint32_t r;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
-    return __uint_as_float(r);
+    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
 // ---------------------------------------------------------------- mbarrier
@@ -87,6 +92,29 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
         if (done) return true;
     }
     return false;
+}
+
+// Plain arrive (count one) on `bar`.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Barrier 1 over the first `nthreads` threads of the CTA (a multiple of 32).
+__device__ __forceinline__ void named_sync(uint32_t nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
+
+// Barrier 1 over the first `nthreads` threads that also ORs `pred` across
+// them: every participant gets the same answer.
+__device__ __forceinline__ bool named_sync_or(uint32_t nthreads, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+        " selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------- TMEM
@@ -195,6 +223,11 @@ __device__ __forceinline__ void bulk_wait_all() {
 // its shared-memory source (the global writes may still be in flight).
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Hint: bring `bytes` (a multiple of 16) at `src` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
