@@ -62,7 +62,7 @@ struct Op {
 using OpX = Op<128, 0>;   // A: [X_b; QX_b] then [Ktil; Qtil], K = 128 channels
 using OpY = Op<16, 0>;    // B: Y_b of a 16-token block, K = 128 channels
 using OpY32 = Op<32, 0>;  // B: Y_b of a 32-token block, K = 128 channels
-using OpKH = Op<128, 0>;  // A: Khat^T, rows = key channel, K = 64 tokens
+using OpKH = Op<128, 16>; // A: Khat^T, rows = key channel, K = 64 tokens (written per K index)
 using OpTP = Op<128, 0>;  // A: [T; P], K = 64 tokens
 using OpXV = Op<32, 16>;  // B: X^T and U^T, rows = value column, K = 64 tokens
 using OpS = Op<32, 16>;   // B: S^T, rows = value column, K = 128 key channels
@@ -102,14 +102,14 @@ constexpr uint32_t RB_TM = (RB_AM + 64 * AP * 4 + 15) & ~15u;  // FP32 T [64][TP
 constexpr uint32_t PS_GAM = 2 * RAW_BUF;                     // FP32 Gamma [64][KP]
 constexpr uint32_t PS_OPX = PS_GAM + 64 * KP * 4;            // A operand of the A/P products
 constexpr uint32_t PS_Y = PS_OPX + OpX::bytes(128);          // B operands Y_b
-constexpr uint32_t PS_BETA = PS_Y + 4 * OpY::bytes(128);
+constexpr uint32_t PS_BETA = PS_Y + OpKH::bytes(64);
 constexpr uint32_t PS_GH = PS_BETA + 64 * 4;
 constexpr uint32_t PS_BAR = PS_GH + 128 * 4;  // bar_tma[2], bar_mma, TMEM base
 constexpr uint32_t PS_TOTAL = PS_BAR + 64;
 static_assert(RB_TM + 64 * TPP * 4 <= RB_GMID, "solve arrays overlap the reference rows");
 static_assert(RB_GLAST + 128 * 4 == RAW_G + RAW_TILE, "reference rows must end the g tile");
 static_assert(2 * OpY32::bytes(128) <= 4 * OpY::bytes(128), "Y_b operands do not fit");
-static_assert(OpKH::bytes(64) <= 4 * OpY::bytes(128), "Khat^T staging does not fit");
+static_assert(4 * OpY::bytes(128) <= OpKH::bytes(64), "Y_b operands do not fit");
 static_assert(PS_OPX % 1024 == 0 && PS_Y % 16 == 0, "operand alignment");
 
 // A chunk whose decays all satisfy g >= -kWideGMin takes 32-token column
@@ -319,13 +319,14 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             unsigned char* dst = sm + b * RAW_BUF;
             tc::fence_async_smem();  // the buffer's previous generic-proxy contents are dead
             tc::mbar_arrive_expect_tx(bar_tma + b, RAW_BUF);
-            const CUtensorMap* mp[3] = {&maps.q, &maps.k, &maps.g};
 #pragma unroll
-            for (int a = 0; a < 3; ++a)
-#pragma unroll
-                for (int half = 0; half < 2; ++half)
-                    tc::tma_load_2d(dst + a * RAW_TILE + half * (RAW_TILE / 2), mp[a], bar_tma + b,
-                                    it.h * D + 64 * half, it.c0);
+            for (int half = 0; half < 2; ++half) {
+                const int x = it.h * D + 64 * half;
+                const uint32_t o2 = half * (RAW_TILE / 2);
+                tc::tma_load_2d(dst + RAW_Q + o2, &maps.q, bar_tma + b, x, it.c0);
+                tc::tma_load_2d(dst + RAW_K + o2, &maps.k, bar_tma + b, x, it.c0);
+                tc::tma_load_2d(dst + RAW_G + o2, &maps.g, bar_tma + b, x, it.c0);
+            }
         }
     };
     auto load_beta = [&](const PrepItem& it) {
@@ -484,13 +485,17 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             // ------------------------------------------------------ P3 [Ktil; Qtil], Khat^T
             // Built in the A/P operand buffers (both products are complete) and
             // sent to the workspace by bulk copies that drain during P4 and P5.
+            // Thread (r, qg) forms token r's channels 4 j .. 4 j + 3: Ktil and
+            // Qtil as 16-byte rows, Khat^T as four 4-byte column entries.
             {
                 const int r = tid & 63, qg = tid >> 6;
                 const bool live = r < L;
+                const float br = BETA[r];  // 0 past the chunk's end
 #pragma unroll 4
                 for (int jj = 0; jj < 8; ++jj) {
                     const int j = qg + 4 * jj;
                     const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
+                    const float4 gl = *reinterpret_cast<const float4*>(GLAST + 4 * j);
                     float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
                     if (!live) kf = qf = make_float4(0.f, 0.f, 0.f, 0.f);
                     const float f0 = __expf(ga.x), f1 = __expf(ga.y), f2 = __expf(ga.z),
@@ -499,20 +504,11 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                         kf.w * f3);
                     st4(sm + PS_OPX, OpX::off(64 + r, 4 * j), KDA_Q_SCALE * qf.x * f0,
                         KDA_Q_SCALE * qf.y * f1, KDA_Q_SCALE * qf.z * f2, KDA_Q_SCALE * qf.w * f3);
-                }
-                const int i = tid & 127, hq = tid >> 7;
-                const float gl = GLAST[i];
-#pragma unroll 2
-                for (int qq = 0; qq < 8; ++qq) {
-                    const int q4 = 2 * qq + hq;  // token quad
-                    float kh[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int s = 4 * q4 + e;
-                        kh[e] = (s < L) ? BETA[s] * raw1(RAWK, s, i) * __expf(gl - GAM[s * KP + i])
-                                        : 0.f;
-                    }
-                    st4(sm + PS_Y, OpKH::off(i, 4 * q4), kh[0], kh[1], kh[2], kh[3]);
+                    float* kh = reinterpret_cast<float*>(sm + PS_Y);
+                    kh[OpKH::off(4 * j, r) / 4] = tc::to_tf32(br * kf.x * __expf(gl.x - ga.x));
+                    kh[OpKH::off(4 * j + 1, r) / 4] = tc::to_tf32(br * kf.y * __expf(gl.y - ga.y));
+                    kh[OpKH::off(4 * j + 2, r) / 4] = tc::to_tf32(br * kf.z * __expf(gl.z - ga.z));
+                    kh[OpKH::off(4 * j + 3, r) / 4] = tc::to_tf32(br * kf.w * __expf(gl.w - ga.w));
                 }
             }
             tc::fence_async_smem();
@@ -790,8 +786,9 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     for (int c0 = start; c0 < end; c0 += C, ++g) {
         const int L = min(C, end - c0);
         const bool more = c0 + C < end;
-        sync_for_mma();  // the previous chunk's state operand is written
-        if (*abort_flag) break;
+        tc::fence_async_smem();  // the previous chunk's state operand is written
+        tc::tc_fence_before();
+        if (__syncthreads_or(*abort_flag)) break;  // every thread takes the same exit
         wait_load(bar_a, ph_a);
         if (tid == 0) --pending;
 
@@ -873,7 +870,9 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         o_c0 = c0;
         o_L = L;
     }
-    if (o_c0 >= 0 && !*abort_flag) write_o();  // the last chunk's output
+    // every thread leaves the loop through the same iteration; agree on the flag
+    const bool aborted = __syncthreads_or(*abort_flag);
+    if (o_c0 >= 0 && !aborted) write_o();  // the last chunk's output
     // An early exit can leave copies in flight: let them land before the
     // shared memory is released (bounded waits).
     if (tid == 0 && pending > 0) {
@@ -881,7 +880,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         tc::mbar_wait(bar_b, ph_b, 1u << 20);
     }
 
-    if (!*abort_flag) {
+    if (!aborted) {
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
             *reinterpret_cast<float4*>(Sg + 4 * q4) =

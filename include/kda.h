@@ -144,8 +144,9 @@ kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* b
  * sequences with the given chunk width and input dtype.  Returns 0 when the
  * call needs none (FP32 inputs or chunk != 64 run without one) or when an
  * argument is invalid.  The BF16, chunk-64 tensor-core path stores the
- * state-independent operands of every (chunk, head) there: about 128.5 KiB
- * per chunk of 64 tokens and head, plus (n_seqs + 1) * 4 bytes. */
+ * state-independent operands of every (chunk, head) there: 131,840 bytes
+ * per chunk of 64 tokens and head (with one chunk of slack per sequence),
+ * plus (n_seqs + 1) * 4 bytes rounded up to 256. */
 size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads, int head_dim,
                                   int in_dtype);
 
