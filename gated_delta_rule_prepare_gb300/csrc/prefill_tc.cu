@@ -126,7 +126,9 @@ constexpr uint32_t SS_OPX = SS_BLOB + BLOB_OPX, SS_TP = SS_BLOB + BLOB_TP,
 constexpr uint32_t SS_XV = SS_BLOB + BLOB_BYTES;
 constexpr uint32_t SS_U = SS_XV + OpXV::bytes(64);
 constexpr uint32_t SS_OPS = SS_U + OpXV::bytes(64);
-constexpr uint32_t SS_RAWV = (SS_OPS + OpS::bytes(128) + 127) & ~127u;
+// value tile [64 tokens][32 columns] BF16, 64-byte swizzle: row r's 16-byte
+// chunk c sits at chunk c ^ ((r >> 1) & 3) (needs a 512-byte aligned base)
+constexpr uint32_t SS_RAWV = (SS_OPS + OpS::bytes(128) + 1023) & ~1023u;
 constexpr uint32_t SS_BAR = SS_RAWV + 64 * DV * 2;
 constexpr uint32_t SS_TOTAL = SS_BAR + 64;
 static_assert(SS_TOTAL <= 232448, "shared memory budget exceeded");
@@ -674,6 +676,10 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         return;
     }
     const long long g0 = __ldg(reinterpret_cast<const int*>(ws) + n);
+    if (tc::smem_u32(sm) & 1023u) {  // the swizzled value tile needs an aligned base
+        if (tid == 0) atomicOr(&g_tc_status, STATUS_SMEM_ALIGN);
+        return;
+    }
 
     float* DEC = reinterpret_cast<float*>(sm + SS_DEC);
     const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + SS_RAWV);
@@ -805,10 +811,15 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
             tc::tmem_ld16(tmem + lane_base + TC_Y + 16 * ch, v);
             tc::tmem_ld_wait();
             if (ln < 64) {
-                const int r = ln;
+                const int r = ln, sw = (r >> 1) & 3;
+                const unsigned char* vrow = reinterpret_cast<const unsigned char*>(RAWV) + r * 64;
+                const uint4 va = *reinterpret_cast<const uint4*>(vrow + (((2 * ch) ^ sw) << 4));
+                const uint4 vb = *reinterpret_cast<const uint4*>(vrow + (((2 * ch + 1) ^ sw) << 4));
+                const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
 #pragma unroll
                 for (int jj = 0; jj < 16; ++jj) {
-                    const float x = (r < L) ? bf(RAWV[r * DV + 16 * ch + jj]) - v[jj] : 0.f;
+                    const uint32_t bits = (jj & 1) ? (w[jj >> 1] & 0xffff0000u) : (w[jj >> 1] << 16);
+                    const float x = (r < L) ? __uint_as_float(bits) - v[jj] : 0.f;
                     *reinterpret_cast<float*>(sm + SS_XV + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(x);
                 }
             } else {
@@ -909,9 +920,9 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // BF16 [rows][cols] with a row pitch of `pitch_elems`; boxes of `box_cols`
-// channels x 64 tokens, optionally with the 128-byte swizzle.
+// channels x 64 tokens with the given shared-memory swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
-              uint32_t box_cols, bool swizzle) {
+              uint32_t box_cols, CUtensorMapSwizzle swizzle) {
     auto fn = encode_fn();
     if (!fn) return false;
     cuuint64_t gdim[2] = {cols, rows};
@@ -919,8 +930,7 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
     cuuint32_t box[2] = {box_cols, (cuuint32_t)C};
     cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -953,10 +963,10 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     PrepMaps maps;
     CUtensorMap vmap;
     const uint64_t hd = (uint64_t)heads * D;
-    if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, true) ||
-        !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, true) ||
-        !make_map(&maps.g, g, hd, rows, hd, 64, true) ||
-        !make_map(&vmap, v, hd, rows, (uint64_t)stride, DV, false)) {
+    if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.g, g, hd, rows, hd, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&vmap, v, hd, rows, (uint64_t)stride, DV, CU_TENSOR_MAP_SWIZZLE_64B)) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
