@@ -9,21 +9,26 @@
 //   T      = (I + A)^-1                    (blocked forward substitution)
 //   Ktil   = e^Gamma (.) k,  Qtil = e^Gamma (.) qh,
 //   Khat_s = beta_s e^(Gamma_{L-1}-Gamma_s) (.) k_s,   dec = e^Gamma_{L-1}
-// prepare_kernel, one CTA per (chunk, head), fully parallel: everything above
-// that does not depend on the carried state.  It writes [Ktil; Qtil],
-// [T; P], Khat^T (as TF32 tensor-core operands, already in the layout the
-// scan consumes) and dec to the workspace: 131,584 bytes per chunk and head.
+// prepare_kernel computes everything above that does not depend on the
+// carried state, for every (chunk, head) item, fully parallel: one persistent
+// CTA per SM walks the items, with the next item's q/k/g tiles arriving by
+// TMA into a second buffer while the current one is processed.  It writes
+// [Ktil; Qtil], [T; P], Khat^T (TF32 tensor-core operands, already in the
+// layout the scan consumes) and dec to the workspace: 131,840 bytes per chunk
+// and head.
 // scan_kernel, one CTA per (sequence, head, 32-column value slice), carries
 // the FP32 state across the sequence's chunks in order:
 //   X = V - Ktil S;  U = T X;  O = Qtil S + P U;  S <- dec (.) S + Khat^T U
 // as three tensor-core round trips per chunk; the chunk's operands arrive by
 // bulk copy from the workspace and the value slice by TMA.
 //
-// A and P come from four tensor-core products, one per 16-column block b with
-// reference token m_b = 16b + 8: e^(Gamma_r-Gamma_s) = e^(Gamma_r-Gamma_mb)
-// e^(Gamma_mb-Gamma_s) with both factors within e^(+-8 |g|max) for every
-// (r >= 16b, s in block b), so FP32 neither overflows nor loses the product
-// for g >= -10; rows above the block are never formed into results.
+// A and P come from tensor-core products over column blocks b with a
+// reference token m_b: e^(Gamma_r-Gamma_s) = e^(Gamma_r-Gamma_mb)
+// e^(Gamma_mb-Gamma_s).  With four 16-token blocks (m_b = 16b + 8) both
+// factors stay within e^(+-8 |g|max) for every (r >= 16b, s in block b), so
+// FP32 neither overflows nor loses the product for g >= -10; rows above the
+// block are never formed into results.  Chunks whose decays all stay above
+// -kWideGMin take two 32-token blocks instead (see kWideGMin).
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
@@ -40,7 +45,7 @@ __device__ unsigned g_tc_status = 0;
 constexpr int C = 64;
 constexpr int DV = 32;
 constexpr int NT = 256;
-constexpr int KP = 132;  // pitch (floats) of FP32 [64][128] staging arrays (16-B rows)
+constexpr int KP = 132;  // pitch (floats) of the FP32 [64][128] Gamma array (16-B rows)
 constexpr int AP = 65;   // pitch (floats) of the FP32 [64][64] A / W array
 constexpr int TPP = 68;  // pitch (floats) of the FP32 [64][64] T array (16-B rows)
 

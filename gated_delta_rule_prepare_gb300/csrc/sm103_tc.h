@@ -3,13 +3,10 @@
 // shared-memory operand descriptors, tcgen05.commit / mbarrier completion,
 // tcgen05.ld of accumulators, and TMA tile loads.
 //
-// Operand layout used throughout (no swizzle, K-major): the operand is a grid
-// of "core matrices" of 8 rows x 16 bytes (8 x 4 TF32 values), each stored as
-// 128 contiguous bytes.  For an operand of R rows and K columns the core
-// matrix holding (row r, column k) starts at
-//     (r / 8) * SBO + (k / 4) * LBO,   LBO = 128 B,   SBO = K * 32 B,
-// i.e. the K core matrices of one 8-row group are adjacent ("rows outer"),
-// so rows [64, 128) of a 128-row operand are one contiguous upper half.
+// Operands are described without swizzle: an operand is a grid of "core
+// matrices" of 8 rows x 16 bytes (8 x 4 TF32 values), each 128 contiguous
+// bytes; a descriptor gives the byte distance between core matrices adjacent
+// along K (LBO) and along M or N (SBO).  The callers choose the placement.
 #pragma once
 
 #include <cuda.h>
@@ -22,11 +19,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Byte offset of element (r, k) of a K-major TF32 operand with K columns.
-__host__ __device__ constexpr uint32_t kmaj_off(int r, int k, int K) {
-    return (uint32_t)((r >> 3) * (K * 32) + (k >> 2) * 128 + (r & 7) * 16 + (k & 3) * 4);
-}
-
 // Shared-memory matrix descriptor: start address, LBO, SBO (bytes), no swizzle.
 __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     uint64_t d = 0;
@@ -35,12 +27,6 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint
     d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
     d |= (uint64_t)1u << 46;  // descriptor version for tcgen05
     return d;                 // base offset 0, relative LBO mode, swizzle none
-}
-
-// Descriptor of the K-step `ks` (8 TF32 columns) of a K-major operand with K
-// columns stored at saddr.
-__device__ __forceinline__ uint64_t kmaj_desc(uint32_t saddr, int K, int ks) {
-    return make_desc(saddr + (uint32_t)ks * 256u, 128u, (uint32_t)K * 32u);
 }
 
 // Instruction descriptor: kind::tf32, FP32 accumulate, A and B K-major.
