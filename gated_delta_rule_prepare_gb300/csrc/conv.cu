@@ -4,12 +4,14 @@
 // and l2_norm_bf16; config.rs: conv state of conv_kernel slots, L2 applied as
 // 1/sqrt(sum + eps)).
 //
-// Kernel 1 (conv_silu_l2_kernel): one CTA per (head-sized group of 128
-// channels, block of 32 consecutive tokens); a thread owns one channel and
-// slides a register window of the last conv_kernel - 1 inputs along the
-// tokens.  History before a sequence's first token comes from the conv
-// state, which this kernel only reads.  The L2 sum over a q/k head's 128
-// channels is a warp shuffle reduction plus a 4-warp smem reduction per token.
+// Kernel 1 (conv_silu_l2_kernel): one CTA of 128 threads per (group of 1024
+// channels = 8 heads, block of 16 consecutive tokens); a thread owns 8
+// adjacent channels (16-byte BF16 loads and stores) and slides a register
+// window of the last conv_kernel - 1 inputs along the tokens.  History
+// before a sequence's first token comes from the conv state, which this
+// kernel only reads.  A q/k head's 128 channels are one half-warp, so its L2
+// sum is a 4-step shuffle reduction within the half-warp, per token, with no
+// shared memory; the conv taps run as packed FP32 pairs (fma.rn.f32x2).
 // Kernel 2 (conv_state_kernel): after kernel 1, each thread rewrites one
 // (sequence, channel) state row to hold that sequence's last conv_kernel
 // inputs, reading the old row first; separating it from kernel 1 keeps any
@@ -23,15 +25,13 @@ namespace {
 
 __device__ unsigned g_conv_status = 0;
 
-constexpr int kTok = 32;        // tokens per CTA
-constexpr int kThreads = D;     // two heads of 128 channels, two channels per thread
+constexpr int kTok = 16;                   // tokens per CTA
+constexpr int kThreads = 128;              // per CTA
+constexpr int kCh = 8;                     // channels per thread
+constexpr int kCtaCh = kThreads * kCh;     // channels per CTA (8 heads)
 
 __device__ __forceinline__ float bf16_to_f32(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
-}
-
-__device__ __forceinline__ uint16_t f32_to_bf16(float f) {
-    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
 __device__ __forceinline__ float2 bf16x2_to_f32(uint32_t u) {
@@ -39,7 +39,8 @@ __device__ __forceinline__ float2 bf16x2_to_f32(uint32_t u) {
 }
 
 __device__ __forceinline__ uint32_t f32x2_to_bf16x2(float a, float b) {
-    return (uint32_t)f32_to_bf16(a) | ((uint32_t)f32_to_bf16(b) << 16);
+    const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);  // one packed conversion
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // Sequence holding packed token tau: largest n with cu[n] <= tau.  Returns
@@ -62,26 +63,45 @@ __device__ __forceinline__ float silu(float a) {
     return __fdividef(a, 1.0f + __expf(-a));  // rounded to BF16 by the caller
 }
 
+// Packed FP32 pair arithmetic (two channels per instruction).
+__device__ __forceinline__ unsigned long long pk(float2 v) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(v.x), "f"(v.y));
+    return r;
+}
+__device__ __forceinline__ float2 upk(unsigned long long r) {
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+// a * b + c on both halves, each rounded once (as fmaf).
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
+    return upk(r);
+}
+
 template <int K>
 __global__ void __launch_bounds__(kThreads)
 conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __restrict__ x,
                     const uint16_t* __restrict__ w, uint16_t* __restrict__ out, int total,
                     int t_per_seq, const int* __restrict__ cu, int n_seqs, int heads,
                     float l2_eps) {
-    __shared__ float red[kThreads / 32][kTok];
-    const int pair = blockIdx.x;  // head groups 2 pair and 2 pair + 1 of the 3H groups
-    const int c = pair * 2 * D + 2 * threadIdx.x;  // first of this thread's two channels
+    const int lane = threadIdx.x & 31;
+    const int c = blockIdx.x * kCtaCh + kCh * threadIdx.x;  // first of this thread's 8 channels
     const size_t conv_dim = (size_t)3 * heads * D;
-    // The first 2H groups (q and k) always pair up fully; with an odd head count the
-    // last v pair has only one group, and its second half of threads stays idle.
+    // conv_dim is a multiple of 128, so a head (16 threads, a half-warp) is
+    // either wholly present or wholly absent here.
     if ((size_t)c >= conv_dim) return;
-    const bool normalise = pair < heads;
-    float w0[K], w1[K];
+    const bool normalise = c < 2 * heads * D;            // a q or k head
+    const unsigned hmask = 0xffffu << (lane & 16);       // this half-warp
+    float2 wv[K][kCh / 2];                               // tap j of channel pairs
 #pragma unroll
-    for (int j = 0; j < K; ++j) {
-        w0[j] = bf16_to_f32(__ldg(w + (size_t)c * K + j));
-        w1[j] = bf16_to_f32(__ldg(w + (size_t)(c + 1) * K + j));
-    }
+    for (int j = 0; j < K; ++j)
+#pragma unroll
+        for (int e = 0; e < kCh / 2; ++e)
+            wv[j][e] = make_float2(bf16_to_f32(__ldg(w + (size_t)(c + 2 * e) * K + j)),
+                                   bf16_to_f32(__ldg(w + (size_t)(c + 2 * e + 1) * K + j)));
 
     const int tok0 = blockIdx.y * kTok;
     const int tok_end = min(total, tok0 + kTok);
@@ -97,45 +117,92 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
         start = n * t_per_seq;
         end = start + t_per_seq;
     }
-    // All of the block's inputs first, as independent loads.
-    const uint32_t* xp = reinterpret_cast<const uint32_t*>(x + (size_t)tok0 * conv_dim + c);
-    const size_t step = conv_dim / 2;  // one token row, in channel pairs
-    float2 xs[kTok];
+    // All of the block's inputs first, as independent 16-byte loads.
+    const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)tok0 * conv_dim + c);
+    const size_t step = conv_dim / kCh;  // one token row, in 16-byte units
+    uint4 xs[kTok];
 #pragma unroll
     for (int m = 0; m < kTok; ++m)
-        xs[m] = (tok0 + m < tok_end) ? bf16x2_to_f32(__ldg(xp + m * step)) : make_float2(0.f, 0.f);
-    // h0[j], h1[j]: the two channels' inputs at token tau - (K - 1) + j.
-    float h0[K > 1 ? K - 1 : 1], h1[K > 1 ? K - 1 : 1];
+        xs[m] = (tok0 + m < tok_end) ? __ldg(xp + m * step) : make_uint4(0u, 0u, 0u, 0u);
+    // hv[j][e]: channel pair e's inputs at token tau - (K - 1) + j.
+    float2 hv[K > 1 ? K - 1 : 1][kCh / 2];
+    auto state_slot = [&](int e2, int slot) {  // the state's slot for channel pair e2
+        const float* st = conv_state + ((size_t)n * conv_dim + c + 2 * e2) * K;
+        return make_float2(__ldg(st + slot), __ldg(st + K + slot));
+    };
     auto state_history = [&]() {  // a sequence's first token: history from its state
-        const float* st = conv_state + ((size_t)n * conv_dim + c) * K;
 #pragma unroll
-        for (int j = 0; j < K - 1; ++j) {
-            h0[j] = __ldg(st + j + 1);
-            h1[j] = __ldg(st + K + j + 1);
-        }
+        for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+            for (int e = 0; e < kCh / 2; ++e) hv[j][e] = state_slot(e, j + 1);
     };
     if (ok) {
-        const float* st = conv_state + ((size_t)n * conv_dim + c) * K;
 #pragma unroll
         for (int j = 0; j < K - 1; ++j) {
             const int src = tok0 - (K - 1) + j;
             if (src >= start) {
-                const float2 v = bf16x2_to_f32(__ldg(reinterpret_cast<const uint32_t*>(
-                    x + (size_t)src * conv_dim + c)));
-                h0[j] = v.x;
-                h1[j] = v.y;
+                const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + (size_t)src * conv_dim + c));
+                hv[j][0] = bf16x2_to_f32(u.x);
+                hv[j][1] = bf16x2_to_f32(u.y);
+                hv[j][2] = bf16x2_to_f32(u.z);
+                hv[j][3] = bf16x2_to_f32(u.w);
             } else {
-                h0[j] = __ldg(st + K + (src - start));
-                h1[j] = __ldg(st + K + K + (src - start));
+#pragma unroll
+                for (int e = 0; e < kCh / 2; ++e) hv[j][e] = state_slot(e, K + (src - start));
             }
         }
     }
-    float2 y[kTok];
+    uint4* op = reinterpret_cast<uint4*>(out + (size_t)tok0 * conv_dim + c);
+    // One token: conv over the window, SiLU, the head's L2 scale, BF16 store.
+    auto token = [&](int m) {
+        const float2 xv[kCh / 2] = {bf16x2_to_f32(xs[m].x), bf16x2_to_f32(xs[m].y),
+                                    bf16x2_to_f32(xs[m].z), bf16x2_to_f32(xs[m].w)};
+        float2 y[kCh / 2];
 #pragma unroll
-    for (int m = 0; m < kTok; ++m) {
+        for (int e = 0; e < kCh / 2; ++e) {
+            float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < K - 1; ++j) a = fma2(wv[j][e], hv[j][e], a);
+            a = fma2(wv[K - 1][e], xv[e], a);
+#pragma unroll
+            for (int j = 0; j + 1 < K - 1; ++j) hv[j][e] = hv[j + 1][e];
+            if constexpr (K > 1) hv[K - 2][e] = xv[e];
+            y[e] = make_float2(silu(a.x), silu(a.y));
+        }
+        if (normalise) {  // uniform per half-warp
+            float p = 0.f;
+#pragma unroll
+            for (int e = 0; e < kCh / 2; ++e) {
+                p = __fmaf_rn(y[e].x, y[e].x, p);
+                p = __fmaf_rn(y[e].y, y[e].y, p);
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) p += __shfl_xor_sync(hmask, p, off);
+            const float inv = rsqrtf(p + l2_eps);
+#pragma unroll
+            for (int e = 0; e < kCh / 2; ++e) {
+                y[e].x *= inv;
+                y[e].y *= inv;
+            }
+        }
+        uint4 o;
+        o.x = f32x2_to_bf16x2(y[0].x, y[0].y);
+        o.y = f32x2_to_bf16x2(y[1].x, y[1].y);
+        o.z = f32x2_to_bf16x2(y[2].x, y[2].y);
+        o.w = f32x2_to_bf16x2(y[3].x, y[3].y);
+        op[m * step] = o;
+    };
+    if (ok && tok0 + kTok <= tok_end && tok0 + kTok <= end) {
+        // Common case: all kTok tokens lie in one sequence; straight-line code
+        // lets the tokens' independent work overlap.
+#pragma unroll
+        for (int m = 0; m < kTok; ++m) token(m);
+        return;
+    }
+#pragma unroll
+    for (int m = 0; m < kTok; ++m) {  // uniform over the CTA: tok_end, ok and the boundaries
         const int tau = tok0 + m;
-        y[m] = make_float2(0.f, 0.f);
-        if (!ok || tau >= tok_end) continue;
+        if (!ok || tau >= tok_end) break;
         if (tau >= end) {  // a new sequence starts at tau (skipping empty ones)
             if (cu) {
                 while (n + 1 < n_seqs && __ldg(cu + n + 1) <= tau) ++n;
@@ -143,7 +210,7 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
                 end = __ldg(cu + n + 1);
                 if (!(start == tau && tau < end)) {
                     ok = false;
-                    continue;
+                    break;
                 }
             } else {
                 ++n;
@@ -152,49 +219,9 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
             }
             state_history();
         }
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int j = 0; j < K - 1; ++j) {
-            a0 = __fmaf_rn(w0[j], h0[j], a0);
-            a1 = __fmaf_rn(w1[j], h1[j], a1);
-        }
-        a0 = __fmaf_rn(w0[K - 1], xs[m].x, a0);
-        a1 = __fmaf_rn(w1[K - 1], xs[m].y, a1);
-#pragma unroll
-        for (int j = 0; j + 1 < K - 1; ++j) {
-            h0[j] = h0[j + 1];
-            h1[j] = h1[j + 1];
-        }
-        if constexpr (K > 1) {
-            h0[K - 2] = xs[m].x;
-            h1[K - 2] = xs[m].y;
-        }
-        y[m] = make_float2(silu(a0), silu(a1));
+        token(m);
     }
     if (!ok && threadIdx.x == 0) atomicOr(&g_conv_status, STATUS_BAD_CU_SEQLENS);
-
-    if (normalise) {  // uniform per CTA: both heads are q/k heads or neither is
-        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-#pragma unroll
-        for (int m = 0; m < kTok; ++m) {
-            float p = y[m].x * y[m].x + y[m].y * y[m].y;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-            if (lane == 0) red[warp][m] = p;
-        }
-        __syncthreads();
-        const int hw = warp & ~1;  // the two warps of this thread's head
-#pragma unroll
-        for (int m = 0; m < kTok; ++m) {
-            const float inv = rsqrtf(red[hw][m] + red[hw + 1][m] + l2_eps);
-            y[m].x *= inv;
-            y[m].y *= inv;
-        }
-    }
-    uint32_t* op = reinterpret_cast<uint32_t*>(out + (size_t)tok0 * conv_dim + c);
-#pragma unroll
-    for (int m = 0; m < kTok; ++m)
-        if (tok0 + m < tok_end) op[m * step] = f32x2_to_bf16x2(y[m].x, y[m].y);
 }
 
 template <int K>
@@ -240,7 +267,7 @@ template <int K>
 kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint16_t* out,
                   int total, int t_per_seq, const int* cu, int n_seqs, int heads, float eps,
                   cudaStream_t s) {
-    dim3 grid((3 * heads + 1) / 2, (total + kTok - 1) / kTok);
+    dim3 grid((unsigned)((3 * heads * D + kCtaCh - 1) / kCtaCh), (total + kTok - 1) / kTok);
     conv_silu_l2_kernel<K><<<grid, kThreads, 0, s>>>(conv_state, x, w, out, total, t_per_seq,
                                                       cu, n_seqs, heads, eps);
     kda_status st = launch_result("kda_conv_silu_l2 (conv)");
