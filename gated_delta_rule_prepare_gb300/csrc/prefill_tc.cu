@@ -44,7 +44,8 @@ __device__ unsigned g_tc_status = 0;
 
 constexpr int C = 64;
 constexpr int DV = 32;
-constexpr int NT = 256;
+constexpr int NT = 256;   // scan threads
+constexpr int NTP = 512;  // prepare threads
 constexpr int KP = 132;  // pitch (floats) of the FP32 [64][128] Gamma array (16-B rows)
 constexpr int AP = 65;   // pitch (floats) of the FP32 [64][64] A / W array
 constexpr int TPP = 68;  // pitch (floats) of the FP32 [64][64] T array (16-B rows)
@@ -108,8 +109,7 @@ constexpr uint32_t PS_GAM = 2 * RAW_BUF;                     // FP32 Gamma [64][
 constexpr uint32_t PS_OPX = PS_GAM + 64 * KP * 4;            // A operand of the A/P products
 constexpr uint32_t PS_Y = PS_OPX + OpX::bytes(128);          // B operands Y_b
 constexpr uint32_t PS_BETA = PS_Y + OpKH::bytes(64);
-constexpr uint32_t PS_GH = PS_BETA + 64 * 4;
-constexpr uint32_t PS_BAR = PS_GH + 128 * 4;  // bar_tma[2], bar_mma, TMEM base
+constexpr uint32_t PS_BAR = PS_BETA + 64 * 4;  // bar_tma[2], bar_mma, TMEM base
 constexpr uint32_t PS_TOTAL = PS_BAR + 64;
 static_assert(RB_TM + 64 * TPP * 4 <= RB_GMID, "solve arrays overlap the reference rows");
 static_assert(RB_GLAST + 128 * 4 == RAW_G + RAW_TILE, "reference rows must end the g tile");
@@ -264,13 +264,13 @@ __device__ __forceinline__ PrepItem prep_item(long long item, int heads, const i
     return it;
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NTP, 1)
 prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict__ beta, int t,
                int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
                unsigned char* __restrict__ ws) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column half
+    const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column quarter
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     const int* chunk_off = reinterpret_cast<const int*>(ws);
@@ -283,7 +283,6 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
 
     float* GAM = reinterpret_cast<float*>(sm + PS_GAM);
     float* BETA = reinterpret_cast<float*>(sm + PS_BETA);
-    float* GH = reinterpret_cast<float*>(sm + PS_GH);
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + PS_BAR);  // one per raw buffer
     uint64_t* bar_mma = bar_tma + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PS_BAR + 24);
@@ -384,26 +383,32 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             ph_tma[b] ^= 1;
 
             // ------------------------------------------------------ P1 Gamma
+            // Four 16-token quarters per channel, then each quarter adds the
+            // totals of the quarters before it.  The totals sit in the other raw
+            // buffer, whose next tiles are requested only after this phase.
             bool wide;
+            float* GH = reinterpret_cast<float*>(sm + (b ^ 1) * RAW_BUF);  // [3][128]
             {
-                const int i = tid & 127, hf = tid >> 7;
+                const int i = tid & 127, qt = tid >> 7;
                 float acc = 0.f, gmin = 0.f;
 #pragma unroll 8
-                for (int rr = 0; rr < 32; ++rr) {
-                    const int r = 32 * hf + rr;
+                for (int rr = 0; rr < 16; ++rr) {
+                    const int r = 16 * qt + rr;
                     const float gv = (r < L) ? raw1(RAWG, r, i) : 0.f;
                     gmin = fminf(gmin, gv);
                     acc = __fadd_rn(acc, gv);
                     GAM[r * KP + i] = acc;
                 }
-                if (hf == 0) GH[i] = acc;
+                if (qt < 3) GH[qt * 128 + i] = acc;
                 wide = __syncthreads_and(gmin >= -kWideGMin);  // false on NaN too
             }
             if (tid >= 128) {
-                const int i = tid & 127;
-                const float base = GH[i];
+                const int i = tid & 127, qt = tid >> 7;
+                float base = GH[i];
+                if (qt > 1) base = __fadd_rn(base, GH[128 + i]);
+                if (qt > 2) base = __fadd_rn(base, GH[256 + i]);
 #pragma unroll 8
-                for (int rr = 0; rr < 32; ++rr) GAM[(32 + rr) * KP + i] += base;
+                for (int rr = 0; rr < 16; ++rr) GAM[(16 * qt + rr) * KP + i] += base;
             }
             if (tid == 0) tc::bulk_wait_read_all();  // the last item's operands left OPX and Y
             __syncthreads();  // the g tile is dead from here on
@@ -424,9 +429,9 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                 const int r = tid & 63, qg = tid >> 6;
                 if (r >= r0) {
                     const bool live = r < L;
-#pragma unroll 4
-                    for (int jj = 0; jj < 8; ++jj) {
-                        const int j = qg + 4 * jj;
+#pragma unroll
+                    for (int jj = 0; jj < 32 / (NTP / 64); ++jj) {
+                        const int j = qg + (NTP / 64) * jj;
                         const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
                         const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
                         float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
@@ -443,7 +448,7 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             };
             // Y_b row s of block b = s >> bshift: k_s e^(Gamma_mb - Gamma_s).
             auto build_y = [&](int bshift, int gm_row0, uint32_t ybytes, auto op) {
-                for (int e = tid; e < 64 * 32; e += NT) {
+                for (int e = tid; e < 64 * 32; e += NTP) {
                     const int s = e & 63, j = e >> 6, bb = s >> bshift;
                     const float4 gm =
                         *reinterpret_cast<const float4*>(GMID + (gm_row0 + bb) * 128 + 4 * j);
@@ -498,9 +503,9 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                 const int r = tid & 63, qg = tid >> 6;
                 const bool live = r < L;
                 const float br = BETA[r];  // 0 past the chunk's end
-#pragma unroll 4
-                for (int jj = 0; jj < 8; ++jj) {
-                    const int j = qg + 4 * jj;
+#pragma unroll
+                for (int jj = 0; jj < 32 / (NTP / 64); ++jj) {
+                    const int j = qg + (NTP / 64) * jj;
                     const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
                     const float4 gl = *reinterpret_cast<const float4*>(GLAST + 4 * j);
                     float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
@@ -527,35 +532,33 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             }
 
             // ------------------------------------------------------ P4 read A, P
-            {
-                float v[32];
-                tc::tmem_ld16(tmem + lane_base + TC_AP + 32 * ch, *reinterpret_cast<float(*)[16]>(v));
-                tc::tmem_ld16(tmem + lane_base + TC_AP + 32 * ch + 16,
-                              *reinterpret_cast<float(*)[16]>(v + 16));
+            {   // thread (lane ln, quarter ch) reads columns [16 ch, 16 ch + 16)
+                float v[16];
+                tc::tmem_ld16(tmem + lane_base + TC_AP + 16 * ch, v);
                 tc::tmem_ld_wait();
                 if (ln < 64) {
                     const int r = ln;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        const int s = 32 * ch + c;
+                    for (int c = 0; c < 16; ++c) {
+                        const int s = 16 * ch + c;
                         AM[r * AP + s] = (s < r) ? v[c] * BETA[s] : 0.f;
                     }
                 } else if (!failed) {
                     const int r = ln - 64;
 #pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
+                    for (int c4 = 0; c4 < 4; ++c4) {
                         float p[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const int s = 32 * ch + 4 * c4 + e;
+                            const int s = 16 * ch + 4 * c4 + e;
                             p[e] = (s <= r) ? v[4 * c4 + e] * BETA[s] : 0.f;
                         }
-                        stg4(blob + BLOB_TP + OpTP::off(64 + r, 32 * ch + 4 * c4), p[0], p[1], p[2],
+                        stg4(blob + BLOB_TP + OpTP::off(64 + r, 16 * ch + 4 * c4), p[0], p[1], p[2],
                              p[3]);
                     }
                 }
             }
-            for (int e = tid; e < 64 * 64; e += NT) TM[(e >> 6) * TPP + (e & 63)] = 0.f;
+            for (int e = tid; e < 64 * 64; e += NTP) TM[(e >> 6) * TPP + (e & 63)] = 0.f;
             tc::tc_fence_before();
             __syncthreads();
 
@@ -578,10 +581,11 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             // Below the diagonal, with W_ac = T_aa A_ac:  T_ab = -sum_{c=b}^{a-1} W_ac T_cb.
             // Work in 1 x 4 tiles (one row, four consecutive columns) per thread.
             {
-                float4 w[2];
+                constexpr int kWm = (6 * 64 + NTP - 1) / NTP;
+                float4 w[kWm];
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const int e = tid + NT * m;
+                for (int m = 0; m < kWm; ++m) {
+                    const int e = tid + NTP * m;
                     w[m] = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (e < 6 * 64) {
                         const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
@@ -601,8 +605,8 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                 }
                 __syncthreads();
 #pragma unroll
-                for (int m = 0; m < 2; ++m) {
-                    const int e = tid + NT * m;
+                for (int m = 0; m < kWm; ++m) {
+                    const int e = tid + NTP * m;
                     if (e < 6 * 64) {
                         const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
                         const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
@@ -643,8 +647,8 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             if (!failed) {  // T into rows 0..63 of [T; P]
                 const int r = tid & 63, qg = tid >> 6;
 #pragma unroll
-                for (int jj = 0; jj < 4; ++jj) {
-                    const int j = qg + 4 * jj;
+                for (int jj = 0; jj < 16 / (NTP / 64); ++jj) {
+                    const int j = qg + (NTP / 64) * jj;
                     const float4 tr = *reinterpret_cast<const float4*>(TM + r * TPP + 4 * j);
                     stg4(blob + BLOB_TP + OpTP::off(r, 4 * j), tr.x, tr.y, tr.z, tr.w);
                 }
@@ -998,7 +1002,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         return KDA_ERR_CUDA;
     }
     const unsigned grid = (unsigned)(items < sms ? items : sms);
-    prepare_kernel<<<grid, NT, PS_TOTAL, s>>>(
+    prepare_kernel<<<grid, NTP, PS_TOTAL, s>>>(
         maps, (const uint16_t*)beta, t, t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;
