@@ -44,7 +44,8 @@ __device__ unsigned g_tc_status = 0;
 
 constexpr int C = 64;
 constexpr int DV = 32;
-constexpr int NT = 256;   // scan threads
+constexpr int NTS = 256;  // scan threads
+constexpr int SC = DV / (NTS / 128);  // state columns per scan thread
 constexpr int NTP = 512;  // prepare threads
 constexpr int KP = 132;  // pitch (floats) of the FP32 [64][128] Gamma array (16-B rows)
 constexpr int AP = 65;   // pitch (floats) of the FP32 [64][64] A / W array
@@ -72,6 +73,7 @@ using OpKH = Op<128, 16>; // A: Khat^T, rows = key channel, K = 64 tokens (writt
 using OpTP = Op<128, 0>;  // A: [T; P], K = 64 tokens
 using OpXV = Op<32, 16>;  // B: X^T and U^T, rows = value column, K = 64 tokens
 using OpS = Op<32, 16>;   // B: S^T, rows = value column, K = 128 key channels
+using OpX1 = Op<64, 0>;   // A: [X_1; QX_1] of the second 32-token block, rows 32..63 only
 
 // ------------------------------------------------------------ workspace
 // [chunk_off: (n_seqs + 1) int32, padded to 256 B][blob (g, h) for every
@@ -446,6 +448,44 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                     }
                 }
             };
+            // Both 32-token blocks in one pass: X_0 for every row into OPX, X_1 for
+            // rows 32..63 into a compact 64-row operand (k rows, then q rows) in
+            // the idle raw buffer; the second product's 64 padding rows read the
+            // next K group (or the 1 KB after the operand) and are never used.
+            unsigned char* x1buf = sm + (b ^ 1) * RAW_BUF;
+            auto build_x_wide = [&]() {
+                const int r = tid & 63, qg = tid >> 6;
+                const bool live = r < L;
+                const float* gm0 = GMID + 4 * 128;
+                const float* gm1 = GMID + 5 * 128;
+#pragma unroll
+                for (int jj = 0; jj < 32 / (NTP / 64); ++jj) {
+                    const int j = qg + (NTP / 64) * jj;
+                    const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
+                    float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
+                    if (!live) kf = qf = make_float4(0.f, 0.f, 0.f, 0.f);
+                    qf = make_float4(KDA_Q_SCALE * qf.x, KDA_Q_SCALE * qf.y, KDA_Q_SCALE * qf.z,
+                                     KDA_Q_SCALE * qf.w);
+                    {
+                        const float4 gm = *reinterpret_cast<const float4*>(gm0 + 4 * j);
+                        const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
+                                    f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
+                        st4(sm + PS_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
+                            kf.w * f3);
+                        st4(sm + PS_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1, qf.z * f2,
+                            qf.w * f3);
+                    }
+                    if (r >= 32) {
+                        const float4 gm = *reinterpret_cast<const float4*>(gm1 + 4 * j);
+                        const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
+                                    f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
+                        st4(x1buf, OpX1::off(r - 32, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
+                            kf.w * f3);
+                        st4(x1buf, OpX1::off(r, 4 * j), qf.x * f0, qf.y * f1, qf.z * f2,
+                            qf.w * f3);
+                    }
+                }
+            };
             // Y_b row s of block b = s >> bshift: k_s e^(Gamma_mb - Gamma_s).
             auto build_y = [&](int bshift, int gm_row0, uint32_t ybytes, auto op) {
                 for (int e = tid; e < 64 * 32; e += NTP) {
@@ -463,19 +503,17 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             if (wide) {
                 // Two 32-token column blocks (every g of the chunk is >= -kWideGMin).
                 build_y(5, 4, OpY32::bytes(128), OpY32{});
-                for (int bb = 0; bb < 2; ++bb) {
-                    build_x(32 * bb, GMID + (4 + bb) * 128);
-                    sync_for_mma();
-                    if (tid == 0) {
-                        tc::tc_fence_after();
-                        issue_mma<OpX, OpY32>(tmem + TC_AP + 32 * bb, s_opx,
-                                              s_y + bb * OpY32::bytes(128), 16,
-                                              tc::idesc_tf32(128, 32));
-                        tc::mma_commit(bar_mma);
-                    }
-                    if (bb == 0) fetch_next();
-                    wait_mma();
+                build_x_wide();
+                sync_for_mma();
+                if (tid == 0) {
+                    tc::tc_fence_after();
+                    issue_mma<OpX, OpY32>(tmem + TC_AP, s_opx, s_y, 16, tc::idesc_tf32(128, 32));
+                    issue_mma<OpX1, OpY32>(tmem + TC_AP + 32, tc::smem_u32(x1buf),
+                                           s_y + OpY32::bytes(128), 16, tc::idesc_tf32(128, 32));
+                    tc::mma_commit(bar_mma);
                 }
+                wait_mma();
+                fetch_next();  // the compact X_1 in the other buffer has been read
             } else {
                 // Four 16-token column blocks with reference token 16 b + 8.
                 build_y(4, 0, OpY::bytes(128), OpY{});
@@ -536,7 +574,33 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                 float v[16];
                 tc::tmem_ld16(tmem + lane_base + TC_AP + 16 * ch, v);
                 tc::tmem_ld_wait();
-                if (ln < 64) {
+                if (wide && ch >= 2) {
+                    // Second 32-token block from the compact operand: lane l < 32
+                    // holds A row 32 + l, lane 32 + l holds P row 32 + l; P rows
+                    // 0..31 are zero in these columns (s >= 32 > r).
+                    if (ln < 32) {
+                        const int r = 32 + ln;
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            const int s = 16 * ch + c;
+                            AM[r * AP + s] = (s < r) ? v[c] * BETA[s] : 0.f;
+                        }
+                    } else if (ln < 96 && !failed) {
+                        const int r = (ln < 64) ? ln : ln - 64;
+                        const bool zero = ln >= 64;
+#pragma unroll
+                        for (int c4 = 0; c4 < 4; ++c4) {
+                            float p[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int s = 16 * ch + 4 * c4 + e;
+                                p[e] = (!zero && s <= r) ? v[4 * c4 + e] * BETA[s] : 0.f;
+                            }
+                            stg4(blob + BLOB_TP + OpTP::off(64 + r, 16 * ch + 4 * c4), p[0], p[1],
+                                 p[2], p[3]);
+                        }
+                    }
+                } else if (ln < 64) {
                     const int r = ln;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
@@ -669,14 +733,14 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
     }
 }
 
-__global__ void __launch_bounds__(NT, 1)
+__global__ void __launch_bounds__(NTS, 1)
 scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
             float* __restrict__ o, int t, int t_pad, int heads, const int* __restrict__ cu,
             int n_seqs, const unsigned char* __restrict__ ws) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column half
+    const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column group of SC
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
     int start, end;
@@ -717,10 +781,10 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     uint32_t ph_mma = 0;
 
     // state slice: thread (key ln, half ch) owns S[ln][16 ch .. 16 ch + 15]
-    float* Sg = state + ((size_t)n * heads + h) * D * D + (size_t)ln * D + slice * DV + ch * 16;
-    float sreg[16];
+    float* Sg = state + ((size_t)n * heads + h) * D * D + (size_t)ln * D + slice * DV + ch * SC;
+    float sreg[SC];
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < SC / 4; ++q4) {
         const float4 v4 = *reinterpret_cast<const float4*>(Sg + 4 * q4);
         sreg[4 * q4] = v4.x;
         sreg[4 * q4 + 1] = v4.y;
@@ -728,8 +792,8 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         sreg[4 * q4 + 3] = v4.w;
     }
 #pragma unroll
-    for (int jj = 0; jj < 16; ++jj)
-        *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(ch * 16 + jj, ln)) = tc::to_tf32(sreg[jj]);
+    for (int jj = 0; jj < SC; ++jj)
+        *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(ch * SC + jj, ln)) = tc::to_tf32(sreg[jj]);
 
     auto wait_mma = [&]() {
         if (!tc::mbar_wait(bar_mma, ph_mma)) {
@@ -778,18 +842,18 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
 
     // O = Qtil S + P U of a chunk is written while the next chunk's first
     // product runs: it is off the state's dependency chain.
-    float qs[16];
+    float qs[SC];
     int o_c0 = -1, o_L = 0;  // the chunk whose O is still to be written
     auto write_o = [&]() {
         if (ln >= 64) {
-            float v[16];
-            tc::tmem_ld16(tmem + lane_base + TC_PU + 16 * ch, v);
+            float v[SC];
+            tc::tmem_ld(tmem + lane_base + TC_PU + SC * ch, v);
             tc::tmem_ld_wait();
             const int r = ln - 64;
             if (r < o_L) {
-                float* orow = o + ((size_t)(o_c0 + r) * heads + h) * D + slice * DV + 16 * ch;
+                float* orow = o + ((size_t)(o_c0 + r) * heads + h) * D + slice * DV + SC * ch;
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
+                for (int q4 = 0; q4 < SC / 4; ++q4)
                     *reinterpret_cast<float4*>(orow + 4 * q4) =
                         make_float4(qs[4 * q4] + v[4 * q4], qs[4 * q4 + 1] + v[4 * q4 + 1],
                                     qs[4 * q4 + 2] + v[4 * q4 + 2], qs[4 * q4 + 3] + v[4 * q4 + 3]);
@@ -816,24 +880,31 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         if (o_c0 >= 0) write_o();  // the previous chunk's output
         wait_mma();
         {
-            float v[16];
-            tc::tmem_ld16(tmem + lane_base + TC_Y + 16 * ch, v);
+            float v[SC];
+            tc::tmem_ld(tmem + lane_base + TC_Y + SC * ch, v);
             tc::tmem_ld_wait();
             if (ln < 64) {
                 const int r = ln, sw = (r >> 1) & 3;
                 const unsigned char* vrow = reinterpret_cast<const unsigned char*>(RAWV) + r * 64;
-                const uint4 va = *reinterpret_cast<const uint4*>(vrow + (((2 * ch) ^ sw) << 4));
-                const uint4 vb = *reinterpret_cast<const uint4*>(vrow + (((2 * ch + 1) ^ sw) << 4));
-                const uint32_t w[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+                uint32_t w[SC / 2];  // SC BF16 values: SC / 8 chunks of 16 bytes
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) {
+                for (int q = 0; q < SC / 8; ++q) {
+                    const uint4 vq = *reinterpret_cast<const uint4*>(
+                        vrow + ((((SC / 8) * ch + q) ^ sw) << 4));
+                    w[4 * q] = vq.x;
+                    w[4 * q + 1] = vq.y;
+                    w[4 * q + 2] = vq.z;
+                    w[4 * q + 3] = vq.w;
+                }
+#pragma unroll
+                for (int jj = 0; jj < SC; ++jj) {
                     const uint32_t bits = (jj & 1) ? (w[jj >> 1] & 0xffff0000u) : (w[jj >> 1] << 16);
                     const float x = (r < L) ? __uint_as_float(bits) - v[jj] : 0.f;
-                    *reinterpret_cast<float*>(sm + SS_XV + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(x);
+                    *reinterpret_cast<float*>(sm + SS_XV + OpXV::off(SC * ch + jj, r)) = tc::to_tf32(x);
                 }
             } else {
 #pragma unroll
-                for (int jj = 0; jj < 16; ++jj) qs[jj] = v[jj];
+                for (int jj = 0; jj < SC; ++jj) qs[jj] = v[jj];
             }
         }
         sync_for_mma();
@@ -853,14 +924,14 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         }
         wait_mma();
         if (ln < 64) {
-            float v[16];
-            tc::tmem_ld16(tmem + lane_base + TC_U + 16 * ch, v);
+            float v[SC];
+            tc::tmem_ld(tmem + lane_base + TC_U + SC * ch, v);
             tc::tmem_ld_wait();
             const int r = ln;
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
+            for (int jj = 0; jj < SC; ++jj) {
                 const float u = (r < L) ? v[jj] : 0.f;
-                *reinterpret_cast<float*>(sm + SS_U + OpXV::off(16 * ch + jj, r)) = tc::to_tf32(u);
+                *reinterpret_cast<float*>(sm + SS_U + OpXV::off(SC * ch + jj, r)) = tc::to_tf32(u);
             }
         }
         sync_for_mma();
@@ -878,13 +949,13 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
             ++pending;
         }
         {   // S <- dec (.) S + Khat^T U
-            float v[16];
-            tc::tmem_ld16(tmem + lane_base + TC_E + 16 * ch, v);
+            float v[SC];
+            tc::tmem_ld(tmem + lane_base + TC_E + SC * ch, v);
             tc::tmem_ld_wait();
 #pragma unroll
-            for (int jj = 0; jj < 16; ++jj) {
+            for (int jj = 0; jj < SC; ++jj) {
                 sreg[jj] = __fmaf_rn(dk, sreg[jj], v[jj]);
-                *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(16 * ch + jj, ln)) = tc::to_tf32(sreg[jj]);
+                *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(SC * ch + jj, ln)) = tc::to_tf32(sreg[jj]);
             }
         }
         o_c0 = c0;
@@ -902,7 +973,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
 
     if (!aborted) {
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
+        for (int q4 = 0; q4 < SC / 4; ++q4)
             *reinterpret_cast<float4*>(Sg + 4 * q4) =
                 make_float4(sreg[4 * q4], sreg[4 * q4 + 1], sreg[4 * q4 + 2], sreg[4 * q4 + 3]);
     }
@@ -1006,7 +1077,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         maps, (const uint16_t*)beta, t, t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;
-    scan_kernel<<<dim3(D / DV, heads, n_seqs), NT, SS_TOTAL, s>>>(vmap, state, o, t, t_pad, heads,
+    scan_kernel<<<dim3(D / DV, heads, n_seqs), NTS, SS_TOTAL, s>>>(vmap, state, o, t, t_pad, heads,
                                                                   cu, n_seqs, ws);
     return launch_result("kda_prefill (scan)");
 }
