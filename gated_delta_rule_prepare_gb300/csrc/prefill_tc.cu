@@ -392,37 +392,37 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             float* GH = reinterpret_cast<float*>(sm + (b ^ 1) * RAW_BUF);  // [3][128]
             {
                 const int i = tid & 127, qt = tid >> 7;
-                float acc = 0.f, gmin = 0.f;
-#pragma unroll 8
+                float acc[16];
+                float run = 0.f, gmin = 0.f;
+#pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
                     const int r = 16 * qt + rr;
                     const float gv = (r < L) ? raw1(RAWG, r, i) : 0.f;
                     gmin = fminf(gmin, gv);
-                    acc = __fadd_rn(acc, gv);
-                    GAM[r * KP + i] = acc;
+                    run = __fadd_rn(run, gv);
+                    acc[rr] = run;
                 }
-                if (qt < 3) GH[qt * 128 + i] = acc;
+                if (qt < 3) GH[qt * 128 + i] = run;
                 wide = __syncthreads_and(gmin >= -kWideGMin);  // false on NaN too
-            }
-            if (tid >= 128) {
-                const int i = tid & 127, qt = tid >> 7;
-                float base = GH[i];
+                // the g tile is dead from here on: its end takes the reference rows
+                float base = 0.f;
+                if (qt > 0) base = GH[i];
                 if (qt > 1) base = __fadd_rn(base, GH[128 + i]);
                 if (qt > 2) base = __fadd_rn(base, GH[256 + i]);
-#pragma unroll 8
-                for (int rr = 0; rr < 16; ++rr) GAM[(16 * qt + rr) * KP + i] += base;
+#pragma unroll
+                for (int rr = 0; rr < 16; ++rr) {
+                    const float gr = (qt > 0) ? __fadd_rn(acc[rr], base) : acc[rr];
+                    GAM[(16 * qt + rr) * KP + i] = gr;
+                    if (rr == 8) GMID[qt * 128 + i] = gr;              // rows 8, 24, 40, 56
+                    if (rr == 1 && qt == 1) GMID[4 * 128 + i] = gr;    // row 17
+                    if (rr == 1 && qt == 3) GMID[5 * 128 + i] = gr;    // row 49
+                    if (rr == 15 && qt == 3) {                         // row 63
+                        GLAST[i] = gr;
+                        if (!failed) reinterpret_cast<float*>(blob + BLOB_DEC)[i] = __expf(gr);
+                    }
+                }
             }
             if (tid == 0) tc::bulk_wait_read_all();  // the last item's operands left OPX and Y
-            __syncthreads();  // the g tile is dead from here on
-            if (tid < 128) {
-#pragma unroll
-                for (int a = 0; a < 4; ++a) GMID[a * 128 + tid] = GAM[(16 * a + 8) * KP + tid];
-                GMID[4 * 128 + tid] = GAM[17 * KP + tid];
-                GMID[5 * 128 + tid] = GAM[49 * KP + tid];
-                const float gl = GAM[63 * KP + tid];
-                GLAST[tid] = gl;
-                if (!failed) reinterpret_cast<float*>(blob + BLOB_DEC)[tid] = __expf(gl);
-            }
             __syncthreads();
 
             // ------------------------------------------------------ P2 A and P blocks

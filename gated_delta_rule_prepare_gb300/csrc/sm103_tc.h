@@ -35,15 +35,15 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
            ((uint32_t)(M >> 4) << 24);
 }
 
-// Round an FP32 value to TF32 (10 explicit mantissa bits), to nearest with
-// ties away from zero: add half of the dropped 13-bit field to the magnitude
-// bits, then clear the field.  A carry out of the mantissa bumps the exponent
-// (the correct rounded value); infinities and the NaNs arithmetic produces
-// keep their class (a NaN whose payload lies only in the 13 dropped bits
-// would become an infinity; BF16-derived and computed NaNs never do).  Two
-// full-rate integer operations instead of a conversion instruction.
+// Round an FP32 value for use as a kind::tf32 MMA operand, to nearest with
+// ties away from zero: add half of the 13 low mantissa bits' range.  The
+// tensor core truncates those 13 bits of its FP32 operands (checked on
+// GB300: 1 + 2^-11 + 2^-13 enters a product as 1), so after the addition the
+// value it uses is the correctly rounded TF32 number; a carry out of the
+// mantissa bumps the exponent as it should.  One integer operation; the
+// result is only ever consumed by the tensor core.
 __device__ __forceinline__ float to_tf32(float x) {
-    return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+    return __uint_as_float(__float_as_uint(x) + 0x1000u);
 }
 
 // ---------------------------------------------------------------- mbarrier
