@@ -87,6 +87,8 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
                     const uint16_t* __restrict__ w, uint16_t* __restrict__ out, int total,
                     int t_per_seq, const int* __restrict__ cu, int n_seqs, int heads,
                     float l2_eps) {
+    pdl_wait();
+    pdl_release();
     const int lane = threadIdx.x & 31;
     const int c = blockIdx.x * kCtaCh + kCh * threadIdx.x;  // first of this thread's 8 channels
     const size_t conv_dim = (size_t)3 * heads * D;
@@ -228,6 +230,8 @@ template <int K>
 __global__ void conv_state_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
                                   int total, int t_per_seq, const int* __restrict__ cu,
                                   int n_seqs, int heads) {
+    pdl_wait();  // the conv kernel has read the old state
+    pdl_release();
     const size_t conv_dim = (size_t)3 * heads * D;
     const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (idx >= (size_t)n_seqs * conv_dim) return;
@@ -268,14 +272,13 @@ kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint1
                   int total, int t_per_seq, const int* cu, int n_seqs, int heads, float eps,
                   cudaStream_t s) {
     dim3 grid((unsigned)((3 * heads * D + kCtaCh - 1) / kCtaCh), (total + kTok - 1) / kTok);
-    conv_silu_l2_kernel<K><<<grid, kThreads, 0, s>>>(conv_state, x, w, out, total, t_per_seq,
-                                                      cu, n_seqs, heads, eps);
+    launch_pdl(conv_silu_l2_kernel<K>, grid, dim3(kThreads), 0, s, conv_state, x, w, out, total,
+               t_per_seq, cu, n_seqs, heads, eps);
     kda_status st = launch_result("kda_conv_silu_l2 (conv)");
     if (st != KDA_OK) return st;
     const size_t rows = (size_t)n_seqs * 3 * heads * D;
-    conv_state_kernel<K><<<(unsigned)((rows + 255) / 256), 256, 0, s>>>(conv_state, x, total,
-                                                                        t_per_seq, cu, n_seqs,
-                                                                        heads);
+    launch_pdl(conv_state_kernel<K>, dim3((unsigned)((rows + 255) / 256)), dim3(256), 0, s,
+               conv_state, x, total, t_per_seq, cu, n_seqs, heads);
     return launch_result("kda_conv_silu_l2 (state)");
 }
 

@@ -116,6 +116,11 @@ __device__ __forceinline__ void token_step(float4 (&s)[kRows], TokenSmem& sm,
     }
 }
 
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_release();
+}
+
 __device__ __forceinline__ void load_state(float4 (&s)[kRows], const float* __restrict__ S) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
@@ -136,6 +141,7 @@ decode_kernel(float* __restrict__ state, const float* __restrict__ q,
               const float* __restrict__ g, const float* __restrict__ beta,
               float* __restrict__ o) {
     __shared__ TokenSmem sm;
+    pdl_enter();
     const size_t nh = blockIdx.x;  // n * heads + h
     float* S = state + nh * (size_t)(D * D);
     float4 s[kRows];
@@ -156,6 +162,7 @@ decode_k_kernel(float* __restrict__ state, const float* __restrict__ q,
                 const float* __restrict__ g, const float* __restrict__ beta,
                 float* __restrict__ o, int heads, int krows, SnapList snaps, int n_snap) {
     __shared__ TokenSmem sm;
+    pdl_enter();
     const size_t nh = blockIdx.x;
     const size_t n = nh / heads, h = nh % heads;
     float* S = state + nh * (size_t)(D * D);
@@ -200,7 +207,8 @@ extern "C" kda_status kda_decode(float* state, const float* q, const float* k, c
     kda_status st = check_common("kda_decode", state, q, k, v, g, beta, o, n_seqs, heads,
                                  head_dim);
     if (st != KDA_OK) return st;
-    decode_kernel<<<n_seqs * heads, kThreads, 0, as_stream(stream)>>>(state, q, k, v, g, beta, o);
+    launch_pdl(decode_kernel, dim3(n_seqs * heads), dim3(kThreads), 0, as_stream(stream), state,
+               q, k, v, g, beta, o);
     return launch_result("kda_decode");
 }
 
@@ -225,7 +233,7 @@ extern "C" kda_status kda_decode_k(float* state, const float* q, const float* k,
                     "kda_decode_k: snapshot %d aliases the state", t);
         sl.p[t] = snapshots[t];
     }
-    decode_k_kernel<<<n_seqs * heads, kThreads, 0, as_stream(stream)>>>(
-        state, q, k, v, g, beta, o, heads, krows, sl, n_snap);
+    launch_pdl(decode_k_kernel, dim3(n_seqs * heads), dim3(kThreads), 0, as_stream(stream),
+               state, q, k, v, g, beta, o, heads, krows, sl, n_snap);
     return launch_result("kda_decode_k");
 }

@@ -49,6 +49,32 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
                              int heads, long long stride, const int* cu, int n_seqs,
                              void* workspace, cudaStream_t s);
 
+// Programmatic dependent launch.  Kernels launched with launch_pdl() may be
+// scheduled while the previous kernel on the stream drains: pdl_wait() blocks
+// until that kernel has finished and its writes are visible (call it before
+// the first global access that may depend on it), pdl_release() lets the
+// next such launch begin scheduling.  Without the attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 #define KDA_REQUIRE(cond, code, ...)      \
     do {                                  \
         if (!(cond)) {                    \

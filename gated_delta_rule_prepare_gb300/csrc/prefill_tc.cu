@@ -187,6 +187,8 @@ constexpr int MAP_THREADS = 1024;
 __global__ void __launch_bounds__(MAP_THREADS)
 chunk_map_kernel(const int* __restrict__ cu, int n_seqs, int t, int* __restrict__ chunk_off) {
     __shared__ int part[MAP_THREADS];
+    pdl_wait();
+    pdl_release();
     const int per = (n_seqs + MAP_THREADS - 1) / MAP_THREADS;
     const int lo = threadIdx.x * per, hi = min(n_seqs, lo + per);
     int sum = 0;
@@ -275,6 +277,8 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column quarter
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
+    pdl_wait();  // the chunk map (and the callers' inputs) are complete
+    pdl_release();
     const int* chunk_off = reinterpret_cast<const int*>(ws);
     const long long items = (long long)__ldg(chunk_off + n_seqs) * heads;
     if ((long long)blockIdx.x >= items) return;
@@ -743,6 +747,8 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column group of SC
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
+    pdl_wait();  // the prepared operands (and the callers' state) are complete
+    pdl_release();
     int start, end;
     if (!seq_range(cu, n, n_seqs, t, t_pad, start, end)) {
         if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
@@ -1061,7 +1067,8 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         return KDA_ERR_CUDA;
     }
     unsigned char* ws = static_cast<unsigned char*>(workspace);
-    chunk_map_kernel<<<1, MAP_THREADS, 0, s>>>(cu, n_seqs, cu ? 0 : t, reinterpret_cast<int*>(ws));
+    launch_pdl(chunk_map_kernel, dim3(1), dim3(MAP_THREADS), 0, s, cu, n_seqs, cu ? 0 : t,
+               reinterpret_cast<int*>(ws));
     kda_status st = launch_result("kda_prefill (chunk map)");
     if (st != KDA_OK) return st;
     // Persistent prepare: one CTA per SM (shared memory allows no more),
@@ -1073,12 +1080,12 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         return KDA_ERR_CUDA;
     }
     const unsigned grid = (unsigned)(items < sms ? items : sms);
-    prepare_kernel<<<grid, NTP, PS_TOTAL, s>>>(
-        maps, (const uint16_t*)beta, t, t_pad, heads, cu, n_seqs, ws);
+    launch_pdl(prepare_kernel, dim3(grid), dim3(NTP), PS_TOTAL, s, maps, (const uint16_t*)beta, t,
+               t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;
-    scan_kernel<<<dim3(D / DV, heads, n_seqs), NTS, SS_TOTAL, s>>>(vmap, state, o, t, t_pad, heads,
-                                                                  cu, n_seqs, ws);
+    launch_pdl(scan_kernel, dim3(D / DV, heads, n_seqs), dim3(NTS), SS_TOTAL, s, vmap, state, o,
+               t, t_pad, heads, cu, n_seqs, (const unsigned char*)ws);
     return launch_result("kda_prefill (scan)");
 }
 
