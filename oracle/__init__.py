@@ -46,6 +46,9 @@ def lib():
         L.kda_oracle_conv_silu_l2.restype = None
         L.kda_oracle_conv_silu_l2.argtypes = ([ctypes.c_int, _ip] + [ctypes.c_int] * 3
                                               + [ctypes.c_double] + [_dp] * 4)
+        L.kda_oracle_o_norm_gated.restype = None
+        L.kda_oracle_o_norm_gated.argtypes = ([ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_double] + [_dp] * 4)
         _LIB = L
     return _LIB
 
@@ -161,3 +164,15 @@ def conv_silu_l2(x, w, conv_state, cu_seqlens, heads, head_dim=128, l2_eps=1e-6)
     lib().kda_oracle_conv_silu_l2(N, cu.ctypes.data_as(_ip), heads, head_dim, K,
                                   float(l2_eps), _p(x), _p(w), _p(st), _p(out))
     return out, st
+
+
+def o_norm_gated(core, gate, w, eps=1e-6):
+    """Sigmoid-gated RMSNorm: core [rows, H, D] (pre-norm core output), gate
+    [rows, H*D] or [rows, H, D], w [D]; returns out [rows, H, D] (FP64)."""
+    core, gate, w = f64(core), f64(gate), f64(w)
+    rows, H, D = core.shape
+    gate = np.ascontiguousarray(gate.reshape(rows, H, D))
+    assert w.shape == (D,)
+    out = np.zeros_like(core)
+    lib().kda_oracle_o_norm_gated(rows, H, D, float(eps), _p(core), _p(gate), _p(w), _p(out))
+    return out

@@ -281,3 +281,27 @@ void kda_oracle_conv_silu_l2(int N, const int* cu_seqlens, int H, int D, int K, 
         free(y);
     }
 }
+
+/*
+ * Sigmoid-gated RMSNorm of the core output (module index, block pipeline:
+ * "sigmoid-gated RMSNorm(o_norm, g_b(g_a(h)))"; Glm5NextKdaWorkspace: core
+ * [T, heads, head_dim] FP32 pre-norm, out_gate [T, qkv], o_norm_out [T, qkv];
+ * config.rs: o_norm [head_dim], rms_norm_eps read by o_norm).  The pages fix
+ * the inputs, not the formula; the reading taken here: per token and head,
+ *     out[j] = core[j] / sqrt(mean_j core[j]^2 + eps) * w[j] * sigmoid(gate[j])
+ * with the norm over the head's D channels and w shared by all heads.
+ */
+void kda_oracle_o_norm_gated(long rows, int H, int D, double eps, const double* core,
+                             const double* gate, const double* w, double* out) {
+#pragma omp parallel for schedule(static)
+    for (long rh = 0; rh < rows * H; ++rh) {
+        const double* y = core + (size_t)rh * D;
+        double ss = 0.0;
+        for (int d = 0; d < D; ++d) ss += y[d] * y[d];
+        const double r = 1.0 / sqrt(ss / D + eps);
+        for (int d = 0; d < D; ++d) {
+            const double gt = gate[(size_t)rh * D + d];
+            out[(size_t)rh * D + d] = y[d] * r * w[d] * (1.0 / (1.0 + exp(-gt)));
+        }
+    }
+}

@@ -356,6 +356,70 @@ def test_conv_streaming_equals_prefill(orc):
     np.testing.assert_array_equal(s, st_end)
 
 
+# ------------------------------------------------------------ gated RMSNorm
+
+def _onorm_inputs(r, rows, H, D):
+    core = r.standard_normal((rows, H, D)) * 3.0
+    gate = r.standard_normal((rows, H * D))
+    w = r.standard_normal(D)
+    return core, gate, w
+
+
+def test_o_norm_unit_rms_when_gate_open(orc):
+    """w = 1, sigmoid(gate) = 1, eps = 0: every (token, head) comes out with
+    mean square exactly 1 -- the norm runs over the head's channels."""
+    r = rng(31)
+    core, _, _ = _onorm_inputs(r, 5, 3, 16)
+    out = orc.o_norm_gated(core, np.full((5, 48), 60.0), np.ones(16), eps=0.0)
+    np.testing.assert_allclose((out * out).mean(-1), 1.0, rtol=1e-12)
+
+
+def test_o_norm_scale_invariant_and_odd(orc):
+    r = rng(32)
+    core, gate, w = _onorm_inputs(r, 4, 2, 8)
+    base = orc.o_norm_gated(core, gate, w, eps=0.0)
+    np.testing.assert_allclose(orc.o_norm_gated(core * 7.5, gate, w, eps=0.0), base, rtol=1e-12)
+    np.testing.assert_allclose(orc.o_norm_gated(-core, gate, w, eps=0.0), -base, rtol=1e-12)
+
+
+def test_o_norm_gate_is_a_sigmoid(orc):
+    """gate 0 halves the open-gate output; gate -g scales by 1 - sigmoid(g)."""
+    r = rng(33)
+    core, gate, w = _onorm_inputs(r, 3, 2, 8)
+    open_ = orc.o_norm_gated(core, np.full(gate.shape, 60.0), w)
+    np.testing.assert_allclose(orc.o_norm_gated(core, np.zeros(gate.shape), w), 0.5 * open_,
+                               rtol=1e-12)
+    pos = orc.o_norm_gated(core, gate, w)
+    neg = orc.o_norm_gated(core, -gate, w)
+    np.testing.assert_allclose(pos + neg, open_, rtol=1e-12, atol=1e-15)
+
+
+def test_o_norm_weight_per_channel(orc):
+    r = rng(34)
+    core, gate, w = _onorm_inputs(r, 3, 4, 8)
+    one = orc.o_norm_gated(core, gate, np.ones(8))
+    np.testing.assert_allclose(orc.o_norm_gated(core, gate, w), one * w, rtol=1e-12)
+
+
+def test_o_norm_eps_closed_form(orc):
+    """A head whose channels all equal a: out = a / sqrt(a^2 + eps)."""
+    a, eps = 0.01, 1e-4
+    core = np.full((1, 1, 16), a)
+    out = orc.o_norm_gated(core, np.full((1, 16), 60.0), np.ones(16), eps=eps)
+    np.testing.assert_allclose(out, a / math.sqrt(a * a + eps), rtol=1e-12)
+
+
+def test_o_norm_heads_and_rows_independent(orc):
+    r = rng(35)
+    core, gate, w = _onorm_inputs(r, 4, 3, 8)
+    out = orc.o_norm_gated(core, gate, w)
+    perm = [2, 0, 1]
+    g3 = gate.reshape(4, 3, 8)
+    out_p = orc.o_norm_gated(core[:, perm], g3[:, perm].reshape(4, 24), w)
+    np.testing.assert_allclose(out_p, out[:, perm], rtol=1e-13)
+    np.testing.assert_allclose(orc.o_norm_gated(core[1:2], gate[1:2], w), out[1:2], rtol=1e-13)
+
+
 # ------------------------------------------------------------ input recipe
 
 def test_workload_inputs_follow_recipe():
