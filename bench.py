@@ -45,6 +45,7 @@ DECODE_BYTES = 2 * DECODE_N * H * D * D * 4 + 4 * DECODE_N * H * D * 4 + DECODE_
 DK_N, DK_K = 128, 4
 CONV_K = 4
 DK_BYTES = (2 + DK_K) * DK_N * H * D * D * 4 + 4 * DK_N * DK_K * H * D * 4 + DK_N * DK_K * H * 4
+ONORM_BYTES = T_PREFILL * 32 * 128 * (4 + 2 + 2) + 128 * 2  # core FP32, gate and out BF16, w
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor ratio of the part
 
 
@@ -230,7 +231,18 @@ def run_gpu(args):
 
         for _ in range(5):
             decode()
-        dec_per, _ = time_launches(decode, DECODE_STEPS, stream)
+        # The chain of 100 steps is the unit: one event pair around it, so the
+        # launches follow each other as in a serving loop; reported per step.
+        dec_per = []
+        for _ in range(3):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(DECODE_STEPS):
+                decode()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            dec_per.append(e0.elapsed_time(e1) / DECODE_STEPS)
+        dec_per = [statistics.median(dec_per)]
         del dq, dk, dv, dg, db, dS
 
         # ---------------- decode_k workload
@@ -247,6 +259,21 @@ def run_gpu(args):
             decode_k()
         dk_per, _ = time_launches(decode_k, 20, stream)
         del kS, snaps, kin
+
+        # ---------------- gated RMSNorm of a prefill-sized core output
+        ngen = torch.Generator(device="cpu").manual_seed(0)
+        n_core = torch.randn((T_PREFILL, H, D), generator=ngen).to(dev)
+        n_gate = torch.randn((T_PREFILL, H * D), generator=ngen).to(torch.bfloat16).to(dev)
+        n_w = torch.ones(D, dtype=torch.bfloat16, device=dev)
+        n_out = torch.empty((T_PREFILL, H * D), dtype=torch.bfloat16, device=dev)
+
+        def o_norm():
+            K.kda_o_norm_gated(n_core, n_gate, n_w, n_out)
+
+        for _ in range(3):
+            o_norm()
+        on_per, _ = time_launches(o_norm, 20, stream)
+        del n_core, n_gate, n_out
 
         # ---------------- front end + core: 16 packed sequences, conv then prefill
         fe = wl.frontend()
@@ -369,6 +396,13 @@ def run_gpu(args):
             "workload": wl.DECODE_K.name, "value": DK_BYTES / dk_s / 1e9, "unit": "GB/s",
             "frac_of_hbm_peak": DK_BYTES / dk_s / 1e9 / pk["hbm_gbs"],
             "us_per_call": dk_s * 1e6, "algorithmic_bytes": DK_BYTES,
+        },
+        "o_norm": {
+            "workload": "sigmoid-gated RMSNorm of a prefill-sized core output (8192 x 32 x 128)",
+            "value": ONORM_BYTES / (statistics.mean(on_per) / 1e3) / 1e9, "unit": "GB/s",
+            "frac_of_hbm_peak": ONORM_BYTES / (statistics.mean(on_per) / 1e3) / 1e9
+            / pk["hbm_gbs"],
+            "us_per_call": statistics.mean(on_per) * 1e3, "algorithmic_bytes": ONORM_BYTES,
         },
         "conv": {
             "workload": wl.FRONTEND.name + " (conv + SiLU + L2 stage)",

@@ -7,8 +7,8 @@ library's CUDA kernels; there is no fallback.  Importing this package on a
 machine without the built library raises immediately.
 
 Entry points (same names as the C ABI): ``kda_decode``, ``kda_decode_k``,
-``kda_prefill``, ``kda_conv_silu_l2``, ``kda_prefill_workspace_size``,
-``kda_sync_status``.
+``kda_prefill``, ``kda_conv_silu_l2``, ``kda_o_norm_gated``,
+``kda_prefill_workspace_size``, ``kda_sync_status``.
 """
 
 from __future__ import annotations
@@ -46,6 +46,7 @@ def _load():
         "kda_prefill": [_vp] * 7 + [_i, _i, _i, _f, _i, _i, _i, _i64, _vp, _i, _vp, _sz, _u64],
         "kda_conv_silu_l2": [_vp] * 4 + [_i, _i, _vp, _i, _f, _i, _i, _u64],
         "kda_sync_status": [_u64],
+        "kda_o_norm_gated": [_vp] * 4 + [_i64, _i, _i, _f, _u64],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -219,6 +220,23 @@ def kda_conv_silu_l2(conv_state, x, w, out, cu_seqlens=None, n_seqs=None, l2_eps
     _check(LIB.kda_conv_silu_l2(_ptr(conv_state, torch.float32, "conv_state"), _ptr(x), _ptr(w),
                                 _ptr(out), t, N, _ptr(cu_seqlens), K, float(l2_eps), H,
                                 HEAD_DIM, _stream(x)))
+
+
+def kda_o_norm_gated(core, gate, w, out, eps=1e-6):
+    """Sigmoid-gated RMSNorm: core FP32 [rows, H, 128] (or [rows, H*128]),
+    gate and out BF16 [rows, H*128], w BF16 [128]."""
+    for n_, t_ in (("core", core), ("gate", gate), ("w", w), ("out", out)):
+        _contig(t_, n_)
+    rows = core.shape[0]
+    hd = core.numel() // max(rows, 1) if rows else gate.shape[-1]
+    if hd % HEAD_DIM or gate.numel() != core.numel() or out.numel() != core.numel():
+        raise ValueError("kda_o_norm_gated: core, gate and out must hold rows x H x 128 values")
+    if w.numel() != HEAD_DIM:
+        raise ValueError("kda_o_norm_gated: w must hold 128 values")
+    b16 = torch.bfloat16
+    _check(LIB.kda_o_norm_gated(_ptr(core, torch.float32, "core"), _ptr(gate, b16, "gate"),
+                                _ptr(w, b16, "w"), _ptr(out, b16, "out"), int(rows),
+                                hd // HEAD_DIM, HEAD_DIM, float(eps), _stream(core)))
 
 
 def kda_sync_status(device=None):

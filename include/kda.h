@@ -178,6 +178,29 @@ kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, const uint16_t
                             int conv_kernel, float l2_eps, int heads, int head_dim,
                             uint64_t stream);
 
+/*
+ * kda_o_norm_gated -- sigmoid-gated RMSNorm of the core output, the block
+ * pipeline's step after the core ("sigmoid-gated RMSNorm(o_norm,
+ * g_b(g_a(h)))", glm5next_kda module index; Glm5NextKdaWorkspace core,
+ * out_gate and o_norm_out; config.rs o_norm [head_dim] BF16, rms_norm_eps).
+ * Per token row and head, over the head's 128 channels j:
+ *     out[j] = core[j] / sqrt(mean_j core[j]^2 + eps) * w[j] * sigmoid(gate[j])
+ * computed in FP32, rounded once to BF16 (the pages fix the inputs and the
+ * sigmoid gate; the exact composition is this library's reading).
+ *
+ *   core : FP32 [rows][heads][128], e.g. kda_prefill's o or kda_decode's o
+ *          (16-byte aligned)
+ *   gate : BF16 [rows][heads * 128], the output-gate projection (8-byte aligned)
+ *   w    : BF16 [128], shared by all heads (8-byte aligned)
+ *   out  : BF16 [rows][heads * 128] (8-byte aligned); may not alias core
+ *   rows >= 0 (0 launches nothing and the pointers may then be NULL),
+ *   heads >= 1, head_dim == 128, eps >= 0.
+ * One kernel is enqueued on `stream`.
+ */
+kda_status kda_o_norm_gated(const float* core, const uint16_t* gate, const uint16_t* w,
+                            uint16_t* out, int64_t rows, int heads, int head_dim, float eps,
+                            uint64_t stream);
+
 /* Size of the library-owned device array kda_prefill_static_ws uses as its
  * workspace: 64 MiB on every GPU that loads the library, held until exit. */
 #define KDA_STATIC_WORKSPACE_BYTES (64u << 20)

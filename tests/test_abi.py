@@ -132,3 +132,16 @@ def test_prefill_refuses_a_small_workspace(lib):
     f.argtypes = [V] * 7 + [I, I, I, F, I, I, I, ctypes.c_int64, V, I, V, SZ, U64]
     assert f(P, P, P, P, P, P, P, 128, 128, 64, 0.0, 2, 128, 1, 256, None, 1, P, 64, 0) == 3
     assert b"workspace" in lib.kda_last_error()
+
+
+def test_o_norm_refuses_bad_arguments(lib):
+    f = lib.kda_o_norm_gated
+    f.argtypes = [V] * 4 + [ctypes.c_int64, I, I, F, U64]
+    assert f(None, P, P, P, 4, 2, 128, 1e-6, 0) == 1
+    assert f(None, None, None, None, 0, 2, 128, 1e-6, 0) == 0  # zero rows: nothing to touch
+    assert f(P, P, P, P, 4, 2, 64, 1e-6, 0) == 2       # head_dim
+    assert f(P, P, P, P, -1, 2, 128, 1e-6, 0) == 1     # rows
+    assert f(P, P, P, P, 4, 0, 128, 1e-6, 0) == 1      # heads
+    assert f(P, P, P, P, 4, 2, 128, -1.0, 0) == 1      # eps
+    assert f(ctypes.c_void_p(P.value + 4), P, P, P, 4, 2, 128, 1e-6, 0) == 1  # core alignment
+    assert b"kda_o_norm_gated" in lib.kda_last_error()
