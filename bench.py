@@ -46,6 +46,8 @@ DK_N, DK_K = 128, 4
 CONV_K = 4
 DK_BYTES = (2 + DK_K) * DK_N * H * D * D * 4 + 4 * DK_N * DK_K * H * D * 4 + DK_N * DK_K * H * 4
 ONORM_BYTES = T_PREFILL * 32 * 128 * (4 + 2 + 2) + 128 * 2  # core FP32, gate and out BF16, w
+SHORT_T = 4
+SHORT_BYTES = 2 * DECODE_N * H * D * D * 4 + 5 * DECODE_N * SHORT_T * H * D * 4 + DECODE_N * SHORT_T * H * 4
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor ratio of the part
 
 
@@ -260,6 +262,29 @@ def run_gpu(args):
         dk_per, _ = time_launches(decode_k, 20, stream)
         del kS, snaps, kin
 
+        # ---------------- short FP32 prefill (t = 4): decode_k's row walk vs the
+        # SIMT chunk kernel it replaces (pinned through KDA_PREFILL_IMPL=simt)
+        sgen = torch.Generator(device="cpu").manual_seed(0)
+        sd = wl.core_inputs(sgen, (DECODE_N, SHORT_T), H, torch.float32)
+        s_in = {n: sd[n].to(dev) for n in ("q", "k", "v", "g", "beta")}
+        s_S = wl.state(sgen, (DECODE_N,), H, 0.02).to(dev)
+        s_o = torch.empty((DECODE_N, SHORT_T, H, D), device=dev)
+
+        def short_prefill():
+            K.kda_prefill(s_S, s_in["q"], s_in["k"], s_in["v"], s_in["g"], s_in["beta"], s_o,
+                          SHORT_T, 16)
+
+        short_us = {}
+        for mode in ("row_walk", "simt"):
+            if mode == "simt":
+                os.environ["KDA_PREFILL_IMPL"] = "simt"
+            for _ in range(3):
+                short_prefill()
+            per, _ = time_launches(short_prefill, 20, stream)
+            short_us[mode] = statistics.mean(per) * 1e3
+            os.environ.pop("KDA_PREFILL_IMPL", None)
+        del s_in, s_S, s_o
+
         # ---------------- gated RMSNorm of a prefill-sized core output
         ngen = torch.Generator(device="cpu").manual_seed(0)
         n_core = torch.randn((T_PREFILL, H, D), generator=ngen).to(dev)
@@ -396,6 +421,13 @@ def run_gpu(args):
             "workload": wl.DECODE_K.name, "value": DK_BYTES / dk_s / 1e9, "unit": "GB/s",
             "frac_of_hbm_peak": DK_BYTES / dk_s / 1e9 / pk["hbm_gbs"],
             "us_per_call": dk_s * 1e6, "algorithmic_bytes": DK_BYTES,
+        },
+        "short_prefill": {
+            "workload": "FP32 prefill, 64 sequences x 4 tokens x 32 heads (decode_k's row walk)",
+            "value": SHORT_BYTES / short_us["row_walk"] / 1e3, "unit": "GB/s",
+            "frac_of_hbm_peak": SHORT_BYTES / short_us["row_walk"] / 1e3 / pk["hbm_gbs"],
+            "us_per_call": short_us["row_walk"], "simt_chunk_kernel_us": short_us["simt"],
+            "algorithmic_bytes": SHORT_BYTES,
         },
         "o_norm": {
             "workload": "sigmoid-gated RMSNorm of a prefill-sized core output (8192 x 32 x 128)",

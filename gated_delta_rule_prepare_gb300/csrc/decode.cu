@@ -160,7 +160,8 @@ __global__ void __launch_bounds__(kThreads, 2)
 decode_k_kernel(float* __restrict__ state, const float* __restrict__ q,
                 const float* __restrict__ k, const float* __restrict__ v,
                 const float* __restrict__ g, const float* __restrict__ beta,
-                float* __restrict__ o, int heads, int krows, SnapList snaps, int n_snap) {
+                float* __restrict__ o, int heads, int krows, long long seq_rows, SnapList snaps,
+                int n_snap) {
     __shared__ TokenSmem sm;
     pdl_enter();
     const size_t nh = blockIdx.x;
@@ -169,7 +170,7 @@ decode_k_kernel(float* __restrict__ state, const float* __restrict__ q,
     float4 s[kRows];
     load_state(s, S);
     for (int t = 0; t < krows; ++t) {
-        const size_t row = (n * krows + t) * heads + h;
+        const size_t row = (n * (size_t)seq_rows + t) * heads + h;
         stage_token(sm, q + row * D, k + row * D, v + row * D, g + row * D, __ldg(beta + row));
         __syncthreads();
         token_step(s, sm, o + row * D);
@@ -197,6 +198,21 @@ kda_status check_common(const char* fn, float* state, const float* q, const floa
 }
 
 }  // namespace
+}  // namespace kda
+
+namespace kda {
+
+// The decode_k row walk over n_seqs sequences of krows consecutive token rows,
+// sequences seq_rows rows apart (arguments checked by the caller), no
+// snapshots: kda_prefill's route for short FP32 sequences.
+kda_status launch_row_walk(float* state, const float* q, const float* k, const float* v,
+                           const float* g, const float* beta, float* o, int n_seqs, int krows,
+                           long long seq_rows, int heads, cudaStream_t s) {
+    launch_pdl(decode_k_kernel, dim3(n_seqs * heads), dim3(kThreads), 0, s, state, q, k, v, g,
+               beta, o, heads, krows, seq_rows, SnapList{}, 0);
+    return launch_result("kda_prefill (row walk)");
+}
+
 }  // namespace kda
 
 using namespace kda;
@@ -234,6 +250,6 @@ extern "C" kda_status kda_decode_k(float* state, const float* q, const float* k,
         sl.p[t] = snapshots[t];
     }
     launch_pdl(decode_k_kernel, dim3(n_seqs * heads), dim3(kThreads), 0, as_stream(stream),
-               state, q, k, v, g, beta, o, heads, krows, sl, n_snap);
+               state, q, k, v, g, beta, o, heads, krows, (long long)krows, sl, n_snap);
     return launch_result("kda_decode_k");
 }

@@ -228,11 +228,16 @@ __global__ void pad_fill_kernel(TIn* q, TIn* k, TIn* v, TIn* g, TIn* beta, int t
     }
 }
 
+// True when the caller pins the SIMT chunk kernel (KDA_PREFILL_IMPL=simt,
+// for comparisons).
+bool simt_pinned() {
+    const char* impl = getenv("KDA_PREFILL_IMPL");
+    return impl && strcmp(impl, "simt") == 0;
+}
+
 // True when this call runs on the tensor-core kernels (which need a workspace).
 bool uses_tensor_cores(int chunk, int in_dtype) {
-    if (in_dtype != KDA_BF16 || chunk != 64) return false;
-    const char* impl = getenv("KDA_PREFILL_IMPL");
-    return !(impl && strcmp(impl, "simt") == 0);
+    return in_dtype == KDA_BF16 && chunk == 64 && !simt_pinned();
 }
 
 template <typename TIn>
@@ -251,6 +256,15 @@ kda_status launch(float* state, void* q, void* k, void* v, void* g, void* beta, 
                                                     fill);
         kda_status st = launch_result("kda_prefill (pad fill)");
         if (st != KDA_OK) return st;
+    }
+    // Short FP32 sequences (uniform form, heads packed in each token row) take
+    // decode_k's row walk, the pages' dispatch for pieces that do not take the
+    // chunked arm: one state read, t token steps in registers, one state write.
+    if constexpr (sizeof(TIn) == 4) {
+        if (!cu && t <= KDA_MAX_K && stride == (long long)heads * D && !simt_pinned())
+            return launch_row_walk(state, (const float*)q, (const float*)k, (const float*)v,
+                                   (const float*)g, (const float*)beta, o, n_seqs, t, t_pad,
+                                   heads, s);
     }
     // BF16 inputs with chunk 64 take the tensor-core kernels unless the caller
     // pins the SIMT kernel (KDA_PREFILL_IMPL=simt, for comparisons).

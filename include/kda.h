@@ -129,6 +129,12 @@ kda_status kda_decode_k(float* state, const float* q, const float* k, const floa
  *   o     : FP32 [rows][heads][128]; rows of padding are not written
  *   chunk : 16, 32 or 64 (the chunk width C; 128 is refused as unsupported)
  *   in_dtype : KDA_F32 or KDA_BF16 (applies to q, k, v, g, beta)
+ * Routing: FP32 inputs in the uniform form with t <= KDA_MAX_K and
+ * qkv_row_stride == heads*128 run decode_k's row walk (the pages' dispatch
+ * for pieces that do not take the chunked arm: state read once, t token steps,
+ * state written once); BF16 inputs with chunk 64 run the tensor-core prepare
+ * and scan kernels; everything else runs the FP32 SIMT chunk kernel.
+ *
  *   workspace : device scratch, 16-byte aligned, of at least
  *           kda_prefill_workspace_size(...) bytes (may be NULL when that
  *           size is 0).  Its contents on entry do not matter; calls that

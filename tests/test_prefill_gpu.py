@@ -220,3 +220,38 @@ def test_prefill_mixes_wide_and_narrow_decay_blocks(orc):
     o_ref, S_ref = orc.prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["state"][0])
     assert rel_err(o, o_ref) < TOL_PREFILL
     assert rel_err(S[0], S_ref) < TOL_PREFILL
+
+
+@pytest.mark.parametrize("t,t_pad", [(1, 1), (5, 8), (8, 8)])
+def test_short_fp32_prefill_takes_the_row_walk(orc, t, t_pad):
+    """FP32 sequences of t <= 8 tokens (uniform form) run decode_k's row walk:
+    oracle parity per sequence, padded rows ignored, and the same bits as an
+    explicit kda_decode_k over the same rows."""
+    from _util import TOL_DECODE
+    K = kda()
+    gen = torch.Generator().manual_seed(60 + t)
+    N, H = 3, 2
+    d = wl.core_inputs(gen, (N, t_pad), H, torch.float32)
+    S0 = wl.state(gen, (N,), H, 0.02)
+    dev = {}
+    for n in ("q", "k", "v", "g", "beta"):
+        x = d[n].clone()
+        x[:, t:] = float("nan")
+        dev[n] = x.cuda()
+    S = S0.clone().cuda()
+    o = torch.full((N, t_pad, H, 128), 12345.0, device="cuda")
+    K.kda_prefill(S, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], o, t, 16,
+                  pad_fill=0.0)
+    torch.cuda.synchronize()
+    assert torch.all(o[:, t:] == 12345.0)  # padding rows are not written
+    for n in range(N):
+        o_ref, S_ref = orc.prefill(d["q"][n, :t], d["k"][n, :t], d["v"][n, :t], d["g"][n, :t],
+                                   d["beta"][n, :t], S0[n])
+        assert rel_err(o[n, :t], o_ref) < TOL_DECODE
+        assert rel_err(S[n], S_ref) < TOL_DECODE
+    if t == t_pad:
+        S2 = S0.clone().cuda()
+        o2 = torch.empty_like(o)
+        K.kda_decode_k(S2, *(d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta")), o2)
+        torch.cuda.synchronize()
+        assert torch.equal(S2, S) and torch.equal(o2, o)
