@@ -48,6 +48,8 @@ DK_BYTES = (2 + DK_K) * DK_N * H * D * D * 4 + 4 * DK_N * DK_K * H * D * 4 + DK_
 ONORM_BYTES = T_PREFILL * 32 * 128 * (4 + 2 + 2) + 128 * 2  # core FP32, gate and out BF16, w
 SHORT_T = 4
 SHORT_BYTES = 2 * DECODE_N * H * D * D * 4 + 5 * DECODE_N * SHORT_T * H * D * 4 + DECODE_N * SHORT_T * H * 4
+CONVK_BYTES = (DK_N * DK_K * 3 * H * D * 2 * 2 + 3 * H * D * CONV_K * 2
+               + (2 + DK_K) * DK_N * 3 * H * D * CONV_K * 4)  # x, out, w, state R/W, snapshots
 TF32_OVER_BF16 = 1.1 / 2.25   # nominal dense TF32 : BF16 tensor ratio of the part
 
 
@@ -285,6 +287,22 @@ def run_gpu(args):
             os.environ.pop("KDA_PREFILL_IMPL", None)
         del s_in, s_S, s_o
 
+        # ---------------- k-row conv with snapshots (decode_k's front end)
+        cgen = torch.Generator(device="cpu").manual_seed(0)
+        ck_x = torch.randn((DK_N, DK_K, 3 * H * D), generator=cgen).to(torch.bfloat16).to(dev)
+        ck_w = (torch.randn((3 * H * D, CONV_K), generator=cgen) * 0.5).to(torch.bfloat16).to(dev)
+        ck_st = torch.zeros((DK_N, 3 * H * D, CONV_K), device=dev)
+        ck_o = torch.empty_like(ck_x)
+        ck_snaps = [torch.empty_like(ck_st) for _ in range(DK_K)]
+
+        def conv_k():
+            K.kda_conv_silu_l2_k(ck_st, ck_x, ck_w, ck_o, ck_snaps)
+
+        for _ in range(3):
+            conv_k()
+        ck_per, _ = time_launches(conv_k, 20, stream)
+        del ck_x, ck_st, ck_o, ck_snaps
+
         # ---------------- gated RMSNorm of a prefill-sized core output
         ngen = torch.Generator(device="cpu").manual_seed(0)
         n_core = torch.randn((T_PREFILL, H, D), generator=ngen).to(dev)
@@ -428,6 +446,14 @@ def run_gpu(args):
             "frac_of_hbm_peak": SHORT_BYTES / short_us["row_walk"] / 1e3 / pk["hbm_gbs"],
             "us_per_call": short_us["row_walk"], "simt_chunk_kernel_us": short_us["simt"],
             "algorithmic_bytes": SHORT_BYTES,
+        },
+        "conv_k": {
+            "workload": "k-row conv + SiLU + L2, 128 sequences x 4 rows x 12288 channels, 4 snapshots",
+            "value": CONVK_BYTES / (statistics.mean(ck_per) / 1e3) / 1e9, "unit": "GB/s",
+            "frac_of_hbm_peak": CONVK_BYTES / (statistics.mean(ck_per) / 1e3) / 1e9
+            / pk["hbm_gbs"],
+            "us_per_call": statistics.mean(ck_per) * 1e3, "algorithmic_bytes": CONVK_BYTES,
+            "gpu_launches_per_call": 2,
         },
         "o_norm": {
             "workload": "sigmoid-gated RMSNorm of a prefill-sized core output (8192 x 32 x 128)",

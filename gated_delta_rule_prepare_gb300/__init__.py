@@ -7,7 +7,7 @@ library's CUDA kernels; there is no fallback.  Importing this package on a
 machine without the built library raises immediately.
 
 Entry points (same names as the C ABI): ``kda_decode``, ``kda_decode_k``,
-``kda_prefill``, ``kda_conv_silu_l2``, ``kda_o_norm_gated``,
+``kda_prefill``, ``kda_conv_silu_l2``, ``kda_conv_silu_l2_k``, ``kda_o_norm_gated``,
 ``kda_prefill_workspace_size``, ``kda_sync_status``.
 """
 
@@ -47,6 +47,7 @@ def _load():
         "kda_conv_silu_l2": [_vp] * 4 + [_i, _i, _vp, _i, _f, _i, _i, _u64],
         "kda_sync_status": [_u64],
         "kda_o_norm_gated": [_vp] * 4 + [_i64, _i, _i, _f, _u64],
+        "kda_conv_silu_l2_k": [_vp] * 4 + [_i, _i, _i, _f, _i, _i, _vp, _i, _u64],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -220,6 +221,30 @@ def kda_conv_silu_l2(conv_state, x, w, out, cu_seqlens=None, n_seqs=None, l2_eps
     _check(LIB.kda_conv_silu_l2(_ptr(conv_state, torch.float32, "conv_state"), _ptr(x), _ptr(w),
                                 _ptr(out), t, N, _ptr(cu_seqlens), K, float(l2_eps), H,
                                 HEAD_DIM, _stream(x)))
+
+
+def kda_conv_silu_l2_k(conv_state, x, w, out, snapshots=(), l2_eps=1e-6):
+    """k rows per sequence through the conv front end: x, out BF16 [N, k,
+    3*H*128]; conv_state FP32 [N, 3*H*128, K] in place; snapshots: up to k
+    FP32 tensors shaped like conv_state, snapshots[t] = conv state after row t."""
+    for n_, t_ in (("conv_state", conv_state), ("x", x), ("w", w), ("out", out)):
+        _contig(t_, n_)
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise TypeError("kda_conv_silu_l2_k: x, w, out must be bfloat16")
+    N, krows, conv_dim = x.shape
+    if conv_dim % (3 * HEAD_DIM) or conv_state.shape != (N, conv_dim, w.shape[1]):
+        raise ValueError("kda_conv_silu_l2_k: shape mismatch")
+    snaps = list(snapshots)
+    for s_ in snaps:
+        _contig(s_, "snapshot")
+        if s_.shape != conv_state.shape or s_.dtype != torch.float32:
+            raise ValueError("kda_conv_silu_l2_k: snapshot shape/dtype mismatch")
+    arr = (_c.c_void_p * max(1, len(snaps)))(*[s_.data_ptr() for s_ in snaps])
+    _check(LIB.kda_conv_silu_l2_k(_ptr(conv_state, torch.float32, "conv_state"), _ptr(x),
+                                  _ptr(w), _ptr(out), N, krows, w.shape[1], float(l2_eps),
+                                  conv_dim // (3 * HEAD_DIM), HEAD_DIM,
+                                  _c.cast(arr, _c.c_void_p) if snaps else None, len(snaps),
+                                  _stream(x)))
 
 
 def kda_o_norm_gated(core, gate, w, out, eps=1e-6):

@@ -226,10 +226,15 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
     if (!ok && threadIdx.x == 0) atomicOr(&g_conv_status, STATUS_BAD_CU_SEQLENS);
 }
 
+// Up to KDA_MAX_K snapshot targets, each [n_seqs][conv_dim][K] FP32.
+struct ConvSnaps {
+    float* p[KDA_MAX_K];
+};
+
 template <int K>
 __global__ void conv_state_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
                                   int total, int t_per_seq, const int* __restrict__ cu,
-                                  int n_seqs, int heads) {
+                                  int n_seqs, int heads, ConvSnaps snaps, int n_snap) {
     pdl_wait();  // the conv kernel has read the old state
     pdl_release();
     const size_t conv_dim = (size_t)3 * heads * D;
@@ -255,22 +260,54 @@ __global__ void conv_state_kernel(float* __restrict__ conv_state, const uint16_t
     const int len = end - start;
     float* st = conv_state + idx * K;
     float old[K], nw[K];
+    // a state row of 4 slots moves as one 16-byte access (rows are 16-byte
+    // aligned: conv_state is, and K = 4 makes every row 16 bytes)
+    auto store_row = [&](float* dst, const float (&r)[K]) {
+        if constexpr (K == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(r[0], r[1], r[2], r[3]);
+        } else {
 #pragma unroll
-    for (int j = 0; j < K; ++j) old[j] = st[j];
+            for (int j = 0; j < K; ++j) dst[j] = r[j];
+        }
+    };
+    if constexpr (K == 4) {
+        const float4 o4 = *reinterpret_cast<const float4*>(st);
+        old[0] = o4.x;
+        old[1] = o4.y;
+        old[2] = o4.z;
+        old[3] = o4.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < K; ++j) old[j] = st[j];
+    }
+    // snapshot t: the state after the sequence's row t, i.e. its window of
+    // the K inputs ending at row t (older slots from the old state)
+    for (int tt = 0; tt < n_snap && tt < len; ++tt) {
+        float sv[K];
+#pragma unroll
+        for (int j = 0; j < K; ++j) {
+            const int rel = tt + 1 - K + j;
+            float val = old[K - 1];
+#pragma unroll
+            for (int jj = 0; jj < K; ++jj)
+                if (rel < 0 && jj == K + rel) val = old[jj];
+            sv[j] = (rel >= 0) ? bf16_to_f32(__ldg(x + (size_t)(start + rel) * conv_dim + c)) : val;
+        }
+        store_row(snaps.p[tt] + idx * K, sv);
+    }
 #pragma unroll
     for (int j = 0; j < K; ++j) {
         const int rel = len - K + j;  // position relative to the sequence start
         nw[j] = (rel >= 0) ? bf16_to_f32(__ldg(x + (size_t)(start + rel) * conv_dim + c))
                            : old[(j + len < K) ? j + len : K - 1];
     }
-#pragma unroll
-    for (int j = 0; j < K; ++j) st[j] = nw[j];
+    store_row(st, nw);
 }
 
 template <int K>
 kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint16_t* out,
                   int total, int t_per_seq, const int* cu, int n_seqs, int heads, float eps,
-                  cudaStream_t s) {
+                  cudaStream_t s, ConvSnaps snaps = {}, int n_snap = 0) {
     dim3 grid((unsigned)((3 * heads * D + kCtaCh - 1) / kCtaCh), (total + kTok - 1) / kTok);
     launch_pdl(conv_silu_l2_kernel<K>, grid, dim3(kThreads), 0, s, conv_state, x, w, out, total,
                t_per_seq, cu, n_seqs, heads, eps);
@@ -278,7 +315,7 @@ kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint1
     if (st != KDA_OK) return st;
     const size_t rows = (size_t)n_seqs * 3 * heads * D;
     launch_pdl(conv_state_kernel<K>, dim3((unsigned)((rows + 255) / 256)), dim3(256), 0, s,
-               conv_state, x, total, t_per_seq, cu, n_seqs, heads);
+               conv_state, x, total, t_per_seq, cu, n_seqs, heads, snaps, n_snap);
     return launch_result("kda_conv_silu_l2 (state)");
 }
 
@@ -325,5 +362,49 @@ extern "C" kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, con
         case 2: return launch<2>(conv_state, x, w, out, (int)total, tps, cu_seqlens, n_seqs, heads, l2_eps, s);
         case 3: return launch<3>(conv_state, x, w, out, (int)total, tps, cu_seqlens, n_seqs, heads, l2_eps, s);
         default: return launch<4>(conv_state, x, w, out, (int)total, tps, cu_seqlens, n_seqs, heads, l2_eps, s);
+    }
+}
+
+extern "C" kda_status kda_conv_silu_l2_k(float* conv_state, const uint16_t* x, const uint16_t* w,
+                                         uint16_t* out, int n_seqs, int krows, int conv_kernel,
+                                         float l2_eps, int heads, int head_dim,
+                                         float* const* snapshots, int n_snap, uint64_t stream) {
+    KDA_REQUIRE(krows >= 1 && krows <= KDA_MAX_K, KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2_k: k = %d outside [1, %d]", krows, KDA_MAX_K);
+    KDA_REQUIRE(n_snap >= 0 && n_snap <= krows, KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2_k: n_snap = %d outside [0, k = %d]", n_snap, krows);
+    KDA_REQUIRE(n_snap == 0 || snapshots, KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2_k: snapshots is NULL with n_snap = %d", n_snap);
+    KDA_REQUIRE(conv_state && x && w && out, KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2_k: null pointer argument");
+    KDA_REQUIRE(aligned16(conv_state) && aligned16(x) && aligned16(out), KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2_k: conv_state, x and out must be 16-byte aligned");
+    KDA_REQUIRE(head_dim == D, KDA_ERR_UNSUPPORTED,
+                "kda_conv_silu_l2_k: head_dim %d unsupported (only 128)", head_dim);
+    KDA_REQUIRE(heads >= 1 && n_seqs >= 1, KDA_ERR_INVALID_ARG,
+                "kda_conv_silu_l2_k: heads (%d) and n_seqs (%d) must be >= 1", heads, n_seqs);
+    KDA_REQUIRE(conv_kernel >= 1 && conv_kernel <= KDA_MAX_CONV_KERNEL, KDA_ERR_UNSUPPORTED,
+                "kda_conv_silu_l2_k: conv_kernel %d outside [1, %d]", conv_kernel,
+                KDA_MAX_CONV_KERNEL);
+    KDA_REQUIRE(l2_eps >= 0.f, KDA_ERR_INVALID_ARG, "kda_conv_silu_l2_k: l2_eps must be >= 0");
+    const long long total = (long long)krows * n_seqs;
+    KDA_REQUIRE(total <= 0x7fffffffLL && (long long)3 * heads * D * total < (1LL << 46) &&
+                    (total + kTok - 1) / kTok <= 65535,
+                KDA_ERR_INVALID_ARG, "kda_conv_silu_l2_k: problem too large");
+    ConvSnaps sn = {};
+    for (int t = 0; t < n_snap; ++t) {
+        KDA_REQUIRE(snapshots[t] && aligned16(snapshots[t]) && snapshots[t] != conv_state,
+                    KDA_ERR_INVALID_ARG,
+                    "kda_conv_silu_l2_k: snapshot %d is NULL, misaligned or the conv state", t);
+        sn.p[t] = snapshots[t];
+    }
+    KDA_REQUIRE(!fault_injected(), KDA_ERR_CUDA, "kda_conv_silu_l2_k: injected launch failure");
+    cudaStream_t s = as_stream(stream);
+    const int tot = (int)total;
+    switch (conv_kernel) {
+        case 1: return launch<1>(conv_state, x, w, out, tot, krows, nullptr, n_seqs, heads, l2_eps, s, sn, n_snap);
+        case 2: return launch<2>(conv_state, x, w, out, tot, krows, nullptr, n_seqs, heads, l2_eps, s, sn, n_snap);
+        case 3: return launch<3>(conv_state, x, w, out, tot, krows, nullptr, n_seqs, heads, l2_eps, s, sn, n_snap);
+        default: return launch<4>(conv_state, x, w, out, tot, krows, nullptr, n_seqs, heads, l2_eps, s, sn, n_snap);
     }
 }

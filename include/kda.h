@@ -207,6 +207,28 @@ kda_status kda_o_norm_gated(const float* core, const uint16_t* gate, const uint1
                             uint16_t* out, int64_t rows, int heads, int head_dim, float eps,
                             uint64_t stream);
 
+/*
+ * kda_conv_silu_l2_k -- the front end's half of decode_k: k rows of each of
+ * n_seqs sequences through the conv + SiLU + L2 of kda_conv_silu_l2, with
+ * optional conv-state snapshots (Glm5NextKdaLayer::decode_k: snapshots[t] is
+ * the pair (h_dst, conv_dst) receiving the state after row t; kda_decode_k
+ * fills h_dst, this call conv_dst).  Rows are walked in order, so the output
+ * and the final conv state equal k single-token kda_conv_silu_l2 calls bit
+ * for bit, and snapshots[t] equals the conv state after the t + 1-th.
+ *
+ *   conv_state : FP32 [n_seqs][conv_dim][conv_kernel], in place
+ *   x, out     : BF16 [n_seqs][krows][conv_dim];  w : BF16 [conv_dim][conv_kernel]
+ *   snapshots  : HOST array of n_snap DEVICE pointers, each FP32
+ *                [n_seqs][conv_dim][conv_kernel], 16-byte aligned, distinct from
+ *                conv_state (read on the host during the call only)
+ *   1 <= krows <= KDA_MAX_K; 0 <= n_snap <= krows; other limits as
+ *   kda_conv_silu_l2.  Two kernels are enqueued.
+ */
+kda_status kda_conv_silu_l2_k(float* conv_state, const uint16_t* x, const uint16_t* w,
+                              uint16_t* out, int n_seqs, int krows, int conv_kernel, float l2_eps,
+                              int heads, int head_dim, float* const* snapshots, int n_snap,
+                              uint64_t stream);
+
 /* Size of the library-owned device array kda_prefill_static_ws uses as its
  * workspace: 64 MiB on every GPU that loads the library, held until exit. */
 #define KDA_STATIC_WORKSPACE_BYTES (64u << 20)

@@ -145,3 +145,14 @@ def test_o_norm_refuses_bad_arguments(lib):
     assert f(P, P, P, P, 4, 2, 128, -1.0, 0) == 1      # eps
     assert f(ctypes.c_void_p(P.value + 4), P, P, P, 4, 2, 128, 1e-6, 0) == 1  # core alignment
     assert b"kda_o_norm_gated" in lib.kda_last_error()
+
+
+def test_conv_k_refuses_bad_arguments(lib):
+    f = lib.kda_conv_silu_l2_k
+    f.argtypes = [V] * 4 + [I, I, I, F, I, I, V, I, U64]
+    assert f(P, P, P, P, 2, 0, 4, 1e-6, 1, 128, None, 0, 0) == 1      # k = 0
+    assert f(P, P, P, P, 2, 9, 4, 1e-6, 1, 128, None, 0, 0) == 1      # k above KDA_MAX_K
+    assert f(P, P, P, P, 2, 3, 4, 1e-6, 1, 128, None, 4, 0) == 1      # n_snap > k
+    assert f(P, P, P, P, 2, 3, 4, 1e-6, 1, 128, None, 2, 0) == 1      # snapshots NULL
+    assert f(P, P, P, P, 2, 3, 5, 1e-6, 1, 128, None, 0, 0) == 2      # conv_kernel
+    assert b"kda_conv_silu_l2_k" in lib.kda_last_error()

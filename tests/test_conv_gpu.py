@@ -79,3 +79,33 @@ def test_conv_frontend_workload_sampled(orc):
                                        [0, b - a], 32)
         bf16_close(out[a:b], ref)
         np.testing.assert_array_equal(st[n].cpu().double().numpy(), st_ref[0])
+
+
+@pytest.mark.parametrize("K_,krows,n_snap", [(4, 4, 4), (4, 6, 3), (3, 1, 1), (2, 8, 0)])
+def test_conv_k_rows_equal_serial_calls_with_snapshots(orc, K_, krows, n_snap):
+    """kda_conv_silu_l2_k over k rows gives the bits of k single-token calls,
+    and snapshots[t] the conv state after row t; the oracle agrees."""
+    K = kda()
+    H, N = 1, 5
+    ch = 3 * H * 128
+    gen = torch.Generator().manual_seed(70 + krows)
+    x = torch.randn((N, krows, ch), generator=gen).to(torch.bfloat16).cuda()
+    w = (torch.randn((ch, K_), generator=gen) * 0.5).to(torch.bfloat16).cuda()
+    st0 = torch.randn((N, ch, K_), generator=gen).cuda()
+    st_k = st0.clone()
+    out_k = torch.empty_like(x)
+    snaps = [torch.full_like(st0, float("nan")) for _ in range(n_snap)]
+    K.kda_conv_silu_l2_k(st_k, x, w, out_k, snaps)
+    st_s = st0.clone()
+    for t in range(krows):
+        o1 = torch.empty((N, ch), dtype=torch.bfloat16, device="cuda")
+        K.kda_conv_silu_l2(st_s, x[:, t].contiguous(), w, o1, n_seqs=N)
+        assert torch.equal(o1, out_k[:, t])
+        if t < n_snap:
+            assert torch.equal(snaps[t], st_s)
+    assert torch.equal(st_k, st_s)
+    xc = x.reshape(N * krows, ch).cpu()
+    cu = [krows * n for n in range(N + 1)]
+    ref, st_ref = orc.conv_silu_l2(xc, w.cpu(), st0.cpu(), cu, H)
+    bf16_close(out_k.reshape(N * krows, ch).cpu(), ref)
+    np.testing.assert_array_equal(st_k.cpu().double().numpy(), st_ref)
