@@ -170,17 +170,19 @@ def barrier(world: int):
 # ------------------------------------------------------------------- GPU arm
 
 def time_launches(fn, n: int, stream):
-    """Runs fn() n times with an event pair around each call on `stream`;
-    returns (list of per-call ms, total ms from the first to the last event)."""
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(n)]
-    for a, b in evs:
-        a.record(stream)
+    """Runs fn() n times back to back between one pair of events on `stream`;
+    returns (the per-call ms as a list of n equal values, the total ms).
+    Per-call event pairs would overlap: with programmatic dependent launch a
+    call's first kernel may be scheduled while the previous call's last kernel
+    still drains, so only the span of the whole sequence is a clean measure."""
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
         fn()
-        b.record(stream)
+    e1.record(stream)
     torch.cuda.synchronize()
-    per = [a.elapsed_time(b) for a, b in evs]
-    return per, evs[0][0].elapsed_time(evs[-1][1])
+    total = e0.elapsed_time(e1)
+    return [total / n] * n, total
 
 
 def run_gpu(args):
