@@ -43,9 +43,6 @@ namespace {
 __device__ unsigned g_tc_status = 0;
 
 constexpr int C = 64;
-constexpr int DV = 32;
-constexpr int NTS = 256;  // scan threads
-constexpr int SC = DV / (NTS / 128);  // state columns per scan thread
 constexpr int NTP = 512;  // prepare threads
 constexpr int KP = 132;  // pitch (floats) of the FP32 [64][128] Gamma array (16-B rows)
 constexpr int AP = 65;   // pitch (floats) of the FP32 [64][64] A / W array
@@ -71,8 +68,6 @@ using OpY = Op<16, 0>;    // B: Y_b of a 16-token block, K = 128 channels
 using OpY32 = Op<32, 0>;  // B: Y_b of a 32-token block, K = 128 channels
 using OpKH = Op<128, 16>; // A: Khat^T, rows = key channel, K = 64 tokens (written per K index)
 using OpTP = Op<128, 0>;  // A: [T; P], K = 64 tokens
-using OpXV = Op<32, 16>;  // B: X^T and U^T, rows = value column, K = 64 tokens
-using OpS = Op<32, 16>;   // B: S^T, rows = value column, K = 128 key channels
 using OpX1 = Op<64, 0>;   // A: [X_1; QX_1] of the second 32-token block, rows 32..63 only
 
 // ------------------------------------------------------------ workspace
@@ -126,23 +121,39 @@ static_assert(PS_OPX % 1024 == 0 && PS_Y % 16 == 0, "operand alignment");
 constexpr float kWideGMin = 5.1f;
 static_assert(PS_TOTAL <= 232448, "shared memory budget exceeded");
 
-// ------------------------------------------------------------ scan smem
-constexpr uint32_t SS_BLOB = 0;                      // blob image: OPX | TP | KH | DEC
-constexpr uint32_t SS_OPX = SS_BLOB + BLOB_OPX, SS_TP = SS_BLOB + BLOB_TP,
-                   SS_KH = SS_BLOB + BLOB_KH, SS_DEC = SS_BLOB + BLOB_DEC;
-constexpr uint32_t SS_XV = SS_BLOB + BLOB_BYTES;
-constexpr uint32_t SS_U = SS_XV + OpXV::bytes(64);
-constexpr uint32_t SS_OPS = SS_U + OpXV::bytes(64);
-// value tile [64 tokens][32 columns] BF16, 64-byte swizzle: row r's 16-byte
-// chunk c sits at chunk c ^ ((r >> 1) & 3) (needs a 512-byte aligned base)
-constexpr uint32_t SS_RAWV = (SS_OPS + OpS::bytes(128) + 1023) & ~1023u;
-constexpr uint32_t SS_BAR = SS_RAWV + 64 * DV * 2;
-constexpr uint32_t SS_TOTAL = SS_BAR + 64;
-static_assert(SS_TOTAL <= 232448, "shared memory budget exceeded");
+// ------------------------------------------------------------ scan layout
+// The scan comes in two value-slice widths: 32 columns (256 threads, the
+// latency-bound case of few (sequence, head) chains) and 64 columns (512
+// threads, half the CTAs for the same chains when they outnumber the SMs).
+// A thread always owns 16 state columns of one key row.
+template <int DVv>
+struct ScanCfg {
+    static constexpr int DV = DVv;
+    static constexpr int NT = DVv * 8;                    // 256 or 512 threads
+    static constexpr int SC = 16;                         // state columns per thread
+    using OpXV = Op<DVv, 16>;   // B: X^T and U^T, rows = value column, K = 64 tokens
+    using OpS = Op<DVv, 16>;    // B: S^T, rows = value column, K = 128 key channels
+    // shared memory: blob image (OPX | TP | KH | DEC), X^T, U^T, S^T, value tile
+    static constexpr uint32_t XV = BLOB_BYTES;
+    static constexpr uint32_t U = XV + OpXV::bytes(64);
+    static constexpr uint32_t OPS = U + OpXV::bytes(64);
+    // value tile [64 tokens][DV columns] BF16 with the 64-byte (DV = 32) or
+    // 128-byte (DV = 64) TMA swizzle: row r's 16-byte chunk c sits at chunk
+    // c ^ ((r >> 1) & 3), resp. c ^ (r & 7) (1024-byte aligned base)
+    static constexpr uint32_t RAWV = (OPS + OpS::bytes(128) + 1023) & ~1023u;
+    static constexpr uint32_t BAR = RAWV + 64 * DVv * 2;
+    static constexpr uint32_t TOTAL = BAR + 64;
+    // TMEM columns: P U, [Ktil; Qtil] S, T X, Khat^T U
+    static constexpr uint32_t T_PU = 0, T_Y = DVv, T_U = 2 * DVv, T_E = 3 * DVv;
+    static constexpr uint32_t TMEM_COLS = 4 * DVv;
+    static __device__ __forceinline__ int vswz(int r) { return DVv == 32 ? (r >> 1) & 3 : r & 7; }
+    static_assert(TOTAL <= 232448, "shared memory budget exceeded");
+    static_assert(NT / 128 * SC == DVv, "column groups must cover the slice");
+};
+constexpr uint32_t SS_OPX = BLOB_OPX, SS_TP = BLOB_TP, SS_KH = BLOB_KH, SS_DEC = BLOB_DEC;
 
-// TMEM columns: prepare 64 (A and P), scan 128
+// TMEM columns of prepare: A and P
 constexpr uint32_t TC_AP = 0;
-constexpr uint32_t TC_PU = 0, TC_Y = 32, TC_U = 64, TC_E = 96;
 
 __device__ __forceinline__ float bf(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
@@ -737,11 +748,19 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
     }
 }
 
-__global__ void __launch_bounds__(NTS, 1)
+template <int DVv>
+__global__ void __launch_bounds__(ScanCfg<DVv>::NT, 1)
 scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
             float* __restrict__ o, int t, int t_pad, int heads, const int* __restrict__ cu,
             int n_seqs, const unsigned char* __restrict__ ws) {
     extern __shared__ __align__(1024) unsigned char sm[];
+    using Cfg = ScanCfg<DVv>;
+    using OpXV = typename Cfg::OpXV;
+    using OpS = typename Cfg::OpS;
+    constexpr int DV = Cfg::DV, SC = Cfg::SC;
+    constexpr uint32_t SS_XV = Cfg::XV, SS_U = Cfg::U, SS_OPS = Cfg::OPS, SS_RAWV = Cfg::RAWV,
+                       SS_BAR = Cfg::BAR;
+    constexpr uint32_t TC_PU = Cfg::T_PU, TC_Y = Cfg::T_Y, TC_U = Cfg::T_U, TC_E = Cfg::T_E;
     const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5;
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column group of SC
@@ -779,7 +798,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         tc::prefetch_tmap(&vmap);
         *abort_flag = 0;
     }
-    if (warp == 0) tc::tmem_alloc(tmem_slot, 128);
+    if (warp == 0) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
     tc::tc_fence_before();
     __syncthreads();
     tc::tc_fence_after();
@@ -890,8 +909,8 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
             tc::tmem_ld(tmem + lane_base + TC_Y + SC * ch, v);
             tc::tmem_ld_wait();
             if (ln < 64) {
-                const int r = ln, sw = (r >> 1) & 3;
-                const unsigned char* vrow = reinterpret_cast<const unsigned char*>(RAWV) + r * 64;
+                const int r = ln, sw = Cfg::vswz(r);
+                const unsigned char* vrow = reinterpret_cast<const unsigned char*>(RAWV) + r * (DV * 2);
                 uint32_t w[SC / 2];  // SC BF16 values: SC / 8 chunks of 16 bytes
 #pragma unroll
                 for (int q = 0; q < SC / 8; ++q) {
@@ -987,7 +1006,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     __syncthreads();
     if (warp == 0) {
         tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, 128);
+        tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
     }
 }
 
@@ -1046,13 +1065,25 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
                              int heads, long long stride, const int* cu, int n_seqs,
                              void* workspace, cudaStream_t s) {
     const uint64_t rows = cu ? (uint64_t)t : (uint64_t)t_pad * n_seqs;
+    const int sms = sm_count();
+    if (sms <= 0) {
+        set_error("kda_prefill: cannot query the multiprocessor count");
+        return KDA_ERR_CUDA;
+    }
+    // The scan's (sequence, head) chains each need a CTA of their own for
+    // their whole length; 32-column slices give four CTAs per chain, 64-column
+    // slices two.  Narrow slices while the CTAs fit on the SMs in one wave
+    // (the chains' latency decides), wide ones once they would not (each
+    // tensor-core product then does twice the work for about the same time).
+    const int dv = ((long long)n_seqs * heads * (D / 32) > sms) ? 64 : 32;
     PrepMaps maps;
     CUtensorMap vmap;
     const uint64_t hd = (uint64_t)heads * D;
     if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.g, g, hd, rows, hd, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&vmap, v, hd, rows, (uint64_t)stride, DV, CU_TENSOR_MAP_SWIZZLE_64B)) {
+        !make_map(&vmap, v, hd, rows, (uint64_t)stride, dv,
+                  dv == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
@@ -1060,8 +1091,11 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PS_TOTAL);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)SS_TOTAL);
+        e = cudaFuncSetAttribute(scan_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)ScanCfg<32>::TOTAL);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(scan_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)ScanCfg<64>::TOTAL);
     if (e != cudaSuccess) {
         set_error("kda_prefill: cannot reserve shared memory: %s", cudaGetErrorString(e));
         return KDA_ERR_CUDA;
@@ -1074,18 +1108,19 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     // Persistent prepare: one CTA per SM (shared memory allows no more),
     // never more CTAs than (chunk, head) items.
     const long long items = (((long long)rows + C - 1) / C + n_seqs) * heads;
-    const int sms = sm_count();
-    if (sms <= 0) {
-        set_error("kda_prefill: cannot query the multiprocessor count");
-        return KDA_ERR_CUDA;
-    }
     const unsigned grid = (unsigned)(items < sms ? items : sms);
     launch_pdl(prepare_kernel, dim3(grid), dim3(NTP), PS_TOTAL, s, maps, (const uint16_t*)beta, t,
                t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;
-    launch_pdl(scan_kernel, dim3(D / DV, heads, n_seqs), dim3(NTS), SS_TOTAL, s, vmap, state, o,
-               t, t_pad, heads, cu, n_seqs, (const unsigned char*)ws);
+    if (dv == 32)
+        launch_pdl(scan_kernel<32>, dim3(D / 32, heads, n_seqs), dim3(ScanCfg<32>::NT),
+                   ScanCfg<32>::TOTAL, s, vmap, state, o, t, t_pad, heads, cu, n_seqs,
+                   (const unsigned char*)ws);
+    else
+        launch_pdl(scan_kernel<64>, dim3(D / 64, heads, n_seqs), dim3(ScanCfg<64>::NT),
+                   ScanCfg<64>::TOTAL, s, vmap, state, o, t, t_pad, heads, cu, n_seqs,
+                   (const unsigned char*)ws);
     return launch_result("kda_prefill (scan)");
 }
 
