@@ -68,7 +68,7 @@ def peaks():
 def kernel_source_sha() -> str:
     """Hash of the sources the prefill kernels are built from."""
     h = hashlib.sha256()
-    for name in ("prefill_tc.cu", "prefill.cu", "sm103_tc.h", "kda_common.h"):
+    for name in ("prefill_tc.cu", "prefill.cu", "sm103_tc.h", "kda_common.h", "tma_map.h"):
         h.update(open(os.path.join(ROOT, "gated_delta_rule_prepare_gb300", "csrc", name),
                       "rb").read())
     return h.hexdigest()[:16]

@@ -5,13 +5,16 @@
 // 1/sqrt(sum + eps)).
 //
 // Kernel 1 (conv_silu_l2_kernel): one CTA of 128 threads per (group of 1024
-// channels = 8 heads, block of 16 consecutive tokens); a thread owns 8
-// adjacent channels (16-byte BF16 loads and stores) and slides a register
-// window of the last conv_kernel - 1 inputs along the tokens.  History
-// before a sequence's first token comes from the conv state, which this
-// kernel only reads.  A q/k head's 128 channels are one half-warp, so its L2
-// sum is a 4-step shuffle reduction within the half-warp, per token, with no
-// shared memory; the conv taps run as packed FP32 pairs (fma.rn.f32x2).
+// channels = 8 heads, span of consecutive tokens), about three CTAs per SM in
+// one wave.  The span's x rows arrive by TMA in blocks of 16 tokens, double
+// buffered behind an mbarrier each, so the next block is in flight while the
+// current one is computed.  A thread owns 8 adjacent channels (16-byte shared
+// loads and global stores) and carries a register window of the last
+// conv_kernel - 1 inputs from block to block.  History before a sequence's
+// first token comes from the conv state, which this kernel only reads.  A
+// q/k head's 128 channels are one half-warp, so its L2 sum is a 4-step
+// shuffle reduction within the half-warp, per token, with no shared memory;
+// the conv taps run as packed FP32 pairs (fma.rn.f32x2).
 // Kernel 2 (conv_state_kernel): after kernel 1, each thread rewrites one
 // (sequence, channel) state row to hold that sequence's last conv_kernel
 // inputs, reading the old row first; separating it from kernel 1 keeps any
@@ -19,6 +22,8 @@
 #include <cuda_bf16.h>
 
 #include "kda_common.h"
+#include "sm103_tc.h"
+#include "tma_map.h"
 
 namespace kda {
 namespace {
@@ -81,33 +86,64 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     return upk(r);
 }
 
+// x arrives in blocks of kTok tokens x 1024 channels through TMA, as four
+// boxes of 256 channels ([box][token][256] in shared memory), double-buffered.
+constexpr int kBoxCh = 256;
+constexpr uint32_t kBlkBytes = kTok * kCtaCh * 2;   // 32 KB
+constexpr uint32_t kConvSmem = 2 * kBlkBytes + 64;  // two blocks + two mbarriers
+
 template <int K>
-__global__ void __launch_bounds__(kThreads)
-conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __restrict__ x,
-                    const uint16_t* __restrict__ w, uint16_t* __restrict__ out, int total,
-                    int t_per_seq, const int* __restrict__ cu, int n_seqs, int heads,
-                    float l2_eps) {
+__global__ void __launch_bounds__(kThreads, 3)
+conv_silu_l2_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restrict__ conv_state,
+                    const uint16_t* __restrict__ x, const uint16_t* __restrict__ w,
+                    uint16_t* __restrict__ out, int total, int t_per_seq,
+                    const int* __restrict__ cu, int n_seqs, int heads, float l2_eps, int span) {
+    extern __shared__ __align__(128) unsigned char sm[];
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 2 * kBlkBytes);
     pdl_wait();
     pdl_release();
-    const int lane = threadIdx.x & 31;
-    const int c = blockIdx.x * kCtaCh + kCh * threadIdx.x;  // first of this thread's 8 channels
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int ch0 = blockIdx.x * kCtaCh;
+    const int c = ch0 + kCh * tid;  // first of this thread's 8 channels
     const size_t conv_dim = (size_t)3 * heads * D;
     // conv_dim is a multiple of 128, so a head (16 threads, a half-warp) is
-    // either wholly present or wholly absent here.
-    if ((size_t)c >= conv_dim) return;
+    // either wholly present or wholly absent; absent threads stay for the barriers.
+    const bool active = (size_t)c < conv_dim;
     const bool normalise = c < 2 * heads * D;            // a q or k head
     const unsigned hmask = 0xffffu << (lane & 16);       // this half-warp
-    float2 wv[K][kCh / 2];                               // tap j of channel pairs
+    const int tok0 = blockIdx.y * span;
+    if (tok0 >= total) return;  // the whole CTA
+    const int tok_end = min(total, tok0 + span);
+    const int nblk = (tok_end - tok0 + kTok - 1) / kTok;
+
+    if (tid == 0) {
+        tc::mbar_init(bar, 1);
+        tc::mbar_init(bar + 1, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    // boxes holding at least one channel of this group (conv_dim is a
+    // multiple of 384, so the last group may cover fewer than four)
+    const int nbox = min(kCtaCh / kBoxCh, (int)((conv_dim - ch0 + kBoxCh - 1) / kBoxCh));
+    auto load_block = [&](int i) {  // block i into buffer i & 1 (thread 0)
+        uint64_t* b = bar + (i & 1);
+        tc::mbar_arrive_expect_tx(b, (uint32_t)nbox * (kTok * kBoxCh * 2));
+        for (int bx = 0; bx < nbox; ++bx)
+            tc::tma_load_2d(sm + (i & 1) * kBlkBytes + bx * (kTok * kBoxCh * 2), &xmap, b,
+                            ch0 + bx * kBoxCh, tok0 + i * kTok);
+    };
+    if (tid == 0) load_block(0);
+
+    float2 wv[K][kCh / 2];  // tap j of channel pairs
 #pragma unroll
     for (int j = 0; j < K; ++j)
 #pragma unroll
         for (int e = 0; e < kCh / 2; ++e)
-            wv[j][e] = make_float2(bf16_to_f32(__ldg(w + (size_t)(c + 2 * e) * K + j)),
-                                   bf16_to_f32(__ldg(w + (size_t)(c + 2 * e + 1) * K + j)));
+            wv[j][e] = active ? make_float2(bf16_to_f32(__ldg(w + (size_t)(c + 2 * e) * K + j)),
+                                            bf16_to_f32(__ldg(w + (size_t)(c + 2 * e + 1) * K + j)))
+                              : make_float2(0.f, 0.f);
 
-    const int tok0 = blockIdx.y * kTok;
-    const int tok_end = min(total, tok0 + kTok);
-    // The block's tokens are consecutive: find the first one's sequence once,
+    // The span's tokens are consecutive: find the first one's sequence once,
     // then step to the next sequence whenever a token reaches its end.
     int n, start, end;
     bool ok = true;
@@ -119,13 +155,6 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
         start = n * t_per_seq;
         end = start + t_per_seq;
     }
-    // All of the block's inputs first, as independent 16-byte loads.
-    const uint4* xp = reinterpret_cast<const uint4*>(x + (size_t)tok0 * conv_dim + c);
-    const size_t step = conv_dim / kCh;  // one token row, in 16-byte units
-    uint4 xs[kTok];
-#pragma unroll
-    for (int m = 0; m < kTok; ++m)
-        xs[m] = (tok0 + m < tok_end) ? __ldg(xp + m * step) : make_uint4(0u, 0u, 0u, 0u);
     // hv[j][e]: channel pair e's inputs at token tau - (K - 1) + j.
     float2 hv[K > 1 ? K - 1 : 1][kCh / 2];
     auto state_slot = [&](int e2, int slot) {  // the state's slot for channel pair e2
@@ -136,12 +165,15 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
 #pragma unroll
         for (int j = 0; j < K - 1; ++j)
 #pragma unroll
-            for (int e = 0; e < kCh / 2; ++e) hv[j][e] = state_slot(e, j + 1);
+            for (int e = 0; e < kCh / 2; ++e)
+                hv[j][e] = active ? state_slot(e, j + 1) : make_float2(0.f, 0.f);
     };
-    if (ok) {
 #pragma unroll
-        for (int j = 0; j < K - 1; ++j) {
-            const int src = tok0 - (K - 1) + j;
+    for (int j = 0; j < K - 1; ++j) {
+        const int src = tok0 - (K - 1) + j;
+#pragma unroll
+        for (int e = 0; e < kCh / 2; ++e) hv[j][e] = make_float2(0.f, 0.f);
+        if (ok && active) {
             if (src >= start) {
                 const uint4 u = __ldg(reinterpret_cast<const uint4*>(x + (size_t)src * conv_dim + c));
                 hv[j][0] = bf16x2_to_f32(u.x);
@@ -154,76 +186,91 @@ conv_silu_l2_kernel(const float* __restrict__ conv_state, const uint16_t* __rest
             }
         }
     }
-    uint4* op = reinterpret_cast<uint4*>(out + (size_t)tok0 * conv_dim + c);
-    // One token: conv over the window, SiLU, the head's L2 scale, BF16 store.
-    auto token = [&](int m) {
-        const float2 xv[kCh / 2] = {bf16x2_to_f32(xs[m].x), bf16x2_to_f32(xs[m].y),
-                                    bf16x2_to_f32(xs[m].z), bf16x2_to_f32(xs[m].w)};
-        float2 y[kCh / 2];
-#pragma unroll
-        for (int e = 0; e < kCh / 2; ++e) {
-            float2 a = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < K - 1; ++j) a = fma2(wv[j][e], hv[j][e], a);
-            a = fma2(wv[K - 1][e], xv[e], a);
-#pragma unroll
-            for (int j = 0; j + 1 < K - 1; ++j) hv[j][e] = hv[j + 1][e];
-            if constexpr (K > 1) hv[K - 2][e] = xv[e];
-            y[e] = make_float2(silu(a.x), silu(a.y));
-        }
-        if (normalise) {  // uniform per half-warp
-            float p = 0.f;
+    // this thread's 16 bytes of token row m inside a block buffer
+    const uint32_t xoff = (uint32_t)(tid / (kBoxCh / kCh)) * (kTok * kBoxCh * 2) +
+                          (uint32_t)((kCh * tid) % kBoxCh) * 2;
+    bool timed_out = false;
+    for (int i = 0; i < nblk; ++i) {
+        const int tb = tok0 + i * kTok;
+        if (tid == 0 && i + 1 < nblk) load_block(i + 1);  // its buffer was released below
+        if (!tc::mbar_wait(bar + (i & 1), (uint32_t)(i >> 1) & 1u)) timed_out = true;
+        const unsigned char* xb = sm + (i & 1) * kBlkBytes + xoff;
+        uint4* op = reinterpret_cast<uint4*>(out + (size_t)tb * conv_dim + c);
+        // One token: conv over the window, SiLU, the head's L2 scale, BF16 store.
+        auto token = [&](int m) {
+            const uint4 xm = *reinterpret_cast<const uint4*>(xb + m * (kBoxCh * 2));
+            const float2 xv[kCh / 2] = {bf16x2_to_f32(xm.x), bf16x2_to_f32(xm.y),
+                                        bf16x2_to_f32(xm.z), bf16x2_to_f32(xm.w)};
+            float2 y[kCh / 2];
 #pragma unroll
             for (int e = 0; e < kCh / 2; ++e) {
-                p = __fmaf_rn(y[e].x, y[e].x, p);
-                p = __fmaf_rn(y[e].y, y[e].y, p);
+                float2 a = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < K - 1; ++j) a = fma2(wv[j][e], hv[j][e], a);
+                a = fma2(wv[K - 1][e], xv[e], a);
+#pragma unroll
+                for (int j = 0; j + 1 < K - 1; ++j) hv[j][e] = hv[j + 1][e];
+                if constexpr (K > 1) hv[K - 2][e] = xv[e];
+                y[e] = make_float2(silu(a.x), silu(a.y));
             }
+            if (normalise) {  // uniform per half-warp
+                float p = 0.f;
 #pragma unroll
-            for (int off = 8; off > 0; off >>= 1) p += __shfl_xor_sync(hmask, p, off);
-            const float inv = rsqrtf(p + l2_eps);
-#pragma unroll
-            for (int e = 0; e < kCh / 2; ++e) {
-                y[e].x *= inv;
-                y[e].y *= inv;
-            }
-        }
-        uint4 o;
-        o.x = f32x2_to_bf16x2(y[0].x, y[0].y);
-        o.y = f32x2_to_bf16x2(y[1].x, y[1].y);
-        o.z = f32x2_to_bf16x2(y[2].x, y[2].y);
-        o.w = f32x2_to_bf16x2(y[3].x, y[3].y);
-        op[m * step] = o;
-    };
-    if (ok && tok0 + kTok <= tok_end && tok0 + kTok <= end) {
-        // Common case: all kTok tokens lie in one sequence; straight-line code
-        // lets the tokens' independent work overlap.
-#pragma unroll
-        for (int m = 0; m < kTok; ++m) token(m);
-        return;
-    }
-#pragma unroll
-    for (int m = 0; m < kTok; ++m) {  // uniform over the CTA: tok_end, ok and the boundaries
-        const int tau = tok0 + m;
-        if (!ok || tau >= tok_end) break;
-        if (tau >= end) {  // a new sequence starts at tau (skipping empty ones)
-            if (cu) {
-                while (n + 1 < n_seqs && __ldg(cu + n + 1) <= tau) ++n;
-                start = __ldg(cu + n);
-                end = __ldg(cu + n + 1);
-                if (!(start == tau && tau < end)) {
-                    ok = false;
-                    break;
+                for (int e = 0; e < kCh / 2; ++e) {
+                    p = __fmaf_rn(y[e].x, y[e].x, p);
+                    p = __fmaf_rn(y[e].y, y[e].y, p);
                 }
-            } else {
-                ++n;
-                start = n * t_per_seq;
-                end = start + t_per_seq;
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1) p += __shfl_xor_sync(hmask, p, off);
+                const float inv = rsqrtf(p + l2_eps);
+#pragma unroll
+                for (int e = 0; e < kCh / 2; ++e) {
+                    y[e].x *= inv;
+                    y[e].y *= inv;
+                }
             }
-            state_history();
+            if (active) {
+                uint4 o;
+                o.x = f32x2_to_bf16x2(y[0].x, y[0].y);
+                o.y = f32x2_to_bf16x2(y[1].x, y[1].y);
+                o.z = f32x2_to_bf16x2(y[2].x, y[2].y);
+                o.w = f32x2_to_bf16x2(y[3].x, y[3].y);
+                op[(size_t)m * (conv_dim / kCh)] = o;
+            }
+        };
+        if (ok && tb + kTok <= tok_end && tb + kTok <= end) {
+            // Common case: the block's tokens lie in one sequence; straight-line
+            // code lets the tokens' independent work overlap.
+#pragma unroll
+            for (int m = 0; m < kTok; ++m) token(m);
+        } else {
+#pragma unroll 1
+            for (int m = 0; m < kTok; ++m) {  // uniform over the CTA
+                const int tau = tb + m;
+                if (!ok || tau >= tok_end) break;
+                if (tau >= end) {  // a new sequence starts at tau (skipping empty ones)
+                    if (cu) {
+                        while (n + 1 < n_seqs && __ldg(cu + n + 1) <= tau) ++n;
+                        start = __ldg(cu + n);
+                        end = __ldg(cu + n + 1);
+                        if (!(start == tau && tau < end)) {
+                            ok = false;
+                            break;
+                        }
+                    } else {
+                        ++n;
+                        start = n * t_per_seq;
+                        end = start + t_per_seq;
+                    }
+                    state_history();
+                }
+                token(m);
+            }
         }
-        token(m);
+        __syncthreads();  // every thread is done with buffer i & 1: block i + 2 may land there
     }
-    if (!ok && threadIdx.x == 0) atomicOr(&g_conv_status, STATUS_BAD_CU_SEQLENS);
+    if (tid == 0 && (!ok || timed_out))
+        atomicOr(&g_conv_status, timed_out ? STATUS_TIMEOUT : STATUS_BAD_CU_SEQLENS);
 }
 
 // Up to KDA_MAX_K snapshot targets, each [n_seqs][conv_dim][K] FP32.
@@ -308,9 +355,36 @@ template <int K>
 kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint16_t* out,
                   int total, int t_per_seq, const int* cu, int n_seqs, int heads, float eps,
                   cudaStream_t s, ConvSnaps snaps = {}, int n_snap = 0) {
-    dim3 grid((unsigned)((3 * heads * D + kCtaCh - 1) / kCtaCh), (total + kTok - 1) / kTok);
-    launch_pdl(conv_silu_l2_kernel<K>, grid, dim3(kThreads), 0, s, conv_state, x, w, out, total,
-               t_per_seq, cu, n_seqs, heads, eps);
+    const int conv_dim = 3 * heads * D;
+    const int groups = (conv_dim + kCtaCh - 1) / kCtaCh;
+    const int sms = sm_count();
+    if (sms <= 0) {
+        set_error("kda_conv_silu_l2: cannot query the multiprocessor count");
+        return KDA_ERR_CUDA;
+    }
+    // Token spans sized for about three resident CTAs per SM (the shared
+    // memory of two x blocks allows three), in whole blocks of kTok tokens.
+    const long long target = 3LL * sms;
+    long long span = ((long long)total * groups + target - 1) / target;
+    span = (span + kTok - 1) / kTok * kTok;
+    if (span < kTok) span = kTok;
+    const long long spans = (total + span - 1) / span;
+    CUtensorMap xmap;
+    if (!tma_map_bf16(&xmap, x, (uint64_t)conv_dim, (uint64_t)total, (uint64_t)conv_dim, kBoxCh,
+                      kTok, CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        set_error("kda_conv_silu_l2: cannot encode the TMA tensor map");
+        return KDA_ERR_CUDA;
+    }
+    cudaError_t e = cudaFuncSetAttribute(conv_silu_l2_kernel<K>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kConvSmem);
+    if (e != cudaSuccess) {
+        set_error("kda_conv_silu_l2: cannot reserve shared memory: %s", cudaGetErrorString(e));
+        return KDA_ERR_CUDA;
+    }
+    launch_pdl(conv_silu_l2_kernel<K>, dim3((unsigned)groups, (unsigned)spans), dim3(kThreads),
+               kConvSmem, s, xmap, conv_state, x, w, out, total, t_per_seq, cu, n_seqs, heads,
+               eps, (int)span);
     kda_status st = launch_result("kda_conv_silu_l2 (conv)");
     if (st != KDA_OK) return st;
     const size_t rows = (size_t)n_seqs * 3 * heads * D;
@@ -352,8 +426,6 @@ extern "C" kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, con
     const long long total = cu_seqlens ? (long long)t : (long long)t * n_seqs;
     KDA_REQUIRE(total <= 0x7fffffffLL && (long long)3 * heads * D * total < (1LL << 46),
                 KDA_ERR_INVALID_ARG, "kda_conv_silu_l2: problem too large");
-    KDA_REQUIRE((total + kTok - 1) / kTok <= 65535, KDA_ERR_INVALID_ARG,
-                "kda_conv_silu_l2: more than %d tokens in one call", 65535 * kTok);
     KDA_REQUIRE(!fault_injected(), KDA_ERR_CUDA, "kda_conv_silu_l2: injected launch failure");
     cudaStream_t s = as_stream(stream);
     const int tps = cu_seqlens ? 0 : t;
@@ -388,8 +460,7 @@ extern "C" kda_status kda_conv_silu_l2_k(float* conv_state, const uint16_t* x, c
                 KDA_MAX_CONV_KERNEL);
     KDA_REQUIRE(l2_eps >= 0.f, KDA_ERR_INVALID_ARG, "kda_conv_silu_l2_k: l2_eps must be >= 0");
     const long long total = (long long)krows * n_seqs;
-    KDA_REQUIRE(total <= 0x7fffffffLL && (long long)3 * heads * D * total < (1LL << 46) &&
-                    (total + kTok - 1) / kTok <= 65535,
+    KDA_REQUIRE(total <= 0x7fffffffLL && (long long)3 * heads * D * total < (1LL << 46),
                 KDA_ERR_INVALID_ARG, "kda_conv_silu_l2_k: problem too large");
     ConvSnaps sn = {};
     for (int t = 0; t < n_snap; ++t) {

@@ -36,6 +36,7 @@
 
 #include "kda_common.h"
 #include "sm103_tc.h"
+#include "tma_map.h"
 
 namespace kda {
 namespace {
@@ -1010,45 +1011,11 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
-                                            cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
 // BF16 [rows][cols] with a row pitch of `pitch_elems`; boxes of `box_cols`
 // channels x 64 tokens with the given shared-memory swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
               uint32_t box_cols, CUtensorMapSwizzle swizzle) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t gdim[2] = {cols, rows};
-    cuuint64_t gstride[1] = {pitch_elems * 2};
-    cuuint32_t box[2] = {box_cols, (cuuint32_t)C};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-int sm_count() {
-    static int counts[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (!counts[dev]) {
-        int n = 0;
-        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        counts[dev] = n;
-    }
-    return counts[dev];
+    return tma_map_bf16(m, base, cols, rows, pitch_elems, box_cols, (uint32_t)C, swizzle);
 }
 
 }  // namespace

@@ -1,0 +1,58 @@
+// Host helpers shared by the kernels that load tiles with TMA: the driver's
+// tensor-map encoder (resolved once through the runtime's entry-point query,
+// so the library links no driver library itself), a 2-D BF16 map, and the
+// multiprocessor count of the current device.
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+namespace kda {
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tma_encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                            cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// BF16 [rows][cols] with a row pitch of `pitch_elems` elements, copied in
+// boxes of box_cols x box_rows with the given shared-memory swizzle.  Rows
+// past the end read as zero.
+inline bool tma_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                         uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows,
+                         CUtensorMapSwizzle swizzle) {
+    auto fn = tma_encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {pitch_elems * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+inline int sm_count() {
+    static int counts[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!counts[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
+}  // namespace kda
