@@ -30,7 +30,7 @@ namespace {
 
 __device__ unsigned g_conv_status = 0;
 
-constexpr int kTok = 16;                   // tokens per CTA
+constexpr int kTok = 16;                   // tokens per x block
 constexpr int kThreads = 128;              // per CTA
 constexpr int kCh = 8;                     // channels per thread
 constexpr int kCtaCh = kThreads * kCh;     // channels per CTA (8 heads)
@@ -64,9 +64,6 @@ __device__ __forceinline__ bool find_seq(const int* __restrict__ cu, int n_seqs,
     return start >= 0 && start <= tau && tau < end;
 }
 
-__device__ __forceinline__ float silu(float a) {
-    return __fdividef(a, 1.0f + __expf(-a));  // rounded to BF16 by the caller
-}
 
 // Packed FP32 pair arithmetic (two channels per instruction).
 __device__ __forceinline__ unsigned long long pk(float2 v) {
@@ -85,21 +82,53 @@ __device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
     asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)), "l"(pk(c)));
     return upk(r);
 }
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
+    return upk(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(pk(a)), "l"(pk(b)));
+    return upk(r);
+}
+__device__ __forceinline__ float ex2_approx(float x) {  // 2^x, hardware approximation
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {  // 1/x, hardware approximation
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// SiLU of a channel pair, a / (1 + e^-a) with e^-a = 2^(-a log2 e), in FP32
+// (rounded to BF16 by the caller).
+__device__ __forceinline__ float2 silu2(float2 a) {
+    constexpr float kNegLog2e = -1.4426950408889634f;
+    const float2 t = mul2(a, make_float2(kNegLog2e, kNegLog2e));
+    const float2 d = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.f, 1.f));
+    return mul2(a, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
 
 // x arrives in blocks of kTok tokens x 1024 channels through TMA, as four
-// boxes of 256 channels ([box][token][256] in shared memory), double-buffered.
+// boxes of 256 channels ([box][token][256] in shared memory), in a ring of
+// kStages buffers with one mbarrier each.
 constexpr int kBoxCh = 256;
-constexpr uint32_t kBlkBytes = kTok * kCtaCh * 2;   // 32 KB
-constexpr uint32_t kConvSmem = 2 * kBlkBytes + 64;  // two blocks + two mbarriers
+constexpr int kStages = 2;
+constexpr int kCtasPerSm = 3;                                  // shared memory allows three
+constexpr uint32_t kBlkBytes = kTok * kCtaCh * 2;              // 32 KB
+constexpr uint32_t kConvSmem = kStages * kBlkBytes + 8 * kStages;
 
 template <int K>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 conv_silu_l2_kernel(const __grid_constant__ CUtensorMap xmap, const float* __restrict__ conv_state,
                     const uint16_t* __restrict__ x, const uint16_t* __restrict__ w,
                     uint16_t* __restrict__ out, int total, int t_per_seq,
                     const int* __restrict__ cu, int n_seqs, int heads, float l2_eps, int span) {
     extern __shared__ __align__(128) unsigned char sm[];
-    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 2 * kBlkBytes);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + kStages * kBlkBytes);
     pdl_wait();
     pdl_release();
     const int tid = threadIdx.x, lane = tid & 31;
@@ -117,22 +146,22 @@ conv_silu_l2_kernel(const __grid_constant__ CUtensorMap xmap, const float* __res
     const int nblk = (tok_end - tok0 + kTok - 1) / kTok;
 
     if (tid == 0) {
-        tc::mbar_init(bar, 1);
-        tc::mbar_init(bar + 1, 1);
+        for (int b = 0; b < kStages; ++b) tc::mbar_init(bar + b, 1);
         tc::fence_mbar_init();
     }
     __syncthreads();
     // boxes holding at least one channel of this group (conv_dim is a
     // multiple of 384, so the last group may cover fewer than four)
     const int nbox = min(kCtaCh / kBoxCh, (int)((conv_dim - ch0 + kBoxCh - 1) / kBoxCh));
-    auto load_block = [&](int i) {  // block i into buffer i & 1 (thread 0)
-        uint64_t* b = bar + (i & 1);
+    auto load_block = [&](int i) {  // block i into buffer i % kStages (thread 0)
+        uint64_t* b = bar + i % kStages;
         tc::mbar_arrive_expect_tx(b, (uint32_t)nbox * (kTok * kBoxCh * 2));
         for (int bx = 0; bx < nbox; ++bx)
-            tc::tma_load_2d(sm + (i & 1) * kBlkBytes + bx * (kTok * kBoxCh * 2), &xmap, b,
+            tc::tma_load_2d(sm + (i % kStages) * kBlkBytes + bx * (kTok * kBoxCh * 2), &xmap, b,
                             ch0 + bx * kBoxCh, tok0 + i * kTok);
     };
-    if (tid == 0) load_block(0);
+    if (tid == 0)
+        for (int i = 0; i < kStages - 1 && i < nblk; ++i) load_block(i);
 
     float2 wv[K][kCh / 2];  // tap j of channel pairs
 #pragma unroll
@@ -192,9 +221,10 @@ conv_silu_l2_kernel(const __grid_constant__ CUtensorMap xmap, const float* __res
     bool timed_out = false;
     for (int i = 0; i < nblk; ++i) {
         const int tb = tok0 + i * kTok;
-        if (tid == 0 && i + 1 < nblk) load_block(i + 1);  // its buffer was released below
-        if (!tc::mbar_wait(bar + (i & 1), (uint32_t)(i >> 1) & 1u)) timed_out = true;
-        const unsigned char* xb = sm + (i & 1) * kBlkBytes + xoff;
+        // block i + kStages - 1 reuses the buffer released at the end of iteration i - 1
+        if (tid == 0 && i + kStages - 1 < nblk) load_block(i + kStages - 1);
+        if (!tc::mbar_wait(bar + i % kStages, (uint32_t)(i / kStages) & 1u)) timed_out = true;
+        const unsigned char* xb = sm + (i % kStages) * kBlkBytes + xoff;
         uint4* op = reinterpret_cast<uint4*>(out + (size_t)tb * conv_dim + c);
         // One token: conv over the window, SiLU, the head's L2 scale, BF16 store.
         auto token = [&](int m) {
@@ -204,30 +234,30 @@ conv_silu_l2_kernel(const __grid_constant__ CUtensorMap xmap, const float* __res
             float2 y[kCh / 2];
 #pragma unroll
             for (int e = 0; e < kCh / 2; ++e) {
-                float2 a = make_float2(0.f, 0.f);
+                float2 a;
+                if constexpr (K > 1) {
+                    a = mul2(wv[0][e], hv[0][e]);
 #pragma unroll
-                for (int j = 0; j < K - 1; ++j) a = fma2(wv[j][e], hv[j][e], a);
-                a = fma2(wv[K - 1][e], xv[e], a);
+                    for (int j = 1; j < K - 1; ++j) a = fma2(wv[j][e], hv[j][e], a);
+                    a = fma2(wv[K - 1][e], xv[e], a);
+                } else {
+                    a = mul2(wv[0][e], xv[e]);
+                }
 #pragma unroll
                 for (int j = 0; j + 1 < K - 1; ++j) hv[j][e] = hv[j + 1][e];
                 if constexpr (K > 1) hv[K - 2][e] = xv[e];
-                y[e] = make_float2(silu(a.x), silu(a.y));
+                y[e] = silu2(a);
             }
             if (normalise) {  // uniform per half-warp
-                float p = 0.f;
+                float2 p2 = mul2(y[0], y[0]);
 #pragma unroll
-                for (int e = 0; e < kCh / 2; ++e) {
-                    p = __fmaf_rn(y[e].x, y[e].x, p);
-                    p = __fmaf_rn(y[e].y, y[e].y, p);
-                }
+                for (int e = 1; e < kCh / 2; ++e) p2 = fma2(y[e], y[e], p2);
+                float p = p2.x + p2.y;
 #pragma unroll
                 for (int off = 8; off > 0; off >>= 1) p += __shfl_xor_sync(hmask, p, off);
                 const float inv = rsqrtf(p + l2_eps);
 #pragma unroll
-                for (int e = 0; e < kCh / 2; ++e) {
-                    y[e].x *= inv;
-                    y[e].y *= inv;
-                }
+                for (int e = 0; e < kCh / 2; ++e) y[e] = mul2(y[e], make_float2(inv, inv));
             }
             if (active) {
                 uint4 o;
@@ -267,7 +297,7 @@ conv_silu_l2_kernel(const __grid_constant__ CUtensorMap xmap, const float* __res
                 token(m);
             }
         }
-        __syncthreads();  // every thread is done with buffer i & 1: block i + 2 may land there
+        __syncthreads();  // every thread is done with buffer i % kStages
     }
     if (tid == 0 && (!ok || timed_out))
         atomicOr(&g_conv_status, timed_out ? STATUS_TIMEOUT : STATUS_BAD_CU_SEQLENS);
@@ -362,9 +392,9 @@ kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint1
         set_error("kda_conv_silu_l2: cannot query the multiprocessor count");
         return KDA_ERR_CUDA;
     }
-    // Token spans sized for about three resident CTAs per SM (the shared
-    // memory of two x blocks allows three), in whole blocks of kTok tokens.
-    const long long target = 3LL * sms;
+    // Token spans sized for one wave of kCtasPerSm resident CTAs per SM, in
+    // whole blocks of kTok tokens.
+    const long long target = (long long)kCtasPerSm * sms;
     long long span = ((long long)total * groups + target - 1) / target;
     span = (span + kTok - 1) / kTok * kTok;
     if (span < kTok) span = kTok;
