@@ -19,6 +19,9 @@
 // (sequence, channel) state row to hold that sequence's last conv_kernel
 // inputs, reading the old row first; separating it from kernel 1 keeps any
 // CTA from reading a state row another CTA has already replaced.
+// Kernel 3 (conv_rows_kernel) replaces the pair for uniform batches of short
+// sequences (decode, the k-row form): one thread per (sequence, 8 channels)
+// walks the rows and rewrites its own state rows, and writes the snapshots.
 #include <cuda_bf16.h>
 
 #include "kda_common.h"
@@ -110,6 +113,34 @@ __device__ __forceinline__ float2 silu2(float2 a) {
     const float2 t = mul2(a, make_float2(kNegLog2e, kNegLog2e));
     const float2 d = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.f, 1.f));
     return mul2(a, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
+}
+
+// The end of one token for a thread's 8 channels, given the conv sums a:
+// SiLU, then (q and k heads) the head's L2 scale from a half-warp reduction,
+// then one rounding to BF16.  Both conv kernels go through this function, so
+// the same token gives the same bits whichever kernel computes it.
+__device__ __forceinline__ uint4 silu_l2_bf16(const float2 (&a)[kCh / 2], bool normalise,
+                                              unsigned hmask, float l2_eps) {
+    float2 y[kCh / 2];
+#pragma unroll
+    for (int e = 0; e < kCh / 2; ++e) y[e] = silu2(a[e]);
+    if (normalise) {  // uniform per half-warp
+        float2 p2 = mul2(y[0], y[0]);
+#pragma unroll
+        for (int e = 1; e < kCh / 2; ++e) p2 = fma2(y[e], y[e], p2);
+        float p = p2.x + p2.y;
+#pragma unroll
+        for (int off = 8; off > 0; off >>= 1) p += __shfl_xor_sync(hmask, p, off);
+        const float inv = rsqrtf(p + l2_eps);
+#pragma unroll
+        for (int e = 0; e < kCh / 2; ++e) y[e] = mul2(y[e], make_float2(inv, inv));
+    }
+    uint4 o;
+    o.x = f32x2_to_bf16x2(y[0].x, y[0].y);
+    o.y = f32x2_to_bf16x2(y[1].x, y[1].y);
+    o.z = f32x2_to_bf16x2(y[2].x, y[2].y);
+    o.w = f32x2_to_bf16x2(y[3].x, y[3].y);
+    return o;
 }
 
 // x arrives in blocks of kTok tokens x 1024 channels through TMA, as four
@@ -231,42 +262,23 @@ conv_silu_l2_kernel(const __grid_constant__ CUtensorMap xmap, const float* __res
             const uint4 xm = *reinterpret_cast<const uint4*>(xb + m * (kBoxCh * 2));
             const float2 xv[kCh / 2] = {bf16x2_to_f32(xm.x), bf16x2_to_f32(xm.y),
                                         bf16x2_to_f32(xm.z), bf16x2_to_f32(xm.w)};
-            float2 y[kCh / 2];
+            float2 a[kCh / 2];
 #pragma unroll
             for (int e = 0; e < kCh / 2; ++e) {
-                float2 a;
                 if constexpr (K > 1) {
-                    a = mul2(wv[0][e], hv[0][e]);
+                    a[e] = mul2(wv[0][e], hv[0][e]);
 #pragma unroll
-                    for (int j = 1; j < K - 1; ++j) a = fma2(wv[j][e], hv[j][e], a);
-                    a = fma2(wv[K - 1][e], xv[e], a);
+                    for (int j = 1; j < K - 1; ++j) a[e] = fma2(wv[j][e], hv[j][e], a[e]);
+                    a[e] = fma2(wv[K - 1][e], xv[e], a[e]);
                 } else {
-                    a = mul2(wv[0][e], xv[e]);
+                    a[e] = mul2(wv[0][e], xv[e]);
                 }
 #pragma unroll
                 for (int j = 0; j + 1 < K - 1; ++j) hv[j][e] = hv[j + 1][e];
                 if constexpr (K > 1) hv[K - 2][e] = xv[e];
-                y[e] = silu2(a);
             }
-            if (normalise) {  // uniform per half-warp
-                float2 p2 = mul2(y[0], y[0]);
-#pragma unroll
-                for (int e = 1; e < kCh / 2; ++e) p2 = fma2(y[e], y[e], p2);
-                float p = p2.x + p2.y;
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1) p += __shfl_xor_sync(hmask, p, off);
-                const float inv = rsqrtf(p + l2_eps);
-#pragma unroll
-                for (int e = 0; e < kCh / 2; ++e) y[e] = mul2(y[e], make_float2(inv, inv));
-            }
-            if (active) {
-                uint4 o;
-                o.x = f32x2_to_bf16x2(y[0].x, y[0].y);
-                o.y = f32x2_to_bf16x2(y[1].x, y[1].y);
-                o.z = f32x2_to_bf16x2(y[2].x, y[2].y);
-                o.w = f32x2_to_bf16x2(y[3].x, y[3].y);
-                op[(size_t)m * (conv_dim / kCh)] = o;
-            }
+            const uint4 o = silu_l2_bf16(a, normalise, hmask, l2_eps);
+            if (active) op[(size_t)m * (conv_dim / kCh)] = o;
         };
         if (ok && tb + kTok <= tok_end && tb + kTok <= end) {
             // Common case: the block's tokens lie in one sequence; straight-line
@@ -311,7 +323,7 @@ struct ConvSnaps {
 template <int K>
 __global__ void conv_state_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
                                   int total, int t_per_seq, const int* __restrict__ cu,
-                                  int n_seqs, int heads, ConvSnaps snaps, int n_snap) {
+                                  int n_seqs, int heads) {
     pdl_wait();  // the conv kernel has read the old state
     pdl_release();
     const size_t conv_dim = (size_t)3 * heads * D;
@@ -339,14 +351,6 @@ __global__ void conv_state_kernel(float* __restrict__ conv_state, const uint16_t
     float old[K], nw[K];
     // a state row of 4 slots moves as one 16-byte access (rows are 16-byte
     // aligned: conv_state is, and K = 4 makes every row 16 bytes)
-    auto store_row = [&](float* dst, const float (&r)[K]) {
-        if constexpr (K == 4) {
-            *reinterpret_cast<float4*>(dst) = make_float4(r[0], r[1], r[2], r[3]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < K; ++j) dst[j] = r[j];
-        }
-    };
     if constexpr (K == 4) {
         const float4 o4 = *reinterpret_cast<const float4*>(st);
         old[0] = o4.x;
@@ -357,28 +361,141 @@ __global__ void conv_state_kernel(float* __restrict__ conv_state, const uint16_t
 #pragma unroll
         for (int j = 0; j < K; ++j) old[j] = st[j];
     }
-    // snapshot t: the state after the sequence's row t, i.e. its window of
-    // the K inputs ending at row t (older slots from the old state)
-    for (int tt = 0; tt < n_snap && tt < len; ++tt) {
-        float sv[K];
-#pragma unroll
-        for (int j = 0; j < K; ++j) {
-            const int rel = tt + 1 - K + j;
-            float val = old[K - 1];
-#pragma unroll
-            for (int jj = 0; jj < K; ++jj)
-                if (rel < 0 && jj == K + rel) val = old[jj];
-            sv[j] = (rel >= 0) ? bf16_to_f32(__ldg(x + (size_t)(start + rel) * conv_dim + c)) : val;
-        }
-        store_row(snaps.p[tt] + idx * K, sv);
-    }
 #pragma unroll
     for (int j = 0; j < K; ++j) {
         const int rel = len - K + j;  // position relative to the sequence start
-        nw[j] = (rel >= 0) ? bf16_to_f32(__ldg(x + (size_t)(start + rel) * conv_dim + c))
-                           : old[(j + len < K) ? j + len : K - 1];
+        float kept = old[K - 1];  // old[min(j + len, K - 1)], selected without indexing
+#pragma unroll
+        for (int jj = 0; jj < K - 1; ++jj)
+            if (jj == j + len) kept = old[jj];
+        nw[j] = (rel >= 0) ? bf16_to_f32(__ldg(x + (size_t)(start + rel) * conv_dim + c)) : kept;
     }
-    store_row(st, nw);
+    if constexpr (K == 4) {
+        *reinterpret_cast<float4*>(st) = make_float4(nw[0], nw[1], nw[2], nw[3]);
+    } else {
+#pragma unroll
+        for (int j = 0; j < K; ++j) st[j] = nw[j];
+    }
+}
+
+// Uniform batches of short sequences (rows <= KDA_MAX_K tokens each: the
+// decode-time update and the k-row form).  One thread per (sequence, 8
+// channels) takes its window from the sequence's conv state, runs the rows in
+// order and writes the outputs, snapshot t (the window ending at row t) and
+// the new state.  A state row is read and rewritten by the thread that owns
+// it, so this one launch replaces the conv and state-rewrite pair.
+constexpr int kRowsThreads = 256;
+
+template <int K>
+__global__ void __launch_bounds__(kRowsThreads)
+conv_rows_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
+                 const uint16_t* __restrict__ w, uint16_t* __restrict__ out, int rows, int n_seqs,
+                 int heads, float l2_eps, ConvSnaps snaps, int n_snap) {
+    pdl_wait();
+    pdl_release();
+    const int conv_dim = 3 * heads * D;
+    const int per_seq = conv_dim / kCh;  // threads per sequence, a multiple of 16
+    const long long idx = (long long)blockIdx.x * kRowsThreads + threadIdx.x;
+    // n_seqs * per_seq is a multiple of 16: a half-warp is wholly in or out
+    if (idx >= (long long)n_seqs * per_seq) return;
+    const int n = (int)(idx / per_seq);
+    const int c = (int)(idx % per_seq) * kCh;
+    const bool normalise = c < 2 * heads * D;
+    const unsigned hmask = 0xffffu << (threadIdx.x & 16);
+
+    float2 wv[K][kCh / 2];
+    bool w_vec = false;
+    if constexpr (K == 4) w_vec = (reinterpret_cast<uintptr_t>(w) & 15) == 0;
+    if (w_vec) {
+        // the 8 channels' taps are 64 contiguous bytes: four 16-byte loads
+        const uint4* w4 = reinterpret_cast<const uint4*>(w + (size_t)c * K);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {  // q covers channels 2q and 2q + 1
+            const uint4 u = __ldg(w4 + q);
+            const float2 lo0 = bf16x2_to_f32(u.x), lo1 = bf16x2_to_f32(u.y);  // channel 2q
+            const float2 hi0 = bf16x2_to_f32(u.z), hi1 = bf16x2_to_f32(u.w);  // channel 2q+1
+            wv[0][q] = make_float2(lo0.x, hi0.x);
+            wv[1 % K][q] = make_float2(lo0.y, hi0.y);  // (K == 4 here)
+            wv[2 % K][q] = make_float2(lo1.x, hi1.x);
+            wv[3 % K][q] = make_float2(lo1.y, hi1.y);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < K; ++j)
+#pragma unroll
+            for (int e = 0; e < kCh / 2; ++e)
+                wv[j][e] = make_float2(bf16_to_f32(__ldg(w + (size_t)(c + 2 * e) * K + j)),
+                                       bf16_to_f32(__ldg(w + (size_t)(c + 2 * e + 1) * K + j)));
+    }
+    // win[j][e]: channel pair e's input at row r - (K - 1) + j; before row 0,
+    // slots 1..K-1 of the state are the inputs before the sequence.
+    float* st = conv_state + ((size_t)n * conv_dim + c) * K;  // 8 channels x K slots
+    float2 win[K][kCh / 2];
+    if constexpr (K == 4) {
+#pragma unroll
+        for (int e = 0; e < kCh / 2; ++e) {
+            const float4 s0 = __ldg(reinterpret_cast<const float4*>(st) + 2 * e);
+            const float4 s1 = __ldg(reinterpret_cast<const float4*>(st) + 2 * e + 1);
+            win[0][e] = make_float2(s0.y, s1.y);
+            win[1][e] = make_float2(s0.z, s1.z);
+            win[2][e] = make_float2(s0.w, s1.w);
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < K - 1; ++j)
+#pragma unroll
+            for (int e = 0; e < kCh / 2; ++e)
+                win[j][e] = make_float2(__ldg(st + (2 * e) * K + j + 1),
+                                        __ldg(st + (2 * e + 1) * K + j + 1));
+    }
+    // window of K slots of 8 channels to a [channel][slot] state row
+    auto store_window = [&](float* dst) {
+        if constexpr (K == 4) {
+#pragma unroll
+            for (int e = 0; e < kCh / 2; ++e) {
+                reinterpret_cast<float4*>(dst)[2 * e] =
+                    make_float4(win[0][e].x, win[1][e].x, win[2][e].x, win[3][e].x);
+                reinterpret_cast<float4*>(dst)[2 * e + 1] =
+                    make_float4(win[0][e].y, win[1][e].y, win[2][e].y, win[3][e].y);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < K; ++j)
+#pragma unroll
+                for (int e = 0; e < kCh / 2; ++e) {
+                    dst[(2 * e) * K + j] = win[j][e].x;
+                    dst[(2 * e + 1) * K + j] = win[j][e].y;
+                }
+        }
+    };
+    const size_t row0 = (size_t)n * rows;
+    uint4 xn = __ldg(reinterpret_cast<const uint4*>(x + row0 * conv_dim + c));
+#pragma unroll
+    for (int r = 0; r < KDA_MAX_K; ++r) {  // unrolled: snaps.p[r] stays a parameter read
+        if (r >= rows) continue;
+        const uint4 xm = xn;
+        if (r + 1 < rows)  // the next row's load overlaps this row's arithmetic
+            xn = __ldg(reinterpret_cast<const uint4*>(x + (row0 + r + 1) * conv_dim + c));
+        win[K - 1][0] = bf16x2_to_f32(xm.x);
+        win[K - 1][1] = bf16x2_to_f32(xm.y);
+        win[K - 1][2] = bf16x2_to_f32(xm.z);
+        win[K - 1][3] = bf16x2_to_f32(xm.w);
+        float2 a[kCh / 2];
+#pragma unroll
+        for (int e = 0; e < kCh / 2; ++e) {  // the same operations as the span kernel
+            a[e] = mul2(wv[0][e], win[0][e]);
+#pragma unroll
+            for (int j = 1; j < K; ++j) a[e] = fma2(wv[j][e], win[j][e], a[e]);
+        }
+        const uint4 o = silu_l2_bf16(a, normalise, hmask, l2_eps);
+        *reinterpret_cast<uint4*>(out + (row0 + r) * conv_dim + c) = o;
+        if (r < n_snap) store_window(snaps.p[r] + ((size_t)n * conv_dim + c) * K);
+        if (r + 1 == rows) store_window(st);
+#pragma unroll
+        for (int j = 0; j + 1 < K; ++j)
+#pragma unroll
+            for (int e = 0; e < kCh / 2; ++e) win[j][e] = win[j + 1][e];
+    }
 }
 
 template <int K>
@@ -386,6 +503,14 @@ kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint1
                   int total, int t_per_seq, const int* cu, int n_seqs, int heads, float eps,
                   cudaStream_t s, ConvSnaps snaps = {}, int n_snap = 0) {
     const int conv_dim = 3 * heads * D;
+    if (!cu && t_per_seq <= KDA_MAX_K) {
+        const long long threads = (long long)n_seqs * (conv_dim / kCh);
+        launch_pdl(conv_rows_kernel<K>,
+                   dim3((unsigned)((threads + kRowsThreads - 1) / kRowsThreads)),
+                   dim3(kRowsThreads), 0, s, conv_state, x, w, out, t_per_seq, n_seqs, heads, eps,
+                   snaps, n_snap);
+        return launch_result("kda_conv_silu_l2 (rows)");
+    }
     const int groups = (conv_dim + kCtaCh - 1) / kCtaCh;
     const int sms = sm_count();
     if (sms <= 0) {
@@ -419,7 +544,7 @@ kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint1
     if (st != KDA_OK) return st;
     const size_t rows = (size_t)n_seqs * 3 * heads * D;
     launch_pdl(conv_state_kernel<K>, dim3((unsigned)((rows + 255) / 256)), dim3(256), 0, s,
-               conv_state, x, total, t_per_seq, cu, n_seqs, heads, snaps, n_snap);
+               conv_state, x, total, t_per_seq, cu, n_seqs, heads);
     return launch_result("kda_conv_silu_l2 (state)");
 }
 

@@ -175,9 +175,13 @@ size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads
  *       ([n_seqs][t][conv_dim]); decode is t == 1.
  *   cu_seqlens != NULL: DEVICE int32 [n_seqs + 1] offsets, t = total tokens;
  *       checked on the device like kda_prefill's.
- *   1 <= conv_kernel <= KDA_MAX_CONV_KERNEL; (2*heads*128) % 256 == 0.
- * Two kernels are enqueued: the conv (reads the old state) and the state
- * update (writes the last conv_kernel inputs of each sequence).
+ *   1 <= conv_kernel <= KDA_MAX_CONV_KERNEL.
+ * With cu_seqlens == NULL and t <= KDA_MAX_K (decode and other short uniform
+ * batches) one kernel is enqueued: each thread carries 8 channels of one
+ * sequence through its t rows and rewrites that sequence's state rows itself.
+ * Otherwise two: the conv over spans of tokens (reads the old state) and the
+ * state update (writes the last conv_kernel inputs of each sequence).  Both
+ * forms give the same bits for the same tokens.
  */
 kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, const uint16_t* w,
                             uint16_t* out, int t, int n_seqs, const int* cu_seqlens,
@@ -222,7 +226,8 @@ kda_status kda_o_norm_gated(const float* core, const uint16_t* gate, const uint1
  *                [n_seqs][conv_dim][conv_kernel], 16-byte aligned, distinct from
  *                conv_state (read on the host during the call only)
  *   1 <= krows <= KDA_MAX_K; 0 <= n_snap <= krows; other limits as
- *   kda_conv_silu_l2.  Two kernels are enqueued.
+ *   kda_conv_silu_l2.  One kernel is enqueued (kda_conv_silu_l2's short-rows
+ *   form, which also writes the snapshots).
  */
 kda_status kda_conv_silu_l2_k(float* conv_state, const uint16_t* x, const uint16_t* w,
                               uint16_t* out, int n_seqs, int krows, int conv_kernel, float l2_eps,

@@ -42,19 +42,29 @@ def test_conv_varlen_matches_oracle(orc, K_, lengths):
     np.testing.assert_array_equal(st_d.cpu().double().numpy(), st_ref)
 
 
-def test_conv_decode_stream_equals_prefill():
-    """Eight single-token calls for 5 sequences at once (decode) give the
-    same bits as one 8-token prefill call per sequence."""
+@pytest.mark.parametrize("K_,T", [(4, 8), (4, 20), (3, 8), (1, 5)])
+def test_conv_decode_stream_equals_prefill(K_, T):
+    """T single-token calls for 5 sequences at once (decode, the short-rows
+    kernel) give the same bits as one T-token prefill call per sequence, in
+    the uniform form (short-rows kernel for T <= 8) and in the varlen form
+    (the token-span kernel)."""
     K = kda()
-    H, N, T, K_ = 1, 5, 8, 4
+    H, N = 1, 5
     ch = 3 * H * 128
-    gen = torch.Generator().manual_seed(3)
+    gen = torch.Generator().manual_seed(3 + T + K_)
     x = torch.randn((N, T, ch), generator=gen).to(torch.bfloat16).cuda()
     w = (torch.randn((ch, K_), generator=gen) * 0.5).to(torch.bfloat16).cuda()
     st0 = torch.randn((N, ch, K_), generator=gen).cuda()
     out_p = torch.empty_like(x)
     st_p = st0.clone()
     K.kda_conv_silu_l2(st_p, x.reshape(N * T, ch), w, out_p.reshape(N * T, ch), n_seqs=N)
+    out_v = torch.empty_like(x)
+    st_v = st0.clone()
+    cu = torch.arange(0, N * T + 1, T, dtype=torch.int32, device="cuda")
+    K.kda_conv_silu_l2(st_v, x.reshape(N * T, ch), w, out_v.reshape(N * T, ch), cu_seqlens=cu)
+    K.kda_sync_status()
+    assert torch.equal(out_v, out_p)
+    assert torch.equal(st_v, st_p)
     st_d = st0.clone()
     for t in range(T):
         o1 = torch.empty((N, ch), dtype=torch.bfloat16, device="cuda")
