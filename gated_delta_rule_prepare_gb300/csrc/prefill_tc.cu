@@ -21,6 +21,11 @@
 //   X = V - Ktil S;  U = T X;  O = Qtil S + P U;  S <- dec (.) S + Khat^T U
 // as three tensor-core round trips per chunk; the chunk's operands arrive by
 // bulk copy from the workspace and the value slice by TMA.
+// prefill_fused_kernel runs both in one cooperative grid when there are few
+// (sequence, head) chains: one SM per chain carries the whole state in the
+// transposed form (scan_t_role, chain operands in TMEM) while the other SMs
+// walk the prepare items in chunk order and release a ready flag per item,
+// so the prepare work no longer precedes the scan.
 //
 // A and P come from tensor-core products over column blocks b with a
 // reference token m_b: e^(Gamma_r-Gamma_s) = e^(Gamma_r-Gamma_mb)
@@ -32,6 +37,9 @@
 #include <cuda_bf16.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "kda_common.h"
@@ -197,10 +205,15 @@ __device__ __forceinline__ bool seq_range(const int* __restrict__ cu, int n, int
 // chunk_off[n] = number of chunks of all sequences before n (one CTA).
 constexpr int MAP_THREADS = 1024;
 __global__ void __launch_bounds__(MAP_THREADS)
-chunk_map_kernel(const int* __restrict__ cu, int n_seqs, int t, int* __restrict__ chunk_off) {
+chunk_map_kernel(const int* __restrict__ cu, int n_seqs, int t, int* __restrict__ chunk_off,
+                 unsigned* __restrict__ ready, long long n_ready) {
     __shared__ int part[MAP_THREADS];
     pdl_wait();
     pdl_release();
+    // the fused grid's ready flags start cleared (n_ready is a multiple of 4
+    // and `ready` 16-byte aligned)
+    for (long long i = threadIdx.x; i < n_ready / 4; i += MAP_THREADS)
+        reinterpret_cast<uint4*>(ready)[i] = make_uint4(0u, 0u, 0u, 0u);
     const int per = (n_seqs + MAP_THREADS - 1) / MAP_THREADS;
     const int lo = threadIdx.x * per, hi = min(n_seqs, lo + per);
     int sum = 0;
@@ -280,20 +293,22 @@ __device__ __forceinline__ PrepItem prep_item(long long item, int heads, const i
     return it;
 }
 
-__global__ void __launch_bounds__(NTP, 1)
-prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict__ beta, int t,
-               int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
-               unsigned char* __restrict__ ws) {
+// The prepare walk of one CTA: items first, first + stride, ...  When `ready`
+// is set, each finished item's flag (ready[item]) is released once its
+// operands are in the workspace.
+__device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_t* __restrict__ beta,
+                                             int t, int t_pad, int heads,
+                                             const int* __restrict__ cu, int n_seqs,
+                                             unsigned char* __restrict__ ws, long long first,
+                                             long long stride, unsigned* __restrict__ ready) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column quarter
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
 
-    pdl_wait();  // the chunk map (and the callers' inputs) are complete
-    pdl_release();
     const int* chunk_off = reinterpret_cast<const int*>(ws);
     const long long items = (long long)__ldg(chunk_off + n_seqs) * heads;
-    if ((long long)blockIdx.x >= items) return;
+    if (first >= items) return;
     if (tc::smem_u32(sm) & 1023u) {  // the swizzled tiles need a 1024-byte aligned base
         if (tid == 0) atomicOr(&g_tc_status, STATUS_SMEM_ALIGN);
         return;
@@ -359,14 +374,14 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                    : 0.f;
     };
 
-    long long item = blockIdx.x;
+    long long item = first;
     PrepItem cur = prep_item(item, heads, cu, chunk_off, n_seqs, t, t_pad);
     load_raw(cur, 0);
     float beta_cur = load_beta(cur);
 
     for (int iter = 0; item < items; ++iter) {
         const int b = iter & 1;
-        const long long nitem = item + gridDim.x;
+        const long long nitem = item + stride;
         PrepItem nxt = {};
         nxt.valid = false;
         float beta_nxt = 0.f;
@@ -736,6 +751,12 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
             tc::tc_fence_before();
             __syncthreads();  // buffer b is free for the item after next
         }
+        // every thread's stores of this item precede the barrier above (an
+        // invalid item stores nothing)
+        if (ready && tid == 0) {
+            tc::bulk_wait_all();
+            tc::flag_release(ready + item, 1u);
+        }
         item = nitem;
         cur = nxt;
         beta_cur = beta_nxt;
@@ -747,6 +768,15 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 64);
     }
+}
+
+__global__ void __launch_bounds__(NTP, 1)
+prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict__ beta, int t,
+               int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
+               unsigned char* __restrict__ ws) {
+    pdl_wait();  // the chunk map (and the callers' inputs) are complete
+    pdl_release();
+    prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x, nullptr);
 }
 
 template <int DVv>
@@ -1011,6 +1041,339 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     }
 }
 
+// ------------------------------------------------------------ transposed scan
+// One CTA per (sequence, head) carries the whole 128 x 128 state through the
+// chunks in transposed form, so that each matrix on the state's chain is the
+// A operand of the next product and stays in TMEM (lane = value column j,
+// one column per K index):
+//   X^T = V^T - S^T Ktil^T;  U^T = X^T T^T;  O^T = S^T Qtil^T + U^T P^T;
+//   S^T <- S^T diag(dec) + U^T Khat
+// The prepared operands are the B operands, in the layouts prepare writes:
+// [Ktil; Qtil] (rows = tokens), [T; P] (rows = tokens) and Khat^T (rows = key
+// channels).  S^T, X^T and U^T enter TMEM by tcgen05.st from the threads that
+// computed them, so no operand passes through shared memory on the chain.
+struct ScanT {
+    static constexpr int NT = 512;  // 4 lane quarters x 4 column groups
+    // shared memory: blob image (OPX | TP | KH | DEC; its OPX is operand
+    // buffer 0), value tile [64][128] BF16 (no swizzle), a copy of dec,
+    // operand buffer 1 for [Ktil; Qtil], barriers
+    static constexpr uint32_t RAWV = (BLOB_BYTES + 1023) & ~1023u;
+    static constexpr uint32_t DECC = RAWV + 64 * D * 2;
+    static constexpr uint32_t OPX1 = (DECC + D * 4 + 1023) & ~1023u;
+    static constexpr uint32_t BAR = OPX1 + OpX::bytes(128);
+    static constexpr uint32_t TOTAL = BAR + 64;
+    // TMEM columns: S^T (A); two 128-column chunk regions used alternately
+    // (Ktil S | Qtil S then O, or X^T / U^T (A) | T X); Khat^T U as dS^T
+    static constexpr uint32_t T_S = 0, R0 = 128, R1 = 256, T_D3 = 384;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(TOTAL <= 232448, "shared memory budget exceeded");
+};
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    float a[16], b[16];
+    tc::tmem_ld16(taddr, a);
+    tc::tmem_ld16(taddr + 16, b);
+    tc::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        v[i] = a[i];
+        v[16 + i] = b[i];
+    }
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+    float a[16], b[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        a[i] = v[i];
+        b[i] = v[16 + i];
+    }
+    tc::tmem_st16(taddr, a);
+    tc::tmem_st16(taddr + 16, b);
+}
+
+// The chain of (sequence n, head h).  When `ready` is set, chunk g's operands
+// are read only after ready[g * heads + h] has been released by the CTA that
+// prepared them (the prepare and scan roles then share one cooperative grid).
+//
+// Per chunk: three tensor-core round trips of 16, 8 and 16 K-steps (the
+// tensor core takes about the same time per instruction for any N <= 128,
+// so Qtil S rides with Ktil S and P U with Khat^T U).  [Ktil; Qtil] is
+// double-buffered and requested a chunk ahead; the value tile and [T; P],
+// Khat^T, dec as soon as their buffers are consumed.
+__device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __restrict__ state,
+                                            float* __restrict__ o, int t, int t_pad, int heads,
+                                            const int* __restrict__ cu, int n_seqs,
+                                            const unsigned char* __restrict__ ws, int h, int n,
+                                            const unsigned* __restrict__ ready) {
+    extern __shared__ __align__(1024) unsigned char sm[];
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int qd = warp & 3, cg = warp >> 2;  // TMEM lane quarter, column group
+    const int j = 32 * qd + (tid & 31);       // value column = TMEM lane
+    const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+
+    int start, end;
+    if (!seq_range(cu, n, n_seqs, t, t_pad, start, end)) {
+        if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
+        return;
+    }
+    const long long g0 = __ldg(reinterpret_cast<const int*>(ws) + n);
+    if (tc::smem_u32(sm) & 1023u) {
+        if (tid == 0) atomicOr(&g_tc_status, STATUS_SMEM_ALIGN);
+        return;
+    }
+
+    const float* DEC = reinterpret_cast<const float*>(sm + SS_DEC);
+    float* DECC = reinterpret_cast<float*>(sm + ScanT::DECC);
+    const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + ScanT::RAWV);
+    uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + ScanT::BAR);  // [2]: operand buffers
+    uint64_t* bar_v = bar_x + 2;
+    uint64_t* bar_b = bar_x + 3;
+    uint64_t* bar_mma = bar_x + 4;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ScanT::BAR + 48);
+    int* abort_flag = reinterpret_cast<int*>(sm + ScanT::BAR + 52);
+    const uint32_t s_opx0 = tc::smem_u32(sm + SS_OPX), s_opx1 = tc::smem_u32(sm + ScanT::OPX1);
+    const uint32_t s_tp = tc::smem_u32(sm + SS_TP), s_kh = tc::smem_u32(sm + SS_KH);
+
+    if (tid == 0) {
+        for (int i = 0; i < 5; ++i) tc::mbar_init(bar_x + i, 1);
+        tc::fence_mbar_init();
+        tc::prefetch_tmap(&vmap);
+        *abort_flag = 0;
+    }
+    if (warp == 0) tc::tmem_alloc(tmem_slot, ScanT::TMEM_COLS);
+    tc::tc_fence_before();
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t my = tmem + lane_base;  // this thread's TMEM lane
+
+    // state: thread (j, cg) owns S[32 cg + i][j], i < 32, kept in FP32
+    float* Sg = state + ((size_t)n * heads + h) * D * D + (size_t)(32 * cg) * D + j;
+    float sreg[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) sreg[i] = Sg[(size_t)i * D];
+    {
+        float sv[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[i] = tc::to_tf32(sreg[i]);
+        tmem_st32(my + ScanT::T_S + 32 * cg, sv);
+        tc::tmem_st_wait();
+    }
+
+    uint32_t ph_mma = 0, ph_v = 0, ph_b = 0, ph_x = 0;  // ph_x: bit per buffer
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+        if (!tc::mbar_wait(bar, parity)) {
+            atomicOr(&g_tc_status, STATUS_TIMEOUT);
+            *abort_flag = 1;
+        }
+    };
+    // Copies (thread 0).  Outstanding ones are tracked so an early exit can
+    // let them land before the shared memory is released.
+    uint32_t out_x = 0;  // bit per operand buffer
+    bool out_v = false, out_b = false;
+    auto load_x = [&](long long gg, int xb) {  // [Ktil; Qtil] of chunk gg, after its flag
+        if (ready && !tc::flag_acquire(ready + gg * heads + h)) {
+            atomicOr(&g_tc_status, STATUS_TIMEOUT);
+            *abort_flag = 1;
+        }
+        const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
+        unsigned char* dst = sm + (xb ? ScanT::OPX1 : (uint32_t)SS_OPX);
+        tc::mbar_arrive_expect_tx(bar_x + xb, OpX::bytes(128));
+        tc::bulk_load(dst, blob + BLOB_OPX, OpX::bytes(128), bar_x + xb);
+        out_x |= 1u << xb;
+    };
+    auto load_v = [&](int cc0) {
+        tc::mbar_arrive_expect_tx(bar_v, 64 * D * 2);
+        tc::tma_load_2d(sm + ScanT::RAWV, &vmap, bar_v, h * D, cc0);
+        out_v = true;
+    };
+    auto load_b = [&](long long gg) {  // issued after load_x(gg): its flag is observed
+        const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
+        tc::mbar_arrive_expect_tx(bar_b, OpTP::bytes(64) + OpKH::bytes(64) + 128 * 4);
+        tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTP::bytes(64), bar_b);
+        tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKH::bytes(64), bar_b);
+        tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_b);
+        out_b = true;
+    };
+    if (tid == 0 && start < end) {
+        load_x(g0, 0);
+        load_v(start);
+        load_b(g0);
+    }
+
+    // O of a chunk is read back during the next chunk's first product (off
+    // the state's chain): the chunk regions alternate, chunk parity xb
+    // computing [Ktil S | Qtil S -> O] in R_xb and X^T, U^T (A) and T X in
+    // R_(1-xb), so the next chunk's T X lands on this chunk's O only after it
+    // has been read.
+    int o_c0 = -1, o_L = 0;  // the chunk whose O is still to be written
+    uint32_t o_reg = 0;
+    auto write_o = [&]() {  // O[r][j], r = 16 cg + i
+        float v[16];
+        tc::tmem_ld16(my + o_reg + 16 * cg, v);
+        tc::tmem_ld_wait();
+        float* orow = o + ((size_t)o_c0 * heads + h) * D + j;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * cg + i;
+            if (r < o_L) orow[(size_t)r * heads * D] = v[i];
+        }
+    };
+
+    long long g = g0;
+    int xb = 0;
+    for (int c0 = start; c0 < end; c0 += C, ++g, xb ^= 1) {
+        const int L = min(C, end - c0);
+        const bool more = c0 + C < end;
+        const uint32_t r_d1 = xb ? ScanT::R1 : ScanT::R0;  // Ktil S, then Qtil S / O at +64
+        const uint32_t r_a = xb ? ScanT::R0 : ScanT::R1;   // X^T / U^T (A), then T X at +64
+        tc::tc_fence_before();
+        if (__syncthreads_or(*abort_flag)) break;  // every thread takes the same exit
+        wait_bar(bar_x + xb, (ph_x >> xb) & 1u);
+        ph_x ^= 1u << xb;
+        if (tid == 0) out_x &= ~(1u << xb);
+        wait_bar(bar_v, ph_v);
+        ph_v ^= 1;
+        if (tid == 0) out_v = false;
+
+        // ---------------------------------------------------------- S^T [Ktil; Qtil]^T
+        // (one N = 128 product: Ktil S into r_d1, Qtil S into r_d1 + 64)
+        if (tid == 0) {
+            tc::tc_fence_after();
+            for (int ks = 0; ks < 16; ++ks)
+                tc::mma_tf32_ta(tmem + r_d1, tmem + ScanT::T_S + 8 * ks,
+                                OpX::desc(xb ? s_opx1 : s_opx0, ks), tc::idesc_tf32(128, 128),
+                                ks > 0);
+            tc::mma_commit(bar_mma);
+            // the next chunk's [Ktil; Qtil] (its ready flag and the copy) while
+            // this product runs; that buffer's last products have completed
+            if (more) load_x(g + 1, xb ^ 1);
+        }
+        if (o_c0 >= 0) write_o();  // the previous chunk's output, in r_a + 64
+        float vr[16];  // V[16 cg + i][j], read while the product runs
+#pragma unroll
+        for (int i = 0; i < 16; ++i) vr[i] = bf(RAWV[(16 * cg + i) * D + j]);
+        wait_bar(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        tc::tc_fence_after();
+        {   // X^T[j][r] = V[r][j] - (Ktil S)[r][j], r = 16 cg + i
+            float v[16];
+            tc::tmem_ld16(my + r_d1 + 16 * cg, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * cg + i;
+                const float x = (r < L) ? vr[i] - v[i] : 0.f;
+                v[i] = tc::to_tf32(x);
+            }
+            tc::tmem_st16(my + r_a + 16 * cg, v);
+            tc::tmem_st_wait();
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+        if (tid == 0 && more) load_v(c0 + C);  // the value tile is consumed
+        wait_bar(bar_b, ph_b);
+        ph_b ^= 1;
+        if (tid == 0) out_b = false;
+        if (tid < D) DECC[tid] = DEC[tid];  // read after the next barrier
+
+        // ---------------------------------------------------------- U^T = X^T T^T
+        if (tid == 0) {
+            tc::tc_fence_after();
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_tf32_ta(tmem + r_a + 64, tmem + r_a + 8 * ks, OpTP::desc(s_tp, ks),
+                                tc::idesc_tf32(128, 64), ks > 0);
+            tc::mma_commit(bar_mma);
+        }
+        wait_bar(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        tc::tc_fence_after();
+        {
+            float v[16];
+            tc::tmem_ld16(my + r_a + 64 + 16 * cg, v);
+            tc::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = tc::to_tf32(v[i]);
+            tc::tmem_st16(my + r_a + 16 * cg, v);
+            tc::tmem_st_wait();
+        }
+        tc::tc_fence_before();
+        __syncthreads();
+
+        // ---------------------------------------------------------- U^T Khat; O^T += U^T P^T
+        if (tid == 0) {
+            tc::tc_fence_after();
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_tf32_ta(tmem + ScanT::T_D3, tmem + r_a + 8 * ks, OpKH::desc(s_kh, ks),
+                                tc::idesc_tf32(128, 128), ks > 0);
+            for (int ks = 0; ks < 8; ++ks)  // P = rows 64..127 of [T; P]
+                tc::mma_tf32_ta(tmem + r_d1 + 64, tmem + r_a + 8 * ks,
+                                OpTP::desc(s_tp + 8 * 128, ks), tc::idesc_tf32(128, 64), true);
+            tc::mma_commit(bar_mma);
+        }
+        wait_bar(bar_mma, ph_mma);
+        ph_mma ^= 1;
+        tc::tc_fence_after();
+        if (tid == 0 && more) load_b(g + 1);  // [T; P] and Khat^T are consumed
+        {   // S[32 cg + i][j] <- dec * S + (Khat^T U)[32 cg + i][j]
+            float v[32];
+            tmem_ld32(my + ScanT::T_D3 + 32 * cg, v);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                sreg[i] = __fmaf_rn(DECC[32 * cg + i], sreg[i], v[i]);
+                v[i] = tc::to_tf32(sreg[i]);
+            }
+            tmem_st32(my + ScanT::T_S + 32 * cg, v);
+            tc::tmem_st_wait();
+        }
+        o_c0 = c0;
+        o_L = L;
+        o_reg = r_d1 + 64;
+    }
+    // every thread leaves the loop through the same iteration; agree on the flag
+    const bool aborted = __syncthreads_or(*abort_flag);
+    if (o_c0 >= 0 && !aborted) write_o();  // the last chunk's output
+    if (tid == 0) {  // copies still in flight land before the exit (bounded waits)
+        for (int b2 = 0; b2 < 2; ++b2)
+            if ((out_x >> b2) & 1u) tc::mbar_wait(bar_x + b2, (ph_x >> b2) & 1u, 1u << 20);
+        if (out_v) tc::mbar_wait(bar_v, ph_v, 1u << 20);
+        if (out_b) tc::mbar_wait(bar_b, ph_b, 1u << 20);
+    }
+    if (!aborted) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) Sg[(size_t)i * D] = sreg[i];
+    }
+    tc::tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, ScanT::TMEM_COLS);
+    }
+}
+
+// prepare and the transposed scan in one cooperative grid: CTAs [0, chains)
+// run the (sequence, head) chains, the others walk the prepare items in
+// chunk-major order and release each item's ready flag, so a chain consumes
+// chunk g as soon as its operands are out, with the rest of the sequence
+// still being prepared on the other SMs.  All CTAs are resident at once
+// (cooperative launch), so every wait on a flag ends.
+static_assert(ScanT::NT == NTP, "the two roles share the block size");
+static_assert(ScanT::TOTAL <= PS_TOTAL, "the two roles share the shared-memory size");
+__global__ void __launch_bounds__(NTP, 1)
+prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constant__ CUtensorMap vmap,
+                     const uint16_t* __restrict__ beta, float* __restrict__ state,
+                     float* __restrict__ o, int t, int t_pad, int heads,
+                     const int* __restrict__ cu, int n_seqs, unsigned char* __restrict__ ws,
+                     unsigned* __restrict__ ready) {
+    const int chains = n_seqs * heads;
+    if ((int)blockIdx.x < chains)
+        scan_t_role(vmap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
+                    (int)blockIdx.x / heads, ready);
+    else
+        prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, (long long)blockIdx.x - chains,
+                     (long long)gridDim.x - chains, ready);
+}
+
 // BF16 [rows][cols] with a row pitch of `pitch_elems`; boxes of `box_cols`
 // channels x 64 tokens with the given shared-memory swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
@@ -1018,12 +1381,26 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
     return tma_map_bf16(m, base, cols, rows, pitch_elems, box_cols, (uint32_t)C, swizzle);
 }
 
+// Ready flags of the fused grid: one 32-bit word per (chunk, head) blob,
+// after the blobs, padded to 256 bytes.
+size_t ready_offset(long long chunks, int n_seqs, int heads) {
+    return header_bytes(n_seqs) + (size_t)chunks * heads * BLOB_BYTES;
+}
+size_t ready_words(long long chunks, int heads) {
+    return (((size_t)chunks * heads * 4 + 255) & ~(size_t)255) / 4;
+}
+
 }  // namespace
 
 size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads) {
     const long long chunks = (rows + C - 1) / C + n_seqs;
-    return header_bytes(n_seqs) + (size_t)chunks * heads * BLOB_BYTES;
+    return ready_offset(chunks, n_seqs, heads) + ready_words(chunks, heads) * 4;
 }
+
+// Per-SM cost figures measured on GB300 (T = 8192, 32 heads) that choose
+// between the fused grid and the two kernels: a prepare item, and a chunk of
+// the transposed and of the 32-column scan chain.
+constexpr double kPrepItemUs = 9.7, kScanTChunkUs = 3.7, kScan32ChunkUs = 2.2;
 
 // Launches the tensor-core prefill (BF16 inputs, chunk 64); arguments,
 // including the workspace size, are validated by kda_prefill.
@@ -1042,15 +1419,31 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     // slices two.  Narrow slices while the CTAs fit on the SMs in one wave
     // (the chains' latency decides), wide ones once they would not (each
     // tensor-core product then does twice the work for about the same time).
-    const int dv = ((long long)n_seqs * heads * (D / 32) > sms) ? 64 : 32;
+    const long long chains = (long long)n_seqs * heads;
+    const int dv = (chains * (D / 32) > sms) ? 64 : 32;
+    // The fused grid (one SM per chain running the transposed scan, the other
+    // SMs preparing ahead of it) when its chain, not the prepare walk, is the
+    // longer part and still shorter than prepare followed by the 32-column
+    // scan: per chunk of a chain, max(chains x item / (sms - chains), scan_t)
+    // against chains x item / sms + scan_32.
+    const char* impl = getenv("KDA_PREFILL_IMPL");
+    const bool fused_allowed = !(impl && strcmp(impl, "unfused") == 0);
+    bool fused = false;
+    if (fused_allowed && dv == 32 && chains * 4 <= sms) {
+        const double per_chunk_fused =
+            std::max((double)chains * kPrepItemUs / (double)(sms - chains), kScanTChunkUs);
+        const double per_chunk_two = (double)chains * kPrepItemUs / sms + kScan32ChunkUs;
+        fused = per_chunk_fused < per_chunk_two;
+    }
     PrepMaps maps;
-    CUtensorMap vmap;
+    CUtensorMap vmap, vmap_t;
     const uint64_t hd = (uint64_t)heads * D;
     if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.g, g, hd, rows, hd, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&vmap, v, hd, rows, (uint64_t)stride, dv,
-                  dv == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B)) {
+                  dv == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) ||
+        (fused && !make_map(&vmap_t, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE))) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
@@ -1063,15 +1456,39 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(scan_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)ScanCfg<64>::TOTAL);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)PS_TOTAL);
     if (e != cudaSuccess) {
         set_error("kda_prefill: cannot reserve shared memory: %s", cudaGetErrorString(e));
         return KDA_ERR_CUDA;
     }
     unsigned char* ws = static_cast<unsigned char*>(workspace);
+    const long long chunk_bound = ((long long)rows + C - 1) / C + n_seqs;
+    unsigned* ready = reinterpret_cast<unsigned*>(ws + ready_offset(chunk_bound, n_seqs, heads));
+    const long long n_ready = fused ? (long long)ready_words(chunk_bound, heads) : 0;
     launch_pdl(chunk_map_kernel, dim3(1), dim3(MAP_THREADS), 0, s, cu, n_seqs, cu ? 0 : t,
-               reinterpret_cast<int*>(ws));
+               reinterpret_cast<int*>(ws), ready, n_ready);
     kda_status st = launch_result("kda_prefill (chunk map)");
     if (st != KDA_OK) return st;
+    if (fused) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)sms);
+        cfg.blockDim = dim3(NTP);
+        cfg.dynamicSmemBytes = PS_TOTAL;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, prefill_fused_kernel, maps, vmap_t, (const uint16_t*)beta,
+                               state, o, t, t_pad, heads, cu, n_seqs, ws, ready);
+        if (e == cudaSuccess) return launch_result("kda_prefill (fused)");
+        // the grid could not be made resident (e.g. SMs held by other work):
+        // run the two kernels instead
+        (void)cudaGetLastError();
+    }
     // Persistent prepare: one CTA per SM (shared memory allows no more),
     // never more CTAs than (chunk, head) items.
     const long long items = (((long long)rows + C - 1) / C + n_seqs) * heads;

@@ -141,6 +141,18 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, one K-step, issued by one thread.  A sits
+// in TMEM with lane = row and one 32-bit column per K index (M = 128: lanes
+// 0..127), so `a_tmem` advances by 8 columns per K-step.
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread has
 // completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -183,6 +195,26 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Write 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
+// The thread's tcgen05.st writes are complete (before a sync that hands the
+// columns to an MMA).
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* map,
                                             uint64_t* bar, int x, int y) {
@@ -218,6 +250,30 @@ __device__ __forceinline__ void bulk_commit() {
 // Wait until every committed bulk store of this thread has completed.
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Publish / observe a ready flag in global memory between CTAs of one grid.
+// The producer has completed its bulk stores (bulk_wait_all) and passed a CTA
+// barrier after its other threads' stores; the proxy fence orders the bulk
+// (async-proxy) writes before the release.  The consumer orders its acquire
+// before the bulk loads it issues next with the same proxy fence.
+__device__ __forceinline__ void flag_release(unsigned* flag, unsigned v) {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+// Spin (bounded) until *flag != 0; false when the limit ran out.
+__device__ __forceinline__ bool flag_acquire(const unsigned* flag, uint32_t limit = 1u << 22) {
+    for (uint32_t i = 0; i < limit; ++i) {
+        unsigned v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+        if (v) {
+            asm volatile("fence.proxy.async.global;" ::: "memory");
+            return true;
+        }
+        __nanosleep(64);
+    }
+    return false;
 }
 
 // Wait until every committed bulk store of this thread has finished reading

@@ -133,7 +133,12 @@ kda_status kda_decode_k(float* state, const float* q, const float* k, const floa
  * qkv_row_stride == heads*128 run decode_k's row walk (the pages' dispatch
  * for pieces that do not take the chunked arm: state read once, t token steps,
  * state written once); BF16 inputs with chunk 64 run the tensor-core prepare
- * and scan kernels; everything else runs the FP32 SIMT chunk kernel.
+ * and scan kernels -- as one cooperative grid (the scan consuming each chunk
+ * as soon as another SM has prepared it) when there are few (sequence, head)
+ * chains relative to the SMs, e.g. one sequence of 32 heads; everything else
+ * runs the FP32 SIMT chunk kernel.  The environment variable
+ * KDA_PREFILL_IMPL=simt pins the SIMT kernel and KDA_PREFILL_IMPL=unfused
+ * the two-kernel tensor-core path (for comparisons).
  *
  *   workspace : device scratch, 16-byte aligned, of at least
  *           kda_prefill_workspace_size(...) bytes (may be NULL when that
@@ -152,7 +157,8 @@ kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* b
  * argument is invalid.  The BF16, chunk-64 tensor-core path stores the
  * state-independent operands of every (chunk, head) there: 131,840 bytes
  * per chunk of 64 tokens and head (with one chunk of slack per sequence),
- * plus (n_seqs + 1) * 4 bytes rounded up to 256. */
+ * plus (n_seqs + 1) * 4 bytes rounded up to 256, plus a 4-byte ready flag
+ * per chunk and head rounded up to 256 bytes. */
 size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads, int head_dim,
                                   int in_dtype);
 

@@ -1,0 +1,119 @@
+"""kda_prefill through the fused prepare + scan grid (BF16, chunk 64, one
+sequence of 32 heads: few enough (sequence, head) chains that the library
+runs one cooperative grid in which the transposed scan consumes each chunk
+as soon as another SM has prepared it), against the FP64 oracle, against the
+two-kernel path (KDA_PREFILL_IMPL=unfused), and for pad-fill independence."""
+
+import pytest
+import torch
+
+import kda_workloads as wl
+from _util import TOL_PREFILL, kda, rel_err
+
+pytestmark = pytest.mark.gpu
+
+H = 32  # 32 chains on one sequence: the fused grid's regime
+
+
+def inputs(seed, t, g_low=-5.0):
+    gen = torch.Generator().manual_seed(seed)
+    d = wl.core_inputs(gen, (t,), H, torch.bfloat16, g_low=g_low)
+    d["state"] = wl.state(gen, (1,), H, 0.02)
+    return d
+
+
+def run(K, d, t, t_pad=None, pad_fill=0.0, cu=False, workspace=None):
+    t_pad = t_pad or t
+    dev = {n: wl.pad_rows(d[n][:t], t_pad, float("nan")).cuda()
+           for n in ("q", "k", "v", "g", "beta")}
+    S = d["state"].clone().cuda()
+    o = torch.full((t_pad, H, 128), 12345.0, device="cuda")
+    if cu:
+        cuv = torch.tensor([0, t], dtype=torch.int32, device="cuda")
+        K.kda_prefill(S, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], o, t, 64,
+                      cu_seqlens=cuv, workspace=workspace)
+    else:
+        K.kda_prefill(S, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], o, t, 64,
+                      pad_fill=pad_fill, workspace=workspace)
+    K.kda_sync_status()
+    return o, S
+
+
+def oracle_all_heads(orc, d, t):
+    return orc.prefill(d["q"][:t], d["k"][:t], d["v"][:t], d["g"][:t], d["beta"][:t],
+                       d["state"][0])
+
+
+@pytest.mark.parametrize("t,g_low", [(1000, -5.0), (777, -0.05), (64, -5.0), (1, -5.0),
+                                     (130, -10.0)])
+def test_fused_grid_matches_oracle(orc, t, g_low):
+    """Every head and output row: whole and ragged chunk counts, one-token and
+    one-chunk sequences, slow decay (the state carries across every chunk)
+    and the steepest supported decay."""
+    K = kda()
+    d = inputs(100 + t, t, g_low)
+    o, S = run(K, d, t)
+    o_ref, S_ref = oracle_all_heads(orc, d, t)
+    assert rel_err(o, o_ref) < TOL_PREFILL
+    assert rel_err(S[0], S_ref) < TOL_PREFILL
+
+
+def test_fused_packed_single_sequence_matches_oracle(orc):
+    """The packed form (cu_seqlens = [0, t]) takes the fused grid as well."""
+    K = kda()
+    t = 517
+    d = inputs(7, t)
+    o, S = run(K, d, t, cu=True)
+    o_ref, S_ref = oracle_all_heads(orc, d, t)
+    assert rel_err(o, o_ref) < TOL_PREFILL
+    assert rel_err(S[0], S_ref) < TOL_PREFILL
+
+
+def test_fused_and_two_kernel_paths_agree(orc, monkeypatch):
+    """The fused grid and prepare followed by the 32-column scan compute the
+    same method: both within the tolerance of the oracle and of each other."""
+    K = kda()
+    t = 640
+    d = inputs(13, t, g_low=-1.0)
+    o_f, S_f = run(K, d, t)
+    monkeypatch.setenv("KDA_PREFILL_IMPL", "unfused")
+    o_u, S_u = run(K, d, t)
+    o_ref, S_ref = oracle_all_heads(orc, d, t)
+    for o, S in ((o_f, S_f), (o_u, S_u)):
+        assert rel_err(o, o_ref) < TOL_PREFILL
+        assert rel_err(S[0], S_ref) < TOL_PREFILL
+    assert rel_err(o_f, o_u.double().cpu().numpy()) < TOL_PREFILL
+    assert rel_err(S_f, S_u.double().cpu().numpy()) < TOL_PREFILL
+
+
+def test_fused_pad_fill_has_no_effect():
+    """Bit-identical o[:t] and state for pad_fill 0, NaN and 1e30 on the fused
+    grid; rows [t, t_pad) of o are never written."""
+    K = kda()
+    t, t_pad = 1000, 1024
+    d = inputs(3, t_pad)
+    runs = [run(K, d, t, t_pad=t_pad, pad_fill=f) for f in (0.0, float("nan"), 1e30)]
+    o0, S0 = runs[0]
+    assert torch.isfinite(o0[:t]).all() and torch.isfinite(S0).all()
+    for o, S in runs[1:]:
+        assert torch.equal(o[:t], o0[:t])
+        assert torch.equal(S, S0)
+        assert (o[t:] == 12345.0).all()
+
+
+def test_fused_stale_workspace_and_repeated_calls(orc):
+    """The grid's ready flags are cleared by every call: a workspace whose
+    bytes are all 0xFF (every flag set) still gives the oracle's result, and
+    two calls on the same workspace give the same bits whichever SM prepared
+    which chunk."""
+    K = kda()
+    t = 900
+    d = inputs(5, t)
+    need = K.kda_prefill_workspace_size(t, 1, 64, H)
+    ws = torch.full((need,), 255, dtype=torch.uint8, device="cuda")
+    o1, S1 = run(K, d, t, workspace=ws)
+    o_ref, S_ref = oracle_all_heads(orc, d, t)
+    assert rel_err(o1, o_ref) < TOL_PREFILL
+    assert rel_err(S1[0], S_ref) < TOL_PREFILL
+    o2, S2 = run(K, d, t, workspace=ws)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
