@@ -450,7 +450,8 @@ def run_gpu(args):
             "frac": (achieved / pk["hbm_gbs"]) if bound == "hbm"
             else (PREFILL_FLOPS / avg_launch_s / 1e12) / tf32_peak,
             "traffic": traffic_from_profile(),
-            "kernel": "prefill (kda_prefill)",
+            "kernel": "prefill (kda_prefill: chunk_map_kernel + prefill_fused_kernel, the "
+                      "cooperative prepare + transposed-scan grid)",
             "algorithmic_bytes": PREFILL_BYTES, "algorithmic_flops": PREFILL_FLOPS,
             "avg_launch_us": avg_launch_s * 1e6,
             "peak_source": pk["source"] + " (hbm_gbs)",
@@ -462,7 +463,8 @@ def run_gpu(args):
             "path": "pinned host q/k/v/g/beta -> kda_prefill -> o and state to host; "
                     "copies on two copy streams overlap the neighbouring steps' compute",
         },
-        "gpu_launches": 3 * args.steps,
+        # per prefill call: the chunk map and the fused prepare + scan grid
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks,
         "decode": {
             "workload": wl.DECODE.name, "value": DECODE_BYTES / dec_s / 1e9, "unit": "GB/s",
