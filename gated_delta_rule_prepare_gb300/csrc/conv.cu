@@ -543,8 +543,11 @@ kda_status launch(float* conv_state, const uint16_t* x, const uint16_t* w, uint1
     kda_status st = launch_result("kda_conv_silu_l2 (conv)");
     if (st != KDA_OK) return st;
     const size_t rows = (size_t)n_seqs * 3 * heads * D;
-    launch_pdl(conv_state_kernel<K>, dim3((unsigned)((rows + 255) / 256)), dim3(256), 0, s,
-               conv_state, x, total, t_per_seq, cu, n_seqs, heads);
+    // A plain launch: under programmatic dependent launch its CTAs became
+    // resident while the conv grid still ran, and back-to-back calls on many
+    // sequences (768 CTAs for 16) slowed from 656 to 821 us per call.
+    conv_state_kernel<K><<<dim3((unsigned)((rows + 255) / 256)), dim3(256), 0, s>>>(
+        conv_state, x, total, t_per_seq, cu, n_seqs, heads);
     return launch_result("kda_conv_silu_l2 (state)");
 }
 
