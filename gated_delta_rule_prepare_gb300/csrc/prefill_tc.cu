@@ -279,6 +279,13 @@ __device__ __forceinline__ PrepItem prep_item(long long item, int heads, const i
     PrepItem it;
     it.g = item / heads;
     it.h = (int)(item - it.g * heads);
+    if (!cu) {  // uniform sequences of t tokens, t_pad rows apart: no table lookup
+        const long long cps = (t + C - 1) / C, n = it.g / cps;
+        it.c0 = (int)(n * t_pad + (it.g - n * cps) * C);
+        it.valid = n < n_seqs;
+        it.L = it.valid ? min(C, (int)(n * t_pad) + t - it.c0) : 0;
+        return it;
+    }
     int lo = 0, hi = n_seqs - 1;  // the sequence holding chunk g: largest n with chunk_off[n] <= g
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -305,6 +312,11 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     const int tid = threadIdx.x, warp = tid >> 5;
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column quarter
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    // Thread 0 issues the tensor-core products; a thread of another warp
+    // issues the tile loads and bulk stores and releases the ready flags, so
+    // the stores' completion and the release's fences are waited for while
+    // the next item's A/P product runs instead of between two items.
+    const bool copier = (tid == 128);
 
     const int* chunk_off = reinterpret_cast<const int*>(ws);
     const long long items = (long long)__ldg(chunk_off + n_seqs) * heads;
@@ -354,7 +366,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     // Raw tiles of item `it` into buffer b (thread 0), and its beta (threads
     // 0..63, returned in a register).
     auto load_raw = [&](const PrepItem& it, int b) {
-        if (tid == 0 && it.valid) {
+        if (copier && it.valid) {
             unsigned char* dst = sm + b * RAW_BUF;
             tc::fence_async_smem();  // the buffer's previous generic-proxy contents are dead
             tc::mbar_arrive_expect_tx(bar_tma + b, RAW_BUF);
@@ -372,6 +384,18 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         return (tid < C && it.valid && tid < it.L)
                    ? bf(__ldg(beta + (size_t)(it.c0 + tid) * heads + it.h))
                    : 0.f;
+    };
+
+    // The item whose ready flag is still to be released (copier thread): an
+    // item's flag goes out during the next item's first A/P product, or at
+    // the end of an item that has none, or after the walk.
+    long long pending = -1;
+    auto release_pending = [&]() {
+        if (ready && copier && pending >= 0) {
+            tc::bulk_wait_all();
+            tc::flag_release(ready + pending, 1u);
+            pending = -1;
+        }
     };
 
     long long item = first;
@@ -453,7 +477,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                     }
                 }
             }
-            if (tid == 0) tc::bulk_wait_read_all();  // the last item's operands left OPX and Y
+            if (copier) tc::bulk_wait_read_all();  // the last item's operands left OPX and Y
             __syncthreads();
 
             // ------------------------------------------------------ P2 A and P blocks
@@ -543,6 +567,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                                            s_y + OpY32::bytes(128), 16, tc::idesc_tf32(128, 32));
                     tc::mma_commit(bar_mma);
                 }
+                release_pending();
                 wait_mma();
                 fetch_next();  // the compact X_1 in the other buffer has been read
             } else {
@@ -558,7 +583,10 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                                             tc::idesc_tf32(128, 16));
                         tc::mma_commit(bar_mma);
                     }
-                    if (bb == 0) fetch_next();
+                    if (bb == 0) {
+                        release_pending();
+                        fetch_next();
+                    }
                     wait_mma();
                 }
             }
@@ -594,7 +622,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             }
             tc::fence_async_smem();
             __syncthreads();  // the raw tiles and reference rows are dead from here on
-            if (tid == 0 && !failed) {
+            if (copier && !failed) {
                 tc::bulk_store(blob + BLOB_OPX, sm + PS_OPX, OpX::bytes(128));
                 tc::bulk_store(blob + BLOB_KH, sm + PS_Y, OpKH::bytes(64));
                 tc::bulk_commit();
@@ -753,15 +781,16 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         }
         // every thread's stores of this item precede the barrier above (an
         // invalid item stores nothing)
-        if (ready && tid == 0) {
-            tc::bulk_wait_all();
-            tc::flag_release(ready + item, 1u);
+        if (ready && copier) {
+            release_pending();  // an item without an A/P product in between
+            pending = item;
         }
         item = nitem;
         cur = nxt;
         beta_cur = beta_nxt;
     }
-    if (tid == 0) tc::bulk_wait_all();
+    release_pending();
+    if (copier) tc::bulk_wait_all();
     tc::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -1069,17 +1098,6 @@ struct ScanT {
     static_assert(TOTAL <= 232448, "shared memory budget exceeded");
 };
 
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-    float a[16], b[16];
-    tc::tmem_ld16(taddr, a);
-    tc::tmem_ld16(taddr + 16, b);
-    tc::tmem_ld_wait();
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        v[i] = a[i];
-        v[16 + i] = b[i];
-    }
-}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
     float a[16], b[16];
 #pragma unroll
@@ -1100,7 +1118,8 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
 // so Qtil S rides with Ktil S and P U with Khat^T U).  [Ktil; Qtil] is
 // double-buffered and requested a chunk ahead; the value tile and [T; P],
 // Khat^T, dec as soon as their buffers are consumed.
-__device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __restrict__ state,
+__device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUtensorMap& omap,
+                                            float* __restrict__ state,
                                             float* __restrict__ o, int t, int t_pad, int heads,
                                             const int* __restrict__ cu, int n_seqs,
                                             const unsigned char* __restrict__ ws, int h, int n,
@@ -1110,6 +1129,10 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __re
     const int qd = warp & 3, cg = warp >> 2;  // TMEM lane quarter, column group
     const int j = 32 * qd + (tid & 31);       // value column = TMEM lane
     const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+    // Thread 0 issues the tensor-core products; a thread of another warp
+    // issues every copy (the ready-flag acquire alone is a global-memory
+    // round trip), so neither waits on the other's latency.
+    const bool copier = (tid == 128);
 
     int start, end;
     if (!seq_range(cu, n, n_seqs, t, t_pad, start, end)) {
@@ -1138,6 +1161,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __re
         for (int i = 0; i < 5; ++i) tc::mbar_init(bar_x + i, 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&vmap);
+        tc::prefetch_tmap(&omap);
         *abort_flag = 0;
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, ScanT::TMEM_COLS);
@@ -1167,8 +1191,8 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __re
             *abort_flag = 1;
         }
     };
-    // Copies (thread 0).  Outstanding ones are tracked so an early exit can
-    // let them land before the shared memory is released.
+    // Copies (the copier thread).  Outstanding ones are tracked so an early
+    // exit can let them land before the shared memory is released.
     uint32_t out_x = 0;  // bit per operand buffer
     bool out_v = false, out_b = false;
     auto load_x = [&](long long gg, int xb) {  // [Ktil; Qtil] of chunk gg, after its flag
@@ -1195,29 +1219,26 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __re
         tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_b);
         out_b = true;
     };
-    if (tid == 0 && start < end) {
+    if (copier && start < end) {
         load_x(g0, 0);
         load_v(start);
         load_b(g0);
     }
 
-    // O of a chunk is read back during the next chunk's first product (off
-    // the state's chain): the chunk regions alternate, chunk parity xb
-    // computing [Ktil S | Qtil S -> O] in R_xb and X^T, U^T (A) and T X in
-    // R_(1-xb), so the next chunk's T X lands on this chunk's O only after it
-    // has been read.
-    int o_c0 = -1, o_L = 0;  // the chunk whose O is still to be written
-    uint32_t o_reg = 0;
-    auto write_o = [&]() {  // O[r][j], r = 16 cg + i
-        float v[16];
-        tc::tmem_ld16(my + o_reg + 16 * cg, v);
-        tc::tmem_ld_wait();
-        float* orow = o + ((size_t)o_c0 * heads + h) * D + j;
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = 16 * cg + i;
-            if (r < o_L) orow[(size_t)r * heads * D] = v[i];
+    // O of a whole chunk leaves by one TMA tile store that no thread waits
+    // for: the threads read it from TMEM with the state increment and stage it
+    // row-major in the chunk's [Ktil; Qtil] buffer (consumed by then); the
+    // copier issues the store after the next barrier and lets it finish
+    // reading before that buffer is refilled.  (Per-thread global stores cost
+    // the chain about 1.4K cycles per chunk while the prepare CTAs keep the
+    // memory system busy.)  A partial chunk's rows go out by plain stores.
+    int st_c0 = -1, st_xb = 0;  // the staged chunk whose store is still to be issued
+    auto issue_o_store = [&]() {
+        if (copier && st_c0 >= 0) {
+            tc::tma_store_2d(&omap, sm + (st_xb ? ScanT::OPX1 : (uint32_t)SS_OPX), h * D, st_c0);
+            tc::bulk_commit();
         }
+        st_c0 = -1;
     };
 
     long long g = g0;
@@ -1229,12 +1250,13 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __re
         const uint32_t r_a = xb ? ScanT::R0 : ScanT::R1;   // X^T / U^T (A), then T X at +64
         tc::tc_fence_before();
         if (__syncthreads_or(*abort_flag)) break;  // every thread takes the same exit
+        issue_o_store();  // the previous chunk's staged O
         wait_bar(bar_x + xb, (ph_x >> xb) & 1u);
         ph_x ^= 1u << xb;
-        if (tid == 0) out_x &= ~(1u << xb);
+        if (copier) out_x &= ~(1u << xb);
         wait_bar(bar_v, ph_v);
         ph_v ^= 1;
-        if (tid == 0) out_v = false;
+        if (copier) out_v = false;
 
         // ---------------------------------------------------------- S^T [Ktil; Qtil]^T
         // (one N = 128 product: Ktil S into r_d1, Qtil S into r_d1 + 64)
@@ -1245,11 +1267,14 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __re
                                 OpX::desc(xb ? s_opx1 : s_opx0, ks), tc::idesc_tf32(128, 128),
                                 ks > 0);
             tc::mma_commit(bar_mma);
-            // the next chunk's [Ktil; Qtil] (its ready flag and the copy) while
-            // this product runs; that buffer's last products have completed
-            if (more) load_x(g + 1, xb ^ 1);
         }
-        if (o_c0 >= 0) write_o();  // the previous chunk's output, in r_a + 64
+        // the next chunk's [Ktil; Qtil] (its ready flag and the copy) while
+        // this product runs; that buffer's last products have completed and
+        // the previous chunk's O store has read it
+        if (copier && more) {
+            tc::bulk_wait_read_all();
+            load_x(g + 1, xb ^ 1);
+        }
         float vr[16];  // V[16 cg + i][j], read while the product runs
 #pragma unroll
         for (int i = 0; i < 16; ++i) vr[i] = bf(RAWV[(16 * cg + i) * D + j]);
@@ -1271,10 +1296,10 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __re
         }
         tc::tc_fence_before();
         __syncthreads();
-        if (tid == 0 && more) load_v(c0 + C);  // the value tile is consumed
+        if (copier && more) load_v(c0 + C);  // the value tile is consumed
         wait_bar(bar_b, ph_b);
         ph_b ^= 1;
-        if (tid == 0) out_b = false;
+        if (copier) out_b = false;
         if (tid < D) DECC[tid] = DEC[tid];  // read after the next barrier
 
         // ---------------------------------------------------------- U^T = X^T T^T
@@ -1314,26 +1339,50 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, float* __re
         wait_bar(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::tc_fence_after();
-        if (tid == 0 && more) load_b(g + 1);  // [T; P] and Khat^T are consumed
-        {   // S[32 cg + i][j] <- dec * S + (Khat^T U)[32 cg + i][j]
-            float v[32];
-            tmem_ld32(my + ScanT::T_D3 + 32 * cg, v);
+        if (copier && more) load_b(g + 1);  // [T; P] and Khat^T are consumed
+        {   // S[32 cg + i][j] <- dec * S + (Khat^T U)[32 cg + i][j]; O[16 cg + i][j]
+            float v[32], ov[16];
+            {
+                float a[16], b[16];
+                tc::tmem_ld16(my + ScanT::T_D3 + 32 * cg, a);
+                tc::tmem_ld16(my + ScanT::T_D3 + 32 * cg + 16, b);
+                tc::tmem_ld16(my + r_d1 + 64 + 16 * cg, ov);
+                tc::tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    v[i] = a[i];
+                    v[16 + i] = b[i];
+                }
+            }
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
                 sreg[i] = __fmaf_rn(DECC[32 * cg + i], sreg[i], v[i]);
                 v[i] = tc::to_tf32(sreg[i]);
             }
             tmem_st32(my + ScanT::T_S + 32 * cg, v);
+            if (L == C) {  // staged row-major [64][128] for the tile store
+                float* ost = reinterpret_cast<float*>(sm + (xb ? ScanT::OPX1 : (uint32_t)SS_OPX));
+#pragma unroll
+                for (int i = 0; i < 16; ++i) ost[(16 * cg + i) * D + j] = ov[i];
+                tc::fence_async_smem();
+                st_c0 = c0;
+                st_xb = xb;
+            } else {
+                float* orow = o + ((size_t)c0 * heads + h) * D + j;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = 16 * cg + i;
+                    if (r < L) orow[(size_t)r * heads * D] = ov[i];
+                }
+            }
             tc::tmem_st_wait();
         }
-        o_c0 = c0;
-        o_L = L;
-        o_reg = r_d1 + 64;
     }
     // every thread leaves the loop through the same iteration; agree on the flag
     const bool aborted = __syncthreads_or(*abort_flag);
-    if (o_c0 >= 0 && !aborted) write_o();  // the last chunk's output
-    if (tid == 0) {  // copies still in flight land before the exit (bounded waits)
+    if (!aborted) issue_o_store();  // the last chunk's staged O
+    if (copier) {  // copies still in flight land before the exit (bounded waits)
+        tc::bulk_wait_all();
         for (int b2 = 0; b2 < 2; ++b2)
             if ((out_x >> b2) & 1u) tc::mbar_wait(bar_x + b2, (ph_x >> b2) & 1u, 1u << 20);
         if (out_v) tc::mbar_wait(bar_v, ph_v, 1u << 20);
@@ -1361,13 +1410,13 @@ static_assert(ScanT::NT == NTP, "the two roles share the block size");
 static_assert(ScanT::TOTAL <= PS_TOTAL, "the two roles share the shared-memory size");
 __global__ void __launch_bounds__(NTP, 1)
 prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constant__ CUtensorMap vmap,
-                     const uint16_t* __restrict__ beta, float* __restrict__ state,
+                     const __grid_constant__ CUtensorMap omap, const uint16_t* __restrict__ beta, float* __restrict__ state,
                      float* __restrict__ o, int t, int t_pad, int heads,
                      const int* __restrict__ cu, int n_seqs, unsigned char* __restrict__ ws,
                      unsigned* __restrict__ ready) {
     const int chains = n_seqs * heads;
     if ((int)blockIdx.x < chains)
-        scan_t_role(vmap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
+        scan_t_role(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
                     (int)blockIdx.x / heads, ready);
     else
         prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, (long long)blockIdx.x - chains,
@@ -1400,7 +1449,7 @@ size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads) {
 // Per-SM cost figures measured on GB300 (T = 8192, 32 heads) that choose
 // between the fused grid and the two kernels: a prepare item, and a chunk of
 // the transposed and of the 32-column scan chain.
-constexpr double kPrepItemUs = 9.7, kScanTChunkUs = 3.7, kScan32ChunkUs = 2.2;
+constexpr double kPrepItemUs = 9.3, kScanTChunkUs = 3.3, kScan32ChunkUs = 2.2;
 
 // Launches the tensor-core prefill (BF16 inputs, chunk 64); arguments,
 // including the workspace size, are validated by kda_prefill.
@@ -1436,14 +1485,15 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         fused = per_chunk_fused < per_chunk_two;
     }
     PrepMaps maps;
-    CUtensorMap vmap, vmap_t;
+    CUtensorMap vmap, vmap_t, omap;
     const uint64_t hd = (uint64_t)heads * D;
     if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.g, g, hd, rows, hd, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&vmap, v, hd, rows, (uint64_t)stride, dv,
                   dv == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) ||
-        (fused && !make_map(&vmap_t, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE))) {
+        (fused && !make_map(&vmap_t, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
+        (fused && !tma_map_f32(&omap, o, hd, rows, hd, D, (uint32_t)C))) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
@@ -1482,7 +1532,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, prefill_fused_kernel, maps, vmap_t, (const uint16_t*)beta,
+        e = cudaLaunchKernelEx(&cfg, prefill_fused_kernel, maps, vmap_t, omap, (const uint16_t*)beta,
                                state, o, t, t_pad, heads, cu, n_seqs, ws, ready);
         if (e == cudaSuccess) return launch_result("kda_prefill (fused)");
         // the grid could not be made resident (e.g. SMs held by other work):

@@ -225,6 +225,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* m
         : "memory");
 }
 
+// Tile store shared -> global through a tensor map (rows past the tensor's
+// end are not written); completion is tracked by bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src_smem, int x,
+                                             int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(smem_u32(src_smem))
+        : "memory");
+}
+
 // Contiguous bulk copy global -> shared (bytes a multiple of 16, both ends
 // 16-byte aligned), completing on `bar`.
 __device__ __forceinline__ void bulk_load(void* dst_smem, const void* src, uint32_t bytes,

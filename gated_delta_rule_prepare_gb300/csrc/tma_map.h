@@ -1,7 +1,7 @@
 // Host helpers shared by the kernels that load tiles with TMA: the driver's
 // tensor-map encoder (resolved once through the runtime's entry-point query,
-// so the library links no driver library itself), a 2-D BF16 map, and the
-// multiprocessor count of the current device.
+// so the library links no driver library itself), 2-D BF16 and FP32 maps,
+// and the multiprocessor count of the current device.
 #pragma once
 
 #include <cuda.h>
@@ -41,6 +41,21 @@ inline bool tma_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// FP32 [rows][cols] with a row pitch of `pitch_elems` elements, in boxes of
+// box_cols x box_rows without swizzle (row-major in shared memory).
+inline bool tma_map_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                        uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows) {
+    auto fn = tma_encode_fn();
+    if (!fn) return false;
+    cuuint64_t gdim[2] = {cols, rows};
+    cuuint64_t gstride[1] = {pitch_elems * 4};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), gdim, gstride, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 inline int sm_count() {
