@@ -13,9 +13,17 @@
 // carried state, for every (chunk, head) item, fully parallel: one persistent
 // CTA per SM walks the items, with the next item's q/k/g tiles arriving by
 // TMA into a second buffer while the current one is processed.  It writes
-// [Ktil; Qtil], [T; P], Khat^T (TF32 tensor-core operands, already in the
-// layout the scan consumes) and dec to the workspace: 131,840 bytes per chunk
+// [Ktil; Qtil], [T; P], Khat^T (FP16 tensor-core operands, already in the
+// layout the scan consumes) and dec to the workspace: 66,176 bytes per chunk
 // and head.
+//
+// Precision: prepare forms A and P from TF32 operands (their decay factors
+// span e^(+-8 |g|)); the scan's products take FP16 operands (10 stored
+// significand bits, as TF32) with FP32 accumulation.  Every scan operand is
+// bounded by the inputs' scale: |Ktil|, |Khat| <= |k|, |Qtil| <= |qh|, P, the
+// state S, X = V - Ktil S and U = T X are of the order of v and the initial
+// state, far inside FP16's range for normalised q, k; values below 2^-14
+// keep an absolute error under 2^-25.
 // scan_kernel, one CTA per (sequence, head, 32-column value slice), carries
 // the FP32 state across the sequence's chunks in order:
 //   X = V - Ktil S;  U = T X;  O = Qtil S + P U;  S <- dec (.) S + Khat^T U
@@ -58,34 +66,41 @@ constexpr int AP = 65;   // pitch (floats) of the FP32 [64][64] A / W array
 constexpr int TPP = 68;  // pitch (floats) of the FP32 [64][64] T array (16-B rows)
 
 // K-major operand of R rows in the "K-outer" core-matrix layout: the core
-// matrices of one K group of 4 columns are stacked over all rows (128 B per 8
-// rows); successive K groups are LBO = 16 R + PAD bytes apart.  PAD = 16
-// spreads operands that are written one K index per thread over all banks.
-template <int R, int PAD>
+// matrices of one K group (the 16 bytes of a row: 4 TF32 or 8 FP16 values)
+// are stacked over all rows (128 B per 8 rows); successive K groups are
+// LBO = 16 R + PAD bytes apart.  PAD = 16 spreads operands that are written
+// one K index per thread over all banks.  One MMA K-step reads 32 bytes of K
+// per row (8 TF32 or 16 FP16 values): two K groups.
+template <int R, int PAD, int ES = 4>
 struct Op {
     static constexpr uint32_t LBO = R * 16 + PAD;
+    static constexpr int KG = 16 / ES;  // values per K group
     static __device__ __forceinline__ uint32_t off(int r, int k) {
-        return (uint32_t)((k >> 2) * LBO + (r >> 3) * 128 + (r & 7) * 16 + (k & 3) * 4);
+        return (uint32_t)((k / KG) * LBO + (r >> 3) * 128 + (r & 7) * 16 + (k % KG) * ES);
     }
     static __device__ __forceinline__ uint64_t desc(uint32_t base, int ks) {
         return tc::make_desc(base + (uint32_t)ks * 2u * LBO, LBO, 128u);
     }
-    static __host__ __device__ constexpr uint32_t bytes(int K) { return (uint32_t)(K / 4) * LBO; }
+    static __host__ __device__ constexpr uint32_t bytes(int K) { return (uint32_t)(K / KG) * LBO; }
 };
-using OpX = Op<128, 0>;   // A: [X_b; QX_b] then [Ktil; Qtil], K = 128 channels
+// prepare's A/P products (TF32: their decay factors reach e^(+-8 |g|))
+using OpX = Op<128, 0>;   // A: [X_b; QX_b], K = 128 channels
 using OpY = Op<16, 0>;    // B: Y_b of a 16-token block, K = 128 channels
 using OpY32 = Op<32, 0>;  // B: Y_b of a 32-token block, K = 128 channels
-using OpKH = Op<128, 16>; // A: Khat^T, rows = key channel, K = 64 tokens (written per K index)
-using OpTP = Op<128, 0>;  // A: [T; P], K = 64 tokens
+using OpKH = Op<128, 16>; // sizes the Y_b region, which later holds Khat^T
 using OpX1 = Op<64, 0>;   // A: [X_1; QX_1] of the second 32-token block, rows 32..63 only
+// the scan's operands (FP16: every value is bounded by the inputs' scale)
+using OpXh = Op<128, 0, 2>;    // [Ktil; Qtil], K = 128 channels
+using OpTPh = Op<128, 0, 2>;   // [T; P], K = 64 tokens
+using OpKHh = Op<128, 16, 2>;  // Khat^T, rows = key channel, K = 64 tokens (written per K index)
 
 // ------------------------------------------------------------ workspace
 // [chunk_off: (n_seqs + 1) int32, padded to 256 B][blob (g, h) for every
 // chunk g and head h].  A blob is the byte image of the scan's operands.
 constexpr uint32_t BLOB_OPX = 0;
-constexpr uint32_t BLOB_TP = BLOB_OPX + OpX::bytes(128);
-constexpr uint32_t BLOB_KH = BLOB_TP + OpTP::bytes(64);
-constexpr uint32_t BLOB_DEC = BLOB_KH + OpKH::bytes(64);
+constexpr uint32_t BLOB_TP = BLOB_OPX + OpXh::bytes(128);
+constexpr uint32_t BLOB_KH = BLOB_TP + OpTPh::bytes(64);
+constexpr uint32_t BLOB_DEC = BLOB_KH + OpKHh::bytes(64);
 constexpr uint32_t BLOB_BYTES = BLOB_DEC + 128 * 4;
 static_assert(BLOB_BYTES % 128 == 0, "blobs must stay 128-byte aligned");
 
@@ -140,8 +155,8 @@ struct ScanCfg {
     static constexpr int DV = DVv;
     static constexpr int NT = DVv * 8;                    // 256 or 512 threads
     static constexpr int SC = 16;                         // state columns per thread
-    using OpXV = Op<DVv, 16>;   // B: X^T and U^T, rows = value column, K = 64 tokens
-    using OpS = Op<DVv, 16>;    // B: S^T, rows = value column, K = 128 key channels
+    using OpXV = Op<DVv, 16, 2>;  // B: X^T and U^T, rows = value column, K = 64 tokens
+    using OpS = Op<DVv, 16, 2>;   // B: S^T, rows = value column, K = 128 key channels
     // shared memory: blob image (OPX | TP | KH | DEC), X^T, U^T, S^T, value tile
     static constexpr uint32_t XV = BLOB_BYTES;
     static constexpr uint32_t U = XV + OpXV::bytes(64);
@@ -174,16 +189,31 @@ __device__ __forceinline__ void st4(unsigned char* base, uint32_t off, float a, 
         make_float4(tc::to_tf32(a), tc::to_tf32(b), tc::to_tf32(c), tc::to_tf32(d));
 }
 
+// Four values rounded to FP16, stored as one 8-byte write.
+__device__ __forceinline__ void st4h(unsigned char* p, float a, float b, float c, float d) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(tc::pack_f16x2(a, b), tc::pack_f16x2(c, d));
+}
+__device__ __forceinline__ void st1h(unsigned char* p, float a) {
+    *reinterpret_cast<uint16_t*>(p) = tc::f16_bits(a);
+}
+
 struct PrepMaps {
     CUtensorMap q, k, g;
 };
 
-// D = A . B^T over `ksteps` K-steps of 8, issued by the calling thread.
+// D = A . B^T over `ksteps` TF32 K-steps of 8, issued by the calling thread.
 template <class OA, class OB>
 __device__ __forceinline__ void issue_mma(uint32_t d, uint32_t a, uint32_t b, int ksteps,
                                           uint32_t idesc) {
     for (int ks = 0; ks < ksteps; ++ks)
         tc::mma_tf32(d, OA::desc(a, ks), OB::desc(b, ks), idesc, ks > 0);
+}
+// The same over FP16 K-steps of 16.
+template <class OA, class OB>
+__device__ __forceinline__ void issue_mma16(uint32_t d, uint32_t a, uint32_t b, int ksteps,
+                                            uint32_t idesc) {
+    for (int ks = 0; ks < ksteps; ++ks)
+        tc::mma_f16(d, OA::desc(a, ks), OB::desc(b, ks), idesc, ks > 0);
 }
 
 // Token range [start, end) of sequence n; false when cu_seqlens is malformed.
@@ -258,12 +288,6 @@ __device__ __forceinline__ float4 raw4(const unsigned char* tile, int r, int c) 
     const uint2 u = *reinterpret_cast<const uint2*>(tile + raw_off(r, c));
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
-}
-
-// Four values rounded to TF32, stored as one 16-byte global write.
-__device__ __forceinline__ void stg4(unsigned char* p, float a, float b, float c, float d) {
-    *reinterpret_cast<float4*>(p) =
-        make_float4(tc::to_tf32(a), tc::to_tf32(b), tc::to_tf32(c), tc::to_tf32(d));
 }
 
 // A (chunk, head) item of the prepare walk: item = g * heads + h.
@@ -609,22 +633,22 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                     if (!live) kf = qf = make_float4(0.f, 0.f, 0.f, 0.f);
                     const float f0 = __expf(ga.x), f1 = __expf(ga.y), f2 = __expf(ga.z),
                                 f3 = __expf(ga.w);
-                    st4(sm + PS_OPX, OpX::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
-                        kf.w * f3);
-                    st4(sm + PS_OPX, OpX::off(64 + r, 4 * j), KDA_Q_SCALE * qf.x * f0,
-                        KDA_Q_SCALE * qf.y * f1, KDA_Q_SCALE * qf.z * f2, KDA_Q_SCALE * qf.w * f3);
-                    float* kh = reinterpret_cast<float*>(sm + PS_Y);
-                    kh[OpKH::off(4 * j, r) / 4] = tc::to_tf32(br * kf.x * __expf(gl.x - ga.x));
-                    kh[OpKH::off(4 * j + 1, r) / 4] = tc::to_tf32(br * kf.y * __expf(gl.y - ga.y));
-                    kh[OpKH::off(4 * j + 2, r) / 4] = tc::to_tf32(br * kf.z * __expf(gl.z - ga.z));
-                    kh[OpKH::off(4 * j + 3, r) / 4] = tc::to_tf32(br * kf.w * __expf(gl.w - ga.w));
+                    st4h(sm + PS_OPX + OpXh::off(r, 4 * j), kf.x * f0, kf.y * f1, kf.z * f2,
+                         kf.w * f3);
+                    st4h(sm + PS_OPX + OpXh::off(64 + r, 4 * j), KDA_Q_SCALE * qf.x * f0,
+                         KDA_Q_SCALE * qf.y * f1, KDA_Q_SCALE * qf.z * f2, KDA_Q_SCALE * qf.w * f3);
+                    unsigned char* kh = sm + PS_Y;
+                    st1h(kh + OpKHh::off(4 * j, r), br * kf.x * __expf(gl.x - ga.x));
+                    st1h(kh + OpKHh::off(4 * j + 1, r), br * kf.y * __expf(gl.y - ga.y));
+                    st1h(kh + OpKHh::off(4 * j + 2, r), br * kf.z * __expf(gl.z - ga.z));
+                    st1h(kh + OpKHh::off(4 * j + 3, r), br * kf.w * __expf(gl.w - ga.w));
                 }
             }
             tc::fence_async_smem();
             __syncthreads();  // the raw tiles and reference rows are dead from here on
             if (copier && !failed) {
-                tc::bulk_store(blob + BLOB_OPX, sm + PS_OPX, OpX::bytes(128));
-                tc::bulk_store(blob + BLOB_KH, sm + PS_Y, OpKH::bytes(64));
+                tc::bulk_store(blob + BLOB_OPX, sm + PS_OPX, OpXh::bytes(128));
+                tc::bulk_store(blob + BLOB_KH, sm + PS_Y, OpKHh::bytes(64));
                 tc::bulk_commit();
             }
 
@@ -655,8 +679,8 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                                 const int s = 16 * ch + 4 * c4 + e;
                                 p[e] = (!zero && s <= r) ? v[4 * c4 + e] * BETA[s] : 0.f;
                             }
-                            stg4(blob + BLOB_TP + OpTP::off(64 + r, 16 * ch + 4 * c4), p[0], p[1],
-                                 p[2], p[3]);
+                            st4h(blob + BLOB_TP + OpTPh::off(64 + r, 16 * ch + 4 * c4), p[0],
+                                 p[1], p[2], p[3]);
                         }
                     }
                 } else if (ln < 64) {
@@ -676,8 +700,8 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                             const int s = 16 * ch + 4 * c4 + e;
                             p[e] = (s <= r) ? v[4 * c4 + e] * BETA[s] : 0.f;
                         }
-                        stg4(blob + BLOB_TP + OpTP::off(64 + r, 16 * ch + 4 * c4), p[0], p[1], p[2],
-                             p[3]);
+                        st4h(blob + BLOB_TP + OpTPh::off(64 + r, 16 * ch + 4 * c4), p[0], p[1],
+                             p[2], p[3]);
                     }
                 }
             }
@@ -773,7 +797,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 for (int jj = 0; jj < 16 / (NTP / 64); ++jj) {
                     const int j = qg + (NTP / 64) * jj;
                     const float4 tr = *reinterpret_cast<const float4*>(TM + r * TPP + 4 * j);
-                    stg4(blob + BLOB_TP + OpTP::off(r, 4 * j), tr.x, tr.y, tr.z, tr.w);
+                    st4h(blob + BLOB_TP + OpTPh::off(r, 4 * j), tr.x, tr.y, tr.z, tr.w);
                 }
             }
             tc::tc_fence_before();
@@ -878,7 +902,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     }
 #pragma unroll
     for (int jj = 0; jj < SC; ++jj)
-        *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(ch * SC + jj, ln)) = tc::to_tf32(sreg[jj]);
+        st1h(sm + SS_OPS + OpS::off(ch * SC + jj, ln), sreg[jj]);
 
     auto wait_mma = [&]() {
         if (!tc::mbar_wait(bar_mma, ph_mma)) {
@@ -899,15 +923,15 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
     // by the first product, group B ([T; P], Khat^T, dec) by the last two.
     auto load_a = [&](long long gg, int cc0) {
         const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
-        tc::mbar_arrive_expect_tx(bar_a, OpX::bytes(128) + 64 * DV * 2);
-        tc::bulk_load(sm + SS_OPX, blob + BLOB_OPX, OpX::bytes(128), bar_a);
+        tc::mbar_arrive_expect_tx(bar_a, OpXh::bytes(128) + 64 * DV * 2);
+        tc::bulk_load(sm + SS_OPX, blob + BLOB_OPX, OpXh::bytes(128), bar_a);
         tc::tma_load_2d(sm + SS_RAWV, &vmap, bar_a, h * D + slice * DV, cc0);
     };
     auto load_b = [&](long long gg) {
         const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
-        tc::mbar_arrive_expect_tx(bar_b, OpTP::bytes(64) + OpKH::bytes(64) + 128 * 4);
-        tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTP::bytes(64), bar_b);
-        tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKH::bytes(64), bar_b);
+        tc::mbar_arrive_expect_tx(bar_b, OpTPh::bytes(64) + OpKHh::bytes(64) + 128 * 4);
+        tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTPh::bytes(64), bar_b);
+        tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKHh::bytes(64), bar_b);
         tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_b);
     };
     auto wait_load = [&](uint64_t* bar, uint32_t& ph) {
@@ -959,7 +983,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         // ---------------------------------------------------------- X = V - Ktil S
         if (tid == 0) {
             tc::tc_fence_after();
-            issue_mma<OpX, OpS>(tmem + TC_Y, s_opx, s_ops, 16, tc::idesc_tf32(128, DV));
+            issue_mma16<OpXh, OpS>(tmem + TC_Y, s_opx, s_ops, 8, tc::idesc_f16(128, DV));
             tc::mma_commit(bar_mma);
         }
         if (o_c0 >= 0) write_o();  // the previous chunk's output
@@ -985,7 +1009,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
                 for (int jj = 0; jj < SC; ++jj) {
                     const uint32_t bits = (jj & 1) ? (w[jj >> 1] & 0xffff0000u) : (w[jj >> 1] << 16);
                     const float x = (r < L) ? __uint_as_float(bits) - v[jj] : 0.f;
-                    *reinterpret_cast<float*>(sm + SS_XV + OpXV::off(SC * ch + jj, r)) = tc::to_tf32(x);
+                    st1h(sm + SS_XV + OpXV::off(SC * ch + jj, r), x);
                 }
             } else {
 #pragma unroll
@@ -1004,7 +1028,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         // ---------------------------------------------------------- U = T X
         if (tid == 0) {
             tc::tc_fence_after();
-            issue_mma<OpTP, OpXV>(tmem + TC_U, s_tp, s_xv, 8, tc::idesc_tf32(128, DV));
+            issue_mma16<OpTPh, OpXV>(tmem + TC_U, s_tp, s_xv, 4, tc::idesc_f16(128, DV));
             tc::mma_commit(bar_mma);
         }
         wait_mma();
@@ -1016,7 +1040,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
 #pragma unroll
             for (int jj = 0; jj < SC; ++jj) {
                 const float u = (r < L) ? v[jj] : 0.f;
-                *reinterpret_cast<float*>(sm + SS_U + OpXV::off(SC * ch + jj, r)) = tc::to_tf32(u);
+                st1h(sm + SS_U + OpXV::off(SC * ch + jj, r), u);
             }
         }
         sync_for_mma();
@@ -1024,8 +1048,8 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
         // ---------------------------------------------------------- Khat^T U and P U
         if (tid == 0) {
             tc::tc_fence_after();
-            issue_mma<OpKH, OpXV>(tmem + TC_E, s_opkh, s_opy, 8, tc::idesc_tf32(128, DV));
-            issue_mma<OpTP, OpXV>(tmem + TC_PU, s_tp, s_opy, 8, tc::idesc_tf32(128, DV));
+            issue_mma16<OpKHh, OpXV>(tmem + TC_E, s_opkh, s_opy, 4, tc::idesc_f16(128, DV));
+            issue_mma16<OpTPh, OpXV>(tmem + TC_PU, s_tp, s_opy, 4, tc::idesc_f16(128, DV));
             tc::mma_commit(bar_mma);
         }
         wait_mma();
@@ -1040,7 +1064,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
 #pragma unroll
             for (int jj = 0; jj < SC; ++jj) {
                 sreg[jj] = __fmaf_rn(dk, sreg[jj], v[jj]);
-                *reinterpret_cast<float*>(sm + SS_OPS + OpS::off(SC * ch + jj, ln)) = tc::to_tf32(sreg[jj]);
+                st1h(sm + SS_OPS + OpS::off(SC * ch + jj, ln), sreg[jj]);
             }
         }
         o_c0 = c0;
@@ -1089,25 +1113,16 @@ struct ScanT {
     static constexpr uint32_t RAWV = (BLOB_BYTES + 1023) & ~1023u;
     static constexpr uint32_t DECC = RAWV + 64 * D * 2;
     static constexpr uint32_t OPX1 = (DECC + D * 4 + 1023) & ~1023u;
-    static constexpr uint32_t BAR = OPX1 + OpX::bytes(128);
+    static constexpr uint32_t BAR = OPX1 + OpXh::bytes(128);
     static constexpr uint32_t TOTAL = BAR + 64;
-    // TMEM columns: S^T (A); two 128-column chunk regions used alternately
-    // (Ktil S | Qtil S then O, or X^T / U^T (A) | T X); Khat^T U as dS^T
+    // TMEM columns: S^T (A, FP16 pairs: 64 columns); two 128-column chunk
+    // regions used alternately (Ktil S | Qtil S then O, or X^T / U^T (A, FP16
+    // pairs: 32 columns) | T X at +64); Khat^T U as dS^T
     static constexpr uint32_t T_S = 0, R0 = 128, R1 = 256, T_D3 = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(TOTAL <= 232448, "shared memory budget exceeded");
 };
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
-    float a[16], b[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        a[i] = v[i];
-        b[i] = v[16 + i];
-    }
-    tc::tmem_st16(taddr, a);
-    tc::tmem_st16(taddr + 16, b);
-}
 
 // The chain of (sequence n, head h).  When `ready` is set, chunk g's operands
 // are read only after ready[g * heads + h] has been released by the CTA that
@@ -1176,11 +1191,11 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
     float sreg[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) sreg[i] = Sg[(size_t)i * D];
-    {
-        float sv[32];
+    {   // S^T: K index 32 cg + i in column 16 cg + i / 2
+        uint32_t sv[16];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[i] = tc::to_tf32(sreg[i]);
-        tmem_st32(my + ScanT::T_S + 32 * cg, sv);
+        for (int m = 0; m < 16; ++m) sv[m] = tc::pack_f16x2(sreg[2 * m], sreg[2 * m + 1]);
+        tc::tmem_st16u(my + ScanT::T_S + 16 * cg, sv);
         tc::tmem_st_wait();
     }
 
@@ -1202,8 +1217,8 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         }
         const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
         unsigned char* dst = sm + (xb ? ScanT::OPX1 : (uint32_t)SS_OPX);
-        tc::mbar_arrive_expect_tx(bar_x + xb, OpX::bytes(128));
-        tc::bulk_load(dst, blob + BLOB_OPX, OpX::bytes(128), bar_x + xb);
+        tc::mbar_arrive_expect_tx(bar_x + xb, OpXh::bytes(128));
+        tc::bulk_load(dst, blob + BLOB_OPX, OpXh::bytes(128), bar_x + xb);
         out_x |= 1u << xb;
     };
     auto load_v = [&](int cc0) {
@@ -1213,9 +1228,9 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
     };
     auto load_b = [&](long long gg) {  // issued after load_x(gg): its flag is observed
         const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
-        tc::mbar_arrive_expect_tx(bar_b, OpTP::bytes(64) + OpKH::bytes(64) + 128 * 4);
-        tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTP::bytes(64), bar_b);
-        tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKH::bytes(64), bar_b);
+        tc::mbar_arrive_expect_tx(bar_b, OpTPh::bytes(64) + OpKHh::bytes(64) + 128 * 4);
+        tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTPh::bytes(64), bar_b);
+        tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKHh::bytes(64), bar_b);
         tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_b);
         out_b = true;
     };
@@ -1262,10 +1277,10 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         // (one N = 128 product: Ktil S into r_d1, Qtil S into r_d1 + 64)
         if (tid == 0) {
             tc::tc_fence_after();
-            for (int ks = 0; ks < 16; ++ks)
-                tc::mma_tf32_ta(tmem + r_d1, tmem + ScanT::T_S + 8 * ks,
-                                OpX::desc(xb ? s_opx1 : s_opx0, ks), tc::idesc_tf32(128, 128),
-                                ks > 0);
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_f16_ta(tmem + r_d1, tmem + ScanT::T_S + 8 * ks,
+                               OpXh::desc(xb ? s_opx1 : s_opx0, ks), tc::idesc_f16(128, 128),
+                               ks > 0);
             tc::mma_commit(bar_mma);
         }
         // the next chunk's [Ktil; Qtil] (its ready flag and the copy) while
@@ -1288,10 +1303,12 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 const int r = 16 * cg + i;
-                const float x = (r < L) ? vr[i] - v[i] : 0.f;
-                v[i] = tc::to_tf32(x);
+                v[i] = (r < L) ? vr[i] - v[i] : 0.f;
             }
-            tc::tmem_st16(my + r_a + 16 * cg, v);
+            uint32_t xv[8];  // X^T: token 16 cg + i in column 8 cg + i / 2
+#pragma unroll
+            for (int m = 0; m < 8; ++m) xv[m] = tc::pack_f16x2(v[2 * m], v[2 * m + 1]);
+            tc::tmem_st8u(my + r_a + 8 * cg, xv);
             tc::tmem_st_wait();
         }
         tc::tc_fence_before();
@@ -1305,9 +1322,9 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         // ---------------------------------------------------------- U^T = X^T T^T
         if (tid == 0) {
             tc::tc_fence_after();
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_tf32_ta(tmem + r_a + 64, tmem + r_a + 8 * ks, OpTP::desc(s_tp, ks),
-                                tc::idesc_tf32(128, 64), ks > 0);
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_f16_ta(tmem + r_a + 64, tmem + r_a + 8 * ks, OpTPh::desc(s_tp, ks),
+                               tc::idesc_f16(128, 64), ks > 0);
             tc::mma_commit(bar_mma);
         }
         wait_bar(bar_mma, ph_mma);
@@ -1317,9 +1334,10 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
             float v[16];
             tc::tmem_ld16(my + r_a + 64 + 16 * cg, v);
             tc::tmem_ld_wait();
+            uint32_t uv[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = tc::to_tf32(v[i]);
-            tc::tmem_st16(my + r_a + 16 * cg, v);
+            for (int m = 0; m < 8; ++m) uv[m] = tc::pack_f16x2(v[2 * m], v[2 * m + 1]);
+            tc::tmem_st8u(my + r_a + 8 * cg, uv);
             tc::tmem_st_wait();
         }
         tc::tc_fence_before();
@@ -1328,12 +1346,12 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         // ---------------------------------------------------------- U^T Khat; O^T += U^T P^T
         if (tid == 0) {
             tc::tc_fence_after();
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_tf32_ta(tmem + ScanT::T_D3, tmem + r_a + 8 * ks, OpKH::desc(s_kh, ks),
-                                tc::idesc_tf32(128, 128), ks > 0);
-            for (int ks = 0; ks < 8; ++ks)  // P = rows 64..127 of [T; P]
-                tc::mma_tf32_ta(tmem + r_d1 + 64, tmem + r_a + 8 * ks,
-                                OpTP::desc(s_tp + 8 * 128, ks), tc::idesc_tf32(128, 64), true);
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_f16_ta(tmem + ScanT::T_D3, tmem + r_a + 8 * ks, OpKHh::desc(s_kh, ks),
+                               tc::idesc_f16(128, 128), ks > 0);
+            for (int ks = 0; ks < 4; ++ks)  // P = rows 64..127 of [T; P]
+                tc::mma_f16_ta(tmem + r_d1 + 64, tmem + r_a + 8 * ks,
+                               OpTPh::desc(s_tp + 8 * 128, ks), tc::idesc_f16(128, 64), true);
             tc::mma_commit(bar_mma);
         }
         wait_bar(bar_mma, ph_mma);
@@ -1355,11 +1373,11 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
                 }
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                sreg[i] = __fmaf_rn(DECC[32 * cg + i], sreg[i], v[i]);
-                v[i] = tc::to_tf32(sreg[i]);
-            }
-            tmem_st32(my + ScanT::T_S + 32 * cg, v);
+            for (int i = 0; i < 32; ++i) sreg[i] = __fmaf_rn(DECC[32 * cg + i], sreg[i], v[i]);
+            uint32_t sv[16];
+#pragma unroll
+            for (int m = 0; m < 16; ++m) sv[m] = tc::pack_f16x2(sreg[2 * m], sreg[2 * m + 1]);
+            tc::tmem_st16u(my + ScanT::T_S + 16 * cg, sv);
             if (L == C) {  // staged row-major [64][128] for the tile store
                 float* ost = reinterpret_cast<float*>(sm + (xb ? ScanT::OPX1 : (uint32_t)SS_OPX));
 #pragma unroll
@@ -1449,7 +1467,7 @@ size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads) {
 // Per-SM cost figures measured on GB300 (T = 8192, 32 heads) that choose
 // between the fused grid and the two kernels: a prepare item, and a chunk of
 // the transposed and of the 32-column scan chain.
-constexpr double kPrepItemUs = 9.3, kScanTChunkUs = 3.3, kScan32ChunkUs = 2.2;
+constexpr double kPrepItemUs = 9.3, kScanTChunkUs = 2.9, kScan32ChunkUs = 2.0;
 
 // Launches the tensor-core prefill (BF16 inputs, chunk 64); arguments,
 // including the workspace size, are validated by kda_prefill.

@@ -121,7 +121,8 @@ def test_workspace_size_is_queryable(lib):
     f.restype = SZ
     f.argtypes = [ctypes.c_int64, I, I, I, I, I]
     big = f(8192, 1, 64, 32, 128, 1)          # BF16, chunk 64: tensor-core path
-    assert big >= (8192 // 64) * 32 * 131584
+    # per (chunk, head): FP16 [Ktil; Qtil] 32 KiB, [T; P] 16 KiB, Khat^T 16 KiB, dec 512 B
+    assert big >= (8192 // 64) * 32 * (32768 + 16384 + 16384 + 512)
     assert f(8192, 1, 64, 32, 128, 0) == 0    # FP32 inputs need none
     assert f(8192, 1, 32, 32, 128, 1) == 0    # other chunk widths need none
     assert f(8192, 1, 64, 32, 64, 1) == 0     # invalid head_dim
