@@ -1098,7 +1098,7 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
 // One CTA per (sequence, head) carries the whole 128 x 128 state through the
 // chunks in transposed form, so that each matrix on the state's chain is the
 // A operand of the next product and stays in TMEM (lane = value column j,
-// one column per K index):
+// two FP16 values per column along K):
 //   X^T = V^T - S^T Ktil^T;  U^T = X^T T^T;  O^T = S^T Qtil^T + U^T P^T;
 //   S^T <- S^T diag(dec) + U^T Khat
 // The prepared operands are the B operands, in the layouts prepare writes:
@@ -1107,32 +1107,41 @@ scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
 // computed them, so no operand passes through shared memory on the chain.
 struct ScanT {
     static constexpr int NT = 512;  // 4 lane quarters x 4 column groups
-    // shared memory: blob image (OPX | TP | KH | DEC; its OPX is operand
-    // buffer 0), value tile [64][128] BF16 (no swizzle), a copy of dec,
-    // operand buffer 1 for [Ktil; Qtil], barriers
+    // shared memory: blob image (OPX | TP | KH | DEC: operand group 0 of
+    // [Ktil; Qtil] and of [T; P] | Khat^T | dec), value tile [64][128] BF16
+    // (no swizzle), group 1 of [T; P] | Khat^T | dec, group 1 of
+    // [Ktil; Qtil], the O staging tile [64][128] FP32, barriers
+    static constexpr uint32_t BGRP = BLOB_BYTES - BLOB_TP;  // [T; P] | Khat^T | dec
     static constexpr uint32_t RAWV = (BLOB_BYTES + 1023) & ~1023u;
-    static constexpr uint32_t DECC = RAWV + 64 * D * 2;
-    static constexpr uint32_t OPX1 = (DECC + D * 4 + 1023) & ~1023u;
-    static constexpr uint32_t BAR = OPX1 + OpXh::bytes(128);
-    static constexpr uint32_t TOTAL = BAR + 64;
+    static constexpr uint32_t TP1 = RAWV + 64 * D * 2;
+    static constexpr uint32_t OPX1 = (TP1 + BGRP + 1023) & ~1023u;
+    static constexpr uint32_t OST = OPX1 + OpXh::bytes(128);
+    static constexpr uint32_t BAR = OST + 64 * D * 4;
+    static constexpr uint32_t TOTAL = BAR + 128;
     // TMEM columns: S^T (A, FP16 pairs: 64 columns); two 128-column chunk
     // regions used alternately (Ktil S | Qtil S then O, or X^T / U^T (A, FP16
     // pairs: 32 columns) | T X at +64); Khat^T U as dS^T
     static constexpr uint32_t T_S = 0, R0 = 128, R1 = 256, T_D3 = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(TOTAL <= 232448, "shared memory budget exceeded");
+    static_assert(TP1 % 16 == 0 && OST % 128 == 0, "copy alignment");
 };
-
 
 // The chain of (sequence n, head h).  When `ready` is set, chunk g's operands
 // are read only after ready[g * heads + h] has been released by the CTA that
 // prepared them (the prepare and scan roles then share one cooperative grid).
 //
-// Per chunk: three tensor-core round trips of 16, 8 and 16 K-steps (the
+// Per chunk: three tensor-core round trips of 8, 4 and 8 FP16 K-steps (the
 // tensor core takes about the same time per instruction for any N <= 128,
-// so Qtil S rides with Ktil S and P U with Khat^T U).  [Ktil; Qtil] is
-// double-buffered and requested a chunk ahead; the value tile and [T; P],
-// Khat^T, dec as soon as their buffers are consumed.
+// so Qtil S rides with Ktil S and P U with Khat^T U).  Both operand groups
+// are double-buffered by chunk parity, so chunk g + 1's are requested (after
+// its ready flag) while chunk g's first product runs, a whole chunk ahead;
+// the value tile as soon as it is consumed.  O of chunk g is read from TMEM
+// and staged while chunk g + 1's first product runs (every thread but the
+// issuing one is idle then) and leaves by one TMA tile store that no thread
+// waits for: per-thread global stores of O cost the chain about 1.4K cycles
+// per chunk while the prepare CTAs keep the memory system busy.  Rows of a
+// partial chunk go out by plain stores.
 __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUtensorMap& omap,
                                             float* __restrict__ state,
                                             float* __restrict__ o, int t, int t_pad, int heads,
@@ -1160,20 +1169,19 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         return;
     }
 
-    const float* DEC = reinterpret_cast<const float*>(sm + SS_DEC);
-    float* DECC = reinterpret_cast<float*>(sm + ScanT::DECC);
     const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + ScanT::RAWV);
-    uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + ScanT::BAR);  // [2]: operand buffers
-    uint64_t* bar_v = bar_x + 2;
-    uint64_t* bar_b = bar_x + 3;
-    uint64_t* bar_mma = bar_x + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ScanT::BAR + 48);
-    int* abort_flag = reinterpret_cast<int*>(sm + ScanT::BAR + 52);
-    const uint32_t s_opx0 = tc::smem_u32(sm + SS_OPX), s_opx1 = tc::smem_u32(sm + ScanT::OPX1);
-    const uint32_t s_tp = tc::smem_u32(sm + SS_TP), s_kh = tc::smem_u32(sm + SS_KH);
+    float* OST = reinterpret_cast<float*>(sm + ScanT::OST);
+    uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + ScanT::BAR);  // [2]: [Ktil; Qtil] groups
+    uint64_t* bar_b = bar_x + 2;                                     // [2]: [T; P] | Khat^T | dec
+    uint64_t* bar_v = bar_x + 4;
+    uint64_t* bar_mma = bar_x + 5;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ScanT::BAR + 64);
+    int* abort_flag = reinterpret_cast<int*>(sm + ScanT::BAR + 68);
+    const uint32_t opx_off[2] = {(uint32_t)SS_OPX, ScanT::OPX1};
+    const uint32_t tp_off[2] = {(uint32_t)SS_TP, ScanT::TP1};  // group b: TP, KH, DEC follow
 
     if (tid == 0) {
-        for (int i = 0; i < 5; ++i) tc::mbar_init(bar_x + i, 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(bar_x + i, 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&vmap);
         tc::prefetch_tmap(&omap);
@@ -1199,7 +1207,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         tc::tmem_st_wait();
     }
 
-    uint32_t ph_mma = 0, ph_v = 0, ph_b = 0, ph_x = 0;  // ph_x: bit per buffer
+    uint32_t ph_mma = 0, ph_v = 0, ph_x = 0, ph_b = 0;  // ph_x, ph_b: bit per group
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
         if (!tc::mbar_wait(bar, parity)) {
             atomicOr(&g_tc_status, STATUS_TIMEOUT);
@@ -1208,54 +1216,34 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
     };
     // Copies (the copier thread).  Outstanding ones are tracked so an early
     // exit can let them land before the shared memory is released.
-    uint32_t out_x = 0;  // bit per operand buffer
-    bool out_v = false, out_b = false;
-    auto load_x = [&](long long gg, int xb) {  // [Ktil; Qtil] of chunk gg, after its flag
+    uint32_t out_x = 0, out_b = 0;  // bit per group
+    bool out_v = false;
+    auto load_ops = [&](long long gg, int b) {  // chunk gg's operands into group b, after its flag
         if (ready && !tc::flag_acquire(ready + gg * heads + h)) {
             atomicOr(&g_tc_status, STATUS_TIMEOUT);
             *abort_flag = 1;
         }
         const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
-        unsigned char* dst = sm + (xb ? ScanT::OPX1 : (uint32_t)SS_OPX);
-        tc::mbar_arrive_expect_tx(bar_x + xb, OpXh::bytes(128));
-        tc::bulk_load(dst, blob + BLOB_OPX, OpXh::bytes(128), bar_x + xb);
-        out_x |= 1u << xb;
+        tc::mbar_arrive_expect_tx(bar_x + b, OpXh::bytes(128));
+        tc::bulk_load(sm + opx_off[b], blob + BLOB_OPX, OpXh::bytes(128), bar_x + b);
+        tc::mbar_arrive_expect_tx(bar_b + b, ScanT::BGRP);
+        tc::bulk_load(sm + tp_off[b], blob + BLOB_TP, ScanT::BGRP, bar_b + b);
+        out_x |= 1u << b;
+        out_b |= 1u << b;
     };
     auto load_v = [&](int cc0) {
         tc::mbar_arrive_expect_tx(bar_v, 64 * D * 2);
         tc::tma_load_2d(sm + ScanT::RAWV, &vmap, bar_v, h * D, cc0);
         out_v = true;
     };
-    auto load_b = [&](long long gg) {  // issued after load_x(gg): its flag is observed
-        const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
-        tc::mbar_arrive_expect_tx(bar_b, OpTPh::bytes(64) + OpKHh::bytes(64) + 128 * 4);
-        tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTPh::bytes(64), bar_b);
-        tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKHh::bytes(64), bar_b);
-        tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_b);
-        out_b = true;
-    };
     if (copier && start < end) {
-        load_x(g0, 0);
+        load_ops(g0, 0);
         load_v(start);
-        load_b(g0);
     }
 
-    // O of a whole chunk leaves by one TMA tile store that no thread waits
-    // for: the threads read it from TMEM with the state increment and stage it
-    // row-major in the chunk's [Ktil; Qtil] buffer (consumed by then); the
-    // copier issues the store after the next barrier and lets it finish
-    // reading before that buffer is refilled.  (Per-thread global stores cost
-    // the chain about 1.4K cycles per chunk while the prepare CTAs keep the
-    // memory system busy.)  A partial chunk's rows go out by plain stores.
-    int st_c0 = -1, st_xb = 0;  // the staged chunk whose store is still to be issued
-    auto issue_o_store = [&]() {
-        if (copier && st_c0 >= 0) {
-            tc::tma_store_2d(&omap, sm + (st_xb ? ScanT::OPX1 : (uint32_t)SS_OPX), h * D, st_c0);
-            tc::bulk_commit();
-        }
-        st_c0 = -1;
-    };
-
+    int o_c0 = -1, o_L = 0;  // the chunk whose O is still in TMEM (region o_reg)
+    uint32_t o_reg = 0;
+    bool o_staged = false;  // a staged O waits for its store (copier issues it)
     long long g = g0;
     int xb = 0;
     for (int c0 = start; c0 < end; c0 += C, ++g, xb ^= 1) {
@@ -1263,9 +1251,12 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         const bool more = c0 + C < end;
         const uint32_t r_d1 = xb ? ScanT::R1 : ScanT::R0;  // Ktil S, then Qtil S / O at +64
         const uint32_t r_a = xb ? ScanT::R0 : ScanT::R1;   // X^T / U^T (A), then T X at +64
+        const uint32_t s_tp = tc::smem_u32(sm + tp_off[xb]);
+        const uint32_t s_kh = s_tp + (BLOB_KH - BLOB_TP);
+        const float* DEC = reinterpret_cast<const float*>(sm + tp_off[xb] + (BLOB_DEC - BLOB_TP));
+        if (copier) tc::bulk_wait_read_all();  // the staging tile's last store has read it
         tc::tc_fence_before();
         if (__syncthreads_or(*abort_flag)) break;  // every thread takes the same exit
-        issue_o_store();  // the previous chunk's staged O
         wait_bar(bar_x + xb, (ph_x >> xb) & 1u);
         ph_x ^= 1u << xb;
         if (copier) out_x &= ~(1u << xb);
@@ -1279,16 +1270,32 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
             tc::tc_fence_after();
             for (int ks = 0; ks < 8; ++ks)
                 tc::mma_f16_ta(tmem + r_d1, tmem + ScanT::T_S + 8 * ks,
-                               OpXh::desc(xb ? s_opx1 : s_opx0, ks), tc::idesc_f16(128, 128),
-                               ks > 0);
+                               OpXh::desc(tc::smem_u32(sm + opx_off[xb]), ks),
+                               tc::idesc_f16(128, 128), ks > 0);
             tc::mma_commit(bar_mma);
         }
-        // the next chunk's [Ktil; Qtil] (its ready flag and the copy) while
-        // this product runs; that buffer's last products have completed and
-        // the previous chunk's O store has read it
-        if (copier && more) {
-            tc::bulk_wait_read_all();
-            load_x(g + 1, xb ^ 1);
+        // the next chunk's operands into the other groups, whose last products
+        // completed in the previous chunk
+        if (copier && more) load_ops(g + 1, xb ^ 1);
+        // the previous chunk's O (in r_a + 64, which this chunk's T X
+        // overwrites) into the staging tile, or straight out if partial
+        if (o_c0 >= 0) {
+            float ov[16];
+            tc::tmem_ld16(my + o_reg + 16 * cg, ov);
+            tc::tmem_ld_wait();
+            if (o_L == C) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) OST[(16 * cg + i) * D + j] = ov[i];
+                tc::fence_async_smem();
+                o_staged = true;
+            } else {
+                float* orow = o + ((size_t)o_c0 * heads + h) * D + j;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = 16 * cg + i;
+                    if (r < o_L) orow[(size_t)r * heads * D] = ov[i];
+                }
+            }
         }
         float vr[16];  // V[16 cg + i][j], read while the product runs
 #pragma unroll
@@ -1313,11 +1320,17 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         }
         tc::tc_fence_before();
         __syncthreads();
-        if (copier && more) load_v(c0 + C);  // the value tile is consumed
-        wait_bar(bar_b, ph_b);
-        ph_b ^= 1;
-        if (copier) out_b = false;
-        if (tid < D) DECC[tid] = DEC[tid];  // read after the next barrier
+        if (copier) {
+            if (o_staged) {  // the previous chunk's O, staged by every thread
+                tc::tma_store_2d(&omap, OST, h * D, o_c0);
+                tc::bulk_commit();
+            }
+            if (more) load_v(c0 + C);  // the value tile is consumed
+        }
+        o_staged = false;
+        wait_bar(bar_b + xb, (ph_b >> xb) & 1u);
+        ph_b ^= 1u << xb;
+        if (copier) out_b &= ~(1u << xb);
 
         // ---------------------------------------------------------- U^T = X^T T^T
         if (tid == 0) {
@@ -1357,54 +1370,46 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         wait_bar(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::tc_fence_after();
-        if (copier && more) load_b(g + 1);  // [T; P] and Khat^T are consumed
-        {   // S[32 cg + i][j] <- dec * S + (Khat^T U)[32 cg + i][j]; O[16 cg + i][j]
-            float v[32], ov[16];
-            {
-                float a[16], b[16];
-                tc::tmem_ld16(my + ScanT::T_D3 + 32 * cg, a);
-                tc::tmem_ld16(my + ScanT::T_D3 + 32 * cg + 16, b);
-                tc::tmem_ld16(my + r_d1 + 64 + 16 * cg, ov);
-                tc::tmem_ld_wait();
+        {   // S[32 cg + i][j] <- dec * S + (Khat^T U)[32 cg + i][j]
+            float a[16], b[16];
+            tc::tmem_ld16(my + ScanT::T_D3 + 32 * cg, a);
+            tc::tmem_ld16(my + ScanT::T_D3 + 32 * cg + 16, b);
+            tc::tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    v[i] = a[i];
-                    v[16 + i] = b[i];
-                }
+            for (int i = 0; i < 16; ++i) {
+                sreg[i] = __fmaf_rn(DEC[32 * cg + i], sreg[i], a[i]);
+                sreg[16 + i] = __fmaf_rn(DEC[32 * cg + 16 + i], sreg[16 + i], b[i]);
             }
-#pragma unroll
-            for (int i = 0; i < 32; ++i) sreg[i] = __fmaf_rn(DECC[32 * cg + i], sreg[i], v[i]);
             uint32_t sv[16];
 #pragma unroll
             for (int m = 0; m < 16; ++m) sv[m] = tc::pack_f16x2(sreg[2 * m], sreg[2 * m + 1]);
             tc::tmem_st16u(my + ScanT::T_S + 16 * cg, sv);
-            if (L == C) {  // staged row-major [64][128] for the tile store
-                float* ost = reinterpret_cast<float*>(sm + (xb ? ScanT::OPX1 : (uint32_t)SS_OPX));
-#pragma unroll
-                for (int i = 0; i < 16; ++i) ost[(16 * cg + i) * D + j] = ov[i];
-                tc::fence_async_smem();
-                st_c0 = c0;
-                st_xb = xb;
-            } else {
-                float* orow = o + ((size_t)c0 * heads + h) * D + j;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int r = 16 * cg + i;
-                    if (r < L) orow[(size_t)r * heads * D] = ov[i];
-                }
-            }
             tc::tmem_st_wait();
         }
+        o_c0 = c0;
+        o_L = L;
+        o_reg = r_d1 + 64;
     }
     // every thread leaves the loop through the same iteration; agree on the flag
     const bool aborted = __syncthreads_or(*abort_flag);
-    if (!aborted) issue_o_store();  // the last chunk's staged O
+    if (o_c0 >= 0 && !aborted) {  // the last chunk's O, by plain stores
+        float ov[16];
+        tc::tmem_ld16(my + o_reg + 16 * cg, ov);
+        tc::tmem_ld_wait();
+        float* orow = o + ((size_t)o_c0 * heads + h) * D + j;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * cg + i;
+            if (r < o_L) orow[(size_t)r * heads * D] = ov[i];
+        }
+    }
     if (copier) {  // copies still in flight land before the exit (bounded waits)
         tc::bulk_wait_all();
-        for (int b2 = 0; b2 < 2; ++b2)
+        for (int b2 = 0; b2 < 2; ++b2) {
             if ((out_x >> b2) & 1u) tc::mbar_wait(bar_x + b2, (ph_x >> b2) & 1u, 1u << 20);
+            if ((out_b >> b2) & 1u) tc::mbar_wait(bar_b + b2, (ph_b >> b2) & 1u, 1u << 20);
+        }
         if (out_v) tc::mbar_wait(bar_v, ph_v, 1u << 20);
-        if (out_b) tc::mbar_wait(bar_b, ph_b, 1u << 20);
     }
     if (!aborted) {
 #pragma unroll
