@@ -1118,10 +1118,12 @@ struct ScanT {
     static constexpr uint32_t OST = OPX1 + OpXh::bytes(128);
     static constexpr uint32_t BAR = OST + 64 * D * 4;
     static constexpr uint32_t TOTAL = BAR + 128;
-    // TMEM columns: S^T (A, FP16 pairs: 64 columns); two 128-column chunk
-    // regions used alternately (Ktil S | Qtil S then O, or X^T / U^T (A, FP16
-    // pairs: 32 columns) | T X at +64); Khat^T U as dS^T
-    static constexpr uint32_t T_S = 0, R0 = 128, R1 = 256, T_D3 = 384;
+    // TMEM columns: S^T (A, FP16 pairs: 64 columns), T X (64); two
+    // 128-column chunk regions used alternately: chunk g computes Ktil S |
+    // Qtil S, then O, in R_(g mod 2) and keeps X^T / U^T (A, FP16 pairs: 32
+    // columns) in the first columns of the other region, whose last 64 still
+    // hold chunk g - 1's O until chunk g + 1's first product; Khat^T U as dS^T
+    static constexpr uint32_t T_S = 0, T_TX = 64, R0 = 128, R1 = 256, T_D3 = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(TOTAL <= 232448, "shared memory budget exceeded");
     static_assert(TP1 % 16 == 0 && OST % 128 == 0, "copy alignment");
@@ -1136,12 +1138,13 @@ struct ScanT {
 // so Qtil S rides with Ktil S and P U with Khat^T U).  Both operand groups
 // are double-buffered by chunk parity, so chunk g + 1's are requested (after
 // its ready flag) while chunk g's first product runs, a whole chunk ahead;
-// the value tile as soon as it is consumed.  O of chunk g is read from TMEM
-// and staged while chunk g + 1's first product runs (every thread but the
-// issuing one is idle then) and leaves by one TMA tile store that no thread
-// waits for: per-thread global stores of O cost the chain about 1.4K cycles
-// per chunk while the prepare CTAs keep the memory system busy.  Rows of a
-// partial chunk go out by plain stores.
+// the value tile as soon as it is consumed.  O of chunk g - 1 is read from
+// TMEM and staged while chunk g's last product runs, by the warps that do
+// not issue it (warp 0's rows go to the other warps of its TMEM lane
+// quarter), and leaves by one TMA tile store that no thread waits for:
+// per-thread global stores of O cost the chain about 1.4K cycles per chunk
+// while the prepare CTAs keep the memory system busy.  Rows of a partial
+// chunk go out by plain stores.
 __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUtensorMap& omap,
                                             float* __restrict__ state,
                                             float* __restrict__ o, int t, int t_pad, int heads,
@@ -1243,7 +1246,8 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
 
     int o_c0 = -1, o_L = 0;  // the chunk whose O is still in TMEM (region o_reg)
     uint32_t o_reg = 0;
-    bool o_staged = false;  // a staged O waits for its store (copier issues it)
+    bool o_staged = false;  // a staged O (chunk st_c0) waits for its store
+    int st_c0 = -1;
     long long g = g0;
     int xb = 0;
     for (int c0 = start; c0 < end; c0 += C, ++g, xb ^= 1) {
@@ -1254,9 +1258,13 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         const uint32_t s_tp = tc::smem_u32(sm + tp_off[xb]);
         const uint32_t s_kh = s_tp + (BLOB_KH - BLOB_TP);
         const float* DEC = reinterpret_cast<const float*>(sm + tp_off[xb] + (BLOB_DEC - BLOB_TP));
-        if (copier) tc::bulk_wait_read_all();  // the staging tile's last store has read it
         tc::tc_fence_before();
         if (__syncthreads_or(*abort_flag)) break;  // every thread takes the same exit
+        if (copier && o_staged) {  // chunk g - 2's O, staged during the last chunk
+            tc::tma_store_2d(&omap, OST, h * D, st_c0);
+            tc::bulk_commit();
+        }
+        o_staged = false;
         wait_bar(bar_x + xb, (ph_x >> xb) & 1u);
         ph_x ^= 1u << xb;
         if (copier) out_x &= ~(1u << xb);
@@ -1277,26 +1285,6 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         // the next chunk's operands into the other groups, whose last products
         // completed in the previous chunk
         if (copier && more) load_ops(g + 1, xb ^ 1);
-        // the previous chunk's O (in r_a + 64, which this chunk's T X
-        // overwrites) into the staging tile, or straight out if partial
-        if (o_c0 >= 0) {
-            float ov[16];
-            tc::tmem_ld16(my + o_reg + 16 * cg, ov);
-            tc::tmem_ld_wait();
-            if (o_L == C) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) OST[(16 * cg + i) * D + j] = ov[i];
-                tc::fence_async_smem();
-                o_staged = true;
-            } else {
-                float* orow = o + ((size_t)o_c0 * heads + h) * D + j;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const int r = 16 * cg + i;
-                    if (r < o_L) orow[(size_t)r * heads * D] = ov[i];
-                }
-            }
-        }
         float vr[16];  // V[16 cg + i][j], read while the product runs
 #pragma unroll
         for (int i = 0; i < 16; ++i) vr[i] = bf(RAWV[(16 * cg + i) * D + j]);
@@ -1320,14 +1308,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         }
         tc::tc_fence_before();
         __syncthreads();
-        if (copier) {
-            if (o_staged) {  // the previous chunk's O, staged by every thread
-                tc::tma_store_2d(&omap, OST, h * D, o_c0);
-                tc::bulk_commit();
-            }
-            if (more) load_v(c0 + C);  // the value tile is consumed
-        }
-        o_staged = false;
+        if (copier && more) load_v(c0 + C);  // the value tile is consumed
         wait_bar(bar_b + xb, (ph_b >> xb) & 1u);
         ph_b ^= 1u << xb;
         if (copier) out_b &= ~(1u << xb);
@@ -1336,7 +1317,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         if (tid == 0) {
             tc::tc_fence_after();
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f16_ta(tmem + r_a + 64, tmem + r_a + 8 * ks, OpTPh::desc(s_tp, ks),
+                tc::mma_f16_ta(tmem + ScanT::T_TX, tmem + r_a + 8 * ks, OpTPh::desc(s_tp, ks),
                                tc::idesc_f16(128, 64), ks > 0);
             tc::mma_commit(bar_mma);
         }
@@ -1345,7 +1326,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         tc::tc_fence_after();
         {
             float v[16];
-            tc::tmem_ld16(my + r_a + 64 + 16 * cg, v);
+            tc::tmem_ld16(my + ScanT::T_TX + 16 * cg, v);
             tc::tmem_ld_wait();
             uint32_t uv[8];
 #pragma unroll
@@ -1353,6 +1334,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
             tc::tmem_st8u(my + r_a + 8 * cg, uv);
             tc::tmem_st_wait();
         }
+        if (copier) tc::bulk_wait_read_all();  // the staging tile's last store has read it
         tc::tc_fence_before();
         __syncthreads();
 
@@ -1366,6 +1348,42 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
                 tc::mma_f16_ta(tmem + r_d1 + 64, tmem + r_a + 8 * ks,
                                OpTPh::desc(s_tp + 8 * 128, ks), tc::idesc_f16(128, 64), true);
             tc::mma_commit(bar_mma);
+        }
+        // chunk g - 1's O (the last 64 columns of r_a) into the staging tile
+        // while this product runs, or straight out if partial
+        if (o_c0 >= 0 && warp != 0) {
+            float ov[16];
+            tc::tmem_ld16(my + o_reg + 16 * cg, ov);
+            float ow[8];  // warps 4 and 8 also take rows 0..7 and 8..15 of warp 0
+            const bool extra = (qd == 0) && (cg == 1 || cg == 2);
+            const int wr = (cg == 1) ? 0 : 8;
+            if (extra) tc::tmem_ld8(my + o_reg + wr, ow);
+            tc::tmem_ld_wait();
+            if (o_L == C) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) OST[(16 * cg + i) * D + j] = ov[i];
+                if (extra) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) OST[(wr + i) * D + j] = ow[i];
+                }
+                tc::fence_async_smem();
+            } else {
+                float* orow = o + ((size_t)o_c0 * heads + h) * D + j;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int r = 16 * cg + i;
+                    if (r < o_L) orow[(size_t)r * heads * D] = ov[i];
+                }
+                if (extra) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        if (wr + i < o_L) orow[(size_t)(wr + i) * heads * D] = ow[i];
+                }
+            }
+        }
+        if (o_c0 >= 0 && o_L == C) {
+            o_staged = true;
+            st_c0 = o_c0;
         }
         wait_bar(bar_mma, ph_mma);
         ph_mma ^= 1;
@@ -1392,6 +1410,10 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
     }
     // every thread leaves the loop through the same iteration; agree on the flag
     const bool aborted = __syncthreads_or(*abort_flag);
+    if (copier && o_staged && !aborted) {  // the staged O of the chunk before the last
+        tc::tma_store_2d(&omap, OST, h * D, st_c0);
+        tc::bulk_commit();
+    }
     if (o_c0 >= 0 && !aborted) {  // the last chunk's O, by plain stores
         float ov[16];
         tc::tmem_ld16(my + o_reg + 16 * cg, ov);
