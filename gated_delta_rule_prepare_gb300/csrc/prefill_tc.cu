@@ -301,10 +301,17 @@ __device__ __forceinline__ PrepItem prep_item(long long item, int heads, const i
                                               const int* __restrict__ chunk_off, int n_seqs, int t,
                                               int t_pad) {
     PrepItem it;
-    it.g = item / heads;
-    it.h = (int)(item - it.g * heads);
+    if (item < 0x7fffffffLL) {  // 32-bit divisions (a 64-bit one is a long software routine)
+        const int g32 = (int)item / heads;
+        it.g = g32;
+        it.h = (int)item - g32 * heads;
+    } else {
+        it.g = item / heads;
+        it.h = (int)(item - it.g * heads);
+    }
     if (!cu) {  // uniform sequences of t tokens, t_pad rows apart: no table lookup
-        const long long cps = (t + C - 1) / C, n = it.g / cps;
+        const int cps = (t + C - 1) / C;
+        const long long n = (it.g < 0x7fffffffLL) ? (long long)((int)it.g / cps) : it.g / cps;
         it.c0 = (int)(n * t_pad + (it.g - n * cps) * C);
         it.valid = n < n_seqs;
         it.L = it.valid ? min(C, (int)(n * t_pad) + t - it.c0) : 0;
@@ -404,10 +411,13 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             }
         }
     };
+    // beta of item `it` (threads 0..63): the raw BF16 bits, widened only
+    // when the item starts, so nothing waits on the load before then
     auto load_beta = [&](const PrepItem& it) {
-        return (tid < C && it.valid && tid < it.L)
-                   ? bf(__ldg(beta + (size_t)(it.c0 + tid) * heads + it.h))
-                   : 0.f;
+        uint16_t raw = 0;
+        if (tid < C && it.valid && tid < it.L)
+            raw = __ldg(beta + (size_t)(it.c0 + tid) * heads + it.h);
+        return raw;
     };
 
     // The item whose ready flag is still to be released (copier thread): an
@@ -425,14 +435,14 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     long long item = first;
     PrepItem cur = prep_item(item, heads, cu, chunk_off, n_seqs, t, t_pad);
     load_raw(cur, 0);
-    float beta_cur = load_beta(cur);
+    uint16_t beta_cur = load_beta(cur);
 
     for (int iter = 0; item < items; ++iter) {
         const int b = iter & 1;
         const long long nitem = item + stride;
         PrepItem nxt = {};
         nxt.valid = false;
-        float beta_nxt = 0.f;
+        uint16_t beta_nxt = 0;
         // The next item is resolved (global loads) while the first A/P product
         // runs, and its raw tiles go to the other buffer, which the previous
         // iteration's closing barrier released.
@@ -456,7 +466,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             float* TM = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_TM);
             unsigned char* blob = ws + blob_offset(n_seqs, cur.g, h, heads);
 
-            if (tid < C) BETA[tid] = beta_cur;
+            if (tid < C) BETA[tid] = bf(beta_cur);
             if (!tc::mbar_wait(bar_tma + b, ph_tma[b])) {
                 atomicOr(&g_tc_status, STATUS_TIMEOUT);
                 failed = true;
