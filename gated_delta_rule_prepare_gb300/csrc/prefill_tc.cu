@@ -1,6 +1,6 @@
 // Tensor-core chunked prefill of the KDA core for BF16 inputs and chunk 64:
-// Glm5NextKdaKernels::chunk_prepare and chunk_scan as two kernels around a
-// caller-owned workspace.
+// Glm5NextKdaKernels::chunk_prepare and chunk_scan around a caller-owned
+// workspace, as two kernels or as one cooperative grid.
 //
 // For a chunk of L <= 64 tokens (rows r, s; key channels i; value columns j)
 // of one head, with Gamma_r = sum_{u<=r} g_u and qh = KDA_Q_SCALE q:
@@ -16,6 +16,16 @@
 // [Ktil; Qtil], [T; P], Khat^T (FP16 tensor-core operands, already in the
 // layout the scan consumes) and dec to the workspace: 66,176 bytes per chunk
 // and head.
+// scan_t_kernel, one CTA per (sequence, head), carries the FP32 state across
+// the sequence's chunks in order:
+//   X = V - Ktil S;  U = T X;  O = Qtil S + P U;  S <- dec (.) S + Khat^T U
+// as three tensor-core round trips per chunk, in transposed form with the
+// chain's operands in TMEM; the chunk's operands arrive by bulk copy from the
+// workspace and the value tile by TMA.
+// prefill_fused_kernel runs both in one cooperative grid when there are few
+// (sequence, head) chains: one SM per chain (scan_t_role) while the other SMs
+// walk the prepare items in chunk order and release a ready flag per item,
+// so the prepare work no longer precedes the scan.
 //
 // Precision: prepare forms A and P from TF32 operands (their decay factors
 // span e^(+-8 |g|)); the scan's products take FP16 operands (10 stored
@@ -24,16 +34,6 @@
 // state S, X = V - Ktil S and U = T X are of the order of v and the initial
 // state, far inside FP16's range for normalised q, k; values below 2^-14
 // keep an absolute error under 2^-25.
-// scan_kernel, one CTA per (sequence, head, 32-column value slice), carries
-// the FP32 state across the sequence's chunks in order:
-//   X = V - Ktil S;  U = T X;  O = Qtil S + P U;  S <- dec (.) S + Khat^T U
-// as three tensor-core round trips per chunk; the chunk's operands arrive by
-// bulk copy from the workspace and the value slice by TMA.
-// prefill_fused_kernel runs both in one cooperative grid when there are few
-// (sequence, head) chains: one SM per chain carries the whole state in the
-// transposed form (scan_t_role, chain operands in TMEM) while the other SMs
-// walk the prepare items in chunk order and release a ready flag per item,
-// so the prepare work no longer precedes the scan.
 //
 // A and P come from tensor-core products over column blocks b with a
 // reference token m_b: e^(Gamma_r-Gamma_s) = e^(Gamma_r-Gamma_mb)
@@ -131,7 +131,12 @@ constexpr uint32_t PS_OPX = PS_GAM + 64 * KP * 4;            // A operand of the
 constexpr uint32_t PS_Y = PS_OPX + OpX::bytes(128);          // B operands Y_b
 constexpr uint32_t PS_BETA = PS_Y + OpKH::bytes(64);
 constexpr uint32_t PS_BAR = PS_BETA + 64 * 4;  // bar_tma[2], bar_mma, TMEM base
-constexpr uint32_t PS_TOTAL = PS_BAR + 64;
+// Packed batches of up to SEQ_CACHE sequences keep their chunk map (chunk_off
+// and cu_seqlens, n_seqs + 1 entries each) in shared memory: the item lookup
+// is a binary search, dependent global loads otherwise.
+constexpr int SEQ_CACHE = 128;
+constexpr uint32_t PS_SEQ = PS_BAR + 64;
+constexpr uint32_t PS_TOTAL = PS_SEQ + ((2 * (SEQ_CACHE + 1) * 4 + 15) & ~15u);
 static_assert(RB_TM + 64 * TPP * 4 <= RB_GMID, "solve arrays overlap the reference rows");
 static_assert(RB_GLAST + 128 * 4 == RAW_G + RAW_TILE, "reference rows must end the g tile");
 static_assert(2 * OpY32::bytes(128) <= 4 * OpY::bytes(128), "Y_b operands do not fit");
@@ -145,35 +150,6 @@ static_assert(PS_OPX % 1024 == 0 && PS_Y % 16 == 0, "operand alignment");
 constexpr float kWideGMin = 5.1f;
 static_assert(PS_TOTAL <= 232448, "shared memory budget exceeded");
 
-// ------------------------------------------------------------ scan layout
-// The scan comes in two value-slice widths: 32 columns (256 threads, the
-// latency-bound case of few (sequence, head) chains) and 64 columns (512
-// threads, half the CTAs for the same chains when they outnumber the SMs).
-// A thread always owns 16 state columns of one key row.
-template <int DVv>
-struct ScanCfg {
-    static constexpr int DV = DVv;
-    static constexpr int NT = DVv * 8;                    // 256 or 512 threads
-    static constexpr int SC = 16;                         // state columns per thread
-    using OpXV = Op<DVv, 16, 2>;  // B: X^T and U^T, rows = value column, K = 64 tokens
-    using OpS = Op<DVv, 16, 2>;   // B: S^T, rows = value column, K = 128 key channels
-    // shared memory: blob image (OPX | TP | KH | DEC), X^T, U^T, S^T, value tile
-    static constexpr uint32_t XV = BLOB_BYTES;
-    static constexpr uint32_t U = XV + OpXV::bytes(64);
-    static constexpr uint32_t OPS = U + OpXV::bytes(64);
-    // value tile [64 tokens][DV columns] BF16 with the 64-byte (DV = 32) or
-    // 128-byte (DV = 64) TMA swizzle: row r's 16-byte chunk c sits at chunk
-    // c ^ ((r >> 1) & 3), resp. c ^ (r & 7) (1024-byte aligned base)
-    static constexpr uint32_t RAWV = (OPS + OpS::bytes(128) + 1023) & ~1023u;
-    static constexpr uint32_t BAR = RAWV + 64 * DVv * 2;
-    static constexpr uint32_t TOTAL = BAR + 64;
-    // TMEM columns: P U, [Ktil; Qtil] S, T X, Khat^T U
-    static constexpr uint32_t T_PU = 0, T_Y = DVv, T_U = 2 * DVv, T_E = 3 * DVv;
-    static constexpr uint32_t TMEM_COLS = 4 * DVv;
-    static __device__ __forceinline__ int vswz(int r) { return DVv == 32 ? (r >> 1) & 3 : r & 7; }
-    static_assert(TOTAL <= 232448, "shared memory budget exceeded");
-    static_assert(NT / 128 * SC == DVv, "column groups must cover the slice");
-};
 constexpr uint32_t SS_OPX = BLOB_OPX, SS_TP = BLOB_TP, SS_KH = BLOB_KH, SS_DEC = BLOB_DEC;
 
 // TMEM columns of prepare: A and P
@@ -217,6 +193,9 @@ __device__ __forceinline__ void issue_mma16(uint32_t d, uint32_t a, uint32_t b, 
 }
 
 // Token range [start, end) of sequence n; false when cu_seqlens is malformed.
+// kGlobal: cu is device memory read through the read-only path; otherwise a
+// generic pointer (shared memory).
+template <bool kGlobal = true>
 __device__ __forceinline__ bool seq_range(const int* __restrict__ cu, int n, int n_seqs, int t,
                                           int t_pad, int& start, int& end) {
     if (!cu) {
@@ -224,8 +203,8 @@ __device__ __forceinline__ bool seq_range(const int* __restrict__ cu, int n, int
         end = start + t;
         return true;
     }
-    start = __ldg(cu + n);
-    end = __ldg(cu + n + 1);
+    start = kGlobal ? __ldg(cu + n) : cu[n];
+    end = kGlobal ? __ldg(cu + n + 1) : cu[n + 1];
     bool ok = start >= 0 && start <= end && end <= t;
     if (n == 0) ok = ok && start == 0;
     if (n == n_seqs - 1) ok = ok && end == t;
@@ -317,15 +296,17 @@ __device__ __forceinline__ PrepItem prep_item(long long item, int heads, const i
         it.L = it.valid ? min(C, (int)(n * t_pad) + t - it.c0) : 0;
         return it;
     }
+    // chunk_off and cu are generic pointers (the shared-memory copies, or
+    // device memory for large batches)
     int lo = 0, hi = n_seqs - 1;  // the sequence holding chunk g: largest n with chunk_off[n] <= g
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (__ldg(chunk_off + mid) <= it.g) lo = mid;
+        if (chunk_off[mid] <= it.g) lo = mid;
         else hi = mid - 1;
     }
     int start, end;
-    it.valid = seq_range(cu, lo, n_seqs, t, t_pad, start, end);
-    it.c0 = start + (int)(it.g - __ldg(chunk_off + lo)) * C;
+    it.valid = seq_range<false>(cu, lo, n_seqs, t, t_pad, start, end);
+    it.c0 = start + (int)(it.g - chunk_off[lo]) * C;
     it.valid = it.valid && it.c0 < end;
     it.L = it.valid ? min(C, end - it.c0) : 0;
     return it;
@@ -359,6 +340,15 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
 
     float* GAM = reinterpret_cast<float*>(sm + PS_GAM);
     float* BETA = reinterpret_cast<float*>(sm + PS_BETA);
+    const bool seq_cached = cu && n_seqs <= SEQ_CACHE;
+    int* s_off = reinterpret_cast<int*>(sm + PS_SEQ);
+    int* s_cu = s_off + SEQ_CACHE + 1;
+    if (seq_cached && tid <= n_seqs) {  // visible after the barrier below
+        s_off[tid] = __ldg(chunk_off + tid);
+        s_cu[tid] = __ldg(cu + tid);
+    }
+    const int* map_off = seq_cached ? s_off : chunk_off;
+    const int* map_cu = seq_cached ? s_cu : cu;
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + PS_BAR);  // one per raw buffer
     uint64_t* bar_mma = bar_tma + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PS_BAR + 24);
@@ -433,7 +423,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     };
 
     long long item = first;
-    PrepItem cur = prep_item(item, heads, cu, chunk_off, n_seqs, t, t_pad);
+    PrepItem cur = prep_item(item, heads, map_cu, map_off, n_seqs, t, t_pad);
     load_raw(cur, 0);
     uint16_t beta_cur = load_beta(cur);
 
@@ -447,7 +437,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         // runs, and its raw tiles go to the other buffer, which the previous
         // iteration's closing barrier released.
         auto fetch_next = [&]() {
-            if (nitem < items) nxt = prep_item(nitem, heads, cu, chunk_off, n_seqs, t, t_pad);
+            if (nitem < items) nxt = prep_item(nitem, heads, map_cu, map_off, n_seqs, t, t_pad);
             load_raw(nxt, b ^ 1);
             beta_nxt = load_beta(nxt);
         };
@@ -842,268 +832,6 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
     prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x, nullptr);
 }
 
-template <int DVv>
-__global__ void __launch_bounds__(ScanCfg<DVv>::NT, 1)
-scan_kernel(const __grid_constant__ CUtensorMap vmap, float* __restrict__ state,
-            float* __restrict__ o, int t, int t_pad, int heads, const int* __restrict__ cu,
-            int n_seqs, const unsigned char* __restrict__ ws) {
-    extern __shared__ __align__(1024) unsigned char sm[];
-    using Cfg = ScanCfg<DVv>;
-    using OpXV = typename Cfg::OpXV;
-    using OpS = typename Cfg::OpS;
-    constexpr int DV = Cfg::DV, SC = Cfg::SC;
-    constexpr uint32_t SS_XV = Cfg::XV, SS_U = Cfg::U, SS_OPS = Cfg::OPS, SS_RAWV = Cfg::RAWV,
-                       SS_BAR = Cfg::BAR;
-    constexpr uint32_t TC_PU = Cfg::T_PU, TC_Y = Cfg::T_Y, TC_U = Cfg::T_U, TC_E = Cfg::T_E;
-    const int slice = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
-    const int tid = threadIdx.x, warp = tid >> 5;
-    const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column group of SC
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-
-    pdl_wait();  // the prepared operands (and the callers' state) are complete
-    pdl_release();
-    int start, end;
-    if (!seq_range(cu, n, n_seqs, t, t_pad, start, end)) {
-        if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
-        return;
-    }
-    const long long g0 = __ldg(reinterpret_cast<const int*>(ws) + n);
-    if (tc::smem_u32(sm) & 1023u) {  // the swizzled value tile needs an aligned base
-        if (tid == 0) atomicOr(&g_tc_status, STATUS_SMEM_ALIGN);
-        return;
-    }
-
-    float* DEC = reinterpret_cast<float*>(sm + SS_DEC);
-    const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + SS_RAWV);
-    uint64_t* bar_a = reinterpret_cast<uint64_t*>(sm + SS_BAR);
-    uint64_t* bar_b = bar_a + 1;
-    uint64_t* bar_mma = bar_a + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + SS_BAR + 24);
-    int* abort_flag = reinterpret_cast<int*>(sm + SS_BAR + 28);
-    const uint32_t s_opx = tc::smem_u32(sm + SS_OPX), s_tp = tc::smem_u32(sm + SS_TP),
-                   s_opkh = tc::smem_u32(sm + SS_KH), s_xv = tc::smem_u32(sm + SS_XV),
-                   s_opy = tc::smem_u32(sm + SS_U), s_ops = tc::smem_u32(sm + SS_OPS);
-
-    if (tid == 0) {
-        tc::mbar_init(bar_a, 1);
-        tc::mbar_init(bar_b, 1);
-        tc::mbar_init(bar_mma, 1);
-        tc::fence_mbar_init();
-        tc::prefetch_tmap(&vmap);
-        *abort_flag = 0;
-    }
-    if (warp == 0) tc::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
-    tc::tc_fence_before();
-    __syncthreads();
-    tc::tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    uint32_t ph_mma = 0;
-
-    // state slice: thread (key ln, half ch) owns S[ln][16 ch .. 16 ch + 15]
-    float* Sg = state + ((size_t)n * heads + h) * D * D + (size_t)ln * D + slice * DV + ch * SC;
-    float sreg[SC];
-#pragma unroll
-    for (int q4 = 0; q4 < SC / 4; ++q4) {
-        const float4 v4 = *reinterpret_cast<const float4*>(Sg + 4 * q4);
-        sreg[4 * q4] = v4.x;
-        sreg[4 * q4 + 1] = v4.y;
-        sreg[4 * q4 + 2] = v4.z;
-        sreg[4 * q4 + 3] = v4.w;
-    }
-#pragma unroll
-    for (int jj = 0; jj < SC; ++jj)
-        st1h(sm + SS_OPS + OpS::off(ch * SC + jj, ln), sreg[jj]);
-
-    auto wait_mma = [&]() {
-        if (!tc::mbar_wait(bar_mma, ph_mma)) {
-            atomicOr(&g_tc_status, STATUS_TIMEOUT);
-            *abort_flag = 1;
-        }
-        ph_mma ^= 1;
-        tc::tc_fence_after();
-    };
-    auto sync_for_mma = [&]() {  // generic smem writes and TMEM reads before an MMA
-        tc::fence_async_smem();
-        tc::tc_fence_before();
-        __syncthreads();
-    };
-
-    // Operands arrive in two groups so the next chunk's copies overlap this
-    // chunk's products: group A ([Ktil; Qtil] and the value tile) is consumed
-    // by the first product, group B ([T; P], Khat^T, dec) by the last two.
-    auto load_a = [&](long long gg, int cc0) {
-        const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
-        tc::mbar_arrive_expect_tx(bar_a, OpXh::bytes(128) + 64 * DV * 2);
-        tc::bulk_load(sm + SS_OPX, blob + BLOB_OPX, OpXh::bytes(128), bar_a);
-        tc::tma_load_2d(sm + SS_RAWV, &vmap, bar_a, h * D + slice * DV, cc0);
-    };
-    auto load_b = [&](long long gg) {
-        const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
-        tc::mbar_arrive_expect_tx(bar_b, OpTPh::bytes(64) + OpKHh::bytes(64) + 128 * 4);
-        tc::bulk_load(sm + SS_TP, blob + BLOB_TP, OpTPh::bytes(64), bar_b);
-        tc::bulk_load(sm + SS_KH, blob + BLOB_KH, OpKHh::bytes(64), bar_b);
-        tc::bulk_load(sm + SS_DEC, blob + BLOB_DEC, 128 * 4, bar_b);
-    };
-    auto wait_load = [&](uint64_t* bar, uint32_t& ph) {
-        if (!tc::mbar_wait(bar, ph)) {
-            atomicOr(&g_tc_status, STATUS_TIMEOUT);
-            *abort_flag = 1;
-        }
-        ph ^= 1;
-    };
-    uint32_t ph_a = 0, ph_b = 0;
-    int pending = 0;  // groups in flight (thread 0's view), drained before exit
-    if (tid == 0 && start < end) {
-        load_a(g0, start);
-        load_b(g0);
-        pending = 2;
-    }
-
-    // O = Qtil S + P U of a chunk is written while the next chunk's first
-    // product runs: it is off the state's dependency chain.
-    float qs[SC];
-    int o_c0 = -1, o_L = 0;  // the chunk whose O is still to be written
-    auto write_o = [&]() {
-        if (ln >= 64) {
-            float v[SC];
-            tc::tmem_ld(tmem + lane_base + TC_PU + SC * ch, v);
-            tc::tmem_ld_wait();
-            const int r = ln - 64;
-            if (r < o_L) {
-                float* orow = o + ((size_t)(o_c0 + r) * heads + h) * D + slice * DV + SC * ch;
-#pragma unroll
-                for (int q4 = 0; q4 < SC / 4; ++q4)
-                    *reinterpret_cast<float4*>(orow + 4 * q4) =
-                        make_float4(qs[4 * q4] + v[4 * q4], qs[4 * q4 + 1] + v[4 * q4 + 1],
-                                    qs[4 * q4 + 2] + v[4 * q4 + 2], qs[4 * q4 + 3] + v[4 * q4 + 3]);
-            }
-        }
-    };
-
-    long long g = g0;
-    for (int c0 = start; c0 < end; c0 += C, ++g) {
-        const int L = min(C, end - c0);
-        const bool more = c0 + C < end;
-        tc::fence_async_smem();  // the previous chunk's state operand is written
-        tc::tc_fence_before();
-        if (__syncthreads_or(*abort_flag)) break;  // every thread takes the same exit
-        wait_load(bar_a, ph_a);
-        if (tid == 0) --pending;
-
-        // ---------------------------------------------------------- X = V - Ktil S
-        if (tid == 0) {
-            tc::tc_fence_after();
-            issue_mma16<OpXh, OpS>(tmem + TC_Y, s_opx, s_ops, 8, tc::idesc_f16(128, DV));
-            tc::mma_commit(bar_mma);
-        }
-        if (o_c0 >= 0) write_o();  // the previous chunk's output
-        wait_mma();
-        {
-            float v[SC];
-            tc::tmem_ld(tmem + lane_base + TC_Y + SC * ch, v);
-            tc::tmem_ld_wait();
-            if (ln < 64) {
-                const int r = ln, sw = Cfg::vswz(r);
-                const unsigned char* vrow = reinterpret_cast<const unsigned char*>(RAWV) + r * (DV * 2);
-                uint32_t w[SC / 2];  // SC BF16 values: SC / 8 chunks of 16 bytes
-#pragma unroll
-                for (int q = 0; q < SC / 8; ++q) {
-                    const uint4 vq = *reinterpret_cast<const uint4*>(
-                        vrow + ((((SC / 8) * ch + q) ^ sw) << 4));
-                    w[4 * q] = vq.x;
-                    w[4 * q + 1] = vq.y;
-                    w[4 * q + 2] = vq.z;
-                    w[4 * q + 3] = vq.w;
-                }
-#pragma unroll
-                for (int jj = 0; jj < SC; ++jj) {
-                    const uint32_t bits = (jj & 1) ? (w[jj >> 1] & 0xffff0000u) : (w[jj >> 1] << 16);
-                    const float x = (r < L) ? __uint_as_float(bits) - v[jj] : 0.f;
-                    st1h(sm + SS_XV + OpXV::off(SC * ch + jj, r), x);
-                }
-            } else {
-#pragma unroll
-                for (int jj = 0; jj < SC; ++jj) qs[jj] = v[jj];
-            }
-        }
-        sync_for_mma();
-        if (tid == 0 && more) {  // [Ktil; Qtil] and the value tile are consumed
-            load_a(g + 1, c0 + C);
-            ++pending;
-        }
-        wait_load(bar_b, ph_b);
-        if (tid == 0) --pending;
-        const float dk = DEC[ln];
-
-        // ---------------------------------------------------------- U = T X
-        if (tid == 0) {
-            tc::tc_fence_after();
-            issue_mma16<OpTPh, OpXV>(tmem + TC_U, s_tp, s_xv, 4, tc::idesc_f16(128, DV));
-            tc::mma_commit(bar_mma);
-        }
-        wait_mma();
-        if (ln < 64) {
-            float v[SC];
-            tc::tmem_ld(tmem + lane_base + TC_U + SC * ch, v);
-            tc::tmem_ld_wait();
-            const int r = ln;
-#pragma unroll
-            for (int jj = 0; jj < SC; ++jj) {
-                const float u = (r < L) ? v[jj] : 0.f;
-                st1h(sm + SS_U + OpXV::off(SC * ch + jj, r), u);
-            }
-        }
-        sync_for_mma();
-
-        // ---------------------------------------------------------- Khat^T U and P U
-        if (tid == 0) {
-            tc::tc_fence_after();
-            issue_mma16<OpKHh, OpXV>(tmem + TC_E, s_opkh, s_opy, 4, tc::idesc_f16(128, DV));
-            issue_mma16<OpTPh, OpXV>(tmem + TC_PU, s_tp, s_opy, 4, tc::idesc_f16(128, DV));
-            tc::mma_commit(bar_mma);
-        }
-        wait_mma();
-        if (tid == 0 && more) {  // [T; P], Khat^T and dec are consumed
-            load_b(g + 1);
-            ++pending;
-        }
-        {   // S <- dec (.) S + Khat^T U
-            float v[SC];
-            tc::tmem_ld(tmem + lane_base + TC_E + SC * ch, v);
-            tc::tmem_ld_wait();
-#pragma unroll
-            for (int jj = 0; jj < SC; ++jj) {
-                sreg[jj] = __fmaf_rn(dk, sreg[jj], v[jj]);
-                st1h(sm + SS_OPS + OpS::off(SC * ch + jj, ln), sreg[jj]);
-            }
-        }
-        o_c0 = c0;
-        o_L = L;
-    }
-    // every thread leaves the loop through the same iteration; agree on the flag
-    const bool aborted = __syncthreads_or(*abort_flag);
-    if (o_c0 >= 0 && !aborted) write_o();  // the last chunk's output
-    // An early exit can leave copies in flight: let them land before the
-    // shared memory is released (bounded waits).
-    if (tid == 0 && pending > 0) {
-        tc::mbar_wait(bar_a, ph_a, 1u << 20);
-        tc::mbar_wait(bar_b, ph_b, 1u << 20);
-    }
-
-    if (!aborted) {
-#pragma unroll
-        for (int q4 = 0; q4 < SC / 4; ++q4)
-            *reinterpret_cast<float4*>(Sg + 4 * q4) =
-                make_float4(sreg[4 * q4], sreg[4 * q4 + 1], sreg[4 * q4 + 2], sreg[4 * q4 + 3]);
-    }
-    tc::tc_fence_before();
-    __syncthreads();
-    if (warp == 0) {
-        tc::tc_fence_after();
-        tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
-    }
-}
-
 // ------------------------------------------------------------ transposed scan
 // One CTA per (sequence, head) carries the whole 128 x 128 state through the
 // chunks in transposed form, so that each matrix on the state's chain is the
@@ -1478,6 +1206,18 @@ prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constan
                      (long long)gridDim.x - chains, ready);
 }
 
+// The chains of the two-kernel path: one CTA per (sequence, head), after
+// prepare_kernel has written every chunk's operands.
+__global__ void __launch_bounds__(NTP, 1)
+scan_t_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
+              float* __restrict__ state, float* __restrict__ o, int t, int t_pad, int heads,
+              const int* __restrict__ cu, int n_seqs, const unsigned char* __restrict__ ws) {
+    pdl_wait();  // the prepared operands (and the callers' state) are complete
+    pdl_release();
+    scan_t_role(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
+                (int)blockIdx.x / heads, nullptr);
+}
+
 // BF16 [rows][cols] with a row pitch of `pitch_elems`; boxes of `box_cols`
 // channels x 64 tokens with the given shared-memory swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
@@ -1503,8 +1243,8 @@ size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads) {
 
 // Per-SM cost figures measured on GB300 (T = 8192, 32 heads) that choose
 // between the fused grid and the two kernels: a prepare item, and a chunk of
-// the transposed and of the 32-column scan chain.
-constexpr double kPrepItemUs = 9.3, kScanTChunkUs = 2.9, kScan32ChunkUs = 2.0;
+// the transposed scan's chain.
+constexpr double kPrepItemUs = 9.1, kScanTChunkUs = 2.4;
 
 // Launches the tensor-core prefill (BF16 inputs, chunk 64); arguments,
 // including the workspace size, are validated by kda_prefill.
@@ -1518,37 +1258,29 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         set_error("kda_prefill: cannot query the multiprocessor count");
         return KDA_ERR_CUDA;
     }
-    // The scan's (sequence, head) chains each need a CTA of their own for
-    // their whole length; 32-column slices give four CTAs per chain, 64-column
-    // slices two.  Narrow slices while the CTAs fit on the SMs in one wave
-    // (the chains' latency decides), wide ones once they would not (each
-    // tensor-core product then does twice the work for about the same time).
+    // Every (sequence, head) chain runs on one SM for its whole length.  The
+    // fused grid (one SM per chain, the other SMs preparing just ahead of the
+    // chains) when, per chunk of a chain, max(chains x item / (sms - chains),
+    // chain) beats the two kernels' chains x item / sms + chain (prepare on
+    // every SM, then the chains in one wave).
     const long long chains = (long long)n_seqs * heads;
-    const int dv = (chains * (D / 32) > sms) ? 64 : 32;
-    // The fused grid (one SM per chain running the transposed scan, the other
-    // SMs preparing ahead of it) when its chain, not the prepare walk, is the
-    // longer part and still shorter than prepare followed by the 32-column
-    // scan: per chunk of a chain, max(chains x item / (sms - chains), scan_t)
-    // against chains x item / sms + scan_32.
     const char* impl = getenv("KDA_PREFILL_IMPL");
     const bool fused_allowed = !(impl && strcmp(impl, "unfused") == 0);
     bool fused = false;
-    if (fused_allowed && dv == 32 && chains * 4 <= sms) {
+    if (fused_allowed && chains < sms) {
         const double per_chunk_fused =
             std::max((double)chains * kPrepItemUs / (double)(sms - chains), kScanTChunkUs);
-        const double per_chunk_two = (double)chains * kPrepItemUs / sms + kScan32ChunkUs;
+        const double per_chunk_two = (double)chains * kPrepItemUs / sms + kScanTChunkUs;
         fused = per_chunk_fused < per_chunk_two;
     }
     PrepMaps maps;
-    CUtensorMap vmap, vmap_t, omap;
+    CUtensorMap vmap, omap;
     const uint64_t hd = (uint64_t)heads * D;
     if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.g, g, hd, rows, hd, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&vmap, v, hd, rows, (uint64_t)stride, dv,
-                  dv == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B) ||
-        (fused && !make_map(&vmap_t, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE)) ||
-        (fused && !tma_map_f32(&omap, o, hd, rows, hd, D, (uint32_t)C))) {
+        !make_map(&vmap, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !tma_map_f32(&omap, o, hd, rows, hd, D, (uint32_t)C)) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
@@ -1556,11 +1288,8 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PS_TOTAL);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(scan_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)ScanCfg<32>::TOTAL);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(scan_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)ScanCfg<64>::TOTAL);
+        e = cudaFuncSetAttribute(scan_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)ScanT::TOTAL);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)PS_TOTAL);
@@ -1587,7 +1316,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, prefill_fused_kernel, maps, vmap_t, omap, (const uint16_t*)beta,
+        e = cudaLaunchKernelEx(&cfg, prefill_fused_kernel, maps, vmap, omap, (const uint16_t*)beta,
                                state, o, t, t_pad, heads, cu, n_seqs, ws, ready);
         if (e == cudaSuccess) return launch_result("kda_prefill (fused)");
         // the grid could not be made resident (e.g. SMs held by other work):
@@ -1602,14 +1331,8 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
                t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;
-    if (dv == 32)
-        launch_pdl(scan_kernel<32>, dim3(D / 32, heads, n_seqs), dim3(ScanCfg<32>::NT),
-                   ScanCfg<32>::TOTAL, s, vmap, state, o, t, t_pad, heads, cu, n_seqs,
-                   (const unsigned char*)ws);
-    else
-        launch_pdl(scan_kernel<64>, dim3(D / 64, heads, n_seqs), dim3(ScanCfg<64>::NT),
-                   ScanCfg<64>::TOTAL, s, vmap, state, o, t, t_pad, heads, cu, n_seqs,
-                   (const unsigned char*)ws);
+    launch_pdl(scan_t_kernel, dim3((unsigned)chains), dim3(NTP), ScanT::TOTAL, s, vmap, omap,
+               state, o, t, t_pad, heads, cu, n_seqs, (const unsigned char*)ws);
     return launch_result("kda_prefill (scan)");
 }
 
