@@ -107,6 +107,60 @@ def test_packed_varlen_matches_per_sequence_oracle(orc):
         assert rel_err(S[n], S_ref) < TOL_PREFILL
 
 
+@pytest.mark.parametrize("n_seqs", [128, 129])
+def test_many_packed_sequences_match_per_sequence_oracle(orc, n_seqs):
+    """Packed batches on both sides of prepare's shared-memory chunk map (it
+    holds up to 128 sequences; larger batches search the map in device
+    memory), with empty, one-token and whole-chunk sequences: hundreds of
+    (sequence, head) chains on the two-kernel path."""
+    K = kda()
+    H = 2
+    gen = torch.Generator().manual_seed(40 + n_seqs)
+    lengths = torch.randint(0, 150, (n_seqs,), generator=gen).tolist()
+    lengths[3], lengths[17], lengths[64], lengths[-1] = 0, 1, 64, 128
+    tot = sum(lengths)
+    d = wl.core_inputs(gen, (tot,), H, torch.bfloat16)
+    S0 = wl.state(gen, (n_seqs,), H, 0.02)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]), dtype=torch.int32)
+    dev = {n: d[n].cuda() for n in d}
+    S = S0.clone().cuda()
+    o = torch.zeros((tot, H, 128), device="cuda")
+    K.kda_prefill(S, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], o, tot, 64,
+                  cu_seqlens=cu.cuda())
+    K.kda_sync_status()
+    S, o = S.cpu(), o.cpu()
+    for n, L in enumerate(lengths):
+        a, b = int(cu[n]), int(cu[n + 1])
+        if L == 0:
+            assert torch.equal(S[n], S0[n])
+            continue
+        o_ref, S_ref = orc.prefill(d["q"][a:b], d["k"][a:b], d["v"][a:b], d["g"][a:b],
+                                   d["beta"][a:b], S0[n])
+        assert rel_err(o[a:b], o_ref) < TOL_PREFILL, n
+        assert rel_err(S[n], S_ref) < TOL_PREFILL, n
+
+
+def test_uniform_batch_of_many_chains_matches_oracle(orc):
+    """Three sequences of 32 heads (96 chains): more chains than the fused grid
+    takes, fewer than the SMs, so prepare runs on every SM and then every chain
+    in one wave."""
+    K = kda()
+    N, t, H = 3, 200, 32
+    gen = torch.Generator().manual_seed(21)
+    d = wl.core_inputs(gen, (N, t), H, torch.bfloat16)
+    S0 = wl.state(gen, (N,), H, 0.02)
+    dev = {n: d[n].cuda() for n in d}
+    S = S0.clone().cuda()
+    o = torch.zeros((N, t, H, 128), device="cuda")
+    K.kda_prefill(S, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], o, t, 64)
+    K.kda_sync_status()
+    for n in range(N):
+        o_ref, S_ref = orc.prefill(d["q"][n], d["k"][n], d["v"][n], d["g"][n], d["beta"][n],
+                                   S0[n])
+        assert rel_err(o[n], o_ref) < TOL_PREFILL
+        assert rel_err(S[n], S_ref) < TOL_PREFILL
+
+
 def test_malformed_cu_seqlens_is_reported_by_sync_status():
     K = kda()
     H = 1
