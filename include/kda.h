@@ -155,7 +155,7 @@ kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* b
  * sequences with the given chunk width and input dtype.  Returns 0 when the
  * call needs none (FP32 inputs or chunk != 64 run without one) or when an
  * argument is invalid.  The BF16, chunk-64 tensor-core path stores the
- * state-independent operands of every (chunk, head) there: 131,840 bytes
+ * state-independent operands of every (chunk, head) there: 66,176 bytes
  * per chunk of 64 tokens and head (with one chunk of slack per sequence),
  * plus (n_seqs + 1) * 4 bytes rounded up to 256, plus a 4-byte ready flag
  * per chunk and head rounded up to 256 bytes. */
@@ -255,8 +255,9 @@ kda_status kda_conv_silu_l2_k(float* conv_state, const uint16_t* x, const uint16
  *
  *   Arguments, layouts and results are those of kda_prefill.
  *   Refused with KDA_ERR_WORKSPACE when kda_prefill_workspace_size(...) for
- *   the call exceeds KDA_STATIC_WORKSPACE_BYTES: at 32 heads that is about 15
- *   chunks of 64 tokens in total; fewer heads allow proportionally more.
+ *   the call exceeds KDA_STATIC_WORKSPACE_BYTES: at 32 heads that is 30
+ *   chunks of 64 tokens in total (one sequence of up to 1,920 tokens); fewer
+ *   heads allow proportionally more.
  *   The first call on a device resolves the array's device address for that
  *   device (cudaGetSymbolAddress, with the device current); make that first
  *   call before any stream capture.

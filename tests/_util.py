@@ -6,7 +6,7 @@ import torch
 
 # Tolerances on the normwise relative error max|x - ref| / max|ref|.
 TOL_DECODE = 1e-5    # FP32 decode and decode_k against the FP64 oracle
-TOL_PREFILL = 2e-3   # TF32/BF16 tensor-core (or FP32) chunked prefill
+TOL_PREFILL = 2e-3   # tensor-core chunked prefill (TF32 and FP16 operands) or FP32 SIMT
 
 
 def rel_err(x, ref) -> float:
