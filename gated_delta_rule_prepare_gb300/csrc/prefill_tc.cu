@@ -155,6 +155,14 @@ constexpr uint32_t SS_OPX = BLOB_OPX, SS_TP = BLOB_TP, SS_KH = BLOB_KH, SS_DEC =
 // TMEM columns of prepare: A and P
 constexpr uint32_t TC_AP = 0;
 
+// 1/x by the hardware approximation (subnormal results flush to zero); its
+// callers use it only for TF32 operands, rounded to 11 bits afterwards.
+__device__ __forceinline__ float rcp_fast(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 __device__ __forceinline__ float bf(uint16_t b) {
     return __uint_as_float(static_cast<uint32_t>(b) << 16);
 }
@@ -527,16 +535,20 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                     }
                 }
             };
-            // Both 32-token blocks in one pass: X_0 for every row into OPX, X_1 for
-            // rows 32..63 into a compact 64-row operand (k rows, then q rows) in
-            // the idle raw buffer; the second product's 64 padding rows read the
-            // next K group (or the 1 KB after the operand) and are never used.
+            // Both 32-token blocks' operands in one pass: X_0 for every row into
+            // OPX, X_1 for rows 32..63 into a compact 64-row operand (k rows, then q
+            // rows) in the idle raw buffer (the second product's 64 padding rows
+            // read the next K group, or the 1 KB after the operand, and are never
+            // used), and Y_b for the rows of block b, whose factor
+            // e^(Gamma_mb - Gamma_s) is the reciprocal of the row's own X_b factor
+            // (both within e^(+-17 kWideGMin), normal FP32 numbers).
             unsigned char* x1buf = sm + (b ^ 1) * RAW_BUF;
-            auto build_x_wide = [&]() {
+            auto build_xy_wide = [&]() {
                 const int r = tid & 63, qg = tid >> 6;
                 const bool live = r < L;
                 const float* gm0 = GMID + 4 * 128;
                 const float* gm1 = GMID + 5 * 128;
+                unsigned char* ydst = sm + PS_Y + (r >> 5) * OpY32::bytes(128);
 #pragma unroll
                 for (int jj = 0; jj < 32 / (NTP / 64); ++jj) {
                     const int j = qg + (NTP / 64) * jj;
@@ -553,6 +565,9 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                             kf.w * f3);
                         st4(sm + PS_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1, qf.z * f2,
                             qf.w * f3);
+                        if (r < 32)
+                            st4(ydst, OpY32::off(r, 4 * j), kf.x * rcp_fast(f0),
+                                kf.y * rcp_fast(f1), kf.z * rcp_fast(f2), kf.w * rcp_fast(f3));
                     }
                     if (r >= 32) {
                         const float4 gm = *reinterpret_cast<const float4*>(gm1 + 4 * j);
@@ -562,6 +577,8 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                             kf.w * f3);
                         st4(x1buf, OpX1::off(r, 4 * j), qf.x * f0, qf.y * f1, qf.z * f2,
                             qf.w * f3);
+                        st4(ydst, OpY32::off(r - 32, 4 * j), kf.x * rcp_fast(f0),
+                            kf.y * rcp_fast(f1), kf.z * rcp_fast(f2), kf.w * rcp_fast(f3));
                     }
                 }
             };
@@ -581,8 +598,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             };
             if (wide) {
                 // Two 32-token column blocks (every g of the chunk is >= -kWideGMin).
-                build_y(5, 4, OpY32::bytes(128), OpY32{});
-                build_x_wide();
+                build_xy_wide();
                 sync_for_mma();
                 if (tid == 0) {
                     tc::tc_fence_after();
