@@ -124,6 +124,8 @@ constexpr uint32_t RAW_Q = 0, RAW_K = RAW_TILE, RAW_G = 2 * RAW_TILE;
 // Gamma_{L-1} at the end of the g tile; once the operands are out: the solve
 constexpr uint32_t RB_GMID = RAW_G + RAW_TILE - 7 * 128 * 4;  // 6 x 128: 4 + 2 reference rows
 constexpr uint32_t RB_GLAST = RB_GMID + 6 * 128 * 4;
+// wide path: e^Gamma_17, e^(Gamma_63 - Gamma_17), e^(Gamma_63 - Gamma_49) per channel
+constexpr uint32_t RB_PC = RB_GMID - 3 * 128 * 4;
 constexpr uint32_t RB_AM = 0;                                 // FP32 A, then W blocks [64][AP]
 constexpr uint32_t RB_TM = (RB_AM + 64 * AP * 4 + 15) & ~15u;  // FP32 T [64][TPP]
 constexpr uint32_t PS_GAM = 2 * RAW_BUF;                     // FP32 Gamma [64][KP]
@@ -137,7 +139,7 @@ constexpr uint32_t PS_BAR = PS_BETA + 64 * 4;  // bar_tma[2], bar_mma, TMEM base
 constexpr int SEQ_CACHE = 128;
 constexpr uint32_t PS_SEQ = PS_BAR + 64;
 constexpr uint32_t PS_TOTAL = PS_SEQ + ((2 * (SEQ_CACHE + 1) * 4 + 15) & ~15u);
-static_assert(RB_TM + 64 * TPP * 4 <= RB_GMID, "solve arrays overlap the reference rows");
+static_assert(RB_TM + 64 * TPP * 4 <= RB_PC, "solve arrays overlap the reference rows");
 static_assert(RB_GLAST + 128 * 4 == RAW_G + RAW_TILE, "reference rows must end the g tile");
 static_assert(2 * OpY32::bytes(128) <= 4 * OpY::bytes(128), "Y_b operands do not fit");
 static_assert(4 * OpY::bytes(128) <= OpKH::bytes(64), "Y_b operands do not fit");
@@ -327,7 +329,8 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                                              int t, int t_pad, int heads,
                                              const int* __restrict__ cu, int n_seqs,
                                              unsigned char* __restrict__ ws, long long first,
-                                             long long stride, unsigned* __restrict__ ready) {
+                                             long long stride, unsigned* __restrict__ ready,
+                                             long long ready_pitch) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column quarter
@@ -425,7 +428,8 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     auto release_pending = [&]() {
         if (ready && copier && pending >= 0) {
             tc::bulk_wait_all();
-            tc::flag_release(ready + pending, 1u);
+            const long long pg = pending / heads;  // flags are head-major: [heads][pitch]
+            tc::flag_release(ready + (pending - pg * heads) * ready_pitch + pg, 1u);
             pending = -1;
         }
     };
@@ -460,6 +464,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             const unsigned char* RAWG = sm + b * RAW_BUF + RAW_G;
             float* GMID = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_GMID);
             float* GLAST = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_GLAST);
+            float* PC = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_PC);
             float* AM = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_AM);
             float* TM = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_TM);
             unsigned char* blob = ws + blob_offset(n_seqs, cur.g, h, heads);
@@ -511,6 +516,15 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             }
             if (copier) tc::bulk_wait_read_all();  // the last item's operands left OPX and Y
             __syncthreads();
+            if (wide) {  // per-channel constants of the operand build below
+                if (tid < 128) {
+                    const float g17 = GMID[4 * 128 + tid], g49 = GMID[5 * 128 + tid];
+                    PC[tid] = __expf(g17);
+                    PC[128 + tid] = __expf(GLAST[tid] - g17);
+                    PC[256 + tid] = __expf(GLAST[tid] - g49);
+                }
+                __syncthreads();
+            }
 
             // ------------------------------------------------------ P2 A and P blocks
             // X_b rows r >= r0: k_r and qh_r times e^(Gamma_r - Gamma_mb).
@@ -543,14 +557,24 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             // e^(Gamma_mb - Gamma_s) is the reciprocal of the row's own X_b factor
             // (both within e^(+-17 kWideGMin), normal FP32 numbers).
             unsigned char* x1buf = sm + (b ^ 1) * RAW_BUF;
+            // The scan's operands of the wide path are formed in the same pass,
+            // from the same factors, and held in registers (FP16 pairs) until
+            // the A/P products have released their buffers:
+            //   Ktil_r = k_r e^(Gamma_r - Gamma_17) e^Gamma_17,
+            //   Khat_r = beta_r k_r e^(Gamma_mb - Gamma_r) e^(Gamma_63 - Gamma_mb).
+            // A product below 2^-24 (flushed, or FP16 zero) has no FP16 value.
+            constexpr int P3J = 32 / (NTP / 64);
+            uint32_t p3k[P3J][2], p3q[P3J][2], p3h[P3J][2];
             auto build_xy_wide = [&]() {
                 const int r = tid & 63, qg = tid >> 6;
                 const bool live = r < L;
+                const float br = BETA[r];  // 0 past the chunk's end
                 const float* gm0 = GMID + 4 * 128;
                 const float* gm1 = GMID + 5 * 128;
+                const float* pcl = PC + (r < 32 ? 128 : 256);  // e^(Gamma_63 - Gamma_mb)
                 unsigned char* ydst = sm + PS_Y + (r >> 5) * OpY32::bytes(128);
 #pragma unroll
-                for (int jj = 0; jj < 32 / (NTP / 64); ++jj) {
+                for (int jj = 0; jj < P3J; ++jj) {
                     const int j = qg + (NTP / 64) * jj;
                     const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
                     float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
@@ -565,9 +589,21 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                             kf.w * f3);
                         st4(sm + PS_OPX, OpX::off(64 + r, 4 * j), qf.x * f0, qf.y * f1, qf.z * f2,
                             qf.w * f3);
-                        if (r < 32)
-                            st4(ydst, OpY32::off(r, 4 * j), kf.x * rcp_fast(f0),
-                                kf.y * rcp_fast(f1), kf.z * rcp_fast(f2), kf.w * rcp_fast(f3));
+                        const float4 c0 = *reinterpret_cast<const float4*>(PC + 4 * j);
+                        const float e0 = f0 * c0.x, e1 = f1 * c0.y, e2 = f2 * c0.z, e3 = f3 * c0.w;
+                        p3k[jj][0] = tc::pack_f16x2(kf.x * e0, kf.y * e1);
+                        p3k[jj][1] = tc::pack_f16x2(kf.z * e2, kf.w * e3);
+                        p3q[jj][0] = tc::pack_f16x2(qf.x * e0, qf.y * e1);
+                        p3q[jj][1] = tc::pack_f16x2(qf.z * e2, qf.w * e3);
+                        if (r < 32) {
+                            const float y0 = rcp_fast(f0), y1 = rcp_fast(f1), y2 = rcp_fast(f2),
+                                        y3 = rcp_fast(f3);
+                            st4(ydst, OpY32::off(r, 4 * j), kf.x * y0, kf.y * y1, kf.z * y2,
+                                kf.w * y3);
+                            const float4 cl = *reinterpret_cast<const float4*>(pcl + 4 * j);
+                            p3h[jj][0] = tc::pack_f16x2(br * kf.x * y0 * cl.x, br * kf.y * y1 * cl.y);
+                            p3h[jj][1] = tc::pack_f16x2(br * kf.z * y2 * cl.z, br * kf.w * y3 * cl.w);
+                        }
                     }
                     if (r >= 32) {
                         const float4 gm = *reinterpret_cast<const float4*>(gm1 + 4 * j);
@@ -577,9 +613,32 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                             kf.w * f3);
                         st4(x1buf, OpX1::off(r, 4 * j), qf.x * f0, qf.y * f1, qf.z * f2,
                             qf.w * f3);
-                        st4(ydst, OpY32::off(r - 32, 4 * j), kf.x * rcp_fast(f0),
-                            kf.y * rcp_fast(f1), kf.z * rcp_fast(f2), kf.w * rcp_fast(f3));
+                        const float y0 = rcp_fast(f0), y1 = rcp_fast(f1), y2 = rcp_fast(f2),
+                                    y3 = rcp_fast(f3);
+                        st4(ydst, OpY32::off(r - 32, 4 * j), kf.x * y0, kf.y * y1, kf.z * y2,
+                            kf.w * y3);
+                        const float4 cl = *reinterpret_cast<const float4*>(pcl + 4 * j);
+                        p3h[jj][0] = tc::pack_f16x2(br * kf.x * y0 * cl.x, br * kf.y * y1 * cl.y);
+                        p3h[jj][1] = tc::pack_f16x2(br * kf.z * y2 * cl.z, br * kf.w * y3 * cl.w);
                     }
+                }
+            };
+            auto p3_store = [&]() {  // the registers above into the freed operand buffers
+                const int r = tid & 63, qg = tid >> 6;
+                unsigned char* kh = sm + PS_Y;
+#pragma unroll
+                for (int jj = 0; jj < P3J; ++jj) {
+                    const int j = qg + (NTP / 64) * jj;
+                    *reinterpret_cast<uint2*>(sm + PS_OPX + OpXh::off(r, 4 * j)) =
+                        make_uint2(p3k[jj][0], p3k[jj][1]);
+                    *reinterpret_cast<uint2*>(sm + PS_OPX + OpXh::off(64 + r, 4 * j)) =
+                        make_uint2(p3q[jj][0], p3q[jj][1]);
+                    *reinterpret_cast<uint16_t*>(kh + OpKHh::off(4 * j, r)) = (uint16_t)p3h[jj][0];
+                    *reinterpret_cast<uint16_t*>(kh + OpKHh::off(4 * j + 1, r)) =
+                        (uint16_t)(p3h[jj][0] >> 16);
+                    *reinterpret_cast<uint16_t*>(kh + OpKHh::off(4 * j + 2, r)) = (uint16_t)p3h[jj][1];
+                    *reinterpret_cast<uint16_t*>(kh + OpKHh::off(4 * j + 3, r)) =
+                        (uint16_t)(p3h[jj][1] >> 16);
                 }
             };
             // Y_b row s of block b = s >> bshift: k_s e^(Gamma_mb - Gamma_s).
@@ -610,6 +669,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 release_pending();
                 wait_mma();
                 fetch_next();  // the compact X_1 in the other buffer has been read
+                p3_store();
             } else {
                 // Four 16-token column blocks with reference token 16 b + 8.
                 build_y(4, 0, OpY::bytes(128), OpY{});
@@ -632,11 +692,12 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             }
 
             // ------------------------------------------------------ P3 [Ktil; Qtil], Khat^T
-            // Built in the A/P operand buffers (both products are complete) and
-            // sent to the workspace by bulk copies that drain during P4 and P5.
-            // Thread (r, qg) forms token r's channels 4 j .. 4 j + 3: Ktil and
-            // Qtil as 16-byte rows, Khat^T as four 4-byte column entries.
-            {
+            // Built in the A/P operand buffers (both products are complete; the
+            // wide path has formed them during its operand build) and sent to
+            // the workspace by bulk copies that drain during P4 and P5.  Thread
+            // (r, qg) forms token r's channels 4 j .. 4 j + 3: Ktil and Qtil as
+            // 8-byte rows, Khat^T as four 2-byte column entries.
+            if (!wide) {
                 const int r = tid & 63, qg = tid >> 6;
                 const bool live = r < L;
                 const float br = BETA[r];  // 0 past the chunk's end
@@ -845,7 +906,7 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict
                unsigned char* __restrict__ ws) {
     pdl_wait();  // the chunk map (and the callers' inputs) are complete
     pdl_release();
-    prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x, nullptr);
+    prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x, nullptr, 0);
 }
 
 // ------------------------------------------------------------ transposed scan
@@ -904,7 +965,8 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
                                             float* __restrict__ o, int t, int t_pad, int heads,
                                             const int* __restrict__ cu, int n_seqs,
                                             const unsigned char* __restrict__ ws, int h, int n,
-                                            const unsigned* __restrict__ ready) {
+                                            const unsigned* __restrict__ ready,
+                                            long long ready_pitch) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
     const int qd = warp & 3, cg = warp >> 2;  // TMEM lane quarter, column group
@@ -975,8 +1037,30 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
     // exit can let them land before the shared memory is released.
     uint32_t out_x = 0, out_b = 0;  // bit per group
     bool out_v = false;
+    // Ready flags (fused grid): head h's flags are consecutive words, read four
+    // at a time with one acquire load, so one global round trip usually covers
+    // several chunks; acq_hi is the last chunk known to be ready.
+    long long acq_hi = -1;
+    auto acquire = [&](long long gg) {
+        if (!ready || gg <= acq_hi) return true;
+        const unsigned* fh = ready + (size_t)h * ready_pitch;
+        const long long g4 = gg & ~3LL;
+        for (uint32_t it = 0; it < (1u << 22); ++it) {
+            const uint4 f = tc::flags4_acquire(fh + g4);
+            const unsigned fl[4] = {f.x, f.y, f.z, f.w};
+            int k = (int)(gg - g4);
+            if (fl[k]) {
+                while (k + 1 < 4 && fl[k + 1]) ++k;
+                tc::flags_proxy_fence();
+                acq_hi = g4 + k;
+                return true;
+            }
+            __nanosleep(64);
+        }
+        return false;
+    };
     auto load_ops = [&](long long gg, int b) {  // chunk gg's operands into group b, after its flag
-        if (ready && !tc::flag_acquire(ready + gg * heads + h)) {
+        if (!acquire(gg)) {
             atomicOr(&g_tc_status, STATUS_TIMEOUT);
             *abort_flag = 1;
         }
@@ -1212,14 +1296,14 @@ prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constan
                      const __grid_constant__ CUtensorMap omap, const uint16_t* __restrict__ beta, float* __restrict__ state,
                      float* __restrict__ o, int t, int t_pad, int heads,
                      const int* __restrict__ cu, int n_seqs, unsigned char* __restrict__ ws,
-                     unsigned* __restrict__ ready) {
+                     unsigned* __restrict__ ready, long long ready_pitch) {
     const int chains = n_seqs * heads;
     if ((int)blockIdx.x < chains)
         scan_t_role(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
-                    (int)blockIdx.x / heads, ready);
+                    (int)blockIdx.x / heads, ready, ready_pitch);
     else
         prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, (long long)blockIdx.x - chains,
-                     (long long)gridDim.x - chains, ready);
+                     (long long)gridDim.x - chains, ready, ready_pitch);
 }
 
 // The chains of the two-kernel path: one CTA per (sequence, head), after
@@ -1231,7 +1315,7 @@ scan_t_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ 
     pdl_wait();  // the prepared operands (and the callers' state) are complete
     pdl_release();
     scan_t_role(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
-                (int)blockIdx.x / heads, nullptr);
+                (int)blockIdx.x / heads, nullptr, 0);
 }
 
 // BF16 [rows][cols] with a row pitch of `pitch_elems`; boxes of `box_cols`
@@ -1242,12 +1326,14 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, ui
 }
 
 // Ready flags of the fused grid: one 32-bit word per (chunk, head) blob,
-// after the blobs, padded to 256 bytes.
+// after the blobs, head-major with each head's run of chunks padded to a
+// multiple of 4 words (16-byte groups), the whole padded to 256 bytes.
 size_t ready_offset(long long chunks, int n_seqs, int heads) {
     return header_bytes(n_seqs) + (size_t)chunks * heads * BLOB_BYTES;
 }
+long long ready_pitch(long long chunks) { return (chunks + 3) & ~3LL; }
 size_t ready_words(long long chunks, int heads) {
-    return (((size_t)chunks * heads * 4 + 255) & ~(size_t)255) / 4;
+    return (((size_t)ready_pitch(chunks) * heads * 4 + 255) & ~(size_t)255) / 4;
 }
 
 }  // namespace
@@ -1260,7 +1346,7 @@ size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads) {
 // Per-SM cost figures measured on GB300 (T = 8192, 32 heads) that choose
 // between the fused grid and the two kernels: a prepare item, and a chunk of
 // the transposed scan's chain.
-constexpr double kPrepItemUs = 9.1, kScanTChunkUs = 2.4;
+constexpr double kPrepItemUs = 8.3, kScanTChunkUs = 2.3;
 
 // Launches the tensor-core prefill (BF16 inputs, chunk 64); arguments,
 // including the workspace size, are validated by kda_prefill.
@@ -1333,7 +1419,8 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, prefill_fused_kernel, maps, vmap, omap, (const uint16_t*)beta,
-                               state, o, t, t_pad, heads, cu, n_seqs, ws, ready);
+                               state, o, t, t_pad, heads, cu, n_seqs, ws, ready,
+                               ready_pitch(chunk_bound));
         if (e == cudaSuccess) return launch_result("kda_prefill (fused)");
         // the grid could not be made resident (e.g. SMs held by other work):
         // run the two kernels instead

@@ -325,28 +325,29 @@ __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
 }
 
-// Publish / observe a ready flag in global memory between CTAs of one grid.
-// The producer has completed its bulk stores (bulk_wait_all) and passed a CTA
+// Publish a ready flag in global memory between CTAs of one grid.  The
+// producer has completed its bulk stores (bulk_wait_all) and passed a CTA
 // barrier after its other threads' stores; the proxy fence orders the bulk
-// (async-proxy) writes before the release.  The consumer orders its acquire
-// before the bulk loads it issues next with the same proxy fence.
+// (async-proxy) writes before the release.  Consumers read flags with
+// flags4_acquire and order their bulk copies after it with flags_proxy_fence.
 __device__ __forceinline__ void flag_release(unsigned* flag, unsigned v) {
     asm volatile("fence.proxy.async.global;" ::: "memory");
     __threadfence();
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
 }
-// Spin (bounded) until *flag != 0; false when the limit ran out.
-__device__ __forceinline__ bool flag_acquire(const unsigned* flag, uint32_t limit = 1u << 22) {
-    for (uint32_t i = 0; i < limit; ++i) {
-        unsigned v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-        if (v) {
-            asm volatile("fence.proxy.async.global;" ::: "memory");
-            return true;
-        }
-        __nanosleep(64);
-    }
-    return false;
+// Four consecutive flags (16-byte aligned) in one load with acquire
+// semantics: what the releases it observes guard is visible to this thread's
+// later loads; flags_proxy_fence() extends that to its later bulk copies.
+__device__ __forceinline__ uint4 flags4_acquire(const unsigned* flags) {
+    uint4 v;
+    asm volatile("ld.acquire.gpu.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(flags)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void flags_proxy_fence() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // Wait until every committed bulk store of this thread has finished reading
