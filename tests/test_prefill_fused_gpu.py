@@ -116,3 +116,38 @@ def test_fused_stale_workspace_and_repeated_calls(orc):
     assert rel_err(S1[0], S_ref) < TOL_PREFILL
     o2, S2 = run(K, d, t, workspace=ws)
     assert torch.equal(o1, o2) and torch.equal(S1, S2)
+
+
+@pytest.mark.parametrize("packed", [True, False])
+def test_fused_grid_two_sequences(orc, packed):
+    """Two sequences of 16 heads (32 chains: the fused grid) whose chunk
+    counts are not multiples of four, so the second sequence's chunks start
+    inside a group of four ready flags; packed and uniform forms."""
+    K = kda()
+    Hs = 16
+    lengths = [300, 517] if packed else [517, 517]
+    gen = torch.Generator().manual_seed(77 + int(packed))
+    tot = sum(lengths)
+    d = wl.core_inputs(gen, (tot,), Hs, torch.bfloat16)
+    S0 = wl.state(gen, (2,), Hs, 0.02)
+    S = S0.clone().cuda()
+    dev = {n: d[n].cuda() for n in d}
+    o = torch.zeros((tot, Hs, 128), device="cuda")
+    if packed:
+        cu = torch.tensor([0, lengths[0], tot], dtype=torch.int32, device="cuda")
+        K.kda_prefill(S, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], o, tot, 64,
+                      cu_seqlens=cu)
+    else:
+        t = lengths[0]
+        view = {n: dev[n].view((2, t) + tuple(dev[n].shape[1:])) for n in dev}
+        K.kda_prefill(S, view["q"], view["k"], view["v"], view["g"], view["beta"],
+                      o.view(2, t, Hs, 128), t, 64)
+    K.kda_sync_status()
+    a = 0
+    for n, L in enumerate(lengths):
+        b = a + L
+        o_ref, S_ref = orc.prefill(d["q"][a:b], d["k"][a:b], d["v"][a:b], d["g"][a:b],
+                                   d["beta"][a:b], S0[n])
+        assert rel_err(o[a:b], o_ref) < TOL_PREFILL
+        assert rel_err(S[n], S_ref) < TOL_PREFILL
+        a = b
