@@ -1,12 +1,15 @@
 // Thin inline-PTX layer over the sm_100-family tensor-core and bulk-copy
-// machinery used by the prefill kernel: TMEM allocation, tcgen05.mma with
-// shared-memory operand descriptors, tcgen05.commit / mbarrier completion,
-// tcgen05.ld of accumulators, and TMA tile loads.
+// machinery used by the prefill kernels: TMEM allocation, tcgen05.mma (TF32
+// and FP16, A from shared memory or TMEM) with shared-memory operand
+// descriptors, tcgen05.commit / mbarrier completion, tcgen05.ld / tcgen05.st,
+// TMA tile loads and stores, bulk copies, and the ready-flag handshake
+// between CTAs of one grid.
 //
 // Operands are described without swizzle: an operand is a grid of "core
 // matrices" of 8 rows x 16 bytes (8 x 4 TF32 or 8 x 8 FP16 values), each 128
-// contiguous bytes; a descriptor gives the byte distance between core matrices adjacent
-// along K (LBO) and along M or N (SBO).  The callers choose the placement.
+// contiguous bytes; a descriptor gives the byte distance between core
+// matrices adjacent along K (LBO) and along M or N (SBO).  The callers choose
+// the placement.
 #pragma once
 
 #include <cuda.h>
@@ -101,29 +104,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     return false;
 }
 
-// Plain arrive (count one) on `bar`.
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Barrier 1 over the first `nthreads` threads of the CTA (a multiple of 32).
-__device__ __forceinline__ void named_sync(uint32_t nthreads) {
-    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
-}
-
-// Barrier 1 over the first `nthreads` threads that also ORs `pred` across
-// them: every participant gets the same answer.
-__device__ __forceinline__ bool named_sync_or(uint32_t nthreads, bool pred) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
-        " selp.u32 %0, 1, 0, q;\n}\n"
-        : "=r"(r)
-        : "r"((uint32_t)pred), "r"(nthreads)
-        : "memory");
-    return r != 0;
-}
-
 // ---------------------------------------------------------------- TMEM
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp executes.
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -186,18 +166,6 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem]^T, one K-step, issued by one thread.  A sits
-// in TMEM with lane = row and one 32-bit column per K index (M = 128: lanes
-// 0..127), so `a_tmem` advances by 8 columns per K-step.
-__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
-                                            uint32_t idesc, bool accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
-        : "memory");
-}
-
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread has
 // completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -233,25 +201,9 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
     for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[8]) { tmem_ld8(taddr, v); }
-__device__ __forceinline__ void tmem_ld(uint32_t taddr, float (&v)[16]) { tmem_ld16(taddr, v); }
 
 __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-// Write 16 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-        "%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15]))
-        : "memory");
 }
 
 // Write 16 (or 8) consecutive 32-bit columns of this thread's TMEM lane.
@@ -354,11 +306,6 @@ __device__ __forceinline__ void flags_proxy_fence() {
 // its shared-memory source (the global writes may still be in flight).
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Hint: bring `bytes` (a multiple of 16) at `src` into L2.
-__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
