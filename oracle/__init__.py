@@ -49,6 +49,9 @@ def lib():
         L.kda_oracle_o_norm_gated.restype = None
         L.kda_oracle_o_norm_gated.argtypes = ([ctypes.c_long, ctypes.c_int, ctypes.c_int,
                                                ctypes.c_double] + [_dp] * 4)
+        L.kda_oracle_gate.restype = None
+        L.kda_oracle_gate.argtypes = ([ctypes.c_long, ctypes.c_int, ctypes.c_int,
+                                       ctypes.c_double] + [_dp] * 6)
         _LIB = L
     return _LIB
 
@@ -176,3 +179,21 @@ def o_norm_gated(core, gate, w, eps=1e-6):
     out = np.zeros_like(core)
     lib().kda_oracle_o_norm_gated(rows, H, D, float(eps), _p(core), _p(gate), _p(w), _p(out))
     return out
+
+
+def gate(g_raw, dt_bias, a_log, lower_bound, b):
+    """Forget gate and beta (the reading stated in kda_oracle.c): g_raw
+    [rows, H*D] or [rows, H, D], dt_bias [H*D], a_log [H], b [rows, H];
+    returns g [rows, H, D] and beta [rows, H] (FP64)."""
+    a_log, b = f64(a_log), f64(b)
+    H = a_log.shape[0]
+    rows = b.shape[0]
+    g_raw = np.ascontiguousarray(f64(g_raw).reshape(rows, H, -1))
+    D = g_raw.shape[2]
+    dt_bias = np.ascontiguousarray(f64(dt_bias).reshape(H * D))
+    assert b.shape == (rows, H)
+    g = np.zeros_like(g_raw)
+    beta = np.zeros_like(b)
+    lib().kda_oracle_gate(rows, H, D, float(lower_bound), _p(g_raw), _p(dt_bias), _p(a_log),
+                          _p(b), _p(g), _p(beta))
+    return g, beta

@@ -27,8 +27,10 @@
  * without FP contraction so the result is the same on x86-64 and aarch64.
  *
  * Parity status: every function here is pinned by the CPU tests (closed forms,
- * special cases, brute force and a library-routine cross-check); the only
- * unpinned choice is the value of the query scale itself, a convention.
+ * special cases, brute force and a library-routine cross-check); the unpinned
+ * choices are conventions the pages leave open: the value of the query scale,
+ * and the formula of the forget gate (kda_oracle_gate, parity unpinned: its
+ * inputs are on the pages, its formula is a reading).
  */
 #include <math.h>
 #include <stdlib.h>
@@ -302,6 +304,37 @@ void kda_oracle_o_norm_gated(long rows, int H, int D, double eps, const double* 
         for (int d = 0; d < D; ++d) {
             const double gt = gate[(size_t)rh * D + d];
             out[(size_t)rh * D + d] = y[d] * r * w[d] * (1.0 / (1.0 + exp(-gt)));
+        }
+    }
+}
+
+/*
+ * Forget gate and beta of the core (module index, block pipeline:
+ * "kda_gate / sigmoid(b_proj)"; Glm5NextKdaWorkspace: gate [T_pad, heads,
+ * head_dim] FP32 "bounded log-decay from kda_gate", g_raw [T, qkv] the
+ * forget-gate projection kda_gate consumes, beta [T_pad, heads] "already
+ * sigmoided"; Glm5NextKdaWeights: dt_bias [heads * head_dim] one value per
+ * channel, a_log [heads] one value per head; config.rs: gate_lower_bound).
+ * The pages give the gate's inputs and that its result is a log-decay bounded
+ * below by gate_lower_bound, not its formula (parity unpinned).  The reading
+ * taken here, for channel c = h * D + d of row r:
+ *     g[r][c]    = lb * sigmoid(exp(a_log[h]) * (g_raw[r][c] + dt_bias[c]))
+ *     beta[r][h] = sigmoid(b[r][h])
+ * so that lb < g < 0 for every finite input.
+ */
+void kda_oracle_gate(long rows, int H, int D, double lb, const double* g_raw,
+                     const double* dt_bias, const double* a_log, const double* b,
+                     double* g, double* beta) {
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) {
+        for (int h = 0; h < H; ++h) {
+            const double rate = exp(a_log[h]);
+            for (int d = 0; d < D; ++d) {
+                const size_t c = (size_t)h * D + d;
+                const double z = rate * (g_raw[(size_t)r * H * D + c] + dt_bias[c]);
+                g[(size_t)r * H * D + c] = lb / (1.0 + exp(-z));
+            }
+            beta[(size_t)r * H + h] = 1.0 / (1.0 + exp(-b[(size_t)r * H + h]));
         }
     }
 }

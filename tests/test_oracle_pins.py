@@ -434,3 +434,73 @@ def test_workload_inputs_follow_recipe():
     d2 = wl.tiny()
     for n in ("q", "k", "v", "g", "beta"):
         assert torch.equal(d[n], d2[n])
+
+
+# ---------------------------------------------------------------- forget gate and beta
+# The formula is a reading (the pages give its inputs and its bound, not the
+# expression): g = lb * sigmoid(exp(a_log[h]) * (g_raw + dt_bias[c])),
+# beta = sigmoid(b).  These pins fix everything but that choice: the closed
+# form at a zero argument, the limits, the range, the monotonicity, and which
+# parameter broadcasts over which axis.
+
+def _gate_inputs(seed, rows=5, H=3, D=8):
+    rng = np.random.default_rng(seed)
+    return (rng.normal(size=(rows, H * D)), rng.normal(size=H * D) * 0.5,
+            rng.normal(size=H) * 0.5, rng.normal(size=(rows, H)))
+
+
+def test_gate_zero_argument_is_half_the_bound(orc):
+    g_raw, dt, al, b = _gate_inputs(1)
+    g, _ = orc.gate(-np.broadcast_to(dt, g_raw.shape), dt, al, -5.0, b)
+    assert np.allclose(g, -2.5, rtol=0, atol=1e-15)
+
+
+def test_gate_hand_value(orc):
+    """a_log = 0 (rate 1) and g_raw + dt_bias = 1: g = lb / (1 + e^-1)."""
+    g, beta = orc.gate(np.ones((1, 4)), np.zeros(4), np.zeros(1), -4.0, np.zeros((1, 1)))
+    assert np.allclose(g, -4.0 * 0.7310585786300049, rtol=0, atol=1e-15)
+    assert beta[0, 0] == 0.5
+
+
+def test_gate_limits_and_range(orc):
+    g_raw, dt, al, b = _gate_inputs(2)
+    lb = -7.0
+    g, _ = orc.gate(g_raw, dt, al, lb, b)
+    assert np.all(g < 0) and np.all(g > lb)
+    big = np.full_like(g_raw, 1e4)
+    g_hi, _ = orc.gate(big, dt, al, lb, b)        # the strongest decay: the bound
+    g_lo, _ = orc.gate(-big, dt, al, lb, b)       # no decay: zero
+    assert np.allclose(g_hi, lb, rtol=0, atol=1e-12)
+    assert np.allclose(g_lo, 0.0, rtol=0, atol=1e-12)
+    g_slow, _ = orc.gate(g_raw, dt, np.full_like(al, -60.0), lb, b)  # rate -> 0
+    assert np.allclose(g_slow, lb / 2, rtol=0, atol=1e-12)
+
+
+def test_gate_is_monotone_in_the_projection(orc):
+    g_raw, dt, al, b = _gate_inputs(3)
+    g1, _ = orc.gate(g_raw, dt, al, -5.0, b)
+    g2, _ = orc.gate(g_raw + 0.1, dt, al, -5.0, b)
+    assert np.all(g2 < g1)  # a larger projection decays faster (lb < 0)
+
+
+def test_gate_broadcasts_bias_per_channel_and_rate_per_head(orc):
+    g_raw, dt, al, b = _gate_inputs(4, rows=4, H=3, D=8)
+    g0, _ = orc.gate(g_raw, dt, al, -5.0, b)
+    dt2 = dt.copy()
+    dt2[8 + 5] += 1.0                      # channel 5 of head 1
+    g1, _ = orc.gate(g_raw, dt2, al, -5.0, b)
+    changed = np.argwhere(np.abs(g1 - g0) > 0)
+    assert set(map(tuple, changed[:, 1:])) == {(1, 5)}
+    al2 = al.copy()
+    al2[2] += 0.5                          # head 2
+    g2, _ = orc.gate(g_raw, dt, al2, -5.0, b)
+    diff = np.abs(g2 - g0) > 0
+    assert diff[:, 2].all() and not diff[:, :2].any()
+
+
+def test_beta_is_the_logistic_function(orc):
+    _, _, _, b = _gate_inputs(5)
+    _, beta = orc.gate(np.zeros((5, 24)), np.zeros(24), np.zeros(3), -5.0, b)
+    _, beta_neg = orc.gate(np.zeros((5, 24)), np.zeros(24), np.zeros(3), -5.0, -b)
+    assert np.allclose(beta + beta_neg, 1.0, rtol=0, atol=1e-15)
+    assert np.allclose(beta, 1.0 / (1.0 + np.exp(-b)), rtol=1e-15, atol=0)
