@@ -46,6 +46,10 @@ DK_N, DK_K = 128, 4
 CONV_K = 4
 DK_BYTES = (2 + DK_K) * DK_N * H * D * D * 4 + 4 * DK_N * DK_K * H * D * 4 + DK_N * DK_K * H * 4
 ONORM_BYTES = T_PREFILL * 32 * 128 * (4 + 2 + 2) + 128 * 2  # core FP32, gate and out BF16, w
+# the forget gate and beta of a prefill-sized problem (8192 rows x 32 heads):
+# BF16 g_raw in and BF16 g out per channel, BF16 b in and BF16 beta out per head,
+# dt_bias and a_log once
+GATE_BYTES = T_PREFILL * H * D * (2 + 2) + T_PREFILL * H * (2 + 2) + H * D * 4 + H * 4
 SHORT_T = 4
 SHORT_BYTES = 2 * DECODE_N * H * D * D * 4 + 5 * DECODE_N * SHORT_T * H * D * 4 + DECODE_N * SHORT_T * H * 4
 CONVK_BYTES = (DK_N * DK_K * 3 * H * D * 2 * 2 + 3 * H * D * CONV_K * 2
@@ -320,6 +324,22 @@ def run_gpu(args):
         on_per, _ = time_launches(o_norm, 20, stream)
         del n_core, n_gate, n_out
 
+        # ---------------- forget gate and beta of a prefill-sized problem
+        g_raw = torch.randn((T_PREFILL, H * D), generator=ngen).to(torch.bfloat16).to(dev)
+        g_b = torch.randn((T_PREFILL, H), generator=ngen).to(torch.bfloat16).to(dev)
+        g_dt = (torch.randn(H * D, generator=ngen) * 0.5).to(dev)
+        g_al = (torch.randn(H, generator=ngen) * 0.5).to(dev)
+        g_out = torch.empty((T_PREFILL, H, D), dtype=torch.bfloat16, device=dev)
+        g_beta = torch.empty((T_PREFILL, H), dtype=torch.bfloat16, device=dev)
+
+        def gate():
+            K.kda_gate(g_raw, g_dt, g_al, g_b, g_out, g_beta, -5.0)
+
+        for _ in range(3):
+            gate()
+        gate_per, _ = time_launches(gate, 20, stream)
+        del g_raw, g_b, g_out, g_beta
+
         # ---------------- front end + core: 16 packed sequences, conv then prefill
         fe = wl.frontend()
         cu = fe["cu_seqlens"].to(dev)
@@ -499,6 +519,13 @@ def run_gpu(args):
             / pk["hbm_gbs"],
             "us_per_call": statistics.mean(on_per) * 1e3, "algorithmic_bytes": ONORM_BYTES,
         },
+        "gate": {
+            "workload": "forget gate and beta of a prefill-sized problem (8192 x 32 x 128, BF16)",
+            "value": GATE_BYTES / (statistics.mean(gate_per) / 1e3) / 1e9, "unit": "GB/s",
+            "frac_of_hbm_peak": GATE_BYTES / (statistics.mean(gate_per) / 1e3) / 1e9
+            / pk["hbm_gbs"],
+            "us_per_call": statistics.mean(gate_per) * 1e3, "algorithmic_bytes": GATE_BYTES,
+        },
         "conv": {
             "workload": wl.FRONTEND.name + " (conv + SiLU + L2 stage)",
             "value": conv_bytes / (statistics.mean(conv_per) / 1e3) / 1e9, "unit": "GB/s",
@@ -595,6 +622,16 @@ def run_case(args):
         fn = lambda: K.kda_prefill(S, q, k, v, g, beta, o, args.seq_len, CHUNK, workspace=ws)
         nbytes = 4 * args.seq_len * H * D * 2 + args.seq_len * H * 2 + args.seq_len * H * D * 4 \
             + 2 * H * D * D * 4
+    elif args.case == "gate":
+        ggen = torch.Generator(device="cpu").manual_seed(0)
+        g_raw = torch.randn((args.seq_len, H * D), generator=ggen).to(torch.bfloat16).to(dev)
+        g_b = torch.randn((args.seq_len, H), generator=ggen).to(torch.bfloat16).to(dev)
+        g_dt = (torch.randn(H * D, generator=ggen) * 0.5).to(dev)
+        g_al = (torch.randn(H, generator=ggen) * 0.5).to(dev)
+        g_out = torch.empty((args.seq_len, H, D), dtype=torch.bfloat16, device=dev)
+        g_beta = torch.empty((args.seq_len, H), dtype=torch.bfloat16, device=dev)
+        fn = lambda: K.kda_gate(g_raw, g_dt, g_al, g_b, g_out, g_beta, -5.0)
+        nbytes = args.seq_len * H * (D * 4 + 4) + H * D * 4 + H * 4
     elif args.case == "decode":
         dd = wl.decode_steps(steps=1)
         S = dd["state"].to(dev)
@@ -637,7 +674,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default=None, choices=["prefill", "decode", "decode_k", "conv"],
+    ap.add_argument("--case", default=None,
+                    choices=["prefill", "decode", "decode_k", "conv", "gate"],
                     help="time one kernel alone (for profiler captures)")
     ap.add_argument("--seq-len", type=int, default=T_PREFILL)
     args = ap.parse_args()

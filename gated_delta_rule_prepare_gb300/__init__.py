@@ -7,7 +7,7 @@ library's CUDA kernels; there is no fallback.  Importing this package on a
 machine without the built library raises immediately.
 
 Entry points (same names as the C ABI): ``kda_decode``, ``kda_decode_k``,
-``kda_prefill``, ``kda_conv_silu_l2``, ``kda_conv_silu_l2_k``, ``kda_o_norm_gated``,
+``kda_prefill``, ``kda_conv_silu_l2``, ``kda_conv_silu_l2_k``, ``kda_gate``, ``kda_o_norm_gated``,
 ``kda_prefill_workspace_size``, ``kda_sync_status``.
 """
 
@@ -47,6 +47,7 @@ def _load():
         "kda_conv_silu_l2": [_vp] * 4 + [_i, _i, _vp, _i, _f, _i, _i, _u64],
         "kda_sync_status": [_u64],
         "kda_o_norm_gated": [_vp] * 4 + [_i64, _i, _i, _f, _u64],
+        "kda_gate": [_vp, _i64, _vp, _vp, _f, _vp, _i64, _vp, _vp, _i, _i64, _i, _i, _u64],
         "kda_conv_silu_l2_k": [_vp] * 4 + [_i, _i, _i, _f, _i, _i, _vp, _i, _u64],
     }
     for name, args in sig.items():
@@ -262,6 +263,31 @@ def kda_o_norm_gated(core, gate, w, out, eps=1e-6):
     _check(LIB.kda_o_norm_gated(_ptr(core, torch.float32, "core"), _ptr(gate, b16, "gate"),
                                 _ptr(w, b16, "w"), _ptr(out, b16, "out"), int(rows),
                                 hd // HEAD_DIM, HEAD_DIM, float(eps), _stream(core)))
+
+
+def kda_gate(g_raw, dt_bias, a_log, b_raw, g_out, beta_out, gate_lower_bound):
+    """Forget gate and beta: g_raw BF16 [rows, >= H*128] (row pitch a multiple
+    of 8 channels), dt_bias FP32 [H*128], a_log FP32 [H], b_raw BF16
+    [rows, >= H]; g_out [rows, H, 128] and beta_out [rows, H] in FP32 or BF16
+    (both the same dtype)."""
+    for n_, t_ in (("dt_bias", dt_bias), ("a_log", a_log), ("g_out", g_out),
+                   ("beta_out", beta_out)):
+        _contig(t_, n_)
+    if g_raw.dim() != 2 or g_raw.stride(1) != 1 or b_raw.dim() != 2 or b_raw.stride(1) != 1:
+        raise ValueError("kda_gate: g_raw and b_raw must be 2-D with unit channel stride")
+    rows, H = g_out.shape[0], a_log.numel()
+    if (g_out.numel() != rows * H * HEAD_DIM or beta_out.numel() != rows * H
+            or dt_bias.numel() != H * HEAD_DIM or g_raw.shape[0] != rows
+            or b_raw.shape[0] != rows or g_raw.shape[1] < H * HEAD_DIM or b_raw.shape[1] < H):
+        raise ValueError("kda_gate: shape mismatch")
+    if g_out.dtype != beta_out.dtype or g_out.dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("kda_gate: g_out and beta_out must both be FP32 or both BF16")
+    b16 = torch.bfloat16
+    _check(LIB.kda_gate(_ptr(g_raw, b16, "g_raw"), int(g_raw.stride(0)),
+                        _ptr(dt_bias, torch.float32, "dt_bias"), _ptr(a_log, torch.float32, "a_log"),
+                        float(gate_lower_bound), _ptr(b_raw, b16, "b_raw"), int(b_raw.stride(0)),
+                        _ptr(g_out), _ptr(beta_out), BF16 if g_out.dtype == b16 else F32,
+                        int(rows), H, HEAD_DIM, _stream(g_out)))
 
 
 def kda_sync_status(device=None):

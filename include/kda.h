@@ -195,6 +195,39 @@ kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, const uint16_t
                             uint64_t stream);
 
 /*
+ * kda_gate -- the forget gate and beta of the core, the block pipeline's step
+ * before it ("kda_gate / sigmoid(b_proj)", glm5next_kda module index;
+ * Glm5NextKdaWorkspace g_raw [T, qkv] "the forget-gate projection kda_gate
+ * consumes", gate [T_pad, heads, head_dim] "bounded log-decay from kda_gate",
+ * beta [T_pad, heads] "already sigmoided"; Glm5NextKdaWeights dt_bias
+ * [heads * head_dim] F32 one per channel, a_log [heads] F32 one per head;
+ * config.rs gate_lower_bound).  The pages give these inputs and that the
+ * decay is bounded below by gate_lower_bound, not the formula; this library's
+ * reading, for channel c = h * 128 + i of token row r:
+ *     g[r][h][i] = gate_lower_bound * sigmoid(exp(a_log[h]) * (g_raw[r][c] + dt_bias[c]))
+ *     beta[r][h] = sigmoid(b_raw[r][h])
+ * in FP32, rounded once to out_dtype; gate_lower_bound < g < 0.  The results
+ * are kda_prefill's g and beta (in_dtype = out_dtype) or, in FP32, decode's.
+ *
+ *   g_raw        : BF16 [rows][g_raw_stride], channels in the first heads*128
+ *                  columns (16-byte aligned; g_raw_stride a multiple of 8)
+ *   dt_bias      : FP32 [heads * 128] (16-byte aligned)
+ *   a_log        : FP32 [heads]
+ *   b_raw        : BF16 [rows][b_stride], the b_proj output in the first heads
+ *                  columns
+ *   g_out        : [rows][heads][128] of out_dtype (16-byte aligned)
+ *   beta_out     : [rows][heads] of out_dtype
+ *   out_dtype    : KDA_F32 or KDA_BF16
+ *   rows >= 0 (0 launches nothing and the pointers may then be NULL),
+ *   heads >= 1, head_dim == 128, gate_lower_bound finite and negative.
+ * One kernel is enqueued on `stream`; the outputs may not alias the inputs.
+ */
+kda_status kda_gate(const uint16_t* g_raw, int64_t g_raw_stride, const float* dt_bias,
+                    const float* a_log, float gate_lower_bound, const uint16_t* b_raw,
+                    int64_t b_stride, void* g_out, void* beta_out, int out_dtype, int64_t rows,
+                    int heads, int head_dim, uint64_t stream);
+
+/*
  * kda_o_norm_gated -- sigmoid-gated RMSNorm of the core output, the block
  * pipeline's step after the core ("sigmoid-gated RMSNorm(o_norm,
  * g_b(g_a(h)))", glm5next_kda module index; Glm5NextKdaWorkspace core,

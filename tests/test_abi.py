@@ -148,6 +148,25 @@ def test_o_norm_refuses_bad_arguments(lib):
     assert b"kda_o_norm_gated" in lib.kda_last_error()
 
 
+def test_gate_refuses_bad_arguments(lib):
+    f = lib.kda_gate
+    f.argtypes = [V, ctypes.c_int64, V, V, F, V, ctypes.c_int64, V, V, I, ctypes.c_int64, I, I,
+                  U64]
+    ok = (P, 256, P, P, -5.0, P, 2, P, P, 1, 4, 2, 128, 0)
+    bad = lambda **kw: f(*[kw.get(k, v) for k, v in zip(
+        ("g", "gs", "dt", "al", "lb", "b", "bs", "go", "bo", "dt_", "rows", "h", "hd", "s"), ok)])
+    assert bad(hd=64) == 2                          # head_dim
+    assert bad(rows=-1) == 1 and bad(h=0) == 1      # rows, heads
+    assert bad(dt_=2) == 1                          # out_dtype
+    assert bad(lb=0.0) == 1 and bad(lb=1.0) == 1    # the bound must be negative
+    assert bad(gs=128) == 1 and bad(gs=260) == 1    # pitch below heads*128, not a multiple of 8
+    assert bad(bs=1) == 1                           # b pitch below heads
+    assert bad(g=None) == 1                         # null pointer
+    assert bad(go=ctypes.c_void_p(P.value + 4)) == 1  # g_out alignment
+    assert bad(rows=0, g=None, b=None, go=None, bo=None) == 0  # zero rows: nothing to touch
+    assert b"kda_gate" in lib.kda_last_error()
+
+
 def test_conv_k_refuses_bad_arguments(lib):
     f = lib.kda_conv_silu_l2_k
     f.argtypes = [V] * 4 + [I, I, I, F, I, I, V, I, U64]
