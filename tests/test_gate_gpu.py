@@ -36,7 +36,10 @@ def ref(orc, g_raw, dt, al, b, H):
     return orc.gate(g_raw[:, :H * 128], dt, al, LB, b[:, :H])
 
 
-@pytest.mark.parametrize("rows,H,extra", [(1, 1, 0), (37, 4, 0), (300, 2, 64)])
+# (40000, 3): every thread walks several steps of 4 rows and the grid is
+# rounded to whole rows of 48 groups; (5, 7): a grid of 7 CTAs, mostly idle.
+@pytest.mark.parametrize("rows,H,extra", [(1, 1, 0), (37, 4, 0), (300, 2, 64), (5, 7, 8),
+                                          (40000, 3, 8)])
 def test_gate_fp32_matches_oracle(orc, rows, H, extra):
     K = kda()
     g_raw, dt, al, b = inputs(rows + H, rows, H, extra)
