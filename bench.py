@@ -72,7 +72,8 @@ def peaks():
 def kernel_source_sha() -> str:
     """Hash of the sources the prefill kernels are built from."""
     h = hashlib.sha256()
-    for name in ("prefill_tc.cu", "prefill.cu", "sm103_tc.h", "kda_common.h", "tma_map.h"):
+    for name in ("prefill_tc.cu", "prefill.cu", "sm103_tc.h", "kda_common.h", "tma_map.h",
+                 "f32x2.h"):
         h.update(open(os.path.join(ROOT, "gated_delta_rule_prepare_gb300", "csrc", name),
                       "rb").read())
     return h.hexdigest()[:16]
@@ -348,6 +349,23 @@ def run_gpu(args):
         gate_per, _ = time_launches(gate, 20, stream)
         del g_sets
 
+        # ---------------- the prefill step with the forget gate and beta formed
+        # inside prepare from their raw inputs (the step's q, k, v and state)
+        pgen = torch.Generator(device="cpu").manual_seed(1)
+        gi = wl.gate_inputs(pgen, T_PREFILL, H)
+        pg_in = {n: gi[n].to(dev) for n in ("g_raw", "dt_bias", "a_log", "b_raw")}
+
+        def prefill_gated():
+            K.kda_prefill_gated(S, q, k, v, pg_in["g_raw"], pg_in["dt_bias"], pg_in["a_log"],
+                                pg_in["b_raw"], o, T_PREFILL, gi["gate_lower_bound"],
+                                workspace=ws)
+
+        for _ in range(3):
+            prefill_gated()
+        K.kda_sync_status()
+        pg_per, _ = time_launches(prefill_gated, 20, stream)
+        del pg_in
+
         # ---------------- front end + core: 16 packed sequences, conv then prefill
         fe = wl.frontend()
         cu = fe["cu_seqlens"].to(dev)
@@ -527,6 +545,13 @@ def run_gpu(args):
             / pk["hbm_gbs"],
             "us_per_call": statistics.mean(on_per) * 1e3, "algorithmic_bytes": ONORM_BYTES,
         },
+        "prefill_gated": {
+            "workload": "the prefill step (8192 x 32 heads, BF16) with g and beta formed in "
+                        "prepare from g_raw, dt_bias, a_log and b_raw",
+            "value": T_PREFILL / (statistics.mean(pg_per) / 1e3), "unit": "tokens/s",
+            "us_per_call": statistics.mean(pg_per) * 1e3,
+            "gate_then_prefill_us": (statistics.mean(gate_per) + ms_step) * 1e3,
+        },
         "gate": {
             "workload": "forget gate and beta of a prefill-sized problem (8192 x 32 x 128, BF16)",
             "value": GATE_BYTES / (statistics.mean(gate_per) / 1e3) / 1e9, "unit": "GB/s",
@@ -631,6 +656,19 @@ def run_case(args):
         fn = lambda: K.kda_prefill(S, q, k, v, g, beta, o, args.seq_len, CHUNK, workspace=ws)
         nbytes = 4 * args.seq_len * H * D * 2 + args.seq_len * H * 2 + args.seq_len * H * D * 4 \
             + 2 * H * D * D * 4
+    elif args.case == "prefill_gated":
+        d = wl.prefill_gated(t=args.seq_len)
+        q, k, v = (d[n].to(dev) for n in ("q", "k", "v"))
+        gin = {n: d[n].to(dev) for n in ("g_raw", "dt_bias", "a_log", "b_raw")}
+        S = d["state"].to(dev)
+        o = torch.empty((args.seq_len, H, D), device=dev)
+        ws = torch.empty(K.kda_prefill_workspace_size(args.seq_len, 1, CHUNK, H),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: K.kda_prefill_gated(S, q, k, v, gin["g_raw"], gin["dt_bias"], gin["a_log"],
+                                         gin["b_raw"], o, args.seq_len, d["gate_lower_bound"],
+                                         workspace=ws)
+        nbytes = 4 * args.seq_len * H * D * 2 + args.seq_len * H * 2 + args.seq_len * H * D * 4 \
+            + 2 * H * D * D * 4 + H * D * 4 + H * 4
     elif args.case == "gate":
         ggen = torch.Generator(device="cpu").manual_seed(0)
         sets = [(torch.randn((args.seq_len, H * D), generator=ggen).to(torch.bfloat16).to(dev),
@@ -690,7 +728,7 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    choices=["prefill", "decode", "decode_k", "conv", "gate"],
+                    choices=["prefill", "prefill_gated", "decode", "decode_k", "conv", "gate"],
                     help="time one kernel alone (for profiler captures)")
     ap.add_argument("--seq-len", type=int, default=T_PREFILL)
     args = ap.parse_args()

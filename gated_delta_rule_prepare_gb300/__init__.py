@@ -48,6 +48,8 @@ def _load():
         "kda_sync_status": [_u64],
         "kda_o_norm_gated": [_vp] * 4 + [_i64, _i, _i, _f, _u64],
         "kda_gate": [_vp, _i64, _vp, _vp, _f, _vp, _i64, _vp, _vp, _i, _i64, _i, _i, _u64],
+        "kda_prefill_gated": [_vp] * 5 + [_i64, _vp, _vp, _f, _vp, _i64, _vp, _i, _i, _i, _i,
+                                          _i64, _vp, _i, _vp, _sz, _u64],
         "kda_conv_silu_l2_k": [_vp] * 4 + [_i, _i, _i, _f, _i, _i, _vp, _i, _u64],
     }
     for name, args in sig.items():
@@ -193,6 +195,60 @@ def kda_prefill(state, q, k, v, g, beta, o, t, chunk, pad_fill=0.0, cu_seqlens=N
                            _ptr(o, torch.float32, "o"), int(t), int(t_pad), int(chunk),
                            float(pad_fill), H, HEAD_DIM, in_dtype, int(stride),
                            _ptr(cu_seqlens), n_seqs, ws_ptr, ws_bytes, _stream(state)))
+
+
+def kda_prefill_gated(state, q, k, v, g_raw, dt_bias, a_log, b_raw, o, t, gate_lower_bound,
+                      cu_seqlens=None, workspace=None):
+    """Tensor-core prefill (BF16 q, k, v; chunk 64) with the forget gate and
+    beta formed in the prepare kernel from g_raw BF16 [rows, >= H*128],
+    dt_bias FP32 [H*128], a_log FP32 [H] and b_raw BF16 [rows, >= H].
+    Without cu_seqlens: q, k, v [N, T_pad, H, 128] (or [T_pad, H, 128]), t
+    valid tokens per sequence, rows [t, T_pad) left as they are and never
+    used.  With cu_seqlens (device int32 [N+1]): packed rows and t = T."""
+    b16 = torch.bfloat16
+    H = q.shape[-2]
+    if q.shape[-1] != HEAD_DIM:
+        raise ValueError("kda_prefill_gated: head_dim must be 128")
+    for n_, t_ in (("q", q), ("k", k), ("v", v)):
+        if t_.dtype != b16 or t_.stride(-1) != 1 or t_.stride(-2) != HEAD_DIM:
+            raise ValueError("kda_prefill_gated: %s must be bfloat16 with unit channel stride "
+                             "and heads packed" % n_)
+    stride = q.stride(-3)
+    if k.stride(-3) != stride or v.stride(-3) != stride:
+        raise ValueError("kda_prefill_gated: q, k, v must share one token-row stride")
+    for n_, t_ in (("dt_bias", dt_bias), ("a_log", a_log), ("o", o), ("state", state)):
+        _contig(t_, n_)
+    if g_raw.dim() != 2 or g_raw.stride(1) != 1 or b_raw.dim() != 2 or b_raw.stride(1) != 1:
+        raise ValueError("kda_prefill_gated: g_raw and b_raw must be 2-D with unit channel stride")
+    if cu_seqlens is not None:
+        n_seqs = cu_seqlens.numel() - 1
+        t_pad = t
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise TypeError("kda_prefill_gated: cu_seqlens must be a CUDA int32 tensor")
+    elif q.dim() == 3:
+        n_seqs, t_pad = 1, q.shape[0]
+    else:
+        n_seqs, t_pad = q.shape[0], q.shape[1]
+        if q.stride(0) != t_pad * stride:
+            raise ValueError("kda_prefill_gated: sequences must be consecutive row blocks")
+    rows = t if cu_seqlens is not None else n_seqs * t_pad
+    if (g_raw.shape[0] != rows or b_raw.shape[0] != rows or g_raw.shape[1] < H * HEAD_DIM
+            or b_raw.shape[1] < H or dt_bias.numel() != H * HEAD_DIM or a_log.numel() != H
+            or o.numel() != rows * H * HEAD_DIM):
+        raise ValueError("kda_prefill_gated: shape mismatch")
+    if state.numel() != n_seqs * H * HEAD_DIM * HEAD_DIM or state.dtype != torch.float32:
+        raise ValueError("kda_prefill_gated: state must be FP32 [N, H, 128, 128]")
+    if workspace is None:
+        # allocated here, outside the library (which never allocates)
+        workspace = torch.empty(kda_prefill_workspace_size(rows, n_seqs, 64, H, b16),
+                                dtype=torch.uint8, device=q.device)
+    _check(LIB.kda_prefill_gated(
+        _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw, b16, "g_raw"), int(g_raw.stride(0)),
+        _ptr(dt_bias, torch.float32, "dt_bias"), _ptr(a_log, torch.float32, "a_log"),
+        float(gate_lower_bound), _ptr(b_raw, b16, "b_raw"), int(b_raw.stride(0)),
+        _ptr(o, torch.float32, "o"), int(t), int(t_pad), H, HEAD_DIM, int(stride),
+        _ptr(cu_seqlens), n_seqs, workspace.data_ptr(),
+        workspace.numel() * workspace.element_size(), _stream(state)))
 
 
 def kda_conv_silu_l2(conv_state, x, w, out, cu_seqlens=None, n_seqs=None, l2_eps=1e-6):

@@ -44,10 +44,20 @@ cudaError_t read_and_clear_status_prefill_tc(unsigned* out);
 // workspace size for `rows` token rows, and the launch (arguments validated by
 // kda_prefill).
 size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads);
+// Forget-gate inputs of kda_prefill_gated: g and beta are then the raw gate
+// projection g_raw and the raw b_proj output, turned into the core's g and
+// beta inside the prepare kernel.
+struct PrefillGate {
+    const float* dt_bias;  // [heads * 128]
+    const float* a_log;    // [heads]
+    float lb;              // gate_lower_bound
+    long long g_stride;    // elements between token rows of g_raw
+    long long b_stride;    // elements between token rows of b_raw
+};
 kda_status launch_prefill_tc(float* state, const void* q, const void* k, const void* v,
                              const void* g, const void* beta, float* o, int t, int t_pad,
                              int heads, long long stride, const int* cu, int n_seqs,
-                             void* workspace, cudaStream_t s);
+                             void* workspace, cudaStream_t s, const PrefillGate* gate = nullptr);
 
 // decode_k's row walk (decode.cu) for kda_prefill's short FP32 sequences:
 // n_seqs sequences of krows token rows, sequence n starting at row

@@ -21,6 +21,8 @@
 // for its slice.  Rows at or past a sequence's end are never loaded.
 #include <cuda_bf16.h>
 
+#include <cmath>
+
 #include "kda_common.h"
 
 namespace kda {
@@ -349,4 +351,53 @@ extern "C" kda_status kda_prefill(float* state, void* q, void* k, void* v, void*
                                 qkv_row_stride, cu_seqlens, n_seqs, workspace, s);
     return launch<float>(state, q, k, v, g, beta, o, t, t_pad, chunk, pad_fill, heads,
                          qkv_row_stride, cu_seqlens, n_seqs, workspace, s);
+}
+
+extern "C" kda_status kda_prefill_gated(float* state, const void* q, const void* k, const void* v,
+                                        const uint16_t* g_raw, int64_t g_raw_stride,
+                                        const float* dt_bias, const float* a_log,
+                                        float gate_lower_bound, const uint16_t* b_raw,
+                                        int64_t b_stride, float* o, int t, int t_pad, int heads,
+                                        int head_dim, int64_t qkv_row_stride,
+                                        const int* cu_seqlens, int n_seqs, void* workspace,
+                                        size_t workspace_bytes, uint64_t stream) {
+    KDA_REQUIRE(state && q && k && v && g_raw && dt_bias && a_log && b_raw && o,
+                KDA_ERR_INVALID_ARG, "kda_prefill_gated: null pointer argument");
+    KDA_REQUIRE(aligned16(state) && aligned16(q) && aligned16(k) && aligned16(v) &&
+                    aligned16(g_raw) && aligned16(o),
+                KDA_ERR_INVALID_ARG,
+                "kda_prefill_gated: state, q, k, v, g_raw and o must be 16-byte aligned");
+    KDA_REQUIRE(head_dim == D, KDA_ERR_UNSUPPORTED, "kda_prefill_gated: head_dim %d unsupported",
+                head_dim);
+    KDA_REQUIRE(heads >= 1 && n_seqs >= 1 && heads <= 65535 && n_seqs <= 65535,
+                KDA_ERR_INVALID_ARG, "kda_prefill_gated: heads (%d) / n_seqs (%d) out of range",
+                heads, n_seqs);
+    KDA_REQUIRE(t >= 1 && t_pad >= t, KDA_ERR_INVALID_ARG,
+                "kda_prefill_gated: need 1 <= t (%d) <= t_pad (%d)", t, t_pad);
+    KDA_REQUIRE(!cu_seqlens || t_pad == t, KDA_ERR_INVALID_ARG,
+                "kda_prefill_gated: packed sequences (cu_seqlens) take no padding: t_pad must "
+                "equal t");
+    KDA_REQUIRE(qkv_row_stride >= (int64_t)heads * D && qkv_row_stride % 8 == 0,
+                KDA_ERR_INVALID_ARG,
+                "kda_prefill_gated: qkv_row_stride must be >= heads * 128 and a multiple of 8");
+    KDA_REQUIRE(g_raw_stride >= (int64_t)heads * D && g_raw_stride % 8 == 0 && b_stride >= heads,
+                KDA_ERR_INVALID_ARG,
+                "kda_prefill_gated: g_raw_stride must be >= heads*128 and a multiple of 8, "
+                "b_stride >= heads");
+    KDA_REQUIRE(gate_lower_bound < 0.f && gate_lower_bound > -INFINITY, KDA_ERR_INVALID_ARG,
+                "kda_prefill_gated: gate_lower_bound must be finite and negative");
+    const long long rows = cu_seqlens ? (long long)t : (long long)t_pad * n_seqs;
+    KDA_REQUIRE(rows <= 0x7fffffffLL, KDA_ERR_INVALID_ARG,
+                "kda_prefill_gated: too many token rows");
+    const size_t need = prefill_tc_workspace_bytes(rows, n_seqs, heads);
+    KDA_REQUIRE(workspace && workspace_bytes >= need, KDA_ERR_WORKSPACE,
+                "kda_prefill_gated: workspace of %zu B given, %zu B needed", workspace_bytes, need);
+    KDA_REQUIRE(aligned16(workspace), KDA_ERR_INVALID_ARG,
+                "kda_prefill_gated: workspace must be 16-byte aligned");
+    KDA_REQUIRE(!fault_injected(), KDA_ERR_CUDA, "kda_prefill_gated: injected launch failure");
+    const PrefillGate gate = {dt_bias, a_log, gate_lower_bound, (long long)g_raw_stride,
+                              (long long)b_stride};
+    return launch_prefill_tc(state, q, k, v, g_raw, b_raw, o, t, t_pad, heads,
+                             (long long)qkv_row_stride, cu_seqlens, n_seqs, workspace,
+                             as_stream(stream), &gate);
 }

@@ -26,6 +26,10 @@
 // (sequence, head) chains: one SM per chain (scan_t_role) while the other SMs
 // walk the prepare items in chunk order and release a ready flag per item,
 // so the prepare work no longer precedes the scan.
+// The <true> instantiations of prepare_kernel and prefill_fused_kernel (the
+// gated prefill) read the raw forget-gate projection where the others read
+// g and the raw b_proj output where they read beta, and form g and beta as
+// they load them (PrepMaps).
 //
 // Precision: prepare forms A and P from TF32 operands (their decay factors
 // span e^(+-8 |g|)); the scan's products take FP16 operands (10 stored
@@ -50,6 +54,7 @@
 #include <cstring>
 #include <mutex>
 
+#include "f32x2.h"
 #include "kda_common.h"
 #include "sm103_tc.h"
 #include "tma_map.h"
@@ -152,7 +157,7 @@ static_assert(PS_OPX % 1024 == 0 && PS_Y % 16 == 0, "operand alignment");
 constexpr float kWideGMin = 5.1f;
 static_assert(PS_TOTAL <= 232448, "shared memory budget exceeded");
 
-constexpr uint32_t SS_OPX = BLOB_OPX, SS_TP = BLOB_TP, SS_KH = BLOB_KH, SS_DEC = BLOB_DEC;
+constexpr uint32_t SS_OPX = BLOB_OPX, SS_TP = BLOB_TP;
 
 // TMEM columns of prepare: A and P
 constexpr uint32_t TC_AP = 0;
@@ -183,9 +188,31 @@ __device__ __forceinline__ void st1h(unsigned char* p, float a) {
     *reinterpret_cast<uint16_t*>(p) = tc::f16_bits(a);
 }
 
+// What prepare reads besides the workspace: TMA maps of the q, k and g tiles,
+// beta's row pitch, and (gated calls) the forget-gate parameters.  In the
+// gated kernels the g tiles hold the gate projection g_raw and beta the raw
+// b_proj output; the first use of each element turns it into the core's input:
+//     g = lb * sigmoid(exp(a_log[h]) * (g_raw + dt_bias[h * 128 + i])),
+//     beta = sigmoid(b),
+// with the FP32 operations, in the same order, of the standalone gate kernel.
 struct PrepMaps {
     CUtensorMap q, k, g;
+    const float* dt_bias;
+    const float* a_log;
+    float lb;
+    long long b_stride;  // elements between token rows of beta
 };
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// sigmoid(z) = 1 / (1 + 2^(-z log2 e)) by the hardware 2^x and 1/x.
+__device__ __forceinline__ float sigmoid_hw(float z) {
+    return rcp_approx(__fadd_rn(ex2_approx(__fmul_rn(z, -kLog2e)), 1.0f));
+}
+// lb * sigmoid(c (x + dt)) given nc = -c log2 e.
+__device__ __forceinline__ float gate_hw(float x, float dt, float nc, float lb) {
+    return __fmul_rn(lb, rcp_approx(__fadd_rn(ex2_approx(__fmul_rn(__fadd_rn(x, dt), nc)), 1.0f)));
+}
 
 // D = A . B^T over `ksteps` TF32 K-steps of 8, issued by the calling thread.
 template <class OA, class OB>
@@ -325,6 +352,7 @@ __device__ __forceinline__ PrepItem prep_item(long long item, int heads, const i
 // The prepare walk of one CTA: items first, first + stride, ...  When `ready`
 // is set, each finished item's flag (ready[item]) is released once its
 // operands are in the workspace.
+template <bool GATED>
 __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_t* __restrict__ beta,
                                              int t, int t_pad, int heads,
                                              const int* __restrict__ cu, int n_seqs,
@@ -417,7 +445,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     auto load_beta = [&](const PrepItem& it) {
         uint16_t raw = 0;
         if (tid < C && it.valid && tid < it.L)
-            raw = __ldg(beta + (size_t)(it.c0 + tid) * heads + it.h);
+            raw = __ldg(beta + (size_t)(it.c0 + tid) * maps.b_stride + it.h);
         return raw;
     };
 
@@ -438,6 +466,15 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     PrepItem cur = prep_item(item, heads, map_cu, map_off, n_seqs, t, t_pad);
     load_raw(cur, 0);
     uint16_t beta_cur = load_beta(cur);
+    // gated calls: dt_bias of this thread's channel (tid & 127 in the Gamma
+    // phase) and a_log of the item's head, loaded one item ahead
+    auto load_gate = [&](const PrepItem& it) {
+        float2 r = make_float2(0.f, 0.f);
+        if (GATED && it.valid)
+            r = make_float2(__ldg(maps.dt_bias + it.h * D + (tid & 127)), __ldg(maps.a_log + it.h));
+        return r;
+    };
+    float2 gate_cur = load_gate(cur);
 
     for (int iter = 0; item < items; ++iter) {
         const int b = iter & 1;
@@ -445,6 +482,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         PrepItem nxt = {};
         nxt.valid = false;
         uint16_t beta_nxt = 0;
+        float2 gate_nxt = make_float2(0.f, 0.f);
         // The next item is resolved (global loads) while the first A/P product
         // runs, and its raw tiles go to the other buffer, which the previous
         // iteration's closing barrier released.
@@ -452,6 +490,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             if (nitem < items) nxt = prep_item(nitem, heads, map_cu, map_off, n_seqs, t, t_pad);
             load_raw(nxt, b ^ 1);
             beta_nxt = load_beta(nxt);
+            gate_nxt = load_gate(nxt);
         };
 
         if (!cur.valid) {
@@ -469,7 +508,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             float* TM = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_TM);
             unsigned char* blob = ws + blob_offset(n_seqs, cur.g, h, heads);
 
-            if (tid < C) BETA[tid] = bf(beta_cur);
+            if (tid < C) BETA[tid] = GATED ? sigmoid_hw(bf(beta_cur)) : bf(beta_cur);
             if (!tc::mbar_wait(bar_tma + b, ph_tma[b])) {
                 atomicOr(&g_tc_status, STATUS_TIMEOUT);
                 failed = true;
@@ -484,12 +523,20 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             float* GH = reinterpret_cast<float*>(sm + (b ^ 1) * RAW_BUF);  // [3][128]
             {
                 const int i = tid & 127, qt = tid >> 7;
+                // gated: -exp(a_log[h]) log2 e, the exponent's factor of this head
+                const float nc = -ex2_approx(gate_cur.y * kLog2e) * kLog2e;
                 float acc[16];
+                if constexpr (GATED) {  // all 16 rows at once (independent), then masked
+#pragma unroll
+                    for (int rr = 0; rr < 16; ++rr)
+                        acc[rr] = gate_hw(raw1(RAWG, 16 * qt + rr, i), gate_cur.x, nc, maps.lb);
+                }
                 float run = 0.f, gmin = 0.f;
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
                     const int r = 16 * qt + rr;
-                    const float gv = (r < L) ? raw1(RAWG, r, i) : 0.f;
+                    float gv = 0.f;
+                    if (r < L) gv = GATED ? acc[rr] : raw1(RAWG, r, i);
                     gmin = fminf(gmin, gv);
                     run = __fadd_rn(run, gv);
                     acc[rr] = run;
@@ -889,6 +936,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         item = nitem;
         cur = nxt;
         beta_cur = beta_nxt;
+        gate_cur = gate_nxt;
     }
     release_pending();
     if (copier) tc::bulk_wait_all();
@@ -900,13 +948,15 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     }
 }
 
+template <bool GATED>
 __global__ void __launch_bounds__(NTP, 1)
 prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict__ beta, int t,
                int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
                unsigned char* __restrict__ ws) {
     pdl_wait();  // the chunk map (and the callers' inputs) are complete
     pdl_release();
-    prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x, nullptr, 0);
+    prepare_role<GATED>(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x,
+                        nullptr, 0);
 }
 
 // ------------------------------------------------------------ transposed scan
@@ -1291,6 +1341,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
 // (cooperative launch), so every wait on a flag ends.
 static_assert(ScanT::NT == NTP, "the two roles share the block size");
 static_assert(ScanT::TOTAL <= PS_TOTAL, "the two roles share the shared-memory size");
+template <bool GATED>
 __global__ void __launch_bounds__(NTP, 1)
 prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap omap, const uint16_t* __restrict__ beta, float* __restrict__ state,
@@ -1302,8 +1353,9 @@ prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constan
         scan_t_role(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
                     (int)blockIdx.x / heads, ready, ready_pitch);
     else
-        prepare_role(maps, beta, t, t_pad, heads, cu, n_seqs, ws, (long long)blockIdx.x - chains,
-                     (long long)gridDim.x - chains, ready, ready_pitch);
+        prepare_role<GATED>(maps, beta, t, t_pad, heads, cu, n_seqs, ws,
+                            (long long)blockIdx.x - chains, (long long)gridDim.x - chains, ready,
+                            ready_pitch);
 }
 
 // The chains of the two-kernel path: one CTA per (sequence, head), after
@@ -1353,7 +1405,7 @@ constexpr double kPrepItemUs = 8.3, kScanTChunkUs = 2.3;
 kda_status launch_prefill_tc(float* state, const void* q, const void* k, const void* v,
                              const void* g, const void* beta, float* o, int t, int t_pad,
                              int heads, long long stride, const int* cu, int n_seqs,
-                             void* workspace, cudaStream_t s) {
+                             void* workspace, cudaStream_t s, const PrefillGate* gate) {
     const uint64_t rows = cu ? (uint64_t)t : (uint64_t)t_pad * n_seqs;
     const int sms = sm_count();
     if (sms <= 0) {
@@ -1378,22 +1430,29 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     PrepMaps maps;
     CUtensorMap vmap, omap;
     const uint64_t hd = (uint64_t)heads * D;
+    maps.dt_bias = gate ? gate->dt_bias : nullptr;
+    maps.a_log = gate ? gate->a_log : nullptr;
+    maps.lb = gate ? gate->lb : 0.f;
+    maps.b_stride = gate ? gate->b_stride : heads;
+    const uint64_t g_pitch = gate ? (uint64_t)gate->g_stride : hd;
     if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&maps.g, g, hd, rows, hd, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&maps.g, g, hd, rows, g_pitch, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&vmap, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !tma_map_f32(&omap, o, hd, rows, hd, D, (uint32_t)C)) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
-    cudaError_t e = cudaFuncSetAttribute(prepare_kernel,
+    auto* prep_k = gate ? prepare_kernel<true> : prepare_kernel<false>;
+    auto* fused_k = gate ? prefill_fused_kernel<true> : prefill_fused_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute(prep_k,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PS_TOTAL);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(scan_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)ScanT::TOTAL);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(prefill_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(fused_k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)PS_TOTAL);
     if (e != cudaSuccess) {
         set_error("kda_prefill: cannot reserve shared memory: %s", cudaGetErrorString(e));
@@ -1418,7 +1477,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, prefill_fused_kernel, maps, vmap, omap, (const uint16_t*)beta,
+        e = cudaLaunchKernelEx(&cfg, fused_k, maps, vmap, omap, (const uint16_t*)beta,
                                state, o, t, t_pad, heads, cu, n_seqs, ws, ready,
                                ready_pitch(chunk_bound));
         if (e == cudaSuccess) return launch_result("kda_prefill (fused)");
@@ -1430,7 +1489,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     // never more CTAs than (chunk, head) items.
     const long long items = (((long long)rows + C - 1) / C + n_seqs) * heads;
     const unsigned grid = (unsigned)(items < sms ? items : sms);
-    launch_pdl(prepare_kernel, dim3(grid), dim3(NTP), PS_TOTAL, s, maps, (const uint16_t*)beta, t,
+    launch_pdl(prep_k, dim3(grid), dim3(NTP), PS_TOTAL, s, maps, (const uint16_t*)beta, t,
                t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;

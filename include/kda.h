@@ -163,6 +163,43 @@ size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads
                                   int in_dtype);
 
 /*
+ * kda_prefill_gated -- kda_prefill on the tensor-core path (BF16 q, k, v;
+ * chunk 64) with the forget gate and beta formed inside the prepare kernel
+ * from their raw inputs: the block pipeline's "kda_gate / sigmoid(b_proj)"
+ * step fused into the core's g and beta loads (glm5next_kda module index;
+ * Glm5NextKdaWeights dt_bias and a_log; config.rs gate_lower_bound).  Each
+ * g element is read once, as BF16, and becomes
+ *     g[r][h][i] = lb * sigmoid(exp(a_log[h]) * (g_raw[r][h*128 + i] + dt_bias[h*128 + i]))
+ *     beta[r][h] = sigmoid(b_raw[r][h])
+ * in FP32 (the hardware 2^x and 1/x; the same operations, in the same order,
+ * as kda_gate's FP32 output), never stored.  The pages give the gate's inputs
+ * and its bound, not this formula: it is the reading kda_gate states.
+ *
+ *   state, q, k, v, o, t, t_pad, heads, head_dim, qkv_row_stride,
+ *   cu_seqlens, n_seqs : as kda_prefill (q, k, v BF16); in the uniform form
+ *           rows [t, t_pad) are not written to (no pad fill) and never read
+ *           into arithmetic
+ *   g_raw : BF16, token row r at g_raw + r * g_raw_stride, head h's channels
+ *           at + h*128 (g_raw_stride >= heads*128, a multiple of 8)
+ *   dt_bias : FP32 [heads*128]      a_log : FP32 [heads]
+ *   gate_lower_bound : finite and negative
+ *   b_raw : BF16, token row r at b_raw + r * b_stride (b_stride >= heads)
+ *   workspace : at least kda_prefill_workspace_size(rows, n_seqs, 64, heads,
+ *           128, KDA_BF16) bytes, 16-byte aligned (never NULL)
+ * Refused (nothing launched): null pointers, misaligned state/q/k/v/g_raw/o,
+ * head_dim != 128, strides out of range, a gate_lower_bound that is not
+ * finite and negative, too small a workspace.  Device-side cu_seqlens checks
+ * and KDA_PREFILL_IMPL=unfused are as for kda_prefill.
+ */
+kda_status kda_prefill_gated(float* state, const void* q, const void* k, const void* v,
+                             const uint16_t* g_raw, int64_t g_raw_stride, const float* dt_bias,
+                             const float* a_log, float gate_lower_bound, const uint16_t* b_raw,
+                             int64_t b_stride, float* o, int t, int t_pad, int heads,
+                             int head_dim, int64_t qkv_row_stride, const int* cu_seqlens,
+                             int n_seqs, void* workspace, size_t workspace_bytes,
+                             uint64_t stream);
+
+/*
  * kda_conv_silu_l2 -- depthwise causal conv1d + SiLU, then L2 over the q and k
  * channels (block pipeline "conv1d + SiLU -> L2(q,k only)";
  * causal_conv1d_update_l2norm at decode, conv_prefill + l2_norm_bf16 at

@@ -166,3 +166,32 @@ def frontend(seed: int = 0, n_seqs: int = 16, lo: int = 512, hi: int = 8192,
         "chunk": 64, "conv_kernel": conv_kernel, "l2_eps": 1e-6,
     }
 
+
+
+def gate_inputs(gen: torch.Generator, rows: int, heads: int, g_pitch_extra: int = 0,
+                b_pitch_extra: int = 0) -> dict:
+    """Raw inputs of the forget gate and beta: the gate projection g_raw BF16
+    [rows, H*D + g_pitch_extra] ~N(0, 1), dt_bias FP32 [H*D] ~N(0, 0.25),
+    a_log FP32 [H] ~N(0, 0.25), the b_proj output b_raw BF16
+    [rows, H + b_pitch_extra] ~N(0, 1), and gate_lower_bound -5."""
+    g_raw = torch.randn((rows, heads * HEAD_DIM + g_pitch_extra), generator=gen,
+                        dtype=torch.float32).to(torch.bfloat16)
+    dt_bias = torch.randn(heads * HEAD_DIM, generator=gen, dtype=torch.float32) * 0.5
+    a_log = torch.randn(heads, generator=gen, dtype=torch.float32) * 0.5
+    b_raw = torch.randn((rows, heads + b_pitch_extra), generator=gen,
+                        dtype=torch.float32).to(torch.bfloat16)
+    return {"g_raw": g_raw, "dt_bias": dt_bias, "a_log": a_log, "b_raw": b_raw,
+            "gate_lower_bound": -5.0}
+
+
+def prefill_gated(seed: int = 0, t: int = 8192, heads: int = 32, g_pitch_extra: int = 0,
+                  b_pitch_extra: int = 0, state_std: float = 0.02) -> dict:
+    """The prefill workload with raw gate inputs in place of g and beta: q, k,
+    v BF16 [t, H, D] as in prefill(), then the gate_inputs() draws, then the
+    state."""
+    gen = _gen(seed)
+    d = core_inputs(gen, (t,), heads, torch.bfloat16)
+    del d["g"], d["beta"]
+    d.update(gate_inputs(gen, t, heads, g_pitch_extra, b_pitch_extra))
+    d["state"] = state(gen, (1,), heads, state_std)
+    return d

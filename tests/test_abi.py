@@ -167,6 +167,29 @@ def test_gate_refuses_bad_arguments(lib):
     assert b"kda_gate" in lib.kda_last_error()
 
 
+def test_prefill_gated_refuses_bad_arguments(lib):
+    f = lib.kda_prefill_gated
+    f.argtypes = [V] * 5 + [ctypes.c_int64, V, V, F, V, ctypes.c_int64, V, I, I, I, I,
+                            ctypes.c_int64, V, I, V, ctypes.c_size_t, U64]
+    big = 1 << 40
+    ok = (P, P, P, P, P, 512, P, P, -5.0, P, 4, P, 100, 128, 4, 128, 512, None, 1, P, big, 0)
+    names = ("S", "q", "k", "v", "g", "gs", "dt", "al", "lb", "b", "bs", "o", "t", "tp", "h",
+             "hd", "st", "cu", "n", "ws", "wsb", "s")
+    bad = lambda **kw: f(*[kw.get(k, v) for k, v in zip(names, ok)])
+    assert bad(hd=64) == 2                                   # head_dim
+    assert bad(t=0) == 1 and bad(tp=99) == 1                 # 1 <= t <= t_pad
+    assert bad(cu=P) == 1                                    # packed rows take no padding
+    assert bad(h=0) == 1 and bad(n=0) == 1                   # heads, sequences
+    assert bad(st=500) == 1 and bad(st=516) == 1             # q/k/v pitch
+    assert bad(gs=500) == 1 and bad(gs=516) == 1             # g_raw pitch
+    assert bad(bs=3) == 1                                    # b_raw pitch below heads
+    assert bad(lb=0.0) == 1 and bad(lb=float("-inf")) == 1   # the bound: finite, negative
+    assert bad(dt=None) == 1 and bad(b=None) == 1            # null pointers
+    assert bad(g=ctypes.c_void_p(P.value + 2)) == 1          # g_raw alignment
+    assert bad(wsb=1024) == 3 and bad(ws=None) == 3          # workspace too small / missing
+    assert b"kda_prefill_gated" in lib.kda_last_error()
+
+
 def test_conv_k_refuses_bad_arguments(lib):
     f = lib.kda_conv_silu_l2_k
     f.argtypes = [V] * 4 + [I, I, I, F, I, I, V, I, U64]
