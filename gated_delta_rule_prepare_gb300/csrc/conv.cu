@@ -347,10 +347,15 @@ __global__ void conv_state_kernel(float* __restrict__ conv_state, const uint16_t
 // order and writes the outputs, snapshot t (the window ending at row t) and
 // the new state.  A state row is read and rewritten by the thread that owns
 // it, so this one launch replaces the conv and state-rewrite pair.
+// With K = 4 a warp's 32 threads own 256 consecutive channels, whose windows
+// are one contiguous 4 KB span of a state array: each window goes out through
+// a per-warp shared-memory tile (XOR-swizzled by 16-byte chunk, so neither
+// side conflicts on banks) as eight 512-byte warp stores, instead of eight
+// 16-byte stores per thread that each touch 32 different lines.
 constexpr int kRowsThreads = 256;
 
 template <int K>
-__global__ void __launch_bounds__(kRowsThreads)
+__global__ void __launch_bounds__(kRowsThreads, 2)
 conv_rows_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
                  const uint16_t* __restrict__ w, uint16_t* __restrict__ out, int rows, int n_seqs,
                  int heads, float l2_eps, ConvSnaps snaps, int n_snap) {
@@ -358,9 +363,14 @@ conv_rows_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
     pdl_release();
     const int conv_dim = 3 * heads * D;
     const int per_seq = conv_dim / kCh;  // threads per sequence, a multiple of 16
-    const long long idx = (long long)blockIdx.x * kRowsThreads + threadIdx.x;
-    // n_seqs * per_seq is a multiple of 16: a half-warp is wholly in or out
-    if (idx >= (long long)n_seqs * per_seq) return;
+    const long long total = (long long)n_seqs * per_seq;
+    const long long idx0 = (long long)blockIdx.x * kRowsThreads + threadIdx.x;
+    // total is a multiple of 16: a half-warp is wholly in or out.  With K = 4
+    // the idle half of the last warp stays (its windows are staged but not
+    // stored) so that the warp's tile copies keep all 32 lanes.
+    if (idx0 >= total && (K != 4 || (idx0 & ~31LL) >= total)) return;
+    const bool live = idx0 < total;
+    const long long idx = live ? idx0 : total - 1;  // idle lanes compute on a valid copy
     const int n = (int)(idx / per_seq);
     const int c = (int)(idx % per_seq) * kCh;
     const bool normalise = c < 2 * heads * D;
@@ -411,16 +421,32 @@ conv_rows_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
                 win[j][e] = make_float2(__ldg(st + (2 * e) * K + j + 1),
                                         __ldg(st + (2 * e + 1) * K + j + 1));
     }
-    // window of K slots of 8 channels to a [channel][slot] state row
-    auto store_window = [&](float* dst) {
+    // window of K slots of 8 channels to a [channel][slot] state row; `base`
+    // is the state array (state, or a snapshot), dst this thread's rows in it
+    __shared__ float4 tile[kRowsThreads / 32][256];  // K = 4: one 4 KB tile per warp
+    const int lane = threadIdx.x & 31;
+    float4* wt = tile[threadIdx.x >> 5];
+    auto store_window = [&](float* base, float* dst) {
         if constexpr (K == 4) {
+            // channel 8 lane + e of the warp -> chunk 8 lane + (e ^ (lane & 7))
 #pragma unroll
             for (int e = 0; e < kCh / 2; ++e) {
-                reinterpret_cast<float4*>(dst)[2 * e] =
+                wt[8 * lane + ((2 * e) ^ (lane & 7))] =
                     make_float4(win[0][e].x, win[1][e].x, win[2][e].x, win[3][e].x);
-                reinterpret_cast<float4*>(dst)[2 * e + 1] =
+                wt[8 * lane + ((2 * e + 1) ^ (lane & 7))] =
                     make_float4(win[0][e].y, win[1][e].y, win[2][e].y, win[3][e].y);
             }
+            __syncwarp();
+            // the warp's 256 channels start at its first thread's channel
+            const long long wfirst = idx0 - lane;
+            float4* wdst = reinterpret_cast<float4*>(base) + wfirst * kCh;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int L = 32 * k + lane, tq = L >> 3;  // channel L belongs to lane tq
+                if (wfirst + tq < total) wdst[L] = wt[8 * tq + ((L & 7) ^ (tq & 7))];
+            }
+            __syncwarp();  // the tile is read before the next window overwrites it
+            (void)dst;
         } else {
 #pragma unroll
             for (int j = 0; j < K; ++j)
@@ -451,9 +477,9 @@ conv_rows_kernel(float* __restrict__ conv_state, const uint16_t* __restrict__ x,
             for (int j = 1; j < K; ++j) a[e] = fma2(wv[j][e], win[j][e], a[e]);
         }
         const uint4 o = silu_l2_bf16(a, normalise, hmask, l2_eps);
-        *reinterpret_cast<uint4*>(out + (row0 + r) * conv_dim + c) = o;
-        if (r < n_snap) store_window(snaps.p[r] + ((size_t)n * conv_dim + c) * K);
-        if (r + 1 == rows) store_window(st);
+        if (live) *reinterpret_cast<uint4*>(out + (row0 + r) * conv_dim + c) = o;
+        if (r < n_snap) store_window(snaps.p[r], snaps.p[r] + ((size_t)n * conv_dim + c) * K);
+        if (r + 1 == rows) store_window(conv_state, st);
 #pragma unroll
         for (int j = 0; j + 1 < K; ++j)
 #pragma unroll
