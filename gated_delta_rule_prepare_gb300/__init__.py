@@ -7,8 +7,9 @@ library's CUDA kernels; there is no fallback.  Importing this package on a
 machine without the built library raises immediately.
 
 Entry points (same names as the C ABI): ``kda_decode``, ``kda_decode_k``,
-``kda_prefill``, ``kda_conv_silu_l2``, ``kda_conv_silu_l2_k``, ``kda_gate``, ``kda_o_norm_gated``,
-``kda_prefill_workspace_size``, ``kda_sync_status``.
+``kda_prefill``, ``kda_prefill_gated``, ``kda_conv_silu_l2``, ``kda_conv_silu_l2_k``,
+``kda_gate``, ``kda_o_norm_gated``, ``kda_prefill_workspace_size``, ``kda_sync_status``.
+``kda_prefill_static_ws`` is reached through ``LIB`` (its callers hold raw pointers).
 """
 
 from __future__ import annotations
