@@ -891,27 +891,50 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 }
             }
             __syncthreads();
+            // The off-diagonal blocks in three steps instead of three levels of
+            // 16, 32 and 48 products: every block's c = b term needs only the
+            // diagonal blocks, so all six run at once, then the c = b + 1 terms
+            // of the blocks two and three below the diagonal, then the last
+            // term of the corner block.  Thread (block, row rr, columns 4 cq ..)
+            // keeps its sum across the steps, adding the terms in the order
+            // of c, as a single sum over c would.
+            {
+                const int blk = tid >> 6, rr = (tid >> 2) & 15, cq = tid & 3;
+                // blocks 0..2: (a, b) = (b + 1, b); 3, 4: (b + 2, b); 5: (3, 0)
+                const int dd = blk < 3 ? 1 : (blk < 5 ? 2 : 3);
+                const int bq = blk < 3 ? blk : (blk < 5 ? blk - 3 : 0);
+                const int a = bq + dd;
+                const bool act = tid < 6 * 64;
+                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+                auto term = [&](int c) {  // x += W_ac T_cb over this thread's row and columns
 #pragma unroll
-            for (int d = 1; d < 4; ++d) {
-                if (tid < (4 - d) * 64) {
-                    const int bq = tid >> 6, a = bq + d, rr = (tid >> 2) & 15, cq = tid & 3;
-                    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                    for (int cd = 0; cd < d; ++cd) {
-                        const int c = bq + cd;
-#pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
-                            const float wv = AM[(16 * a + rr) * AP + 16 * c + kk];
-                            const float4 t4 = *reinterpret_cast<const float4*>(
-                                TM + (16 * c + kk) * TPP + 16 * bq + 4 * cq);
-                            x.x = __fmaf_rn(wv, t4.x, x.x);
-                            x.y = __fmaf_rn(wv, t4.y, x.y);
-                            x.z = __fmaf_rn(wv, t4.z, x.z);
-                            x.w = __fmaf_rn(wv, t4.w, x.w);
-                        }
+                    for (int kk = 0; kk < 16; ++kk) {
+                        const float wv = AM[(16 * a + rr) * AP + 16 * c + kk];
+                        const float4 t4 = *reinterpret_cast<const float4*>(
+                            TM + (16 * c + kk) * TPP + 16 * bq + 4 * cq);
+                        x.x = __fmaf_rn(wv, t4.x, x.x);
+                        x.y = __fmaf_rn(wv, t4.y, x.y);
+                        x.z = __fmaf_rn(wv, t4.z, x.z);
+                        x.w = __fmaf_rn(wv, t4.w, x.w);
                     }
+                };
+                auto put = [&]() {
                     *reinterpret_cast<float4*>(TM + (16 * a + rr) * TPP + 16 * bq + 4 * cq) =
                         make_float4(-x.x, -x.y, -x.z, -x.w);
+                };
+                if (act) {
+                    term(bq);
+                    if (dd == 1) put();
+                }
+                __syncthreads();
+                if (act && dd >= 2) {
+                    term(bq + 1);
+                    if (dd == 2) put();
+                }
+                __syncthreads();
+                if (act && dd == 3) {
+                    term(bq + 2);
+                    put();
                 }
                 __syncthreads();
             }
