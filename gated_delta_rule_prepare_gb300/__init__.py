@@ -240,9 +240,12 @@ def kda_prefill_gated(state, q, k, v, g_raw, dt_bias, a_log, b_raw, o, t, gate_l
     if state.numel() != n_seqs * H * HEAD_DIM * HEAD_DIM or state.dtype != torch.float32:
         raise ValueError("kda_prefill_gated: state must be FP32 [N, H, 128, 128]")
     if workspace is None:
+        need = kda_prefill_workspace_size(rows, n_seqs, 64, H, b16)
+        if need == 0:  # KDA_PREFILL_IMPL=simt makes the size query answer for the SIMT kernel
+            raise KdaError(3, "kda_prefill_gated runs only on the tensor-core "
+                           "kernels: unset KDA_PREFILL_IMPL=simt or pass a workspace")
         # allocated here, outside the library (which never allocates)
-        workspace = torch.empty(kda_prefill_workspace_size(rows, n_seqs, 64, H, b16),
-                                dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(LIB.kda_prefill_gated(
         _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(g_raw, b16, "g_raw"), int(g_raw.stride(0)),
         _ptr(dt_bias, torch.float32, "dt_bias"), _ptr(a_log, torch.float32, "a_log"),

@@ -189,7 +189,10 @@ size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads
  * Refused (nothing launched): null pointers, misaligned state/q/k/v/g_raw/o,
  * head_dim != 128, strides out of range, a gate_lower_bound that is not
  * finite and negative, too small a workspace.  Device-side cu_seqlens checks
- * and KDA_PREFILL_IMPL=unfused are as for kda_prefill.
+ * and KDA_PREFILL_IMPL=unfused are as for kda_prefill; KDA_PREFILL_IMPL=simt
+ * does not apply (this call has no SIMT form), and while it is set
+ * kda_prefill_workspace_size answers 0 for the SIMT kernel, so size the
+ * workspace without it.
  */
 kda_status kda_prefill_gated(float* state, const void* q, const void* k, const void* v,
                              const uint16_t* g_raw, int64_t g_raw_stride, const float* dt_bias,
