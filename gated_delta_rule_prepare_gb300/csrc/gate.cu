@@ -1,9 +1,9 @@
 // Forget gate and beta of the KDA core: the block pipeline's
 // "kda_gate / sigmoid(b_proj)" step (glm5next_kda module index), from the
 // forget-gate projection g_raw = f_b(f_a(h)) [T, heads * head_dim] BF16 and
-// the b_proj output [T, heads] BF16 to the core's inputs gate
-// [T, heads, head_dim] ("bounded log-decay from kda_gate") and beta
-// [T, heads] ("already sigmoided") of Glm5NextKdaWorkspace, with the
+// the b_proj output [T, heads] BF16 to the core's inputs of
+// Glm5NextKdaWorkspace: gate [T, heads, head_dim], a log-decay bounded below,
+// and beta [T, heads], the b_proj output after a sigmoid, with the
 // Glm5NextKdaWeights parameters dt_bias [heads * head_dim] (one per channel)
 // and a_log [heads] (one per head) and config.rs gate_lower_bound.  The pages
 // give these inputs and the bound, not the formula; the reading taken:

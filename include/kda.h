@@ -237,9 +237,10 @@ kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, const uint16_t
 /*
  * kda_gate -- the forget gate and beta of the core, the block pipeline's step
  * before it ("kda_gate / sigmoid(b_proj)", glm5next_kda module index;
- * Glm5NextKdaWorkspace g_raw [T, qkv] "the forget-gate projection kda_gate
- * consumes", gate [T_pad, heads, head_dim] "bounded log-decay from kda_gate",
- * beta [T_pad, heads] "already sigmoided"; Glm5NextKdaWeights dt_bias
+ * Glm5NextKdaWorkspace g_raw [T, qkv], the forget-gate projection that
+ * kda_gate reads, gate [T_pad, heads, head_dim], the log-decay it produces,
+ * bounded below, and beta [T_pad, heads], stored after its sigmoid;
+ * Glm5NextKdaWeights dt_bias
  * [heads * head_dim] F32 one per channel, a_log [heads] F32 one per head;
  * config.rs gate_lower_bound).  The pages give these inputs and that the
  * decay is bounded below by gate_lower_bound, not the formula; this library's

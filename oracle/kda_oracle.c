@@ -10,8 +10,8 @@
  * ("glm5next_kda" module index: the block pipeline and its invariants;
  * Glm5NextKdaLayer: decode / decode_k / prefill_with_pad_fill;
  * Glm5NextKdaKernels: chunk_prepare, chunk_scan, recurrent; config.rs:
- * recurrent_state_elems "FP32 [heads, head_dim, head_dim] K-major",
- * conv_state_elems, and the L2 epsilon "1/sqrt(sum + eps)").
+ * recurrent_state_elems, an FP32 [heads, head_dim, head_dim] state laid out
+ * K-major, conv_state_elems, and the L2 epsilon added under the square root).
  *
  * Notation.  D = head_dim, H = heads.  The state of one head is S[i][j], i the
  * key channel (row), j the value channel (column): "K-major" read as the key
@@ -81,7 +81,7 @@ static void token_step(int D, double scale, const double* q, const double* k,
  *   S          : [N][H][D][D]      in place (state before -> after token T-1)
  *   o          : [N][T][H][D]
  *   snaps      : NULL, or [T][N][H][D][D]: the state after token t
- *                (decode_k's "snapshots[t] receives the state after row t").
+ *                (decode_k's snapshot t holds the state once row t is applied).
  * Single-token decode is T = 1; decode_k is T = k; a prefill is N = 1.
  */
 void kda_oracle_recurrent(int N, int T, int H, int D, double scale, const double* q,
@@ -311,9 +311,9 @@ void kda_oracle_o_norm_gated(long rows, int H, int D, double eps, const double* 
 /*
  * Forget gate and beta of the core (module index, block pipeline:
  * "kda_gate / sigmoid(b_proj)"; Glm5NextKdaWorkspace: gate [T_pad, heads,
- * head_dim] FP32 "bounded log-decay from kda_gate", g_raw [T, qkv] the
- * forget-gate projection kda_gate consumes, beta [T_pad, heads] "already
- * sigmoided"; Glm5NextKdaWeights: dt_bias [heads * head_dim] one value per
+ * head_dim] FP32, the log-decay kda_gate produces, g_raw [T, qkv] the
+ * forget-gate projection kda_gate reads, beta [T_pad, heads] stored after its
+ * sigmoid; Glm5NextKdaWeights: dt_bias [heads * head_dim] one value per
  * channel, a_log [heads] one value per head; config.rs: gate_lower_bound).
  * The pages give the gate's inputs and that its result is a log-decay bounded
  * below by gate_lower_bound, not its formula (parity unpinned).  The reading
