@@ -86,6 +86,10 @@ struct Op {
     static __device__ __forceinline__ uint64_t desc(uint32_t base, int ks) {
         return tc::make_desc(base + (uint32_t)ks * 2u * LBO, LBO, 128u);
     }
+    // Descriptor increment of one MMA K-step (two K groups): the start address
+    // field holds the byte address / 16 in its low 14 bits, and every operand
+    // lies below 228 KB, so adding this never carries out of the field.
+    static constexpr uint64_t KSTEP = (2u * LBO) >> 4;
     static __host__ __device__ constexpr uint32_t bytes(int K) { return (uint32_t)(K / KG) * LBO; }
 };
 // prepare's A/P products (TF32: their decay factors reach e^(+-8 |g|))
@@ -214,19 +218,17 @@ __device__ __forceinline__ float gate_hw(float x, float dt, float nc, float lb) 
     return __fmul_rn(lb, rcp_approx(__fadd_rn(ex2_approx(__fmul_rn(__fadd_rn(x, dt), nc)), 1.0f)));
 }
 
-// D = A . B^T over `ksteps` TF32 K-steps of 8, issued by the calling thread.
-template <class OA, class OB>
-__device__ __forceinline__ void issue_mma(uint32_t d, uint32_t a, uint32_t b, int ksteps,
-                                          uint32_t idesc) {
-    for (int ks = 0; ks < ksteps; ++ks)
-        tc::mma_tf32(d, OA::desc(a, ks), OB::desc(b, ks), idesc, ks > 0);
-}
-// The same over FP16 K-steps of 16.
-template <class OA, class OB>
-__device__ __forceinline__ void issue_mma16(uint32_t d, uint32_t a, uint32_t b, int ksteps,
-                                            uint32_t idesc) {
-    for (int ks = 0; ks < ksteps; ++ks)
-        tc::mma_f16(d, OA::desc(a, ks), OB::desc(b, ks), idesc, ks > 0);
+// D = A . B^T over KS TF32 K-steps of 8, issued by the calling thread.  The
+// loop is unrolled and each K-step's descriptors are the first ones plus a
+// constant: a single issuing thread otherwise spends tens of cycles per
+// instruction rebuilding descriptors, against about 44 cycles per small-N
+// instruction of the tensor core itself.
+template <class OA, class OB, int KS>
+__device__ __forceinline__ void issue_mma(uint32_t d, uint32_t a, uint32_t b, uint32_t idesc) {
+    const uint64_t ad = OA::desc(a, 0), bd = OB::desc(b, 0);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks)
+        tc::mma_tf32(d, ad + ks * OA::KSTEP, bd + ks * OB::KSTEP, idesc, ks > 0);
 }
 
 // Token range [start, end) of sequence n; false when cu_seqlens is malformed.
@@ -441,12 +443,17 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         }
     };
     // beta of item `it` (threads 0..63): the raw BF16 bits, widened only
-    // when the item starts, so nothing waits on the load before then
+    // when the item starts.  Every thread loads from a valid address (the
+    // tensor's first element where the row is not part of the item) and the
+    // mask is applied at that point, so no select waits on the load before
+    // then.  The loaded bits and the mask are packed into one word.
     auto load_beta = [&](const PrepItem& it) {
-        uint16_t raw = 0;
-        if (tid < C && it.valid && tid < it.L)
-            raw = __ldg(beta + (size_t)(it.c0 + tid) * maps.b_stride + it.h);
-        return raw;
+        const bool live = tid < C && it.valid && tid < it.L;
+        const uint16_t* src = live ? beta + (size_t)(it.c0 + tid) * maps.b_stride + it.h : beta;
+        return (uint32_t)__ldg(src) | (live ? 0x10000u : 0u);
+    };
+    auto beta_of = [&](uint32_t w) {
+        return (w & 0x10000u) ? (GATED ? sigmoid_hw(bf((uint16_t)w)) : bf((uint16_t)w)) : 0.f;
     };
 
     // The item whose ready flag is still to be released (copier thread): an
@@ -465,13 +472,15 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     long long item = first;
     PrepItem cur = prep_item(item, heads, map_cu, map_off, n_seqs, t, t_pad);
     load_raw(cur, 0);
-    uint16_t beta_cur = load_beta(cur);
+    uint32_t beta_cur = load_beta(cur);
     // gated calls: dt_bias of this thread's channel (tid & 127 in the Gamma
     // phase) and a_log of the item's head, loaded one item ahead
     auto load_gate = [&](const PrepItem& it) {
         float2 r = make_float2(0.f, 0.f);
-        if (GATED && it.valid)
-            r = make_float2(__ldg(maps.dt_bias + it.h * D + (tid & 127)), __ldg(maps.a_log + it.h));
+        if (GATED) {  // head 0's parameters stand in for an invalid item (never used)
+            const int hh = it.valid ? it.h : 0;
+            r = make_float2(__ldg(maps.dt_bias + hh * D + (tid & 127)), __ldg(maps.a_log + hh));
+        }
         return r;
     };
     float2 gate_cur = load_gate(cur);
@@ -481,7 +490,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         const long long nitem = item + stride;
         PrepItem nxt = {};
         nxt.valid = false;
-        uint16_t beta_nxt = 0;
+        uint32_t beta_nxt = 0;
         float2 gate_nxt = make_float2(0.f, 0.f);
         // The next item is resolved (global loads) while the first A/P product
         // runs, and its raw tiles go to the other buffer, which the previous
@@ -508,7 +517,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             float* TM = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_TM);
             unsigned char* blob = ws + blob_offset(n_seqs, cur.g, h, heads);
 
-            if (tid < C) BETA[tid] = GATED ? sigmoid_hw(bf(beta_cur)) : bf(beta_cur);
+            if (tid < C) BETA[tid] = beta_of(beta_cur);
             if (!tc::mbar_wait(bar_tma + b, ph_tma[b])) {
                 atomicOr(&g_tc_status, STATUS_TIMEOUT);
                 failed = true;
@@ -708,9 +717,9 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 sync_for_mma();
                 if (tid == 0) {
                     tc::tc_fence_after();
-                    issue_mma<OpX, OpY32>(tmem + TC_AP, s_opx, s_y, 16, tc::idesc_tf32(128, 32));
-                    issue_mma<OpX1, OpY32>(tmem + TC_AP + 32, tc::smem_u32(x1buf),
-                                           s_y + OpY32::bytes(128), 16, tc::idesc_tf32(128, 32));
+                    issue_mma<OpX, OpY32, 16>(tmem + TC_AP, s_opx, s_y, tc::idesc_tf32(128, 32));
+                    issue_mma<OpX1, OpY32, 16>(tmem + TC_AP + 32, tc::smem_u32(x1buf),
+                                               s_y + OpY32::bytes(128), tc::idesc_tf32(128, 32));
                     tc::mma_commit(bar_mma);
                 }
                 release_pending();
@@ -725,9 +734,9 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                     sync_for_mma();
                     if (tid == 0) {
                         tc::tc_fence_after();
-                        issue_mma<OpX, OpY>(tmem + TC_AP + 16 * bb, s_opx,
-                                            s_y + bb * OpY::bytes(128), 16,
-                                            tc::idesc_tf32(128, 16));
+                        issue_mma<OpX, OpY, 16>(tmem + TC_AP + 16 * bb, s_opx,
+                                                s_y + bb * OpY::bytes(128),
+                                                tc::idesc_tf32(128, 16));
                         tc::mma_commit(bar_mma);
                     }
                     if (bb == 0) {
@@ -829,122 +838,127 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                     }
                 }
             }
-            for (int e = tid; e < 64 * 64; e += NTP) TM[(e >> 6) * TPP + (e & 63)] = 0.f;
             tc::tc_fence_before();
             __syncthreads();
 
             // ------------------------------------------------------ P5 T = (I + A)^-1
-            if (tid < 64) {  // diagonal 16 x 16 blocks T_aa = (I + A_aa)^-1, one column per thread
-                const int a = tid >> 4, cc = tid & 15, o0 = 16 * a;
-                float col[16];
+            // The diagonal 16 x 16 blocks by forward substitution, one column per
+            // thread with the column in registers: after x_s is final, every later
+            // row subtracts A_rs x_s, so each row's terms are added in the order
+            // of s.  Below the diagonal, two levels of block inversion: the
+            // inverse of [[L11, 0], [L21, L22]] has the lower-left block
+            // -L22^-1 L21 L11^-1; first inside the two 32 x 32 diagonal blocks
+            // (16 x 16 pieces), then for the whole matrix (32 x 32 pieces).  The
+            // products' intermediates sit in T's upper right 32 x 32 block, which
+            // the store below replaces by zeros; the two upper 16 x 16 blocks that
+            // the level-2 products read as part of T are zeroed here.
+            if (tid < 64) {
+                const int o0 = 16 * (tid >> 4), cc = tid & 15;
+                float x[16];
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) {
-                    float x = (rr == cc) ? 1.f : 0.f;
+                for (int rr = 0; rr < 16; ++rr) x[rr] = (rr == cc) ? 1.f : 0.f;
 #pragma unroll
-                    for (int ss = 0; ss < rr; ++ss)
-                        x = __fmaf_rn(-AM[(o0 + rr) * AP + o0 + ss], col[ss], x);
-                    col[rr] = (rr < cc) ? 0.f : x;
+                for (int ss = 0; ss < 15; ++ss) {
+#pragma unroll
+                    for (int rr = ss + 1; rr < 16; ++rr)
+                        x[rr] = __fmaf_rn(-AM[(o0 + rr) * AP + o0 + ss], x[ss], x[rr]);
                 }
 #pragma unroll
-                for (int rr = 0; rr < 16; ++rr) TM[(o0 + rr) * TPP + o0 + cc] = col[rr];
+                for (int rr = 0; rr < 16; ++rr) TM[(o0 + rr) * TPP + o0 + cc] = x[rr];
+            } else if (tid < 128) {  // T_01 and T_23 (above the diagonal) are zero
+                const int e = tid - 64, blk = e >> 5, rr = (e >> 1) & 15, hh = e & 1;
+                float* z = TM + (32 * blk + rr) * TPP + 32 * blk + 16 + 8 * hh;
+                *reinterpret_cast<float4*>(z) = make_float4(0.f, 0.f, 0.f, 0.f);
+                *reinterpret_cast<float4*>(z + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             __syncthreads();
-            // Below the diagonal, with W_ac = T_aa A_ac:  T_ab = -sum_{c=b}^{a-1} W_ac T_cb.
-            // Work in 1 x 4 tiles (one row, four consecutive columns) per thread.
-            {
-                constexpr int kWm = (6 * 64 + NTP - 1) / NTP;
-                float4 w[kWm];
+            // Both levels are register-tiled (each thread forms a 2 x 4 block of
+            // outputs from two column loads and one row load per k): the solve
+            // is bound by shared-memory load instructions, one per cycle per SM
+            // whatever their width.  Warps are laid out so that a product's
+            // triangular operand bounds its k range uniformly inside a warp.
+            if (tid < 64) {   // level 1: warp pr forms T_ab, (a, b) = (2 pr + 1, 2 pr)
+                const int pr = tid >> 5, ln = tid & 31;
+                const int r0 = 2 * (ln >> 2), c0 = 4 * (ln & 3);
+                const int ob = 32 * pr, oa = ob + 16;
+                float* mscr = TM + 32 + 16 * pr;  // M = A_ab T_bb in rows 0..15
+                float m[2][4] = {};
 #pragma unroll
-                for (int m = 0; m < kWm; ++m) {
-                    const int e = tid + NTP * m;
-                    w[m] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if (e < 6 * 64) {
-                        const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
-                        const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
-                        const int c = (pb == 0) ? 0 : (pb < 3) ? pb - 1 : pb - 3;
-                        const float* arow = AM + 16 * c + 4 * cq;
-#pragma unroll
-                        for (int kk = 0; kk < 16; ++kk) {
-                            const float tv = TM[(16 * a + rr) * TPP + 16 * a + kk];
-                            const float* ak = arow + (16 * a + kk) * AP;
-                            w[m].x = __fmaf_rn(tv, ak[0], w[m].x);
-                            w[m].y = __fmaf_rn(tv, ak[1], w[m].y);
-                            w[m].z = __fmaf_rn(tv, ak[2], w[m].z);
-                            w[m].w = __fmaf_rn(tv, ak[3], w[m].w);
-                        }
-                    }
+                for (int k = 0; k < 16; ++k) {
+                    const float a0 = AM[(oa + r0) * AP + ob + k], a1 = AM[(oa + r0 + 1) * AP + ob + k];
+                    const float4 tv = *reinterpret_cast<const float4*>(TM + (ob + k) * TPP + ob + c0);
+                    m[0][0] = __fmaf_rn(a0, tv.x, m[0][0]); m[0][1] = __fmaf_rn(a0, tv.y, m[0][1]);
+                    m[0][2] = __fmaf_rn(a0, tv.z, m[0][2]); m[0][3] = __fmaf_rn(a0, tv.w, m[0][3]);
+                    m[1][0] = __fmaf_rn(a1, tv.x, m[1][0]); m[1][1] = __fmaf_rn(a1, tv.y, m[1][1]);
+                    m[1][2] = __fmaf_rn(a1, tv.z, m[1][2]); m[1][3] = __fmaf_rn(a1, tv.w, m[1][3]);
                 }
-                __syncthreads();
+                *reinterpret_cast<float4*>(mscr + r0 * TPP + c0) = make_float4(m[0][0], m[0][1], m[0][2], m[0][3]);
+                *reinterpret_cast<float4*>(mscr + (r0 + 1) * TPP + c0) = make_float4(m[1][0], m[1][1], m[1][2], m[1][3]);
+                __syncwarp();
+                float t[2][4] = {};
 #pragma unroll
-                for (int m = 0; m < kWm; ++m) {
-                    const int e = tid + NTP * m;
-                    if (e < 6 * 64) {
-                        const int pb = e >> 6, rr = (e >> 2) & 15, cq = e & 3;
-                        const int a = (pb == 0) ? 1 : (pb < 3) ? 2 : 3;
-                        const int c = (pb == 0) ? 0 : (pb < 3) ? pb - 1 : pb - 3;
-                        float* dst = AM + (16 * a + rr) * AP + 16 * c + 4 * cq;
-                        dst[0] = w[m].x;
-                        dst[1] = w[m].y;
-                        dst[2] = w[m].z;
-                        dst[3] = w[m].w;
+                for (int k = 0; k < 16; ++k) {
+                    const float a0 = TM[(oa + r0) * TPP + oa + k], a1 = TM[(oa + r0 + 1) * TPP + oa + k];
+                    const float4 mv = *reinterpret_cast<const float4*>(mscr + k * TPP + c0);
+                    t[0][0] = __fmaf_rn(a0, mv.x, t[0][0]); t[0][1] = __fmaf_rn(a0, mv.y, t[0][1]);
+                    t[0][2] = __fmaf_rn(a0, mv.z, t[0][2]); t[0][3] = __fmaf_rn(a0, mv.w, t[0][3]);
+                    t[1][0] = __fmaf_rn(a1, mv.x, t[1][0]); t[1][1] = __fmaf_rn(a1, mv.y, t[1][1]);
+                    t[1][2] = __fmaf_rn(a1, mv.z, t[1][2]); t[1][3] = __fmaf_rn(a1, mv.w, t[1][3]);
+                }
+                *reinterpret_cast<float4*>(TM + (oa + r0) * TPP + ob + c0) =
+                    make_float4(-t[0][0], -t[0][1], -t[0][2], -t[0][3]);
+                *reinterpret_cast<float4*>(TM + (oa + r0 + 1) * TPP + ob + c0) =
+                    make_float4(-t[1][0], -t[1][1], -t[1][2], -t[1][3]);
+            }
+            __syncthreads();
+            if (tid < 128) {  // level 2: rows 32..63, columns 0..31 (four warps)
+                const int w = tid >> 5, ln = tid & 31;
+                {   // M1 = A_[23][01] T_[01][01]: warp w takes columns 8 w .. 8 w + 7, all
+                    // rows; T_[01][01] is lower triangular, so k starts at 8 w
+                    const int r0 = 2 * (ln >> 1), c0 = 8 * w + 4 * (ln & 1);
+                    float m[2][4] = {};
+                    for (int k = 8 * w; k < 32; ++k) {
+                        const float a0 = AM[(32 + r0) * AP + k], a1 = AM[(33 + r0) * AP + k];
+                        const float4 tv = *reinterpret_cast<const float4*>(TM + k * TPP + c0);
+                        m[0][0] = __fmaf_rn(a0, tv.x, m[0][0]); m[0][1] = __fmaf_rn(a0, tv.y, m[0][1]);
+                        m[0][2] = __fmaf_rn(a0, tv.z, m[0][2]); m[0][3] = __fmaf_rn(a0, tv.w, m[0][3]);
+                        m[1][0] = __fmaf_rn(a1, tv.x, m[1][0]); m[1][1] = __fmaf_rn(a1, tv.y, m[1][1]);
+                        m[1][2] = __fmaf_rn(a1, tv.z, m[1][2]); m[1][3] = __fmaf_rn(a1, tv.w, m[1][3]);
                     }
+                    *reinterpret_cast<float4*>(TM + r0 * TPP + 32 + c0) =
+                        make_float4(m[0][0], m[0][1], m[0][2], m[0][3]);
+                    *reinterpret_cast<float4*>(TM + (r0 + 1) * TPP + 32 + c0) =
+                        make_float4(m[1][0], m[1][1], m[1][2], m[1][3]);
+                }
+                asm volatile("bar.sync 1, 128;" ::: "memory");
+                {   // -T_[23][23] M1: warp w takes rows 8 w .. 8 w + 7, all columns;
+                    // T_[23][23] is lower triangular, so k stops at 8 w + 7
+                    const int r0 = 8 * w + 2 * (ln >> 3), c0 = 4 * (ln & 7);
+                    float t[2][4] = {};
+                    for (int k = 0; k < 8 * w + 8; ++k) {
+                        const float a0 = TM[(32 + r0) * TPP + 32 + k], a1 = TM[(33 + r0) * TPP + 32 + k];
+                        const float4 mv = *reinterpret_cast<const float4*>(TM + k * TPP + 32 + c0);
+                        t[0][0] = __fmaf_rn(a0, mv.x, t[0][0]); t[0][1] = __fmaf_rn(a0, mv.y, t[0][1]);
+                        t[0][2] = __fmaf_rn(a0, mv.z, t[0][2]); t[0][3] = __fmaf_rn(a0, mv.w, t[0][3]);
+                        t[1][0] = __fmaf_rn(a1, mv.x, t[1][0]); t[1][1] = __fmaf_rn(a1, mv.y, t[1][1]);
+                        t[1][2] = __fmaf_rn(a1, mv.z, t[1][2]); t[1][3] = __fmaf_rn(a1, mv.w, t[1][3]);
+                    }
+                    *reinterpret_cast<float4*>(TM + (32 + r0) * TPP + c0) =
+                        make_float4(-t[0][0], -t[0][1], -t[0][2], -t[0][3]);
+                    *reinterpret_cast<float4*>(TM + (33 + r0) * TPP + c0) =
+                        make_float4(-t[1][0], -t[1][1], -t[1][2], -t[1][3]);
                 }
             }
             __syncthreads();
-            // The off-diagonal blocks in three steps instead of three levels of
-            // 16, 32 and 48 products: every block's c = b term needs only the
-            // diagonal blocks, so all six run at once, then the c = b + 1 terms
-            // of the blocks two and three below the diagonal, then the last
-            // term of the corner block.  Thread (block, row rr, columns 4 cq ..)
-            // keeps its sum across the steps, adding the terms in the order
-            // of c, as a single sum over c would.
-            {
-                const int blk = tid >> 6, rr = (tid >> 2) & 15, cq = tid & 3;
-                // blocks 0..2: (a, b) = (b + 1, b); 3, 4: (b + 2, b); 5: (3, 0)
-                const int dd = blk < 3 ? 1 : (blk < 5 ? 2 : 3);
-                const int bq = blk < 3 ? blk : (blk < 5 ? blk - 3 : 0);
-                const int a = bq + dd;
-                const bool act = tid < 6 * 64;
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                auto term = [&](int c) {  // x += W_ac T_cb over this thread's row and columns
-#pragma unroll
-                    for (int kk = 0; kk < 16; ++kk) {
-                        const float wv = AM[(16 * a + rr) * AP + 16 * c + kk];
-                        const float4 t4 = *reinterpret_cast<const float4*>(
-                            TM + (16 * c + kk) * TPP + 16 * bq + 4 * cq);
-                        x.x = __fmaf_rn(wv, t4.x, x.x);
-                        x.y = __fmaf_rn(wv, t4.y, x.y);
-                        x.z = __fmaf_rn(wv, t4.z, x.z);
-                        x.w = __fmaf_rn(wv, t4.w, x.w);
-                    }
-                };
-                auto put = [&]() {
-                    *reinterpret_cast<float4*>(TM + (16 * a + rr) * TPP + 16 * bq + 4 * cq) =
-                        make_float4(-x.x, -x.y, -x.z, -x.w);
-                };
-                if (act) {
-                    term(bq);
-                    if (dd == 1) put();
-                }
-                __syncthreads();
-                if (act && dd >= 2) {
-                    term(bq + 1);
-                    if (dd == 2) put();
-                }
-                __syncthreads();
-                if (act && dd == 3) {
-                    term(bq + 2);
-                    put();
-                }
-                __syncthreads();
-            }
-            if (!failed) {  // T into rows 0..63 of [T; P]
+            if (!failed) {  // T into rows 0..63 of [T; P], zeros above the diagonal
                 const int r = tid & 63, qg = tid >> 6;
 #pragma unroll
                 for (int jj = 0; jj < 16 / (NTP / 64); ++jj) {
                     const int j = qg + (NTP / 64) * jj;
                     const float4 tr = *reinterpret_cast<const float4*>(TM + r * TPP + 4 * j);
-                    st4h(blob + BLOB_TP + OpTPh::off(r, 4 * j), tr.x, tr.y, tr.z, tr.w);
+                    const int c = 4 * j;
+                    st4h(blob + BLOB_TP + OpTPh::off(r, c), c <= r ? tr.x : 0.f,
+                         c + 1 <= r ? tr.y : 0.f, c + 2 <= r ? tr.z : 0.f, c + 3 <= r ? tr.w : 0.f);
                 }
             }
             tc::tc_fence_before();
@@ -1010,8 +1024,9 @@ struct ScanT {
     // 128-column chunk regions used alternately: chunk g computes Ktil S |
     // Qtil S, then O, in R_(g mod 2) and keeps X^T / U^T (A, FP16 pairs: 32
     // columns) in the first columns of the other region, whose last 64 still
-    // hold chunk g - 1's O until chunk g + 1's first product; Khat^T U as dS^T
-    static constexpr uint32_t T_S = 0, T_TX = 64, R0 = 128, R1 = 256, T_D3 = 384;
+    // hold chunk g - 1's O until chunk g + 1's first product; the FP32 state
+    // S^T itself, which the last product of a chunk accumulates into
+    static constexpr uint32_t T_S = 0, T_TX = 64, R0 = 128, R1 = 256, T_SA = 384;
     static constexpr uint32_t TMEM_COLS = 512;
     static_assert(TOTAL <= 232448, "shared memory budget exceeded");
     static_assert(TP1 % 16 == 0 && OST % 128 == 0, "copy alignment");
@@ -1086,16 +1101,20 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
     const uint32_t tmem = *tmem_slot;
     const uint32_t my = tmem + lane_base;  // this thread's TMEM lane
 
-    // state: thread (j, cg) owns S[32 cg + i][j], i < 32, kept in FP32
+    // state: thread (j, cg) moves S[32 cg + i][j], i < 32, between TMEM and
+    // registers; the FP32 state lives in TMEM (T_SA) for the whole sequence
     float* Sg = state + ((size_t)n * heads + h) * D * D + (size_t)(32 * cg) * D + j;
-    float sreg[32];
+    {
+        uint32_t sa[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) sreg[i] = Sg[(size_t)i * D];
-    {   // S^T: K index 32 cg + i in column 16 cg + i / 2
+        for (int i = 0; i < 32; ++i) sa[i] = __float_as_uint(Sg[(size_t)i * D]);
+        // S^T: K index 32 cg + i in column 16 cg + i / 2
         uint32_t sv[16];
 #pragma unroll
-        for (int m = 0; m < 16; ++m) sv[m] = tc::pack_f16x2(sreg[2 * m], sreg[2 * m + 1]);
+        for (int m = 0; m < 16; ++m)
+            sv[m] = tc::pack_f16x2(__uint_as_float(sa[2 * m]), __uint_as_float(sa[2 * m + 1]));
         tc::tmem_st16u(my + ScanT::T_S + 16 * cg, sv);
+        tc::tmem_st32u(my + ScanT::T_SA + 32 * cg, sa);
         tc::tmem_st_wait();
     }
 
@@ -1187,9 +1206,10 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         // (one N = 128 product: Ktil S into r_d1, Qtil S into r_d1 + 64)
         if (tid == 0) {
             tc::tc_fence_after();
+            const uint64_t bd = OpXh::desc(tc::smem_u32(sm + opx_off[xb]), 0);
+#pragma unroll
             for (int ks = 0; ks < 8; ++ks)
-                tc::mma_f16_ta(tmem + r_d1, tmem + ScanT::T_S + 8 * ks,
-                               OpXh::desc(tc::smem_u32(sm + opx_off[xb]), ks),
+                tc::mma_f16_ta(tmem + r_d1, tmem + ScanT::T_S + 8 * ks, bd + ks * OpXh::KSTEP,
                                tc::idesc_f16(128, 128), ks > 0);
             tc::mma_commit(bar_mma);
         }
@@ -1227,10 +1247,29 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         // ---------------------------------------------------------- U^T = X^T T^T
         if (tid == 0) {
             tc::tc_fence_after();
+            const uint64_t bd = OpTPh::desc(s_tp, 0);
+#pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f16_ta(tmem + ScanT::T_TX, tmem + r_a + 8 * ks, OpTPh::desc(s_tp, ks),
+                tc::mma_f16_ta(tmem + ScanT::T_TX, tmem + r_a + 8 * ks, bd + ks * OpTPh::KSTEP,
                                tc::idesc_f16(128, 64), ks > 0);
             tc::mma_commit(bar_mma);
+        }
+        {   // while it runs: S^T <- S^T diag(dec) in TMEM, which the chunk's last
+            // product then accumulates into
+            const float4* dec4 = reinterpret_cast<const float4*>(DEC + 32 * cg);
+            float sv[32];
+            tc::tmem_ld32(my + ScanT::T_SA + 32 * cg, sv);
+            tc::tmem_ld_wait();
+            uint32_t su[32];
+#pragma unroll
+            for (int q4 = 0; q4 < 8; ++q4) {
+                const float4 d4 = dec4[q4];
+                su[4 * q4] = __float_as_uint(__fmul_rn(sv[4 * q4], d4.x));
+                su[4 * q4 + 1] = __float_as_uint(__fmul_rn(sv[4 * q4 + 1], d4.y));
+                su[4 * q4 + 2] = __float_as_uint(__fmul_rn(sv[4 * q4 + 2], d4.z));
+                su[4 * q4 + 3] = __float_as_uint(__fmul_rn(sv[4 * q4 + 3], d4.w));
+            }
+            tc::tmem_st32u(my + ScanT::T_SA + 32 * cg, su);
         }
         wait_bar(bar_mma, ph_mma);
         ph_mma ^= 1;
@@ -1252,12 +1291,15 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         // ---------------------------------------------------------- U^T Khat; O^T += U^T P^T
         if (tid == 0) {
             tc::tc_fence_after();
+            const uint64_t bk = OpKHh::desc(s_kh, 0), bp = OpTPh::desc(s_tp + 8 * 128, 0);
+#pragma unroll
             for (int ks = 0; ks < 4; ++ks)
-                tc::mma_f16_ta(tmem + ScanT::T_D3, tmem + r_a + 8 * ks, OpKHh::desc(s_kh, ks),
-                               tc::idesc_f16(128, 128), ks > 0);
+                tc::mma_f16_ta(tmem + ScanT::T_SA, tmem + r_a + 8 * ks, bk + ks * OpKHh::KSTEP,
+                               tc::idesc_f16(128, 128), true);
+#pragma unroll
             for (int ks = 0; ks < 4; ++ks)  // P = rows 64..127 of [T; P]
-                tc::mma_f16_ta(tmem + r_d1 + 64, tmem + r_a + 8 * ks,
-                               OpTPh::desc(s_tp + 8 * 128, ks), tc::idesc_f16(128, 64), true);
+                tc::mma_f16_ta(tmem + r_d1 + 64, tmem + r_a + 8 * ks, bp + ks * OpTPh::KSTEP,
+                               tc::idesc_f16(128, 64), true);
             tc::mma_commit(bar_mma);
         }
         // chunk g - 1's O (the last 64 columns of r_a) into the staging tile
@@ -1299,20 +1341,14 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         wait_bar(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::tc_fence_after();
-        {   // S[32 cg + i][j] <- dec * S + (Khat^T U)[32 cg + i][j]
-            float a[16], b[16];
-            tc::tmem_ld16(my + ScanT::T_D3 + 32 * cg, a);
-            tc::tmem_ld16(my + ScanT::T_D3 + 32 * cg + 16, b);
+        {   // S^T (FP32, updated in TMEM) into the next chunk's FP16 A operand
+            float sv[32];
+            tc::tmem_ld32(my + ScanT::T_SA + 32 * cg, sv);
             tc::tmem_ld_wait();
+            uint32_t sh[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                sreg[i] = __fmaf_rn(DEC[32 * cg + i], sreg[i], a[i]);
-                sreg[16 + i] = __fmaf_rn(DEC[32 * cg + 16 + i], sreg[16 + i], b[i]);
-            }
-            uint32_t sv[16];
-#pragma unroll
-            for (int m = 0; m < 16; ++m) sv[m] = tc::pack_f16x2(sreg[2 * m], sreg[2 * m + 1]);
-            tc::tmem_st16u(my + ScanT::T_S + 16 * cg, sv);
+            for (int m = 0; m < 16; ++m) sh[m] = tc::pack_f16x2(sv[2 * m], sv[2 * m + 1]);
+            tc::tmem_st16u(my + ScanT::T_S + 16 * cg, sh);
             tc::tmem_st_wait();
         }
         o_c0 = c0;
@@ -1345,8 +1381,11 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         if (out_v) tc::mbar_wait(bar_v, ph_v, 1u << 20);
     }
     if (!aborted) {
+        float sv[32];
+        tc::tmem_ld32(my + ScanT::T_SA + 32 * cg, sv);
+        tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) Sg[(size_t)i * D] = sreg[i];
+        for (int i = 0; i < 32; ++i) Sg[(size_t)i * D] = sv[i];
     }
     tc::tc_fence_before();
     __syncthreads();
