@@ -159,6 +159,12 @@ static_assert(PS_OPX % 1024 == 0 && PS_Y % 16 == 0, "operand alignment");
 // e^(17 |g|) < FLT_MAX, the B-side factor above e^(-17 |g|) (a normal
 // number), and a flushed A-side factor loses under 1.2e-38 e^(14 |g|) < 2e-7.
 constexpr float kWideGMin = 5.1f;
+// Four 16-token blocks (reference token 16 b + 8) keep the A-side factor below
+// e^(8 |g|) < FLT_MAX and a flushed A-side factor's loss under
+// e^(-87.3 + 7 |g|) < 1e-7 while g >= -kNarrowGMin.  A chunk with a steeper
+// decay forms A and P on the CUDA cores, each (row, column) pair's factor
+// e^(Gamma_r - Gamma_s) <= 1 by its own exponential: exact for any g.
+constexpr float kNarrowGMin = 10.0f;
 static_assert(PS_TOTAL <= 232448, "shared memory budget exceeded");
 
 constexpr uint32_t SS_OPX = BLOB_OPX, SS_TP = BLOB_TP;
@@ -409,7 +415,10 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    uint32_t ph_mma = 0, ph_tma[2] = {0, 0};
+    // Per-buffer state is kept as bit masks (bit b): an array indexed by the
+    // buffer would live in local memory, whose lines the small L1 left by the
+    // shared-memory carve-out does not keep -- an L2 round trip per access.
+    uint32_t ph_mma = 0, ph_tma = 0;
     bool failed = false;
 
     auto wait_mma = [&]() {
@@ -445,15 +454,15 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     // beta of item `it` (threads 0..63): the raw BF16 bits, widened only
     // when the item starts.  Every thread loads from a valid address (the
     // tensor's first element where the row is not part of the item) and the
-    // mask is applied at that point, so no select waits on the load before
-    // then.  The loaded bits and the mask are packed into one word.
+    // mask is kept apart and applied at that point: no operation touches the
+    // loaded value, and so waits for it, before then.
+    auto beta_live = [&](const PrepItem& it) { return tid < C && it.valid && tid < it.L; };
     auto load_beta = [&](const PrepItem& it) {
-        const bool live = tid < C && it.valid && tid < it.L;
-        const uint16_t* src = live ? beta + (size_t)(it.c0 + tid) * maps.b_stride + it.h : beta;
-        return (uint32_t)__ldg(src) | (live ? 0x10000u : 0u);
+        const uint16_t* src = beta_live(it) ? beta + (size_t)(it.c0 + tid) * maps.b_stride + it.h : beta;
+        return __ldg(src);
     };
-    auto beta_of = [&](uint32_t w) {
-        return (w & 0x10000u) ? (GATED ? sigmoid_hw(bf((uint16_t)w)) : bf((uint16_t)w)) : 0.f;
+    auto beta_of = [&](uint16_t raw, bool live) {
+        return live ? (GATED ? sigmoid_hw(bf(raw)) : bf(raw)) : 0.f;
     };
 
     // The item whose ready flag is still to be released (copier thread): an
@@ -472,7 +481,8 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     long long item = first;
     PrepItem cur = prep_item(item, heads, map_cu, map_off, n_seqs, t, t_pad);
     load_raw(cur, 0);
-    uint32_t beta_cur = load_beta(cur);
+    uint16_t beta_cur = load_beta(cur);
+    bool blive_cur = beta_live(cur);
     // gated calls: dt_bias of this thread's channel (tid & 127 in the Gamma
     // phase) and a_log of the item's head, loaded one item ahead
     auto load_gate = [&](const PrepItem& it) {
@@ -490,7 +500,8 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         const long long nitem = item + stride;
         PrepItem nxt = {};
         nxt.valid = false;
-        uint32_t beta_nxt = 0;
+        uint16_t beta_nxt = 0;
+        bool blive_nxt = false;
         float2 gate_nxt = make_float2(0.f, 0.f);
         // The next item is resolved (global loads) while the first A/P product
         // runs, and its raw tiles go to the other buffer, which the previous
@@ -499,6 +510,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             if (nitem < items) nxt = prep_item(nitem, heads, map_cu, map_off, n_seqs, t, t_pad);
             load_raw(nxt, b ^ 1);
             beta_nxt = load_beta(nxt);
+            blive_nxt = beta_live(nxt);
             gate_nxt = load_gate(nxt);
         };
 
@@ -517,18 +529,18 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             float* TM = reinterpret_cast<float*>(sm + b * RAW_BUF + RB_TM);
             unsigned char* blob = ws + blob_offset(n_seqs, cur.g, h, heads);
 
-            if (tid < C) BETA[tid] = beta_of(beta_cur);
-            if (!tc::mbar_wait(bar_tma + b, ph_tma[b])) {
+            if (tid < C) BETA[tid] = beta_of(beta_cur, blive_cur);
+            if (!tc::mbar_wait(bar_tma + b, (ph_tma >> b) & 1u)) {
                 atomicOr(&g_tc_status, STATUS_TIMEOUT);
                 failed = true;
             }
-            ph_tma[b] ^= 1;
+            ph_tma ^= 1u << b;
 
             // ------------------------------------------------------ P1 Gamma
             // Four 16-token quarters per channel, then each quarter adds the
             // totals of the quarters before it.  The totals sit in the other raw
             // buffer, whose next tiles are requested only after this phase.
-            bool wide;
+            bool wide, steep;
             float* GH = reinterpret_cast<float*>(sm + (b ^ 1) * RAW_BUF);  // [3][128]
             {
                 const int i = tid & 127, qt = tid >> 7;
@@ -552,6 +564,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 }
                 if (qt < 3) GH[qt * 128 + i] = run;
                 wide = __syncthreads_and(gmin >= -kWideGMin);  // false on NaN too
+                steep = __syncthreads_or(!(gmin >= -kNarrowGMin));  // true on NaN
                 // the g tile is dead from here on: its end takes the reference rows
                 float base = 0.f;
                 if (qt > 0) base = GH[i];
@@ -711,6 +724,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                         kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
                 }
             };
+            float sa[8], sp[8];  // the steep path's A and P (rows tid / 64 + 8 k)
             if (wide) {
                 // Two 32-token column blocks (every g of the chunk is >= -kWideGMin).
                 build_xy_wide();
@@ -726,6 +740,41 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 wait_mma();
                 fetch_next();  // the compact X_1 in the other buffer has been read
                 p3_store();
+            } else if (steep) {
+                // Exact products on the CUDA cores: thread (column s = tid & 63)
+                // forms A_rs and P_rs for rows r = tid / 64 + 8 k.  The results
+                // stay in registers until the raw tiles and Gamma are dead (P4).
+                fetch_next();
+                const int s2 = tid & 63;
+                const bool slive = s2 < L;
+#pragma unroll
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    const int r2 = (tid >> 6) + 8 * k8;
+                    float a = 0.f, pv = 0.f;
+                    if (s2 <= r2) {
+                        const bool rlive = r2 < L;
+#pragma unroll 4
+                        for (int i = 0; i < D; i += 4) {
+                            const float4 gr = *reinterpret_cast<const float4*>(GAM + r2 * KP + i);
+                            const float4 gs = *reinterpret_cast<const float4*>(GAM + s2 * KP + i);
+                            float4 kr = raw4(RAWK, r2, i), qr = raw4(RAWQ, r2, i), ks = raw4(RAWK, s2, i);
+                            if (!rlive) kr = qr = make_float4(0.f, 0.f, 0.f, 0.f);
+                            if (!slive) ks = make_float4(0.f, 0.f, 0.f, 0.f);
+                            const float e0 = __expf(gr.x - gs.x), e1 = __expf(gr.y - gs.y),
+                                        e2 = __expf(gr.z - gs.z), e3 = __expf(gr.w - gs.w);
+                            a = __fmaf_rn(kr.x * ks.x, e0, a);
+                            a = __fmaf_rn(kr.y * ks.y, e1, a);
+                            a = __fmaf_rn(kr.z * ks.z, e2, a);
+                            a = __fmaf_rn(kr.w * ks.w, e3, a);
+                            pv = __fmaf_rn(qr.x * ks.x, e0, pv);
+                            pv = __fmaf_rn(qr.y * ks.y, e1, pv);
+                            pv = __fmaf_rn(qr.z * ks.z, e2, pv);
+                            pv = __fmaf_rn(qr.w * ks.w, e3, pv);
+                        }
+                    }
+                    sa[k8] = a;
+                    sp[k8] = KDA_Q_SCALE * pv;
+                }
             } else {
                 // Four 16-token column blocks with reference token 16 b + 8.
                 build_y(4, 0, OpY::bytes(128), OpY{});
@@ -786,7 +835,18 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             }
 
             // ------------------------------------------------------ P4 read A, P
-            {   // thread (lane ln, quarter ch) reads columns [16 ch, 16 ch + 16)
+            if (steep) {
+                const int s2 = tid & 63;
+                const float bs = BETA[s2];
+#pragma unroll
+                for (int k8 = 0; k8 < 8; ++k8) {
+                    const int r2 = (tid >> 6) + 8 * k8;
+                    AM[r2 * AP + s2] = (s2 < r2) ? sa[k8] * bs : 0.f;
+                    if (!failed)
+                        *reinterpret_cast<uint16_t*>(blob + BLOB_TP + OpTPh::off(64 + r2, s2)) =
+                            tc::f16_bits((s2 <= r2) ? sp[k8] * bs : 0.f);
+                }
+            } else {   // thread (lane ln, quarter ch) reads columns [16 ch, 16 ch + 16)
                 float v[16];
                 tc::tmem_ld16(tmem + lane_base + TC_AP + 16 * ch, v);
                 tc::tmem_ld_wait();
@@ -973,6 +1033,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         item = nitem;
         cur = nxt;
         beta_cur = beta_nxt;
+        blive_cur = blive_nxt;
         gate_cur = gate_nxt;
     }
     release_pending();
@@ -1018,7 +1079,8 @@ struct ScanT {
     static constexpr uint32_t TP1 = RAWV + 64 * D * 2;
     static constexpr uint32_t OPX1 = (TP1 + BGRP + 1023) & ~1023u;
     static constexpr uint32_t OST = OPX1 + OpXh::bytes(128);
-    static constexpr uint32_t BAR = OST + 64 * D * 4;
+    static constexpr uint32_t RAWV1 = OST + 64 * D * 4;  // the second value tile
+    static constexpr uint32_t BAR = RAWV1 + 64 * D * 2;
     static constexpr uint32_t TOTAL = BAR + 128;
     // TMEM columns: S^T (A, FP16 pairs: 64 columns), T X (64); two
     // 128-column chunk regions used alternately: chunk g computes Ktil S |
@@ -1076,19 +1138,20 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         return;
     }
 
-    const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + ScanT::RAWV);
+    // buffers by chunk parity (selects, not arrays: see prepare_role)
+    auto rawv_off = [](int b) { return b ? ScanT::RAWV1 : ScanT::RAWV; };  // value tiles
     float* OST = reinterpret_cast<float*>(sm + ScanT::OST);
     uint64_t* bar_x = reinterpret_cast<uint64_t*>(sm + ScanT::BAR);  // [2]: [Ktil; Qtil] groups
     uint64_t* bar_b = bar_x + 2;                                     // [2]: [T; P] | Khat^T | dec
-    uint64_t* bar_v = bar_x + 4;
-    uint64_t* bar_mma = bar_x + 5;
+    uint64_t* bar_v = bar_x + 4;                                     // [2]: value tiles
+    uint64_t* bar_mma = bar_x + 6;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ScanT::BAR + 64);
     int* abort_flag = reinterpret_cast<int*>(sm + ScanT::BAR + 68);
-    const uint32_t opx_off[2] = {(uint32_t)SS_OPX, ScanT::OPX1};
-    const uint32_t tp_off[2] = {(uint32_t)SS_TP, ScanT::TP1};  // group b: TP, KH, DEC follow
+    auto opx_off = [](int b) { return b ? ScanT::OPX1 : (uint32_t)SS_OPX; };
+    auto tp_off = [](int b) { return b ? ScanT::TP1 : (uint32_t)SS_TP; };  // group b: TP, KH, DEC follow
 
     if (tid == 0) {
-        for (int i = 0; i < 6; ++i) tc::mbar_init(bar_x + i, 1);
+        for (int i = 0; i < 7; ++i) tc::mbar_init(bar_x + i, 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&vmap);
         tc::prefetch_tmap(&omap);
@@ -1118,7 +1181,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         tc::tmem_st_wait();
     }
 
-    uint32_t ph_mma = 0, ph_v = 0, ph_x = 0, ph_b = 0;  // ph_x, ph_b: bit per group
+    uint32_t ph_mma = 0, ph_v = 0, ph_x = 0, ph_b = 0;  // ph_v, ph_x, ph_b: bit per buffer
     auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
         if (!tc::mbar_wait(bar, parity)) {
             atomicOr(&g_tc_status, STATUS_TIMEOUT);
@@ -1128,7 +1191,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
     // Copies (the copier thread).  Outstanding ones are tracked so an early
     // exit can let them land before the shared memory is released.
     uint32_t out_x = 0, out_b = 0;  // bit per group
-    bool out_v = false;
+    uint32_t out_v = 0;  // bit per value tile
     // Ready flags (fused grid): head h's flags are consecutive words, read four
     // at a time with one acquire load, so one global round trip usually covers
     // several chunks; acq_hi is the last chunk known to be ready.
@@ -1139,10 +1202,12 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         const long long g4 = gg & ~3LL;
         for (uint32_t it = 0; it < (1u << 22); ++it) {
             const uint4 f = tc::flags4_acquire(fh + g4);
-            const unsigned fl[4] = {f.x, f.y, f.z, f.w};
+            // the four flags as a bit mask (a runtime-indexed array would live
+            // in local memory)
+            const uint32_t fm = (f.x ? 1u : 0u) | (f.y ? 2u : 0u) | (f.z ? 4u : 0u) | (f.w ? 8u : 0u);
             int k = (int)(gg - g4);
-            if (fl[k]) {
-                while (k + 1 < 4 && fl[k + 1]) ++k;
+            if ((fm >> k) & 1u) {
+                while (k + 1 < 4 && ((fm >> (k + 1)) & 1u)) ++k;
                 tc::flags_proxy_fence();
                 acq_hi = g4 + k;
                 return true;
@@ -1158,20 +1223,23 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         }
         const unsigned char* blob = ws + blob_offset(n_seqs, gg, h, heads);
         tc::mbar_arrive_expect_tx(bar_x + b, OpXh::bytes(128));
-        tc::bulk_load(sm + opx_off[b], blob + BLOB_OPX, OpXh::bytes(128), bar_x + b);
+        tc::bulk_load(sm + opx_off(b), blob + BLOB_OPX, OpXh::bytes(128), bar_x + b);
         tc::mbar_arrive_expect_tx(bar_b + b, ScanT::BGRP);
-        tc::bulk_load(sm + tp_off[b], blob + BLOB_TP, ScanT::BGRP, bar_b + b);
+        tc::bulk_load(sm + tp_off(b), blob + BLOB_TP, ScanT::BGRP, bar_b + b);
         out_x |= 1u << b;
         out_b |= 1u << b;
     };
-    auto load_v = [&](int cc0) {
-        tc::mbar_arrive_expect_tx(bar_v, 64 * D * 2);
-        tc::tma_load_2d(sm + ScanT::RAWV, &vmap, bar_v, h * D, cc0);
-        out_v = true;
+    // Value tiles are double-buffered by chunk parity and requested two chunks
+    // ahead, as soon as the X phase has consumed the buffer.
+    auto load_v = [&](int cc0, int vb) {
+        tc::mbar_arrive_expect_tx(bar_v + vb, 64 * D * 2);
+        tc::tma_load_2d(sm + rawv_off(vb), &vmap, bar_v + vb, h * D, cc0);
+        out_v |= 1u << vb;
     };
     if (copier && start < end) {
         load_ops(g0, 0);
-        load_v(start);
+        load_v(start, 0);
+        if (start + C < end) load_v(start + C, 1);
     }
 
     int o_c0 = -1, o_L = 0;  // the chunk whose O is still in TMEM (region o_reg)
@@ -1185,9 +1253,9 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         const bool more = c0 + C < end;
         const uint32_t r_d1 = xb ? ScanT::R1 : ScanT::R0;  // Ktil S, then Qtil S / O at +64
         const uint32_t r_a = xb ? ScanT::R0 : ScanT::R1;   // X^T / U^T (A), then T X at +64
-        const uint32_t s_tp = tc::smem_u32(sm + tp_off[xb]);
+        const uint32_t s_tp = tc::smem_u32(sm + tp_off(xb));
         const uint32_t s_kh = s_tp + (BLOB_KH - BLOB_TP);
-        const float* DEC = reinterpret_cast<const float*>(sm + tp_off[xb] + (BLOB_DEC - BLOB_TP));
+        const float* DEC = reinterpret_cast<const float*>(sm + tp_off(xb) + (BLOB_DEC - BLOB_TP));
         tc::tc_fence_before();
         if (__syncthreads_or(*abort_flag)) break;  // every thread takes the same exit
         if (copier && o_staged) {  // chunk g - 2's O, staged during the last chunk
@@ -1198,15 +1266,16 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         wait_bar(bar_x + xb, (ph_x >> xb) & 1u);
         ph_x ^= 1u << xb;
         if (copier) out_x &= ~(1u << xb);
-        wait_bar(bar_v, ph_v);
-        ph_v ^= 1;
-        if (copier) out_v = false;
+        wait_bar(bar_v + xb, (ph_v >> xb) & 1u);
+        ph_v ^= 1u << xb;
+        if (copier) out_v &= ~(1u << xb);
+        const uint16_t* RAWV = reinterpret_cast<const uint16_t*>(sm + rawv_off(xb));
 
         // ---------------------------------------------------------- S^T [Ktil; Qtil]^T
         // (one N = 128 product: Ktil S into r_d1, Qtil S into r_d1 + 64)
         if (tid == 0) {
             tc::tc_fence_after();
-            const uint64_t bd = OpXh::desc(tc::smem_u32(sm + opx_off[xb]), 0);
+            const uint64_t bd = OpXh::desc(tc::smem_u32(sm + opx_off(xb)), 0);
 #pragma unroll
             for (int ks = 0; ks < 8; ++ks)
                 tc::mma_f16_ta(tmem + r_d1, tmem + ScanT::T_S + 8 * ks, bd + ks * OpXh::KSTEP,
@@ -1239,7 +1308,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         }
         tc::tc_fence_before();
         __syncthreads();
-        if (copier && more) load_v(c0 + C);  // the value tile is consumed
+        if (copier && c0 + 2 * C < end) load_v(c0 + 2 * C, xb);  // this tile is consumed
         wait_bar(bar_b + xb, (ph_b >> xb) & 1u);
         ph_b ^= 1u << xb;
         if (copier) out_b &= ~(1u << xb);
@@ -1378,7 +1447,8 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
             if ((out_x >> b2) & 1u) tc::mbar_wait(bar_x + b2, (ph_x >> b2) & 1u, 1u << 20);
             if ((out_b >> b2) & 1u) tc::mbar_wait(bar_b + b2, (ph_b >> b2) & 1u, 1u << 20);
         }
-        if (out_v) tc::mbar_wait(bar_v, ph_v, 1u << 20);
+        for (int b2 = 0; b2 < 2; ++b2)
+            if ((out_v >> b2) & 1u) tc::mbar_wait(bar_v + b2, (ph_v >> b2) & 1u, 1u << 20);
     }
     if (!aborted) {
         float sv[32];

@@ -166,6 +166,18 @@ __device__ __forceinline__ void mma_tf32(uint32_t d_tmem, uint64_t adesc, uint64
         : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem]^T, one K-step of 8 TF32 values, issued by
+// one thread.  A sits in TMEM with lane = row and one value per 32-bit
+// column, so `a_tmem` advances by 8 columns per K-step.
+__device__ __forceinline__ void mma_tf32_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, bool accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"((uint32_t)accumulate)
+        : "memory");
+}
+
 // Arrive on `bar` once every previously issued tcgen05.mma of this thread has
 // completed.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -204,6 +216,13 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
         : "r"(taddr));
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Read one 32-bit column of this thread's TMEM lane.
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+    uint32_t r;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+    return __uint_as_float(r);
 }
 
 // Read 8 consecutive 32-bit columns of this thread's TMEM lane.
@@ -268,6 +287,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst_smem, const CUtensorMap* m
         : "memory");
 }
 
+// 3-D tile load global -> shared through a tensor map, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst_smem, const CUtensorMap* map,
+                                            uint64_t* bar, int x, int y, int z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst_smem)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Tile store shared -> global through a tensor map (rows past the tensor's
 // end are not written); completion is tracked by bulk groups.
 __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src_smem, int x,
@@ -299,6 +328,15 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src_smem, uint
 
 __device__ __forceinline__ void bulk_commit() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most the most recent committed bulk-store group of this
+// thread is still pending (completed, or only reading its source: .read).
+__device__ __forceinline__ void bulk_wait_all_but_last() {
+    asm volatile("cp.async.bulk.wait_group 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all_but_last() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // Wait until every committed bulk store of this thread has completed.

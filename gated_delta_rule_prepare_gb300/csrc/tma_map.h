@@ -43,6 +43,24 @@ inline bool tma_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// BF16 [rows][cols] with a row pitch of `pitch_elems` elements, seen as
+// groups of 8 consecutive columns: a box of `box_rows` rows x 128 columns
+// lands in shared memory as [16 groups][box_rows][8], i.e. the MN-major
+// core-matrix layout of an MMA operand whose N index is the column (K-adjacent
+// core matrices 128 bytes apart, N-adjacent ones box_rows x 16 bytes).
+inline bool tma_map_bf16_groups8(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                                 uint64_t pitch_elems, uint32_t box_rows) {
+    auto fn = tma_encode_fn();
+    if (!fn || cols % 8 != 0) return false;
+    cuuint64_t gdim[3] = {8, rows, cols / 8};
+    cuuint64_t gstride[2] = {pitch_elems * 2, 16};
+    cuuint32_t box[3] = {8, box_rows, 16};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), gdim, gstride, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // FP32 [rows][cols] with a row pitch of `pitch_elems` elements, in boxes of
 // box_cols x box_rows without swizzle (row-major in shared memory).
 inline bool tma_map_f32(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,

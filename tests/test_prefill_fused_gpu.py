@@ -45,11 +45,12 @@ def oracle_all_heads(orc, d, t):
 
 
 @pytest.mark.parametrize("t,g_low", [(1000, -5.0), (777, -0.05), (64, -5.0), (1, -5.0),
-                                     (130, -10.0)])
+                                     (130, -10.0), (130, -15.0), (200, -20.0)])
 def test_fused_grid_matches_oracle(orc, t, g_low):
     """Every head and output row: whole and ragged chunk counts, one-token and
-    one-chunk sequences, slow decay (the state carries across every chunk)
-    and the steepest supported decay."""
+    one-chunk sequences, slow decay (the state carries across every chunk),
+    and steep decays: down to -10 the 16-token tensor-core blocks, beyond it
+    the exact per-pair products."""
     K = kda()
     d = inputs(100 + t, t, g_low)
     o, S = run(K, d, t)
@@ -151,3 +152,18 @@ def test_fused_grid_two_sequences(orc, packed):
         assert rel_err(o[a:b], o_ref) < TOL_PREFILL
         assert rel_err(S[n], S_ref) < TOL_PREFILL
         a = b
+
+
+@pytest.mark.parametrize("impl", ["fused", "unfused"])
+def test_steep_decay_matches_oracle_on_both_paths(orc, monkeypatch, impl):
+    """g in [-20, 0]: every chunk is steeper than the tensor-core blocks allow
+    and takes the exact products, on the fused grid and on the two kernels."""
+    if impl == "unfused":
+        monkeypatch.setenv("KDA_PREFILL_IMPL", "unfused")
+    K = kda()
+    t = 300
+    d = inputs(77, t, g_low=-20.0)
+    o, S = run(K, d, t)
+    o_ref, S_ref = oracle_all_heads(orc, d, t)
+    assert rel_err(o, o_ref) < TOL_PREFILL
+    assert rel_err(S[0], S_ref) < TOL_PREFILL

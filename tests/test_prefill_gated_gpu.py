@@ -57,6 +57,24 @@ def test_gated_prefill_matches_oracle(orc, monkeypatch, t, impl):
     assert rel_err(S[0], S_ref) < TOL_PREFILL
 
 
+@pytest.mark.parametrize("impl", ["fused", "unfused"])
+def test_gated_prefill_steep_lower_bound(orc, monkeypatch, impl):
+    """gate_lower_bound -20: the gate reaches decays far steeper than the
+    tensor-core blocks allow; those chunks take the exact products."""
+    if impl == "unfused":
+        monkeypatch.setenv("KDA_PREFILL_IMPL", "unfused")
+    K = kda()
+    H, t = 32, 200
+    d = wl.prefill_gated(seed=17, t=t, heads=H)
+    d["gate_lower_bound"] = -20.0
+    o, S = run(K, d, t, H)
+    g, beta = reference(orc, d, t, H)
+    assert float(g.min()) < -10.0  # the steep path is exercised
+    o_ref, S_ref = orc.prefill(d["q"], d["k"], d["v"], g, beta, d["state"][0])
+    assert rel_err(o, o_ref) < TOL_PREFILL
+    assert rel_err(S[0], S_ref) < TOL_PREFILL
+
+
 def test_gated_prefill_rows_past_t_unused(orc):
     """t = 1000 of 1024 rows: o[:t] and the final state are bit-identical
     whatever the rows past t hold (NaN or 0 in q, k, v, g_raw and b_raw),

@@ -242,11 +242,11 @@ def test_tensor_core_and_simt_kernels_agree(orc, monkeypatch):
     assert rel_err(o_tc, o_si.double().cpu().numpy()) < TOL_PREFILL
 
 
-@pytest.mark.parametrize("g_low", [-0.05, -10.0])
+@pytest.mark.parametrize("g_low", [-0.05, -10.0, -30.0])
 def test_prefill_long_memory_and_strong_decay(orc, g_low):
     """Slow decay (g in [-0.05, 0]: the state carries across all 16 chunks, so
-    rounding in the carried state accumulates) and the steepest supported
-    decay (g in [-10, 0])."""
+    rounding in the carried state accumulates), the steepest decay of the
+    tensor-core blocks (g in [-10, 0]) and one beyond it (exact products)."""
     K = kda()
     gen = torch.Generator().manual_seed(31)
     T, H = 1024, 2
