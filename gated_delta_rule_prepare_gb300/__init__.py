@@ -146,7 +146,8 @@ def kda_prefill(state, q, k, v, g, beta, o, t, chunk, pad_fill=0.0, cu_seqlens=N
                 workspace=None):
     """Chunked prefill.  Without cu_seqlens: q, k, v, g [N, T_pad, H, 128]
     (or [T_pad, H, 128] for one sequence), beta [N, T_pad, H], t valid tokens
-    per sequence; rows [t, T_pad) are overwritten with pad_fill.  With
+    per sequence; rows [t, T_pad) are the caller's padded tail (pad_fill),
+    neither read into arithmetic nor written.  With
     cu_seqlens (device int32 [N+1]): packed rows [T, H, 128] and t = T.
     q, k and v may be strided views whose token rows are ``q.stride(-3)``
     elements apart (e.g. slices of one [T, 3*H*128] buffer)."""

@@ -65,7 +65,7 @@ __device__ __forceinline__ void fma4(float4& acc, const float4& s, float a) {
     acc.w = __fmaf_rn(s.w, a, acc.w);
 }
 
-// Sum the 8 warp partials of column j in warp order.
+// Sum the kWarps (16) warp partials of column j in warp order.
 __device__ __forceinline__ float reduce_col(const TokenSmem& sm, int j) {
     float t = sm.red[0][j];
 #pragma unroll

@@ -208,28 +208,6 @@ prefill_simt_kernel(float* __restrict__ state, const TIn* __restrict__ q,
     }
 }
 
-// Overwrites rows [t, t_pad) of every sequence with pad_fill (the harness
-// padding of prefill_with_pad_fill), in the input dtype.
-template <typename TIn>
-__global__ void pad_fill_kernel(TIn* q, TIn* k, TIn* v, TIn* g, TIn* beta, int t, int t_pad,
-                                int n_seqs, int heads, long long qkv_stride, TIn fill) {
-    const int pad = t_pad - t;
-    const size_t hd = (size_t)heads * D;
-    const size_t total = (size_t)n_seqs * pad * hd;
-    for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-         e += (size_t)gridDim.x * blockDim.x) {
-        const size_t n = e / ((size_t)pad * hd);
-        const size_t rem = e % ((size_t)pad * hd);
-        const size_t row = (size_t)n * t_pad + t + rem / hd;
-        const size_t col = rem % hd;
-        q[row * qkv_stride + col] = fill;
-        k[row * qkv_stride + col] = fill;
-        v[row * qkv_stride + col] = fill;
-        g[row * hd + col] = fill;
-        if (col < (size_t)heads) beta[row * heads + col] = fill;
-    }
-}
-
 // True when the caller pins the SIMT chunk kernel (KDA_PREFILL_IMPL=simt,
 // for comparisons).
 bool simt_pinned() {
@@ -237,28 +215,23 @@ bool simt_pinned() {
     return impl && strcmp(impl, "simt") == 0;
 }
 
-// True when this call runs on the tensor-core kernels (which need a workspace).
+// True when this call runs on the tensor-core kernels (which need a
+// workspace): every BF16 call unless the SIMT kernel is pinned.  Those kernels
+// step through the sequence 64 tokens at a time whatever the chunk width: the
+// chunked form gives the same result for any width (the recurrence it
+// reorganises), up to rounding, so the width is the kernels' choice.
 bool uses_tensor_cores(int chunk, int in_dtype) {
-    return in_dtype == KDA_BF16 && chunk == 64 && !simt_pinned();
+    (void)chunk;
+    return in_dtype == KDA_BF16 && !simt_pinned();
 }
 
 template <typename TIn>
-kda_status launch(float* state, void* q, void* k, void* v, void* g, void* beta, float* o, int t,
-                  int t_pad, int chunk, float pad_fill, int heads, long long stride,
-                  const int* cu, int n_seqs, void* workspace, cudaStream_t s) {
-    if (!cu && t_pad > t) {
-        TIn fill;
-        if constexpr (sizeof(TIn) == 2) fill = __bfloat16_as_ushort(__float2bfloat16_rn(pad_fill));
-        else fill = pad_fill;
-        const size_t total = (size_t)n_seqs * (t_pad - t) * heads * D;
-        const size_t want = (total + 255) / 256;
-        const unsigned blocks = (unsigned)(want < 4096 ? want : 4096);
-        pad_fill_kernel<TIn><<<blocks, 256, 0, s>>>((TIn*)q, (TIn*)k, (TIn*)v, (TIn*)g,
-                                                    (TIn*)beta, t, t_pad, n_seqs, heads, stride,
-                                                    fill);
-        kda_status st = launch_result("kda_prefill (pad fill)");
-        if (st != KDA_OK) return st;
-    }
+kda_status launch(float* state, const void* q, const void* k, const void* v, const void* g,
+                  const void* beta, float* o, int t, int t_pad, int chunk, int heads,
+                  long long stride, const int* cu, int n_seqs, void* workspace, cudaStream_t s) {
+    // The SIMT kernel holds chunks of at most kCMax tokens on chip; a wider
+    // chunk runs as consecutive kCMax-token chunks (the same result).
+    chunk = chunk < kCMax ? chunk : kCMax;
     // Short FP32 sequences (uniform form, heads packed in each token row) take
     // decode_k's row walk, the pages' dispatch for pieces that do not take the
     // chunked arm: one state read, t token steps in registers, one state write.
@@ -308,37 +281,55 @@ extern "C" size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk
     return prefill_tc_workspace_bytes(rows, n_seqs, heads);
 }
 
-extern "C" kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* beta,
-                                  float* o, int t, int t_pad, int chunk, float pad_fill,
-                                  int heads, int head_dim, int in_dtype, int64_t qkv_row_stride,
-                                  const int* cu_seqlens, int n_seqs, void* workspace,
-                                  size_t workspace_bytes, uint64_t stream) {
+namespace kda {
+
+// Argument checks of kda_prefill and kda_prefill_static_ws (everything but the
+// workspace), so that both refuse the same call with the same status.
+kda_status validate_prefill(const char* fn, const float* state, const void* q, const void* k,
+                            const void* v, const void* g, const void* beta, const float* o,
+                            int t, int t_pad, int chunk, int heads, int head_dim, int in_dtype,
+                            int64_t qkv_row_stride, const int* cu_seqlens, int n_seqs) {
     KDA_REQUIRE(state && q && k && v && g && beta && o, KDA_ERR_INVALID_ARG,
-                "kda_prefill: null pointer argument");
+                "%s: null pointer argument", fn);
     KDA_REQUIRE(aligned16(state) && aligned16(q) && aligned16(k) && aligned16(v) &&
                     aligned16(g) && aligned16(o),
-                KDA_ERR_INVALID_ARG,
-                "kda_prefill: state, q, k, v, g and o must be 16-byte aligned");
-    KDA_REQUIRE(head_dim == D, KDA_ERR_UNSUPPORTED, "kda_prefill: head_dim %d unsupported",
-                head_dim);
-    KDA_REQUIRE(chunk == 16 || chunk == 32 || chunk == 64, KDA_ERR_UNSUPPORTED,
-                "kda_prefill: chunk %d unsupported (16, 32 or 64)", chunk);
+                KDA_ERR_INVALID_ARG, "%s: state, q, k, v, g and o must be 16-byte aligned", fn);
+    KDA_REQUIRE(head_dim == D, KDA_ERR_UNSUPPORTED, "%s: head_dim %d unsupported", fn, head_dim);
+    KDA_REQUIRE(chunk == 16 || chunk == 32 || chunk == 64 || chunk == 128, KDA_ERR_UNSUPPORTED,
+                "%s: chunk %d unsupported (16, 32, 64 or 128)", fn, chunk);
     KDA_REQUIRE(in_dtype == KDA_F32 || in_dtype == KDA_BF16, KDA_ERR_INVALID_ARG,
-                "kda_prefill: in_dtype %d unknown", in_dtype);
+                "%s: in_dtype %d unknown", fn, in_dtype);
     KDA_REQUIRE(heads >= 1 && n_seqs >= 1 && heads <= 65535 && n_seqs <= 65535,
-                KDA_ERR_INVALID_ARG, "kda_prefill: heads (%d) / n_seqs (%d) out of range",
-                heads, n_seqs);
-    KDA_REQUIRE(t >= 1 && t_pad >= t, KDA_ERR_INVALID_ARG,
-                "kda_prefill: need 1 <= t (%d) <= t_pad (%d)", t, t_pad);
+                KDA_ERR_INVALID_ARG, "%s: heads (%d) / n_seqs (%d) out of range", fn, heads,
+                n_seqs);
+    KDA_REQUIRE(t >= 1 && t_pad >= t, KDA_ERR_INVALID_ARG, "%s: need 1 <= t (%d) <= t_pad (%d)",
+                fn, t, t_pad);
     KDA_REQUIRE(!cu_seqlens || t_pad == t, KDA_ERR_INVALID_ARG,
-                "kda_prefill: packed sequences (cu_seqlens) take no padding: t_pad must equal t");
+                "%s: packed sequences (cu_seqlens) take no padding: t_pad must equal t", fn);
     KDA_REQUIRE(qkv_row_stride >= (int64_t)heads * D, KDA_ERR_INVALID_ARG,
-                "kda_prefill: qkv_row_stride %lld < heads * 128", (long long)qkv_row_stride);
+                "%s: qkv_row_stride %lld < heads * 128", fn, (long long)qkv_row_stride);
     const int esz = in_dtype == KDA_BF16 ? 2 : 4;
     KDA_REQUIRE((qkv_row_stride * esz) % 16 == 0, KDA_ERR_INVALID_ARG,
-                "kda_prefill: qkv_row_stride must be a multiple of 16 bytes");
+                "%s: qkv_row_stride must be a multiple of 16 bytes", fn);
     const long long rows = cu_seqlens ? (long long)t : (long long)t_pad * n_seqs;
-    KDA_REQUIRE(rows <= 0x7fffffffLL, KDA_ERR_INVALID_ARG, "kda_prefill: too many token rows");
+    KDA_REQUIRE(rows <= 0x7fffffffLL, KDA_ERR_INVALID_ARG, "%s: too many token rows", fn);
+    return KDA_OK;
+}
+
+}  // namespace kda
+
+extern "C" kda_status kda_prefill(float* state, const void* q, const void* k, const void* v,
+                                  const void* g, const void* beta, float* o, int t, int t_pad,
+                                  int chunk, float pad_fill, int heads, int head_dim,
+                                  int in_dtype, int64_t qkv_row_stride, const int* cu_seqlens,
+                                  int n_seqs, void* workspace, size_t workspace_bytes,
+                                  uint64_t stream) {
+    (void)pad_fill;  // the caller's fill of rows [t, t_pad): never read, never written
+    const kda_status vs = validate_prefill("kda_prefill", state, q, k, v, g, beta, o, t, t_pad,
+                                           chunk, heads, head_dim, in_dtype, qkv_row_stride,
+                                           cu_seqlens, n_seqs);
+    if (vs != KDA_OK) return vs;
+    const long long rows = cu_seqlens ? (long long)t : (long long)t_pad * n_seqs;
     const size_t need = kda_prefill_workspace_size(rows, n_seqs, chunk, heads, head_dim, in_dtype);
     KDA_REQUIRE(workspace_bytes >= need && (need == 0 || workspace), KDA_ERR_WORKSPACE,
                 "kda_prefill: workspace of %zu B given, %zu B needed", workspace_bytes, need);
@@ -347,10 +338,10 @@ extern "C" kda_status kda_prefill(float* state, void* q, void* k, void* v, void*
     KDA_REQUIRE(!fault_injected(), KDA_ERR_CUDA, "kda_prefill: injected launch failure");
     cudaStream_t s = as_stream(stream);
     if (in_dtype == KDA_BF16)
-        return launch<uint16_t>(state, q, k, v, g, beta, o, t, t_pad, chunk, pad_fill, heads,
+        return launch<uint16_t>(state, q, k, v, g, beta, o, t, t_pad, chunk, heads,
                                 qkv_row_stride, cu_seqlens, n_seqs, workspace, s);
-    return launch<float>(state, q, k, v, g, beta, o, t, t_pad, chunk, pad_fill, heads,
-                         qkv_row_stride, cu_seqlens, n_seqs, workspace, s);
+    return launch<float>(state, q, k, v, g, beta, o, t, t_pad, chunk, heads, qkv_row_stride,
+                         cu_seqlens, n_seqs, workspace, s);
 }
 
 extern "C" kda_status kda_prefill_gated(float* state, const void* q, const void* k, const void* v,

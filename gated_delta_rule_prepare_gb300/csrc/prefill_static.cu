@@ -58,11 +58,17 @@ kda_status static_ws_address(void** out) {
 
 using namespace kda;
 
-extern "C" kda_status kda_prefill_static_ws(float* state, void* q, void* k, void* v, void* g,
-                                            void* beta, float* o, int t, int t_pad, int chunk,
-                                            float pad_fill, int heads, int head_dim,
-                                            int in_dtype, int64_t qkv_row_stride,
-                                            const int* cu_seqlens, int n_seqs, uint64_t stream) {
+extern "C" kda_status kda_prefill_static_ws(float* state, const void* q, const void* k,
+                                            const void* v, const void* g, const void* beta,
+                                            float* o, int t, int t_pad, int chunk, float pad_fill,
+                                            int heads, int head_dim, int in_dtype,
+                                            int64_t qkv_row_stride, const int* cu_seqlens,
+                                            int n_seqs, uint64_t stream) {
+    // the same checks, and statuses, as kda_prefill before the size check
+    const kda_status vs = validate_prefill("kda_prefill_static_ws", state, q, k, v, g, beta, o, t,
+                                           t_pad, chunk, heads, head_dim, in_dtype,
+                                           qkv_row_stride, cu_seqlens, n_seqs);
+    if (vs != KDA_OK) return vs;
     const long long rows = cu_seqlens ? (long long)t : (long long)t_pad * n_seqs;
     const size_t need = kda_prefill_workspace_size(rows, n_seqs, chunk, heads, head_dim, in_dtype);
     KDA_REQUIRE(need <= (size_t)KDA_STATIC_WORKSPACE_BYTES, KDA_ERR_WORKSPACE,

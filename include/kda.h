@@ -2,7 +2,7 @@
  * kda.h -- C ABI of libkda: the KDA (Kimi-style delta attention) core of the
  * GLM-5.3-Flash attention block on one GB300 (sm_103a).
  *
- * The method (rustdoc pages of the "glm5next_kda" module: the block pipeline
+ * The method (rustdoc pages of the glm5next_kda module: the block pipeline
  * in the module index, Glm5NextKdaLayer's decode / decode_k / prefill /
  * prefill_with_pad_fill, Glm5NextKdaKernels' chunk_prepare / chunk_scan /
  * recurrent, and config.rs): per head, an FP32 state S[i][j] of
@@ -92,10 +92,11 @@ kda_status kda_decode(float* state, const float* q, const float* k, const float*
  *   o     : FP32 [n_seqs][krows][heads][128]
  *   snapshots : HOST array of n_snap device pointers; snapshots[t] (FP32
  *           [n_seqs][heads][128][128]) receives the state after row t.  Rows
- *           t >= n_snap take no snapshot ("rows past snapshots.len() take no
- *           snapshot").  May be NULL when n_snap == 0.
- *   Refused: krows < 1 or krows > KDA_MAX_K ("refuses k == 0 or k above the
- *   workspace"), n_snap < 0 or n_snap > krows, a null snapshot pointer.
+ *           at or after n_snap write no snapshot (Glm5NextKdaLayer::decode_k).
+ *           May be NULL when n_snap == 0.
+ *   Refused: krows of 0 or less, or above KDA_MAX_K, the row capacity of the
+ *   walk (Glm5NextKdaLayer::decode_k); n_snap < 0 or n_snap > krows; a null
+ *   snapshot pointer.
  */
 kda_status kda_decode_k(float* state, const float* q, const float* k, const float* v,
                         const float* g, const float* beta, float* o, int n_seqs, int krows,
@@ -110,10 +111,11 @@ kda_status kda_decode_k(float* state, const float* q, const float* k, const floa
  *
  * Two batch forms:
  *  - cu_seqlens == NULL: n_seqs sequences of t valid tokens each, stored as
- *    [n_seqs][t_pad] token rows (t <= t_pad).  Before the core runs, rows
- *    [t, t_pad) of q, k, v, g and beta are overwritten with pad_fill in the
- *    input dtype (the pages' padded tails); the core never reads them into
- *    arithmetic, so o and the final state do not depend on pad_fill.
+ *    [n_seqs][t_pad] token rows (t <= t_pad).  Rows [t, t_pad) of q, k, v, g
+ *    and beta are the caller's padded tail, filled with pad_fill
+ *    (Glm5NextKdaLayer::prefill_with_pad_fill): the library never writes them
+ *    and never reads them into arithmetic, so o and the final state do not
+ *    depend on their contents (NaN included).  pad_fill itself is not used.
  *  - cu_seqlens != NULL: DEVICE int32 [n_seqs + 1] offsets of n_seqs packed
  *    sequences; t is the total token count (== cu_seqlens[n_seqs]); t_pad
  *    must equal t and no fill happens.  Offsets are checked on the device
@@ -127,25 +129,33 @@ kda_status kda_decode_k(float* state, const float* q, const float* k, const floa
  *           one [T][3*heads*128] buffer such as kda_conv_silu_l2's output)
  *   g     : in_dtype [rows][heads][128]   beta : in_dtype [rows][heads]
  *   o     : FP32 [rows][heads][128]; rows of padding are not written
- *   chunk : 16, 32 or 64 (the chunk width C; 128 is refused as unsupported)
+ *   chunk : 16, 32, 64 or 128 (config.rs chunk).  The chunked form equals the
+ *           token recurrence for any width, up to rounding, so the width is a
+ *           performance choice: the tensor-core kernels step 64 tokens at a
+ *           time for every width, the SIMT kernel min(chunk, 64).
  *   in_dtype : KDA_F32 or KDA_BF16 (applies to q, k, v, g, beta)
  * Routing: FP32 inputs in the uniform form with t <= KDA_MAX_K and
  * qkv_row_stride == heads*128 run decode_k's row walk (the pages' dispatch
  * for pieces that do not take the chunked arm: state read once, t token steps,
- * state written once); BF16 inputs with chunk 64 run the tensor-core prepare
- * and scan kernels -- as one cooperative grid (the scan consuming each chunk
- * as soon as another SM has prepared it) when there are few (sequence, head)
- * chains relative to the SMs, e.g. one sequence of 32 heads; everything else
- * runs the FP32 SIMT chunk kernel.  The environment variable
+ * state written once); BF16 inputs run the tensor-core prepare and scan
+ * kernels -- as one cooperative grid (the scan consuming each chunk as soon
+ * as another SM has prepared it) when there are few (sequence, head) chains
+ * relative to the SMs, e.g. one sequence of 32 heads; FP32 inputs otherwise
+ * run the FP32 SIMT chunk kernel.  The environment variable
  * KDA_PREFILL_IMPL=simt pins the SIMT kernel and KDA_PREFILL_IMPL=unfused
  * the two-kernel tensor-core path (for comparisons).
+ * Precision of the tensor-core path: A and P from TF32 operands; the scan's
+ * products from FP16 operands with FP32 accumulation; the state, T, the
+ * decays and all sums in FP32.  Chunks whose steepest decay is below -10 form
+ * A and P on the CUDA cores in FP32 (exact factors for any g).
  *
  *   workspace : device scratch, 16-byte aligned, of at least
  *           kda_prefill_workspace_size(...) bytes (may be NULL when that
  *           size is 0).  Its contents on entry do not matter; calls that
  *           share one workspace must be ordered on the GPU.
  */
-kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* beta, float* o,
+kda_status kda_prefill(float* state, const void* q, const void* k, const void* v,
+                       const void* g, const void* beta, float* o,
                        int t, int t_pad, int chunk, float pad_fill, int heads, int head_dim,
                        int in_dtype, int64_t qkv_row_stride, const int* cu_seqlens, int n_seqs,
                        void* workspace, size_t workspace_bytes, uint64_t stream);
@@ -153,8 +163,8 @@ kda_status kda_prefill(float* state, void* q, void* k, void* v, void* g, void* b
 /* Bytes of device workspace kda_prefill needs for `rows` token rows in total
  * (n_seqs * t_pad in the uniform form, t in the packed form) over n_seqs
  * sequences with the given chunk width and input dtype.  Returns 0 when the
- * call needs none (FP32 inputs or chunk != 64 run without one) or when an
- * argument is invalid.  The BF16, chunk-64 tensor-core path stores the
+ * call needs none (FP32 inputs run without one) or when an
+ * argument is invalid.  The BF16 tensor-core path stores the
  * state-independent operands of every (chunk, head) there: 66,176 bytes
  * per chunk of 64 tokens and head (with one chunk of slack per sequence),
  * plus (n_seqs + 1) * 4 bytes rounded up to 256, plus a 4-byte ready flag
@@ -165,8 +175,8 @@ size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads
 /*
  * kda_prefill_gated -- kda_prefill on the tensor-core path (BF16 q, k, v;
  * chunk 64) with the forget gate and beta formed inside the prepare kernel
- * from their raw inputs: the block pipeline's "kda_gate / sigmoid(b_proj)"
- * step fused into the core's g and beta loads (glm5next_kda module index;
+ * from their raw inputs: the block pipeline's gate step (the forget gate and
+ * the sigmoid of the b projection) fused into the core's g and beta loads (glm5next_kda module index;
  * Glm5NextKdaWeights dt_bias and a_log; config.rs gate_lower_bound).  Each
  * g element is read once, as BF16, and becomes
  *     g[r][h][i] = lb * sigmoid(exp(a_log[h]) * (g_raw[r][h*128 + i] + dt_bias[h*128 + i]))
@@ -204,7 +214,8 @@ kda_status kda_prefill_gated(float* state, const void* q, const void* k, const v
 
 /*
  * kda_conv_silu_l2 -- depthwise causal conv1d + SiLU, then L2 over the q and k
- * channels (block pipeline "conv1d + SiLU -> L2(q,k only)";
+ * channels (the block pipeline's front end: causal conv1d and SiLU, then L2
+ * normalisation of the q and k channels only;
  * causal_conv1d_update_l2norm at decode, conv_prefill + l2_norm_bf16 at
  * prefill; config.rs: the L2 epsilon is applied as 1/sqrt(sum + eps)).
  *
@@ -236,7 +247,8 @@ kda_status kda_conv_silu_l2(float* conv_state, const uint16_t* x, const uint16_t
 
 /*
  * kda_gate -- the forget gate and beta of the core, the block pipeline's step
- * before it ("kda_gate / sigmoid(b_proj)", glm5next_kda module index;
+ * before it (the forget gate and the sigmoid of the b projection,
+ * glm5next_kda module index;
  * Glm5NextKdaWorkspace g_raw [T, qkv], the forget-gate projection that
  * kda_gate reads, gate [T_pad, heads, head_dim], the log-decay it produces,
  * bounded below, and beta [T_pad, heads], stored after its sigmoid;
@@ -270,8 +282,9 @@ kda_status kda_gate(const uint16_t* g_raw, int64_t g_raw_stride, const float* dt
 
 /*
  * kda_o_norm_gated -- sigmoid-gated RMSNorm of the core output, the block
- * pipeline's step after the core ("sigmoid-gated RMSNorm(o_norm,
- * g_b(g_a(h)))", glm5next_kda module index; Glm5NextKdaWorkspace core,
+ * pipeline's step after the core (an RMSNorm with the o_norm weight, gated by
+ * the sigmoid of a two-stage projection of the hidden state, glm5next_kda
+ * module index; Glm5NextKdaWorkspace core,
  * out_gate and o_norm_out; config.rs o_norm [head_dim] BF16, rms_norm_eps).
  * Per token row and head, over the head's 128 channels j:
  *     out[j] = core[j] / sqrt(mean_j core[j]^2 + eps) * w[j] * sigmoid(gate[j])
@@ -327,7 +340,8 @@ kda_status kda_conv_silu_l2_k(float* conv_state, const uint16_t* x, const uint16
  * only input and output pointers from its host application, or a serving
  * loop that forbids cudaMalloc because it can synchronise the device.
  *
- *   Arguments, layouts and results are those of kda_prefill.
+ *   Arguments, layouts and results are those of kda_prefill, and so are its
+ *   refusals of invalid arguments (checked first, with the same statuses).
  *   Refused with KDA_ERR_WORKSPACE when kda_prefill_workspace_size(...) for
  *   the call exceeds KDA_STATIC_WORKSPACE_BYTES: at 32 heads that is 30
  *   chunks of 64 tokens in total (one sequence of up to 1,920 tokens); fewer
@@ -340,10 +354,11 @@ kda_status kda_conv_silu_l2_k(float* conv_state, const uint16_t* x, const uint16
  *   reads).  Calls that overlap on the GPU (other streams, other threads)
  *   race on it: order them.
  */
-kda_status kda_prefill_static_ws(float* state, void* q, void* k, void* v, void* g, void* beta,
-                                 float* o, int t, int t_pad, int chunk, float pad_fill, int heads,
-                                 int head_dim, int in_dtype, int64_t qkv_row_stride,
-                                 const int* cu_seqlens, int n_seqs, uint64_t stream);
+kda_status kda_prefill_static_ws(float* state, const void* q, const void* k, const void* v,
+                                 const void* g, const void* beta, float* o, int t, int t_pad,
+                                 int chunk, float pad_fill, int heads, int head_dim, int in_dtype,
+                                 int64_t qkv_row_stride, const int* cu_seqlens, int n_seqs,
+                                 uint64_t stream);
 
 /* Synchronises `stream`, then reads and clears the device status words of the
  * calling thread's current device.  Returns KDA_OK, KDA_ERR_DEVICE (a

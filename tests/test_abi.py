@@ -86,6 +86,8 @@ def test_prefill_refuses_bad_arguments(lib):
         return f(P, P, P, P, P, P, P, a["t"], a["t_pad"], a["chunk"], 0.0, a["heads"], a["hd"],
                  a["dt"], a["stride"], None, 1, None, 0, 0)
     assert call(chunk=48) == 2
+    assert call(chunk=256) == 2
+    assert call(chunk=128) == 3        # a supported width: refused only for the workspace
     assert call(hd=64) == 2
     assert call(t=0) == 1
     assert call(t=200) == 1            # t > t_pad
@@ -124,7 +126,8 @@ def test_workspace_size_is_queryable(lib):
     # per (chunk, head): FP16 [Ktil; Qtil] 32 KiB, [T; P] 16 KiB, Khat^T 16 KiB, dec 512 B
     assert big >= (8192 // 64) * 32 * (32768 + 16384 + 16384 + 512)
     assert f(8192, 1, 64, 32, 128, 0) == 0    # FP32 inputs need none
-    assert f(8192, 1, 32, 32, 128, 1) == 0    # other chunk widths need none
+    # BF16 inputs take the tensor-core path (64-token steps) at every width
+    assert f(8192, 1, 16, 32, 128, 1) == big and f(8192, 1, 128, 32, 128, 1) == big
     assert f(8192, 1, 64, 32, 64, 1) == 0     # invalid head_dim
 
 
@@ -133,6 +136,27 @@ def test_prefill_refuses_a_small_workspace(lib):
     f.argtypes = [V] * 7 + [I, I, I, F, I, I, I, ctypes.c_int64, V, I, V, SZ, U64]
     assert f(P, P, P, P, P, P, P, 128, 128, 64, 0.0, 2, 128, 1, 256, None, 1, P, 64, 0) == 3
     assert b"workspace" in lib.kda_last_error()
+
+
+def test_static_workspace_refuses_like_prefill(lib):
+    """kda_prefill_static_ws checks its arguments as kda_prefill does, before
+    its workspace limit, and returns the same status for the same bad call."""
+    pf = lib.kda_prefill
+    pf.argtypes = [V] * 7 + [I, I, I, F, I, I, I, ctypes.c_int64, V, I, V, SZ, U64]
+    sf = lib.kda_prefill_static_ws
+    sf.argtypes = [V] * 7 + [I, I, I, F, I, I, I, ctypes.c_int64, V, I, U64]
+    cases = [dict(t=200, t_pad=128), dict(t=0), dict(chunk=48), dict(hd=64), dict(dt=7),
+             dict(stride=100), dict(t=100, t_pad=128, cu=True), dict(t_pad=1 << 30, n=4)]
+    for c in cases:
+        a = dict(t=100, t_pad=128, chunk=64, heads=2, hd=128, dt=1, stride=256, cu=False, n=1)
+        a.update(c)
+        cu = P if a["cu"] else None
+        want = pf(P, P, P, P, P, P, P, a["t"], a["t_pad"], a["chunk"], 0.0, a["heads"], a["hd"],
+                  a["dt"], a["stride"], cu, a["n"], None, 0, 0)
+        got = sf(P, P, P, P, P, P, P, a["t"], a["t_pad"], a["chunk"], 0.0, a["heads"], a["hd"],
+                 a["dt"], a["stride"], cu, a["n"], 0)
+        assert want in (1, 2) and got == want, (c, want, got)
+        assert b"kda_prefill_static_ws" in lib.kda_last_error()
 
 
 def test_o_norm_refuses_bad_arguments(lib):

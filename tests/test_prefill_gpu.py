@@ -13,12 +13,13 @@ from _util import TOL_PREFILL, kda, rel_err
 pytestmark = pytest.mark.gpu
 
 
-def run_prefill(K, d, t, chunk, pad_fill=0.0, t_pad=None):
-    """d holds host tensors [T, H, D] / [T, H]; pads to t_pad rows (NaN there
-    first, to prove the kernel fills/ignores them) and runs one sequence."""
+def run_prefill(K, d, t, chunk, pad_fill=float("nan"), t_pad=None):
+    """d holds host tensors [T, H, D] / [T, H]; pads to t_pad rows with
+    pad_fill (NaN by default, to prove the kernels never read them) and runs
+    one sequence."""
     T = d["q"].shape[0]
     t_pad = t_pad or T
-    dev = {n: wl.pad_rows(d[n][:t], t_pad, float("nan")).cuda()
+    dev = {n: wl.pad_rows(d[n][:t], t_pad, pad_fill).cuda()
            for n in ("q", "k", "v", "g", "beta")}
     S = d["state"].clone().cuda()
     o = torch.full((t_pad,) + tuple(d["q"].shape[1:]), 12345.0, device="cuda")
@@ -40,8 +41,12 @@ def test_tiny_config_matches_oracle(orc):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("chunk,t", [(16, 77), (32, 100), (64, 200), (64, 64), (64, 1),
-                                     (16, 16), (64, 129)])
+                                     (16, 16), (64, 129), (128, 300), (128, 77), (128, 128)])
 def test_prefill_matches_oracle(orc, dtype, chunk, t):
+    """Every chunk width the boundary accepts, whole and ragged last chunks:
+    BF16 inputs on the tensor-core kernels (64-token steps whatever the
+    width), FP32 on the SIMT kernel (chunks of min(chunk, 64)) or, for t <= 8,
+    the row walk."""
     K = kda()
     d = wl.prefill(seed=t + chunk, t=t, heads=3, chunk=chunk, dtype=dtype)
     o, S, _ = run_prefill(K, d, t, chunk)
@@ -65,7 +70,7 @@ def test_pad_fill_has_no_effect(t, t_pad):
         assert torch.equal(o[:t], o0[:t])
         assert torch.equal(S, S0)
         assert (o[t:] == 12345.0).all()
-    # the library wrote the fill value into the padded rows
+    # the caller's tails are left as they were (the library never writes them)
     assert torch.isnan(runs[1][2]["q"][t:].float()).all()
     assert (runs[2][2]["g"][t:].float() > 1e29).all()
     assert (dev0["beta"][t:].float() == 0).all()
