@@ -174,6 +174,13 @@ def barrier(world: int):
 
 # ------------------------------------------------------------------- GPU arm
 
+def hbm_frac(gbs: float, peak: float):
+    """The fraction of the measured HBM copy peak, or None above 1: a figure
+    over the copy peak means part of the traffic came from L2 and is not an
+    HBM number."""
+    f = gbs / peak
+    return f if f <= 1.0 else None
+
 def time_launches(fn, n: int, stream):
     """Runs fn() n times back to back between one pair of events on `stream`;
     returns (the per-call ms as a list of n equal values, the total ms).
@@ -229,32 +236,46 @@ def run_gpu(args):
         ms_step = max_over_ranks(total_ms / args.steps, world, dev)
 
         # ---------------- decode workload: 100 chained steps
+        # Two batches of 64 sequences (two state sets of 128 MiB) take turns,
+        # as two micro-batches of a serving loop would: each step's state was
+        # last touched two steps ago, with the other 128 MiB set in between,
+        # so the L2 (129 MB) cannot hold it from one step to its next.  The
+        # single-set figure (state partly L2-resident) is reported beside it.
         dd = wl.decode_steps()
-        dS = dd["state"].to(dev)
+        dS_sets = [dd["state"].to(dev), dd["state"].to(dev)]
         dq, dk, dv, dg, db = (dd[n].to(dev) for n in ("q", "k", "v", "g", "beta"))
         do = torch.empty((DECODE_N, H, D), device=dev)
         step = [0]
+        sets_used = [2]
 
         def decode():
             t = step[0] % DECODE_STEPS
-            K.kda_decode(dS, dq[t], dk[t], dv[t], dg[t], db[t], do)
+            K.kda_decode(dS_sets[step[0] % sets_used[0]], dq[t], dk[t], dv[t], dg[t], db[t], do)
             step[0] += 1
 
         for _ in range(5):
             decode()
         # The chain of 100 steps is the unit: one event pair around it, so the
         # launches follow each other as in a serving loop; reported per step.
-        dec_per = []
-        for _ in range(3):
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(DECODE_STEPS):
-                decode()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            dec_per.append(e0.elapsed_time(e1) / DECODE_STEPS)
-        dec_per = [statistics.median(dec_per)]
-        del dq, dk, dv, dg, db, dS
+        def decode_chain():
+            per = []
+            for _ in range(3):
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(DECODE_STEPS):
+                    decode()
+                e1.record(stream)
+                torch.cuda.synchronize()
+                per.append(e0.elapsed_time(e1) / DECODE_STEPS)
+            return [statistics.median(per)]
+
+        dec_per = decode_chain()
+        sets_used[0] = 1
+        for _ in range(5):
+            decode()
+        dec1_per = decode_chain()
+        del dq, dk, dv, dg, db, dS_sets
 
         # ---------------- decode_k workload
         kd = wl.decode_k()
@@ -312,18 +333,24 @@ def run_gpu(args):
 
         # ---------------- gated RMSNorm of a prefill-sized core output
         ngen = torch.Generator(device="cpu").manual_seed(0)
-        n_core = torch.randn((T_PREFILL, H, D), generator=ngen).to(dev)
-        n_gate = torch.randn((T_PREFILL, H * D), generator=ngen).to(torch.bfloat16).to(dev)
+        # Two input/output sets, alternated (537 MB touched per pair of
+        # launches), so no launch finds its inputs in L2.
+        n_sets = [(torch.randn((T_PREFILL, H, D), generator=ngen).to(dev),
+                   torch.randn((T_PREFILL, H * D), generator=ngen).to(torch.bfloat16).to(dev),
+                   torch.empty((T_PREFILL, H * D), dtype=torch.bfloat16, device=dev))
+                  for _ in range(2)]
         n_w = torch.ones(D, dtype=torch.bfloat16, device=dev)
-        n_out = torch.empty((T_PREFILL, H * D), dtype=torch.bfloat16, device=dev)
+        n_turn = [0]
 
         def o_norm():
+            n_core, n_gate, n_out = n_sets[n_turn[0]]
+            n_turn[0] ^= 1
             K.kda_o_norm_gated(n_core, n_gate, n_w, n_out)
 
         for _ in range(3):
             o_norm()
         on_per, _ = time_launches(o_norm, 20, stream)
-        del n_core, n_gate, n_out
+        del n_sets
 
         # ---------------- forget gate and beta of a prefill-sized problem
         # Two input/output sets, alternated: consecutive launches touch 270 MB,
@@ -465,6 +492,7 @@ def run_gpu(args):
     t_flops = PREFILL_FLOPS / (tf32_peak * 1e12)
     bound = "hbm" if t_bytes >= t_flops else "tensor"
     dec_s = statistics.mean(dec_per) / 1e3
+    dec1_s = statistics.mean(dec1_per) / 1e3
     dk_s = statistics.mean(dk_per) / 1e3
     value = world * T_PREFILL / (ms_step / 1e3)
     out = {
@@ -478,13 +506,14 @@ def run_gpu(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32",
+        "dtype": "bf16 in; tf32 (A, P) and fp16 (scan) tensor-core operands; "
+                 "fp32 accumulate, T solve and state",
         "data": "synthetic",
         "config": {
             "workload": wl.PREFILL.name,
             "description": wl.PREFILL.description,
             "seq_len": T_PREFILL, "heads": H, "head_dim": D, "chunk": CHUNK,
-            "global_batch": world, "in_dtype": "bf16",
+            "global_batch": world, "in_dtype": "bf16", "out_dtype": "f32 (o), f32 (state)",
             "l2": "inputs larger than L2 (400 MB per step), no flush",
             "parallelism": "replicas" if world > 1 else "single GPU",
         },
@@ -517,6 +546,11 @@ def run_gpu(args):
             "frac_of_hbm_peak": DECODE_BYTES / dec_s / 1e9 / pk["hbm_gbs"],
             "us_per_step": dec_s * 1e6, "algorithmic_bytes": DECODE_BYTES,
             "steps": DECODE_STEPS,
+            "l2": "two state sets of 128 MiB alternated step by step (256 MiB), no flush",
+            "single_state_set": {
+                "value": DECODE_BYTES / dec1_s / 1e9, "unit": "GB/s",
+                "us_per_step": dec1_s * 1e6,
+                "l2": "one 128 MiB state set, partly L2-resident between steps"},
         },
         "decode_k": {
             "workload": wl.DECODE_K.name, "value": DK_BYTES / dk_s / 1e9, "unit": "GB/s",
@@ -541,9 +575,11 @@ def run_gpu(args):
         "o_norm": {
             "workload": "sigmoid-gated RMSNorm of a prefill-sized core output (8192 x 32 x 128)",
             "value": ONORM_BYTES / (statistics.mean(on_per) / 1e3) / 1e9, "unit": "GB/s",
-            "frac_of_hbm_peak": ONORM_BYTES / (statistics.mean(on_per) / 1e3) / 1e9
-            / pk["hbm_gbs"],
+            "frac_of_hbm_peak": hbm_frac(ONORM_BYTES / (statistics.mean(on_per) / 1e3) / 1e9,
+                                         pk["hbm_gbs"]),
             "us_per_call": statistics.mean(on_per) * 1e3, "algorithmic_bytes": ONORM_BYTES,
+            "l2": "two input/output sets alternated (537 MB touched per pair of launches), "
+                  "no flush",
         },
         "prefill_gated": {
             "workload": "the prefill step (8192 x 32 heads, BF16) with g and beta formed in "
@@ -686,11 +722,16 @@ def run_case(args):
             K.kda_gate(g_raw, g_dt, g_al, g_b, g_out, g_beta, -5.0)
         nbytes = args.seq_len * H * (D * 4 + 4) + H * D * 4 + H * 4
     elif args.case == "decode":
+        # two state sets alternated, as in the full run (256 MiB, beyond L2)
         dd = wl.decode_steps(steps=1)
-        S = dd["state"].to(dev)
+        S_sets = [dd["state"].to(dev), dd["state"].to(dev)]
         ins = [dd[n][0].to(dev) for n in ("q", "k", "v", "g", "beta")]
         o = torch.empty((DECODE_N, H, D), device=dev)
-        fn = lambda: K.kda_decode(S, *ins, o)
+        turn = [0]
+
+        def fn():
+            K.kda_decode(S_sets[turn[0]], *ins, o)
+            turn[0] ^= 1
         nbytes = DECODE_BYTES
     elif args.case == "conv":
         fe = wl.frontend(lengths=[args.seq_len])
@@ -719,6 +760,21 @@ def run_case(args):
                       "GBps": nbytes / us / 1e3}))
 
 
+def spawn_replicas(n: int) -> int:
+    """`python bench.py --gpus N` without a launcher: re-runs this command as N
+    ranks (one process per GPU) under torch.distributed.run, as the multi-GPU
+    launch does, and returns its exit code."""
+    import socket
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           "--nproc-per-node", str(n), "--master-addr", "127.0.0.1", "--master-port", str(port),
+           os.path.abspath(__file__)] + sys.argv[1:]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -734,6 +790,11 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    _, world, _ = dist_env()
+    if args.gpus != world and not args.case:
+        if "RANK" in os.environ or args.gpus < 1:
+            ap.error("--gpus %d does not match WORLD_SIZE=%d" % (args.gpus, world))
+        sys.exit(spawn_replicas(args.gpus))
     if args.case:
         run_case(args)
     elif args.impl == "reference":

@@ -12,9 +12,9 @@ void set_error(const char* fmt, ...) {
     va_end(ap);
 }
 
-bool fault_injected() {
+bool fault_injected(const char* what) {
     const char* s = getenv("KDA_FAULT_INJECT");
-    return s && strcmp(s, "launch") == 0;
+    return s && strcmp(s, what) == 0;
 }
 
 }  // namespace kda

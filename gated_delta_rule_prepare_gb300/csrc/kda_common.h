@@ -19,9 +19,18 @@ constexpr int D = KDA_HEAD_DIM;
 // Thread-local last-error text (kda_last_error).
 void set_error(const char* fmt, ...);
 
-// Returns true when KDA_FAULT_INJECT=launch is set: the API then reports a
-// launch failure without enqueuing anything (host-side failure testing).
-bool fault_injected();
+// Returns true when the environment variable KDA_FAULT_INJECT equals `what`
+// (failure testing, read per call):
+//   "launch"     -- the API reports a launch failure without enqueuing anything;
+//   "ready_wait" -- the fused prefill grid's prepare CTAs release no ready
+//                   flag and the chains' flag wait is cut to a few
+//                   milliseconds, so the waits run out on the device, the
+//                   kernel still returns, and kda_sync_status reports
+//                   KDA_ERR_DEVICE (a bounded wait timed out).
+bool fault_injected(const char* what = "launch");
+
+// Values of the fused prefill grid's `fault` argument.
+enum : uint32_t { FAULT_NONE = 0, FAULT_READY_WAIT = 1 };
 
 inline cudaStream_t as_stream(uint64_t s) { return reinterpret_cast<cudaStream_t>(s); }
 
@@ -40,7 +49,13 @@ cudaError_t read_and_clear_status_prefill(unsigned* out);
 cudaError_t read_and_clear_status_conv(unsigned* out);
 cudaError_t read_and_clear_status_prefill_tc(unsigned* out);
 
-// Tensor-core prefill for BF16 inputs and chunk 64 (prefill_tc.cu): its
+// kda_prefill's argument checks, shared with kda_prefill_static_ws (prefill.cu).
+kda_status validate_prefill(const char* fn, const float* state, const void* q, const void* k,
+                            const void* v, const void* g, const void* beta, const float* o,
+                            int t, int t_pad, int chunk, int heads, int head_dim, int in_dtype,
+                            int64_t qkv_row_stride, const int* cu_seqlens, int n_seqs);
+
+// Tensor-core prefill for BF16 inputs (prefill_tc.cu): its
 // workspace size for `rows` token rows, and the launch (arguments validated by
 // kda_prefill).
 size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads);

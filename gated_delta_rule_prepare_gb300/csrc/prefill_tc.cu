@@ -366,7 +366,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                                              const int* __restrict__ cu, int n_seqs,
                                              unsigned char* __restrict__ ws, long long first,
                                              long long stride, unsigned* __restrict__ ready,
-                                             long long ready_pitch) {
+                                             long long ready_pitch, bool publish = true) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column quarter
@@ -473,7 +473,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         if (ready && copier && pending >= 0) {
             tc::bulk_wait_all();
             const long long pg = pending / heads;  // flags are head-major: [heads][pitch]
-            tc::flag_release(ready + (pending - pg * heads) * ready_pitch + pg, 1u);
+            if (publish) tc::flag_release(ready + (pending - pg * heads) * ready_pitch + pg, 1u);
             pending = -1;
         }
     };
@@ -1116,7 +1116,8 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
                                             const int* __restrict__ cu, int n_seqs,
                                             const unsigned char* __restrict__ ws, int h, int n,
                                             const unsigned* __restrict__ ready,
-                                            long long ready_pitch) {
+                                            long long ready_pitch,
+                                            uint32_t acquire_iters = 1u << 22) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
     const int qd = warp & 3, cg = warp >> 2;  // TMEM lane quarter, column group
@@ -1200,7 +1201,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         if (!ready || gg <= acq_hi) return true;
         const unsigned* fh = ready + (size_t)h * ready_pitch;
         const long long g4 = gg & ~3LL;
-        for (uint32_t it = 0; it < (1u << 22); ++it) {
+        for (uint32_t it = 0; it < acquire_iters; ++it) {
             const uint4 f = tc::flags4_acquire(fh + g4);
             // the four flags as a bit mask (a runtime-indexed array would live
             // in local memory)
@@ -1479,15 +1480,20 @@ prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constan
                      const __grid_constant__ CUtensorMap omap, const uint16_t* __restrict__ beta, float* __restrict__ state,
                      float* __restrict__ o, int t, int t_pad, int heads,
                      const int* __restrict__ cu, int n_seqs, unsigned char* __restrict__ ws,
-                     unsigned* __restrict__ ready, long long ready_pitch) {
+                     unsigned* __restrict__ ready, long long ready_pitch, uint32_t fault) {
+    // fault == FAULT_READY_WAIT (a test of the bounded flag wait, set only
+    // through KDA_FAULT_INJECT): prepare releases no flag and each chain's
+    // wait gives up after a few milliseconds, so every chain records
+    // STATUS_TIMEOUT and returns without writing o or the state.
+    const bool inject = fault == FAULT_READY_WAIT;
     const int chains = n_seqs * heads;
     if ((int)blockIdx.x < chains)
         scan_t_role(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
-                    (int)blockIdx.x / heads, ready, ready_pitch);
+                    (int)blockIdx.x / heads, ready, ready_pitch, inject ? 1u << 12 : 1u << 22);
     else
         prepare_role<GATED>(maps, beta, t, t_pad, heads, cu, n_seqs, ws,
                             (long long)blockIdx.x - chains, (long long)gridDim.x - chains, ready,
-                            ready_pitch);
+                            ready_pitch, !inject);
 }
 
 // The chains of the two-kernel path: one CTA per (sequence, head), after
@@ -1611,7 +1617,8 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         cfg.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg, fused_k, maps, vmap, omap, (const uint16_t*)beta,
                                state, o, t, t_pad, heads, cu, n_seqs, ws, ready,
-                               ready_pitch(chunk_bound));
+                               ready_pitch(chunk_bound),
+                               fault_injected("ready_wait") ? (uint32_t)FAULT_READY_WAIT : 0u);
         if (e == cudaSuccess) return launch_result("kda_prefill (fused)");
         // the grid could not be made resident (e.g. SMs held by other work):
         // run the two kernels instead

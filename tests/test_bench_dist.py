@@ -51,8 +51,8 @@ def test_max_over_ranks_gloo_world2():
 
 def test_reference_arm_prints_on_rank0_only():
     env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
-                        "--steps", "1", "--warmup", "3"], env=env, capture_output=True,
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--steps", "1", "--warmup", "3"], env=env, capture_output=True,
                        text=True, timeout=600)
     assert r.returncode == 0 and r.stdout.strip() == ""
 
@@ -66,3 +66,28 @@ def test_reference_arm_line_shape():
     assert line["impl"] == "reference" and line["unit"] == "tokens/s"
     assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["cores"] >= 1
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["value"] > 0
+
+
+def test_gpus_must_match_world_size():
+    """Under a launcher (RANK set), --gpus N with N != WORLD_SIZE is an error."""
+    env = dict(os.environ, RANK="0", WORLD_SIZE="2", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "4",
+                        "--impl", "reference", "--steps", "1", "--warmup", "3"], env=env,
+                       capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0 and "does not match WORLD_SIZE=2" in r.stderr
+
+
+def test_gpus_without_launcher_spawns_replicas():
+    """`bench.py --gpus 2` with no launcher re-runs itself as two ranks under
+    torch.distributed.run (on CPU through the reference arm, which needs no
+    GPU); rank 0 alone prints the one JSON line and reports n_gpus = 2."""
+    env = {k: v for k, v in os.environ.items()
+           if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT")}
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--steps", "1", "--warmup", "3"], env=env,
+                       capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2

@@ -22,9 +22,10 @@ def inputs(seed, t, g_low=-5.0):
     return d
 
 
-def run(K, d, t, t_pad=None, pad_fill=0.0, cu=False, workspace=None):
+def run(K, d, t, t_pad=None, pad_fill=float("nan"), cu=False, workspace=None):
+    """Rows [t, t_pad) hold pad_fill (the caller's tail; NaN by default)."""
     t_pad = t_pad or t
-    dev = {n: wl.pad_rows(d[n][:t], t_pad, float("nan")).cuda()
+    dev = {n: wl.pad_rows(d[n][:t], t_pad, pad_fill).cuda()
            for n in ("q", "k", "v", "g", "beta")}
     S = d["state"].clone().cuda()
     o = torch.full((t_pad, H, 128), 12345.0, device="cuda")
@@ -167,3 +168,31 @@ def test_steep_decay_matches_oracle_on_both_paths(orc, monkeypatch, impl):
     o_ref, S_ref = oracle_all_heads(orc, d, t)
     assert rel_err(o, o_ref) < TOL_PREFILL
     assert rel_err(S[0], S_ref) < TOL_PREFILL
+
+
+def test_bounded_ready_wait_runs_out_and_reports(orc, monkeypatch):
+    """The chains' wait on a ready flag is bounded.  KDA_FAULT_INJECT=ready_wait
+    makes the prepare CTAs release no flag and cuts the wait to a few
+    milliseconds: every chain gives up, the kernel still returns, and
+    kda_sync_status reports KDA_ERR_DEVICE with the timeout text.  No chain
+    writes its state or o, and the next call on the same context is correct."""
+    K = kda()
+    t = 256
+    d = inputs(21, t)
+    dev = {n: d[n].cuda() for n in ("q", "k", "v", "g", "beta")}
+    S = d["state"].clone().cuda()
+    o = torch.full((t, H, 128), 12345.0, device="cuda")
+    monkeypatch.setenv("KDA_FAULT_INJECT", "ready_wait")
+    K.kda_prefill(S, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], o, t, 64)
+    with pytest.raises(K.KdaError) as err:
+        K.kda_sync_status()
+    assert err.value.status == 5  # KDA_ERR_DEVICE
+    assert "a bounded wait timed out" in str(err.value)
+    assert torch.equal(S.cpu(), d["state"])
+    assert (o == 12345.0).all()
+    monkeypatch.delenv("KDA_FAULT_INJECT")
+    K.kda_sync_status()  # the status word was cleared by the read above
+    o2, S2 = run(K, d, t)
+    o_ref, S_ref = oracle_all_heads(orc, d, t)
+    assert rel_err(o2, o_ref) < TOL_PREFILL
+    assert rel_err(S2[0], S_ref) < TOL_PREFILL
