@@ -692,6 +692,20 @@ def run_case(args):
         fn = lambda: K.kda_prefill(S, q, k, v, g, beta, o, args.seq_len, CHUNK, workspace=ws)
         nbytes = 4 * args.seq_len * H * D * 2 + args.seq_len * H * 2 + args.seq_len * H * D * 4 \
             + 2 * H * D * D * 4
+    elif args.case == "prefill_o_norm":
+        d = wl.prefill(t=args.seq_len)
+        q, k, v, g, beta = (d[n].to(dev) for n in ("q", "k", "v", "g", "beta"))
+        S = d["state"].to(dev)
+        ngen = torch.Generator(device="cpu").manual_seed(3)
+        n_gate = torch.randn((args.seq_len, H * D), generator=ngen).to(torch.bfloat16).to(dev)
+        n_w = torch.ones(D, dtype=torch.bfloat16, device=dev)
+        n_out = torch.empty((args.seq_len, H * D), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(K.kda_prefill_workspace_size(args.seq_len, 1, CHUNK, H),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: K.kda_prefill_o_norm(S, q, k, v, g, beta, n_gate, n_w, n_out, args.seq_len,
+                                          CHUNK, workspace=ws)
+        nbytes = 4 * args.seq_len * H * D * 2 + args.seq_len * H * 2 + 2 * args.seq_len * H * D * 2 \
+            + 2 * H * D * D * 4 + D * 2
     elif args.case == "prefill_gated":
         d = wl.prefill_gated(t=args.seq_len)
         q, k, v = (d[n].to(dev) for n in ("q", "k", "v"))
@@ -784,7 +798,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    choices=["prefill", "prefill_gated", "decode", "decode_k", "conv", "gate"],
+                    choices=["prefill", "prefill_gated", "prefill_o_norm", "decode", "decode_k",
+                             "conv", "gate"],
                     help="time one kernel alone (for profiler captures)")
     ap.add_argument("--seq-len", type=int, default=T_PREFILL)
     args = ap.parse_args()

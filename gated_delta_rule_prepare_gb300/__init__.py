@@ -7,7 +7,8 @@ library's CUDA kernels; there is no fallback.  Importing this package on a
 machine without the built library raises immediately.
 
 Entry points (same names as the C ABI): ``kda_decode``, ``kda_decode_k``,
-``kda_prefill``, ``kda_prefill_gated``, ``kda_conv_silu_l2``, ``kda_conv_silu_l2_k``,
+``kda_prefill``, ``kda_prefill_gated``, ``kda_prefill_o_norm``, ``kda_conv_silu_l2``,
+``kda_conv_silu_l2_k``,
 ``kda_gate``, ``kda_o_norm_gated``, ``kda_prefill_workspace_size``, ``kda_sync_status``.
 ``kda_prefill_static_ws`` is reached through ``LIB`` (its callers hold raw pointers).
 """
@@ -52,6 +53,8 @@ def _load():
         "kda_prefill_gated": [_vp] * 5 + [_i64, _vp, _vp, _f, _vp, _i64, _vp, _i, _i, _i, _i,
                                           _i64, _vp, _i, _vp, _sz, _u64],
         "kda_conv_silu_l2_k": [_vp] * 4 + [_i, _i, _i, _f, _i, _i, _vp, _i, _u64],
+        "kda_prefill_o_norm": [_vp] * 7 + [_i64, _vp, _f, _vp, _i64, _i, _i, _i, _i, _i, _i,
+                                           _i64, _vp, _i, _vp, _sz, _u64],
     }
     for name, args in sig.items():
         fn = getattr(lib, name)
@@ -197,6 +200,73 @@ def kda_prefill(state, q, k, v, g, beta, o, t, chunk, pad_fill=0.0, cu_seqlens=N
                            _ptr(o, torch.float32, "o"), int(t), int(t_pad), int(chunk),
                            float(pad_fill), H, HEAD_DIM, in_dtype, int(stride),
                            _ptr(cu_seqlens), n_seqs, ws_ptr, ws_bytes, _stream(state)))
+
+
+def _row_view(x, rows, hd, name):
+    """(pointer, token-row stride) of a BF16 [rows, >= hd] view with unit
+    channel stride, or of any contiguous tensor of rows x hd values."""
+    if x.dtype != torch.bfloat16 or not x.is_cuda:
+        raise TypeError("%s must be a CUDA bfloat16 tensor" % name)
+    if x.is_contiguous() and x.numel() == rows * hd:
+        return x.data_ptr(), hd
+    if x.dim() == 2 and x.shape[0] == rows and x.shape[1] >= hd and x.stride(1) == 1:
+        return x.data_ptr(), x.stride(0)
+    raise ValueError("%s must hold rows x heads*128 values (contiguous, or a 2-D row view)" % name)
+
+
+def kda_prefill_o_norm(state, q, k, v, g, beta, gate, w, out, t, chunk=64, eps=1e-6,
+                       cu_seqlens=None, workspace=None):
+    """kda_prefill with the sigmoid-gated RMSNorm fused into its epilogue (BF16
+    inputs, tensor-core path): writes out BF16 [rows, H*128] =
+    rmsnorm(o) * w * sigmoid(gate) instead of the FP32 core output o.  gate
+    and out: BF16 with rows x H*128 values (contiguous, or 2-D row views);
+    w: BF16 [128].  The other arguments are kda_prefill's."""
+    if q.dtype != torch.bfloat16:
+        raise TypeError("kda_prefill_o_norm: inputs must be bfloat16")
+    H = q.shape[-2]
+    if q.shape[-1] != HEAD_DIM:
+        raise ValueError("kda_prefill_o_norm: head_dim must be 128")
+    for n_, t_ in (("q", q), ("k", k), ("v", v)):
+        if t_.dtype != q.dtype or t_.stride(-1) != 1 or t_.stride(-2) != HEAD_DIM:
+            raise ValueError("kda_prefill_o_norm: %s must have unit channel stride and heads "
+                             "packed" % n_)
+    stride = q.stride(-3)
+    if k.stride(-3) != stride or v.stride(-3) != stride:
+        raise ValueError("kda_prefill_o_norm: q, k, v must share one token-row stride")
+    for n_, t_ in (("g", g), ("beta", beta), ("state", state), ("w", w)):
+        _contig(t_, n_)
+    if g.dtype != q.dtype or beta.dtype != q.dtype:
+        raise TypeError("kda_prefill_o_norm: g and beta must have the inputs' dtype")
+    if cu_seqlens is not None:
+        n_seqs = cu_seqlens.numel() - 1
+        t_pad = t
+        if cu_seqlens.dtype != torch.int32 or not cu_seqlens.is_cuda:
+            raise TypeError("kda_prefill_o_norm: cu_seqlens must be a CUDA int32 tensor")
+    else:
+        if q.dim() == 3:
+            n_seqs, t_pad = 1, q.shape[0]
+        else:
+            n_seqs, t_pad = q.shape[0], q.shape[1]
+            if q.dim() == 4 and q.stride(0) != t_pad * stride:
+                raise ValueError("kda_prefill_o_norm: sequences must be consecutive row blocks")
+    rows = t if cu_seqlens is not None else n_seqs * t_pad
+    if g.numel() != rows * H * HEAD_DIM or beta.numel() != rows * H:
+        raise ValueError("kda_prefill_o_norm: g/beta sizes do not match the token rows")
+    if state.numel() != n_seqs * H * HEAD_DIM * HEAD_DIM or state.dtype != torch.float32:
+        raise ValueError("kda_prefill_o_norm: state must be FP32 [N, H, 128, 128]")
+    if w.numel() != HEAD_DIM or w.dtype != torch.bfloat16:
+        raise ValueError("kda_prefill_o_norm: w must be BF16 [128]")
+    g_ptr, g_stride = _row_view(gate, rows, H * HEAD_DIM, "gate")
+    o_ptr, o_stride = _row_view(out, rows, H * HEAD_DIM, "out")
+    ws_need = kda_prefill_workspace_size(rows, n_seqs, chunk, H, q.dtype)
+    if workspace is None:
+        workspace = torch.empty(max(ws_need, 1), dtype=torch.uint8, device=q.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(LIB.kda_prefill_o_norm(_ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                  g_ptr, int(g_stride), _ptr(w), float(eps), o_ptr,
+                                  int(o_stride), int(t), int(t_pad), int(chunk), H, HEAD_DIM,
+                                  BF16, int(stride), _ptr(cu_seqlens), n_seqs,
+                                  workspace.data_ptr(), ws_bytes, _stream(state)))
 
 
 def kda_prefill_gated(state, q, k, v, g_raw, dt_bias, a_log, b_raw, o, t, gate_lower_bound,

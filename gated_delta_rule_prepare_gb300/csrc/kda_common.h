@@ -69,10 +69,22 @@ struct PrefillGate {
     long long g_stride;    // elements between token rows of g_raw
     long long b_stride;    // elements between token rows of b_raw
 };
+// The sigmoid-gated RMSNorm fused into the tensor-core prefill's epilogue
+// (kda_prefill_o_norm): BF16 gate and output [rows][heads * 128] with their
+// row pitches, the BF16 o_norm weight [128] and epsilon.
+struct PrefillNorm {
+    const uint16_t* gate;
+    long long gate_stride;
+    const uint16_t* w;
+    float eps;
+    uint16_t* out;
+    long long out_stride;
+};
 kda_status launch_prefill_tc(float* state, const void* q, const void* k, const void* v,
                              const void* g, const void* beta, float* o, int t, int t_pad,
                              int heads, long long stride, const int* cu, int n_seqs,
-                             void* workspace, cudaStream_t s, const PrefillGate* gate = nullptr);
+                             void* workspace, cudaStream_t s, const PrefillGate* gate = nullptr,
+                             const PrefillNorm* norm = nullptr);
 
 // decode_k's row walk (decode.cu) for kda_prefill's short FP32 sequences:
 // n_seqs sequences of krows token rows, sequence n starting at row

@@ -392,3 +392,43 @@ extern "C" kda_status kda_prefill_gated(float* state, const void* q, const void*
                              (long long)qkv_row_stride, cu_seqlens, n_seqs, workspace,
                              as_stream(stream), &gate);
 }
+
+extern "C" kda_status kda_prefill_o_norm(float* state, const void* q, const void* k,
+                                         const void* v, const void* g, const void* beta,
+                                         const uint16_t* gate, int64_t gate_stride,
+                                         const uint16_t* w_norm, float eps, uint16_t* out,
+                                         int64_t out_stride, int t, int t_pad, int chunk,
+                                         int heads, int head_dim, int in_dtype,
+                                         int64_t qkv_row_stride, const int* cu_seqlens,
+                                         int n_seqs, void* workspace, size_t workspace_bytes,
+                                         uint64_t stream) {
+    const char* fn = "kda_prefill_o_norm";
+    // the output stands in for o in the shared checks (non-null, 16-byte aligned)
+    const kda_status vs = validate_prefill(fn, state, q, k, v, g, beta,
+                                           reinterpret_cast<const float*>(out), t, t_pad, chunk,
+                                           heads, head_dim, in_dtype, qkv_row_stride, cu_seqlens,
+                                           n_seqs);
+    if (vs != KDA_OK) return vs;
+    KDA_REQUIRE(in_dtype == KDA_BF16 && !simt_pinned(), KDA_ERR_UNSUPPORTED,
+                "%s: the fused norm runs on the BF16 tensor-core path only", fn);
+    KDA_REQUIRE(gate && w_norm, KDA_ERR_INVALID_ARG, "%s: null gate or o_norm weight", fn);
+    KDA_REQUIRE(aligned16(gate) && (reinterpret_cast<uintptr_t>(w_norm) & 7u) == 0,
+                KDA_ERR_INVALID_ARG, "%s: gate must be 16-byte and w 8-byte aligned", fn);
+    KDA_REQUIRE(gate_stride >= (int64_t)heads * D && gate_stride % 8 == 0 &&
+                    out_stride >= (int64_t)heads * D && out_stride % 8 == 0,
+                KDA_ERR_INVALID_ARG,
+                "%s: gate_stride and out_stride must be >= heads * 128 and multiples of 8", fn);
+    KDA_REQUIRE(eps >= 0.f && eps < INFINITY, KDA_ERR_INVALID_ARG,
+                "%s: eps must be finite and >= 0", fn);
+    const long long rows = cu_seqlens ? (long long)t : (long long)t_pad * n_seqs;
+    const size_t need = kda_prefill_workspace_size(rows, n_seqs, chunk, heads, head_dim, in_dtype);
+    KDA_REQUIRE(workspace && workspace_bytes >= need, KDA_ERR_WORKSPACE,
+                "%s: workspace of %zu B given, %zu B needed", fn, workspace_bytes, need);
+    KDA_REQUIRE(aligned16(workspace), KDA_ERR_INVALID_ARG, "%s: workspace must be 16-byte aligned",
+                fn);
+    KDA_REQUIRE(!fault_injected(), KDA_ERR_CUDA, "%s: injected launch failure", fn);
+    const PrefillNorm nrm = {gate, (long long)gate_stride, w_norm, eps, out, (long long)out_stride};
+    return launch_prefill_tc(state, q, k, v, g, beta, nullptr, t, t_pad, heads,
+                             (long long)qkv_row_stride, cu_seqlens, n_seqs, workspace,
+                             as_stream(stream), nullptr, &nrm);
+}

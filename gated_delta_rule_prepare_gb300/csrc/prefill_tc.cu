@@ -213,11 +213,31 @@ struct PrepMaps {
     long long b_stride;  // elements between token rows of beta
 };
 
+// The sigmoid-gated RMSNorm fused into the scan's epilogue (kda_prefill_o_norm):
+// the gate tiles' load map and the BF16 output's store map (both [rows][heads
+// x 128], boxes of 128 channels x 64 tokens), the o_norm weight, epsilon, and
+// the output again for plain stores (row pitch in elements).
+struct NormArgs {
+    CUtensorMap gmap, nmap;
+    const uint16_t* w;
+    uint16_t* out;
+    long long out_pitch;
+    float eps;
+};
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 // sigmoid(z) = 1 / (1 + 2^(-z log2 e)) by the hardware 2^x and 1/x.
 __device__ __forceinline__ float sigmoid_hw(float z) {
     return rcp_approx(__fadd_rn(ex2_approx(__fmul_rn(z, -kLog2e)), 1.0f));
+}
+// sigmoid(z) = (1 + tanh(z / 2)) / 2 by the hardware tanh: one special-
+// function operation (absolute error about 2^-11 relative to 1), for the
+// fused norm's BF16 output.
+__device__ __forceinline__ float sigmoid_tanh(float z) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * z));
+    return __fmaf_rn(0.5f, t, 0.5f);
 }
 // lb * sigmoid(c (x + dt)) given nc = -c log2 e.
 __device__ __forceinline__ float gate_hw(float x, float dt, float nc, float lb) {
@@ -1075,12 +1095,15 @@ struct ScanT {
     // (no swizzle), group 1 of [T; P] | Khat^T | dec, group 1 of
     // [Ktil; Qtil], the O staging tile [64][128] FP32, barriers
     static constexpr uint32_t BGRP = BLOB_BYTES - BLOB_TP;  // [T; P] | Khat^T | dec
-    static constexpr uint32_t RAWV = (BLOB_BYTES + 1023) & ~1023u;
+    static constexpr uint32_t RAWV = (BLOB_BYTES + 127) & ~127u;
     static constexpr uint32_t TP1 = RAWV + 64 * D * 2;
-    static constexpr uint32_t OPX1 = (TP1 + BGRP + 1023) & ~1023u;
+    static constexpr uint32_t OPX1 = (TP1 + BGRP + 127) & ~127u;
     static constexpr uint32_t OST = OPX1 + OpXh::bytes(128);
     static constexpr uint32_t RAWV1 = OST + 64 * D * 4;  // the second value tile
-    static constexpr uint32_t BAR = RAWV1 + 64 * D * 2;
+    // two gate tiles ([64][128] BF16, kda_prefill_o_norm) by chunk parity;
+    // each is overwritten in place by its chunk's normalised output
+    static constexpr uint32_t GATE0 = RAWV1 + 64 * D * 2, GATE1 = GATE0 + 64 * D * 2;
+    static constexpr uint32_t BAR = GATE1 + 64 * D * 2;
     static constexpr uint32_t TOTAL = BAR + 128;
     // TMEM columns: S^T (A, FP16 pairs: 64 columns), T X (64); two
     // 128-column chunk regions used alternately: chunk g computes Ktil S |
@@ -1110,13 +1133,20 @@ struct ScanT {
 // per-thread global stores of O cost the chain about 1.4K cycles per chunk
 // while the prepare CTAs keep the memory system busy.  Rows of a partial
 // chunk go out by plain stores.
+// NORM (kda_prefill_o_norm): O is not written.  The staged O tile of chunk
+// g - 1 is normalised at the start of chunk g + 1, while its first product
+// runs, by warps 8..15 (the sigmoid-gated RMSNorm with the tile's BF16 gate,
+// loaded by TMA a chunk ahead), and the BF16 result leaves by one TMA tile
+// store; the last chunk's tile is normalised after the loop and written by
+// plain stores.
+template <bool NORM>
 __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUtensorMap& omap,
                                             float* __restrict__ state,
                                             float* __restrict__ o, int t, int t_pad, int heads,
                                             const int* __restrict__ cu, int n_seqs,
                                             const unsigned char* __restrict__ ws, int h, int n,
                                             const unsigned* __restrict__ ready,
-                                            long long ready_pitch,
+                                            long long ready_pitch, const NormArgs* na,
                                             uint32_t acquire_iters = 1u << 22) {
     extern __shared__ __align__(1024) unsigned char sm[];
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -1146,16 +1176,22 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
     uint64_t* bar_b = bar_x + 2;                                     // [2]: [T; P] | Khat^T | dec
     uint64_t* bar_v = bar_x + 4;                                     // [2]: value tiles
     uint64_t* bar_mma = bar_x + 6;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ScanT::BAR + 64);
-    int* abort_flag = reinterpret_cast<int*>(sm + ScanT::BAR + 68);
+    uint64_t* bar_gt = bar_x + 7;  // [2]: the gate tiles (NORM)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + ScanT::BAR + 80);
+    int* abort_flag = reinterpret_cast<int*>(sm + ScanT::BAR + 84);
     auto opx_off = [](int b) { return b ? ScanT::OPX1 : (uint32_t)SS_OPX; };
     auto tp_off = [](int b) { return b ? ScanT::TP1 : (uint32_t)SS_TP; };  // group b: TP, KH, DEC follow
 
     if (tid == 0) {
-        for (int i = 0; i < 7; ++i) tc::mbar_init(bar_x + i, 1);
+        for (int i = 0; i < 9; ++i) tc::mbar_init(bar_x + i, 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&vmap);
-        tc::prefetch_tmap(&omap);
+        if (NORM) {
+            tc::prefetch_tmap(&na->gmap);
+            tc::prefetch_tmap(&na->nmap);
+        } else {
+            tc::prefetch_tmap(&omap);
+        }
         *abort_flag = 0;
     }
     if (warp == 0) tc::tmem_alloc(tmem_slot, ScanT::TMEM_COLS);
@@ -1243,6 +1279,103 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         if (start + C < end) load_v(start + C, 1);
     }
 
+    // NORM: the staged O tile of a chunk is normalised in two halves of 32
+    // token rows, each by warps 8..15: thread tt = tid - 256 takes row
+    // 32 half + tt / 8, channels 4 cb + 32 k (k < 4, cb = tt % 8: a quarter
+    // warp reads a row's 128 consecutive bytes), with the o_norm weight of
+    // those channels kept in registers.
+    uint32_t ph_g = 0, out_g = 0;  // gate buffers: phase, load in flight (bit per buffer)
+    float wn[16];
+    if (NORM && tid >= 256) {
+        const int cb = (tid - 256) & 7;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint2 wv = __ldg(reinterpret_cast<const uint2*>(na->w + 4 * cb + 32 * k));
+            wn[4 * k] = __uint_as_float(wv.x << 16);
+            wn[4 * k + 1] = __uint_as_float(wv.x & 0xffff0000u);
+            wn[4 * k + 2] = __uint_as_float(wv.y << 16);
+            wn[4 * k + 3] = __uint_as_float(wv.y & 0xffff0000u);
+        }
+    }
+    auto gate_off = [](int b) { return b ? ScanT::GATE1 : ScanT::GATE0; };
+    // the gate tile of the chunk at token row cc0 into buffer b (copier), once
+    // the buffer's last output tile has left
+    auto load_gate = [&](int cc0, int b) {
+        tc::bulk_wait_read_all();
+        tc::mbar_arrive_expect_tx(bar_gt + b, 64 * D * 2);
+        tc::tma_load_2d(sm + gate_off(b), &na->gmap, bar_gt + b, h * D, cc0);
+        out_g |= 1u << b;
+    };
+    // Half hf of the sigmoid-gated RMSNorm of the staged O tile (OST, FP32
+    // [64][128]) with the gate tile in buffer b,
+    //     out[j] = o[j] / sqrt(mean_j o[j]^2 + eps) * w[j] * sigmoid(gate[j]),
+    // in FP32 (the sigmoid by the hardware 2^x and reciprocal), rounded once
+    // to BF16: in place over the gate tile (to_tile: each thread overwrites the
+    // gate values it read), or to `out` for the chunk's first `rows` rows at
+    // token row oc0.  Called by every thread (all track the gate's phase).
+    auto norm_half = [&](int hf, int b, bool to_tile, int rows, int oc0) {
+        if (tid >= 256) {
+            if (hf == 0) {
+                if (tid == 256 && !tc::mbar_wait(bar_gt + b, (ph_g >> b) & 1u)) {
+                    atomicOr(&g_tc_status, STATUS_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                asm volatile("bar.sync 2, 256;" ::: "memory");
+            }
+            const int tt = tid - 256, cb = tt & 7, r = 32 * hf + (tt >> 3);
+            uint16_t* GT = reinterpret_cast<uint16_t*>(sm + gate_off(b));
+            float y[16];
+            uint2 gv[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float4 f = *reinterpret_cast<const float4*>(OST + r * D + 4 * cb + 32 * k);
+                y[4 * k] = f.x;
+                y[4 * k + 1] = f.y;
+                y[4 * k + 2] = f.z;
+                y[4 * k + 3] = f.w;
+                gv[k] = *reinterpret_cast<const uint2*>(GT + r * D + 4 * cb + 32 * k);
+            }
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains
+#pragma unroll
+            for (int e = 0; e < 16; ++e) s4[e & 3] = __fmaf_rn(y[e], y[e], s4[e & 3]);
+            float ss = (s4[0] + s4[1]) + (s4[2] + s4[3]);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 4);
+            const float rr = rsqrtf(ss * (1.0f / D) + na->eps);
+            uint2 ob[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float gg[4] = {__uint_as_float(gv[k].x << 16),
+                                     __uint_as_float(gv[k].x & 0xffff0000u),
+                                     __uint_as_float(gv[k].y << 16),
+                                     __uint_as_float(gv[k].y & 0xffff0000u)};
+                float z[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    z[e] = y[4 * k + e] * rr * wn[4 * k + e] * sigmoid_hw(gg[e]);
+                ob[k] = make_uint2(tc::pack_bf16x2(z[0], z[1]), tc::pack_bf16x2(z[2], z[3]));
+            }
+            if (to_tile) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint2*>(GT + r * D + 4 * cb + 32 * k) = ob[k];
+                tc::fence_async_smem();
+            } else if (r < rows) {
+                uint16_t* orow = na->out + (size_t)(oc0 + r) * na->out_pitch + h * D;
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    *reinterpret_cast<uint2*>(orow + 4 * cb + 32 * k) = ob[k];
+            }
+        }
+        if (hf == 1) {
+            ph_g ^= 1u << b;
+            if (copier) out_g &= ~(1u << b);
+        }
+    };
+    bool n_active = false;  // this chunk normalises the staged tile of chunk n_c0 (NORM)
+    int n_c0 = -1, st_b = 0, o_b = 0;  // gate buffers of the staged and the last chunk
+
     int o_c0 = -1, o_L = 0;  // the chunk whose O is still in TMEM (region o_reg)
     uint32_t o_reg = 0;
     bool o_staged = false;  // a staged O (chunk st_c0) waits for its store
@@ -1259,7 +1392,17 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         const float* DEC = reinterpret_cast<const float*>(sm + tp_off(xb) + (BLOB_DEC - BLOB_TP));
         tc::tc_fence_before();
         if (__syncthreads_or(*abort_flag)) break;  // every thread takes the same exit
-        if (copier && o_staged) {  // chunk g - 2's O, staged during the last chunk
+        if (NORM) {
+            // chunk g - 2's O, staged during the last chunk: its first half now,
+            // the second while this chunk's second product runs
+            n_active = o_staged;
+            if (n_active) {
+                n_c0 = st_c0;
+                norm_half(0, st_b, true, C, n_c0);
+            }
+            // the gate of chunk g - 1, whose O is staged in this chunk
+            if (copier && c0 > start) load_gate(c0 - C, xb ^ 1);
+        } else if (copier && o_staged) {  // chunk g - 2's O, staged during the last chunk
             tc::tma_store_2d(&omap, OST, h * D, st_c0);
             tc::bulk_commit();
         }
@@ -1341,6 +1484,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
             }
             tc::tmem_st32u(my + ScanT::T_SA + 32 * cg, su);
         }
+        if (NORM && n_active) norm_half(1, st_b, true, C, n_c0);
         wait_bar(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::tc_fence_after();
@@ -1357,6 +1501,11 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         if (copier) tc::bulk_wait_read_all();  // the staging tile's last store has read it
         tc::tc_fence_before();
         __syncthreads();
+        if (NORM && copier && n_active) {  // chunk n_c0's normalised tile, over its gate
+            tc::tma_store_2d(&na->nmap, sm + gate_off(st_b), h * D, n_c0);
+            tc::bulk_commit();
+        }
+        n_active = false;
 
         // ---------------------------------------------------------- U^T Khat; O^T += U^T P^T
         if (tid == 0) {
@@ -1382,7 +1531,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
             const int wr = (cg == 1) ? 0 : 8;
             if (extra) tc::tmem_ld8(my + o_reg + wr, ow);
             tc::tmem_ld_wait();
-            if (o_L == C) {
+            if (NORM || o_L == C) {  // (inside the loop every chunk but the last is whole)
 #pragma unroll
                 for (int i = 0; i < 16; ++i) OST[(16 * cg + i) * D + j] = ov[i];
                 if (extra) {
@@ -1404,9 +1553,10 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
                 }
             }
         }
-        if (o_c0 >= 0 && o_L == C) {
+        if (o_c0 >= 0 && (NORM || o_L == C)) {
             o_staged = true;
             st_c0 = o_c0;
+            st_b = o_b;
         }
         wait_bar(bar_mma, ph_mma);
         ph_mma ^= 1;
@@ -1422,28 +1572,56 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
             tc::tmem_st_wait();
         }
         o_c0 = c0;
+        o_b = xb;
         o_L = L;
         o_reg = r_d1 + 64;
     }
     // every thread leaves the loop through the same iteration; agree on the flag
     const bool aborted = __syncthreads_or(*abort_flag);
-    if (copier && o_staged && !aborted) {  // the staged O of the chunk before the last
-        tc::tma_store_2d(&omap, OST, h * D, st_c0);
-        tc::bulk_commit();
-    }
-    if (o_c0 >= 0 && !aborted) {  // the last chunk's O, by plain stores
-        float ov[16];
-        tc::tmem_ld16(my + o_reg + 16 * cg, ov);
-        tc::tmem_ld_wait();
-        float* orow = o + ((size_t)o_c0 * heads + h) * D + j;
+    if (NORM) {
+        if (!aborted) {
+            // the staged O of the chunk before the last, then the last chunk's:
+            // normalised and written by plain stores
+            if (o_staged) {
+                norm_half(0, st_b, false, C, st_c0);
+                norm_half(1, st_b, false, C, st_c0);
+            }
+            __syncthreads();  // OST is free
+            if (o_c0 >= 0) {
+                float ov[16];
+                tc::tmem_ld16(my + o_reg + 16 * cg, ov);
+                tc::tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const int r = 16 * cg + i;
-            if (r < o_L) orow[(size_t)r * heads * D] = ov[i];
+                for (int i = 0; i < 16; ++i) OST[(16 * cg + i) * D + j] = ov[i];
+                if (copier) load_gate(o_c0, o_b);
+            }
+            __syncthreads();
+            if (o_c0 >= 0) {
+                norm_half(0, o_b, false, o_L, o_c0);
+                norm_half(1, o_b, false, o_L, o_c0);
+            }
+        }
+    } else {
+        if (copier && o_staged && !aborted) {  // the staged O of the chunk before the last
+            tc::tma_store_2d(&omap, OST, h * D, st_c0);
+            tc::bulk_commit();
+        }
+        if (o_c0 >= 0 && !aborted) {  // the last chunk's O, by plain stores
+            float ov[16];
+            tc::tmem_ld16(my + o_reg + 16 * cg, ov);
+            tc::tmem_ld_wait();
+            float* orow = o + ((size_t)o_c0 * heads + h) * D + j;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int r = 16 * cg + i;
+                if (r < o_L) orow[(size_t)r * heads * D] = ov[i];
+            }
         }
     }
     if (copier) {  // copies still in flight land before the exit (bounded waits)
         tc::bulk_wait_all();
+        for (int b2 = 0; b2 < 2; ++b2)
+            if ((out_g >> b2) & 1u) tc::mbar_wait(bar_gt + b2, (ph_g >> b2) & 1u, 1u << 20);
         for (int b2 = 0; b2 < 2; ++b2) {
             if ((out_x >> b2) & 1u) tc::mbar_wait(bar_x + b2, (ph_x >> b2) & 1u, 1u << 20);
             if ((out_b >> b2) & 1u) tc::mbar_wait(bar_b + b2, (ph_b >> b2) & 1u, 1u << 20);
@@ -1474,10 +1652,11 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
 // (cooperative launch), so every wait on a flag ends.
 static_assert(ScanT::NT == NTP, "the two roles share the block size");
 static_assert(ScanT::TOTAL <= PS_TOTAL, "the two roles share the shared-memory size");
-template <bool GATED>
+template <bool GATED, bool NORM>
 __global__ void __launch_bounds__(NTP, 1)
 prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constant__ CUtensorMap vmap,
-                     const __grid_constant__ CUtensorMap omap, const uint16_t* __restrict__ beta, float* __restrict__ state,
+                     const __grid_constant__ CUtensorMap omap, const __grid_constant__ NormArgs na,
+                     const uint16_t* __restrict__ beta, float* __restrict__ state,
                      float* __restrict__ o, int t, int t_pad, int heads,
                      const int* __restrict__ cu, int n_seqs, unsigned char* __restrict__ ws,
                      unsigned* __restrict__ ready, long long ready_pitch, uint32_t fault) {
@@ -1488,8 +1667,9 @@ prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constan
     const bool inject = fault == FAULT_READY_WAIT;
     const int chains = n_seqs * heads;
     if ((int)blockIdx.x < chains)
-        scan_t_role(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
-                    (int)blockIdx.x / heads, ready, ready_pitch, inject ? 1u << 12 : 1u << 22);
+        scan_t_role<NORM>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
+                          (int)blockIdx.x % heads, (int)blockIdx.x / heads, ready, ready_pitch, &na,
+                          inject ? 1u << 12 : 1u << 22);
     else
         prepare_role<GATED>(maps, beta, t, t_pad, heads, cu, n_seqs, ws,
                             (long long)blockIdx.x - chains, (long long)gridDim.x - chains, ready,
@@ -1498,14 +1678,16 @@ prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constan
 
 // The chains of the two-kernel path: one CTA per (sequence, head), after
 // prepare_kernel has written every chunk's operands.
+template <bool NORM>
 __global__ void __launch_bounds__(NTP, 1)
 scan_t_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
-              float* __restrict__ state, float* __restrict__ o, int t, int t_pad, int heads,
-              const int* __restrict__ cu, int n_seqs, const unsigned char* __restrict__ ws) {
+              const __grid_constant__ NormArgs na, float* __restrict__ state, float* __restrict__ o,
+              int t, int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
+              const unsigned char* __restrict__ ws) {
     pdl_wait();  // the prepared operands (and the callers' state) are complete
     pdl_release();
-    scan_t_role(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws, (int)blockIdx.x % heads,
-                (int)blockIdx.x / heads, nullptr, 0);
+    scan_t_role<NORM>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
+                      (int)blockIdx.x % heads, (int)blockIdx.x / heads, nullptr, 0, &na);
 }
 
 // BF16 [rows][cols] with a row pitch of `pitch_elems`; boxes of `box_cols`
@@ -1543,7 +1725,8 @@ constexpr double kPrepItemUs = 8.3, kScanTChunkUs = 2.3;
 kda_status launch_prefill_tc(float* state, const void* q, const void* k, const void* v,
                              const void* g, const void* beta, float* o, int t, int t_pad,
                              int heads, long long stride, const int* cu, int n_seqs,
-                             void* workspace, cudaStream_t s, const PrefillGate* gate) {
+                             void* workspace, cudaStream_t s, const PrefillGate* gate,
+                             const PrefillNorm* norm) {
     const uint64_t rows = cu ? (uint64_t)t : (uint64_t)t_pad * n_seqs;
     const int sms = sm_count();
     if (sms <= 0) {
@@ -1567,6 +1750,8 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     }
     PrepMaps maps;
     CUtensorMap vmap, omap;
+    NormArgs na;
+    memset(&na, 0, sizeof(na));
     const uint64_t hd = (uint64_t)heads * D;
     maps.dt_bias = gate ? gate->dt_bias : nullptr;
     maps.a_log = gate ? gate->a_log : nullptr;
@@ -1577,17 +1762,30 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&maps.g, g, hd, rows, g_pitch, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&vmap, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !tma_map_f32(&omap, o, hd, rows, hd, D, (uint32_t)C)) {
+        (norm ? !make_map(&na.gmap, norm->gate, hd, rows, (uint64_t)norm->gate_stride, D,
+                          CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                    !make_map(&na.nmap, norm->out, hd, rows, (uint64_t)norm->out_stride, D,
+                              CU_TENSOR_MAP_SWIZZLE_NONE)
+              : !tma_map_f32(&omap, o, hd, rows, hd, D, (uint32_t)C))) {
         set_error("kda_prefill: cannot encode TMA tensor maps");
         return KDA_ERR_CUDA;
     }
+    if (norm) {
+        na.w = norm->w;
+        na.out = norm->out;
+        na.out_pitch = norm->out_stride;
+        na.eps = norm->eps;
+        memset(&omap, 0, sizeof(omap));
+    }
     auto* prep_k = gate ? prepare_kernel<true> : prepare_kernel<false>;
-    auto* fused_k = gate ? prefill_fused_kernel<true> : prefill_fused_kernel<false>;
+    auto* fused_k = norm ? prefill_fused_kernel<false, true>
+                         : (gate ? prefill_fused_kernel<true, false> : prefill_fused_kernel<false, false>);
+    auto* scan_k = norm ? scan_t_kernel<true> : scan_t_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute(prep_k,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PS_TOTAL);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(scan_t_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        e = cudaFuncSetAttribute(scan_k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  (int)ScanT::TOTAL);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(fused_k, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1615,7 +1813,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, fused_k, maps, vmap, omap, (const uint16_t*)beta,
+        e = cudaLaunchKernelEx(&cfg, fused_k, maps, vmap, omap, na, (const uint16_t*)beta,
                                state, o, t, t_pad, heads, cu, n_seqs, ws, ready,
                                ready_pitch(chunk_bound),
                                fault_injected("ready_wait") ? (uint32_t)FAULT_READY_WAIT : 0u);
@@ -1632,7 +1830,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
                t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;
-    launch_pdl(scan_t_kernel, dim3((unsigned)chains), dim3(NTP), ScanT::TOTAL, s, vmap, omap,
+    launch_pdl(scan_k, dim3((unsigned)chains), dim3(NTP), ScanT::TOTAL, s, vmap, omap, na,
                state, o, t, t_pad, heads, cu, n_seqs, (const unsigned char*)ws);
     return launch_result("kda_prefill (scan)");
 }

@@ -59,6 +59,14 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
     return r;
 }
 
+// Two FP32 values rounded to BF16 (nearest even) and packed, `lo` in the
+// low half (the lower address in memory).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
 // Round an FP32 value for use as a kind::tf32 MMA operand, to nearest with
 // ties away from zero: add half of the 13 low mantissa bits' range.  The
 // tensor core truncates those 13 bits of its FP32 operands (checked on

@@ -305,6 +305,38 @@ kda_status kda_o_norm_gated(const float* core, const uint16_t* gate, const uint1
                             uint64_t stream);
 
 /*
+ * kda_prefill_o_norm -- kda_prefill with the sigmoid-gated RMSNorm of
+ * kda_o_norm_gated fused into the scan's epilogue: the core output never
+ * leaves the chip in FP32; what is written is the BF16 normalised output
+ * (glm5next_kda module index, block pipeline: the core, then the gated
+ * RMSNorm with the o_norm weight; Glm5NextKdaWorkspace core and o_norm_out).
+ * Per token row and head, over the head's 128 channels j:
+ *     out[j] = o[j] / sqrt(mean_j o[j]^2 + eps) * w[j] * sigmoid(gate[j])
+ * with o the core output kda_prefill would write, in FP32, rounded once to
+ * BF16 (the same reading as kda_o_norm_gated).
+ *
+ *   state, q, k, v, g, beta, t, t_pad, chunk, heads, head_dim, qkv_row_stride,
+ *   cu_seqlens, n_seqs, workspace, workspace_bytes: as kda_prefill (the same
+ *           argument checks, statuses and workspace size); in_dtype must be
+ *           KDA_BF16: the fused norm exists on the tensor-core path only
+ *           (KDA_ERR_UNSUPPORTED otherwise, and with KDA_PREFILL_IMPL=simt).
+ *   gate  : BF16, token row r of head h at gate + r * gate_stride + h * 128
+ *           (16-byte aligned, gate_stride >= heads * 128, a multiple of 8)
+ *   w_norm: BF16 [128], shared by all heads (8-byte aligned)
+ *   eps   : rms_norm_eps, finite and >= 0
+ *   out   : BF16, token row r of head h at out + r * out_stride + h * 128
+ *           (16-byte aligned, out_stride >= heads * 128, a multiple of 8);
+ *           rows of padding are not written
+ */
+kda_status kda_prefill_o_norm(float* state, const void* q, const void* k, const void* v,
+                              const void* g, const void* beta, const uint16_t* gate,
+                              int64_t gate_stride, const uint16_t* w_norm, float eps,
+                              uint16_t* out, int64_t out_stride, int t, int t_pad, int chunk,
+                              int heads, int head_dim, int in_dtype, int64_t qkv_row_stride,
+                              const int* cu_seqlens, int n_seqs, void* workspace,
+                              size_t workspace_bytes, uint64_t stream);
+
+/*
  * kda_conv_silu_l2_k -- the front end's half of decode_k: k rows of each of
  * n_seqs sequences through the conv + SiLU + L2 of kda_conv_silu_l2, with
  * optional conv-state snapshots (Glm5NextKdaLayer::decode_k: snapshots[t] is

@@ -214,6 +214,31 @@ def test_prefill_gated_refuses_bad_arguments(lib):
     assert b"kda_prefill_gated" in lib.kda_last_error()
 
 
+def test_prefill_o_norm_refuses_bad_arguments(lib):
+    f = lib.kda_prefill_o_norm
+    f.argtypes = [V] * 7 + [ctypes.c_int64, V, F, V, ctypes.c_int64, I, I, I, I, I, I,
+                            ctypes.c_int64, V, I, V, ctypes.c_size_t, U64]
+    big = 1 << 40
+    ok = (P, P, P, P, P, P, P, 512, P, 1e-6, P, 512, 100, 128, 64, 4, 128, 1, 512, None, 1, P,
+          big, 0)
+    names = ("S", "q", "k", "v", "g", "b", "gate", "gs", "w", "eps", "out", "os", "t", "tp",
+             "c", "h", "hd", "dt", "st", "cu", "n", "ws", "wsb", "s")
+    bad = lambda **kw: f(*[kw.get(k, v) for k, v in zip(names, ok)])
+    assert bad(hd=64) == 2 and bad(c=48) == 2                # head_dim, chunk width
+    assert bad(dt=0) == 2                                    # FP32 inputs: no fused norm
+    assert bad(t=0) == 1 and bad(tp=99) == 1                 # 1 <= t <= t_pad
+    assert bad(cu=P) == 1                                    # packed rows take no padding
+    assert bad(gate=None) == 1 and bad(w=None) == 1 and bad(out=None) == 1
+    assert bad(gate=ctypes.c_void_p(P.value + 8)) == 1       # gate alignment (16 bytes)
+    assert bad(out=ctypes.c_void_p(P.value + 8)) == 1        # out alignment (16 bytes)
+    assert bad(w=ctypes.c_void_p(P.value + 4)) == 1          # w alignment (8 bytes)
+    assert bad(gs=500) == 1 and bad(gs=516) == 1             # gate pitch
+    assert bad(os=500) == 1 and bad(os=516) == 1             # out pitch
+    assert bad(eps=-1.0) == 1 and bad(eps=float("inf")) == 1
+    assert bad(wsb=1024) == 3 and bad(ws=None) == 3          # workspace too small / missing
+    assert b"kda_prefill_o_norm" in lib.kda_last_error()
+
+
 def test_conv_k_refuses_bad_arguments(lib):
     f = lib.kda_conv_silu_l2_k
     f.argtypes = [V] * 4 + [I, I, I, F, I, I, V, I, U64]
