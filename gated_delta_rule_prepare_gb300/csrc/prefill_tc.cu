@@ -952,81 +952,71 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 *reinterpret_cast<float4*>(z + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
             }
             __syncthreads();
-            // Both levels are register-tiled (each thread forms a 2 x 4 block of
-            // outputs from two column loads and one row load per k): the solve
-            // is bound by shared-memory load instructions, one per cycle per SM
-            // whatever their width.  Warps are laid out so that a product's
-            // triangular operand bounds its k range uniformly inside a warp.
-            if (tid < 64) {   // level 1: warp pr forms T_ab, (a, b) = (2 pr + 1, 2 pr)
-                const int pr = tid >> 5, ln = tid & 31;
-                const int r0 = 2 * (ln >> 2), c0 = 4 * (ln & 3);
+            // Both levels run on eight warps, register-tiled (a thread forms
+            // 1 x 2 or 2 x 2 outputs per shared-memory row and column load), with
+            // warps laid out so that a product's triangular operand bounds its k
+            // range uniformly inside a warp; the terms left out are exact zeros,
+            // so every sum keeps the order of the full product.
+            if (tid < 256) {  // level 1: warps 4 pr .. 4 pr + 3 form T_ab, (a, b) = (2 pr + 1, 2 pr)
+                const int w = tid >> 5, ln = tid & 31;
+                const int pr = w >> 2, rh = (w >> 1) & 1, chh = w & 1;  // 8 x 8 quadrant
                 const int ob = 32 * pr, oa = ob + 16;
+                const int r = 8 * rh + (ln >> 2), c = 8 * chh + 2 * (ln & 3);
                 float* mscr = TM + 32 + 16 * pr;  // M = A_ab T_bb in rows 0..15
-                float m[2][4] = {};
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float a0 = AM[(oa + r0) * AP + ob + k], a1 = AM[(oa + r0 + 1) * AP + ob + k];
-                    const float4 tv = *reinterpret_cast<const float4*>(TM + (ob + k) * TPP + ob + c0);
-                    m[0][0] = __fmaf_rn(a0, tv.x, m[0][0]); m[0][1] = __fmaf_rn(a0, tv.y, m[0][1]);
-                    m[0][2] = __fmaf_rn(a0, tv.z, m[0][2]); m[0][3] = __fmaf_rn(a0, tv.w, m[0][3]);
-                    m[1][0] = __fmaf_rn(a1, tv.x, m[1][0]); m[1][1] = __fmaf_rn(a1, tv.y, m[1][1]);
-                    m[1][2] = __fmaf_rn(a1, tv.z, m[1][2]); m[1][3] = __fmaf_rn(a1, tv.w, m[1][3]);
+                float m0 = 0.f, m1 = 0.f;
+                // T_bb is lower triangular: its rows below 8 chh add nothing here
+#pragma unroll 4
+                for (int k = 8 * chh; k < 16; ++k) {
+                    const float a = AM[(oa + r) * AP + ob + k];
+                    const float2 tv = *reinterpret_cast<const float2*>(TM + (ob + k) * TPP + ob + c);
+                    m0 = __fmaf_rn(a, tv.x, m0);
+                    m1 = __fmaf_rn(a, tv.y, m1);
                 }
-                *reinterpret_cast<float4*>(mscr + r0 * TPP + c0) = make_float4(m[0][0], m[0][1], m[0][2], m[0][3]);
-                *reinterpret_cast<float4*>(mscr + (r0 + 1) * TPP + c0) = make_float4(m[1][0], m[1][1], m[1][2], m[1][3]);
-                __syncwarp();
-                float t[2][4] = {};
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                    const float a0 = TM[(oa + r0) * TPP + oa + k], a1 = TM[(oa + r0 + 1) * TPP + oa + k];
-                    const float4 mv = *reinterpret_cast<const float4*>(mscr + k * TPP + c0);
-                    t[0][0] = __fmaf_rn(a0, mv.x, t[0][0]); t[0][1] = __fmaf_rn(a0, mv.y, t[0][1]);
-                    t[0][2] = __fmaf_rn(a0, mv.z, t[0][2]); t[0][3] = __fmaf_rn(a0, mv.w, t[0][3]);
-                    t[1][0] = __fmaf_rn(a1, mv.x, t[1][0]); t[1][1] = __fmaf_rn(a1, mv.y, t[1][1]);
-                    t[1][2] = __fmaf_rn(a1, mv.z, t[1][2]); t[1][3] = __fmaf_rn(a1, mv.w, t[1][3]);
+                *reinterpret_cast<float2*>(mscr + r * TPP + c) = make_float2(m0, m1);
+                if (pr == 0) asm volatile("bar.sync 3, 128;" ::: "memory");
+                else asm volatile("bar.sync 4, 128;" ::: "memory");
+                float t0 = 0.f, t1 = 0.f;
+                // T_aa is lower triangular: its columns past 8 rh + 7 add nothing here
+#pragma unroll 4
+                for (int k = 0; k < 8 * rh + 8; ++k) {
+                    const float a = TM[(oa + r) * TPP + oa + k];
+                    const float2 mv = *reinterpret_cast<const float2*>(mscr + k * TPP + c);
+                    t0 = __fmaf_rn(a, mv.x, t0);
+                    t1 = __fmaf_rn(a, mv.y, t1);
                 }
-                *reinterpret_cast<float4*>(TM + (oa + r0) * TPP + ob + c0) =
-                    make_float4(-t[0][0], -t[0][1], -t[0][2], -t[0][3]);
-                *reinterpret_cast<float4*>(TM + (oa + r0 + 1) * TPP + ob + c0) =
-                    make_float4(-t[1][0], -t[1][1], -t[1][2], -t[1][3]);
+                *reinterpret_cast<float2*>(TM + (oa + r) * TPP + ob + c) = make_float2(-t0, -t1);
             }
             __syncthreads();
-            if (tid < 128) {  // level 2: rows 32..63, columns 0..31 (four warps)
+            if (tid < 256) {  // level 2: rows 32..63, columns 0..31 (eight warps)
                 const int w = tid >> 5, ln = tid & 31;
-                {   // M1 = A_[23][01] T_[01][01]: warp w takes columns 8 w .. 8 w + 7, all
-                    // rows; T_[01][01] is lower triangular, so k starts at 8 w
-                    const int r0 = 2 * (ln >> 1), c0 = 8 * w + 4 * (ln & 1);
-                    float m[2][4] = {};
-                    for (int k = 8 * w; k < 32; ++k) {
+                {   // M1 = A_[23][01] T_[01][01]: warp w takes columns 4 w .. 4 w + 3, all
+                    // rows; T_[01][01] is lower triangular, so k starts at 4 w
+                    const int r0 = 2 * (ln >> 1), c0 = 4 * w + 2 * (ln & 1);
+                    float m00 = 0.f, m01 = 0.f, m10 = 0.f, m11 = 0.f;
+#pragma unroll 4
+                    for (int k = 4 * w; k < 32; ++k) {
                         const float a0 = AM[(32 + r0) * AP + k], a1 = AM[(33 + r0) * AP + k];
-                        const float4 tv = *reinterpret_cast<const float4*>(TM + k * TPP + c0);
-                        m[0][0] = __fmaf_rn(a0, tv.x, m[0][0]); m[0][1] = __fmaf_rn(a0, tv.y, m[0][1]);
-                        m[0][2] = __fmaf_rn(a0, tv.z, m[0][2]); m[0][3] = __fmaf_rn(a0, tv.w, m[0][3]);
-                        m[1][0] = __fmaf_rn(a1, tv.x, m[1][0]); m[1][1] = __fmaf_rn(a1, tv.y, m[1][1]);
-                        m[1][2] = __fmaf_rn(a1, tv.z, m[1][2]); m[1][3] = __fmaf_rn(a1, tv.w, m[1][3]);
+                        const float2 tv = *reinterpret_cast<const float2*>(TM + k * TPP + c0);
+                        m00 = __fmaf_rn(a0, tv.x, m00); m01 = __fmaf_rn(a0, tv.y, m01);
+                        m10 = __fmaf_rn(a1, tv.x, m10); m11 = __fmaf_rn(a1, tv.y, m11);
                     }
-                    *reinterpret_cast<float4*>(TM + r0 * TPP + 32 + c0) =
-                        make_float4(m[0][0], m[0][1], m[0][2], m[0][3]);
-                    *reinterpret_cast<float4*>(TM + (r0 + 1) * TPP + 32 + c0) =
-                        make_float4(m[1][0], m[1][1], m[1][2], m[1][3]);
+                    *reinterpret_cast<float2*>(TM + r0 * TPP + 32 + c0) = make_float2(m00, m01);
+                    *reinterpret_cast<float2*>(TM + (r0 + 1) * TPP + 32 + c0) = make_float2(m10, m11);
                 }
-                asm volatile("bar.sync 1, 128;" ::: "memory");
-                {   // -T_[23][23] M1: warp w takes rows 8 w .. 8 w + 7, all columns;
-                    // T_[23][23] is lower triangular, so k stops at 8 w + 7
-                    const int r0 = 8 * w + 2 * (ln >> 3), c0 = 4 * (ln & 7);
-                    float t[2][4] = {};
-                    for (int k = 0; k < 8 * w + 8; ++k) {
+                asm volatile("bar.sync 1, 256;" ::: "memory");
+                {   // -T_[23][23] M1: warp w takes rows 4 w .. 4 w + 3, all columns;
+                    // T_[23][23] is lower triangular, so k stops at 4 w + 3
+                    const int r0 = 4 * w + 2 * (ln >> 4), c0 = 2 * (ln & 15);
+                    float t00 = 0.f, t01 = 0.f, t10 = 0.f, t11 = 0.f;
+#pragma unroll 4
+                    for (int k = 0; k < 4 * w + 4; ++k) {
                         const float a0 = TM[(32 + r0) * TPP + 32 + k], a1 = TM[(33 + r0) * TPP + 32 + k];
-                        const float4 mv = *reinterpret_cast<const float4*>(TM + k * TPP + 32 + c0);
-                        t[0][0] = __fmaf_rn(a0, mv.x, t[0][0]); t[0][1] = __fmaf_rn(a0, mv.y, t[0][1]);
-                        t[0][2] = __fmaf_rn(a0, mv.z, t[0][2]); t[0][3] = __fmaf_rn(a0, mv.w, t[0][3]);
-                        t[1][0] = __fmaf_rn(a1, mv.x, t[1][0]); t[1][1] = __fmaf_rn(a1, mv.y, t[1][1]);
-                        t[1][2] = __fmaf_rn(a1, mv.z, t[1][2]); t[1][3] = __fmaf_rn(a1, mv.w, t[1][3]);
+                        const float2 mv = *reinterpret_cast<const float2*>(TM + k * TPP + 32 + c0);
+                        t00 = __fmaf_rn(a0, mv.x, t00); t01 = __fmaf_rn(a0, mv.y, t01);
+                        t10 = __fmaf_rn(a1, mv.x, t10); t11 = __fmaf_rn(a1, mv.y, t11);
                     }
-                    *reinterpret_cast<float4*>(TM + (32 + r0) * TPP + c0) =
-                        make_float4(-t[0][0], -t[0][1], -t[0][2], -t[0][3]);
-                    *reinterpret_cast<float4*>(TM + (33 + r0) * TPP + c0) =
-                        make_float4(-t[1][0], -t[1][1], -t[1][2], -t[1][3]);
+                    *reinterpret_cast<float2*>(TM + (32 + r0) * TPP + c0) = make_float2(-t00, -t01);
+                    *reinterpret_cast<float2*>(TM + (33 + r0) * TPP + c0) = make_float2(-t10, -t11);
                 }
             }
             __syncthreads();
