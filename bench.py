@@ -350,6 +350,19 @@ def run_gpu(args):
         for _ in range(3):
             o_norm()
         on_per, _ = time_launches(o_norm, 20, stream)
+
+        # ---------------- the prefill step with the gated RMSNorm fused into its
+        # epilogue (BF16 out, no FP32 o), against the step followed by o_norm
+        pn_gate, pn_w, pn_out = n_sets[0][1], n_w, n_sets[0][2]
+
+        def prefill_o_norm():
+            K.kda_prefill_o_norm(S, q, k, v, g, beta, pn_gate, pn_w, pn_out, T_PREFILL, CHUNK,
+                                 workspace=ws)
+
+        for _ in range(3):
+            prefill_o_norm()
+        K.kda_sync_status()
+        pn_per, _ = time_launches(prefill_o_norm, 20, stream)
         del n_sets
 
         # ---------------- forget gate and beta of a prefill-sized problem
@@ -580,6 +593,13 @@ def run_gpu(args):
             "us_per_call": statistics.mean(on_per) * 1e3, "algorithmic_bytes": ONORM_BYTES,
             "l2": "two input/output sets alternated (537 MB touched per pair of launches), "
                   "no flush",
+        },
+        "prefill_o_norm": {
+            "workload": "the prefill step (8192 x 32 heads, BF16) with the sigmoid-gated "
+                        "RMSNorm fused into the scan's epilogue: BF16 out, no FP32 o",
+            "value": T_PREFILL / (statistics.mean(pn_per) / 1e3), "unit": "tokens/s",
+            "us_per_call": statistics.mean(pn_per) * 1e3,
+            "prefill_then_o_norm_us": (ms_step + statistics.mean(on_per)) * 1e3,
         },
         "prefill_gated": {
             "workload": "the prefill step (8192 x 32 heads, BF16) with g and beta formed in "

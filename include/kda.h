@@ -148,6 +148,13 @@ kda_status kda_decode_k(float* state, const float* q, const float* k, const floa
  * products from FP16 operands with FP32 accumulation; the state, T, the
  * decays and all sums in FP32.  Chunks whose steepest decay is below -10 form
  * A and P on the CUDA cores in FP32 (exact factors for any g).
+ * Valid domain of the tensor-core path (the FP16 operands): q and k of unit
+ * norm or less (as kda_conv_silu_l2 leaves them), and |v| and the entries of
+ * the carried state below about 6e4 (FP16's largest value is 65504; larger
+ * values turn into inf); values far below 2^-14 keep an absolute error under
+ * 2^-25 but lose relative precision.  Inputs with v and the initial state
+ * scaled by 1e-4 and by 1e3 are tested within the 2e-3 tolerance.  The FP32
+ * paths (FP32 inputs) have no such limits.
  *
  *   workspace : device scratch, 16-byte aligned, of at least
  *           kda_prefill_workspace_size(...) bytes (may be NULL when that
