@@ -153,6 +153,8 @@ static_assert(RB_GLAST + 128 * 4 == RAW_G + RAW_TILE, "reference rows must end t
 static_assert(2 * OpY32::bytes(128) <= 4 * OpY::bytes(128), "Y_b operands do not fit");
 static_assert(4 * OpY::bytes(128) <= OpKH::bytes(64), "Y_b operands do not fit");
 static_assert(PS_OPX % 1024 == 0 && PS_Y % 16 == 0, "operand alignment");
+static_assert(OpXh::bytes(128) <= OpX::bytes(128) / 2 && 2 * 64 * 64 * 4 <= OpX::bytes(128) / 2,
+              "the steep path's A and P share the A operand region with Ktil and Qtil");
 
 // A chunk whose decays all satisfy g >= -kWideGMin takes 32-token column
 // blocks with reference token 32 b + 17: the A-side factor stays below
@@ -621,7 +623,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 const int r = tid & 63, qg = tid >> 6;
                 if (r >= r0) {
                     const bool live = r < L;
-#pragma unroll
+#pragma unroll 1  // the narrow path only: kept compact
                     for (int jj = 0; jj < 32 / (NTP / 64); ++jj) {
                         const int j = qg + (NTP / 64) * jj;
                         const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
@@ -732,6 +734,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             };
             // Y_b row s of block b = s >> bshift: k_s e^(Gamma_mb - Gamma_s).
             auto build_y = [&](int bshift, int gm_row0, uint32_t ybytes, auto op) {
+#pragma unroll 1  // the narrow path only: kept compact
                 for (int e = tid; e < 64 * 32; e += NTP) {
                     const int s = e & 63, j = e >> 6, bb = s >> bshift;
                     const float4 gm =
@@ -744,7 +747,10 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                         kf.z * __expf(gm.z - ga.z), kf.w * __expf(gm.w - ga.w));
                 }
             };
-            float sa[8], sp[8];  // the steep path's A and P (rows tid / 64 + 8 k)
+            // the steep path's A and P, FP32 [64][64] each, in the second half of
+            // the A operand region (the first half takes Ktil and Qtil in P3)
+            float* SA = reinterpret_cast<float*>(sm + PS_OPX + OpX::bytes(128) / 2);
+            float* SPV = SA + 64 * 64;
             if (wide) {
                 // Two 32-token column blocks (every g of the chunk is >= -kWideGMin).
                 build_xy_wide();
@@ -763,17 +769,20 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             } else if (steep) {
                 // Exact products on the CUDA cores: thread (column s = tid & 63)
                 // forms A_rs and P_rs for rows r = tid / 64 + 8 k.  The results
-                // stay in registers until the raw tiles and Gamma are dead (P4).
+                // wait in shared memory until the raw tiles and Gamma are dead
+                // (P4).  A rare path, kept compact (its loops are not unrolled):
+                // code that the common path's instruction stream skips over
+                // still costs it time.
                 fetch_next();
                 const int s2 = tid & 63;
                 const bool slive = s2 < L;
-#pragma unroll
+#pragma unroll 1
                 for (int k8 = 0; k8 < 8; ++k8) {
                     const int r2 = (tid >> 6) + 8 * k8;
                     float a = 0.f, pv = 0.f;
                     if (s2 <= r2) {
                         const bool rlive = r2 < L;
-#pragma unroll 4
+#pragma unroll 1
                         for (int i = 0; i < D; i += 4) {
                             const float4 gr = *reinterpret_cast<const float4*>(GAM + r2 * KP + i);
                             const float4 gs = *reinterpret_cast<const float4*>(GAM + s2 * KP + i);
@@ -792,12 +801,13 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                             pv = __fmaf_rn(qr.w * ks.w, e3, pv);
                         }
                     }
-                    sa[k8] = a;
-                    sp[k8] = KDA_Q_SCALE * pv;
+                    SA[r2 * 64 + s2] = a;
+                    SPV[r2 * 64 + s2] = KDA_Q_SCALE * pv;
                 }
             } else {
                 // Four 16-token column blocks with reference token 16 b + 8.
                 build_y(4, 0, OpY::bytes(128), OpY{});
+#pragma unroll 1  // a rare path, kept compact
                 for (int bb = 0; bb < 4; ++bb) {
                     build_x(16 * bb, GMID + bb * 128);
                     sync_for_mma();
@@ -826,7 +836,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 const int r = tid & 63, qg = tid >> 6;
                 const bool live = r < L;
                 const float br = BETA[r];  // 0 past the chunk's end
-#pragma unroll
+#pragma unroll 1  // narrow and steep paths only: kept compact
                 for (int jj = 0; jj < 32 / (NTP / 64); ++jj) {
                     const int j = qg + (NTP / 64) * jj;
                     const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
@@ -858,13 +868,13 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
             if (steep) {
                 const int s2 = tid & 63;
                 const float bs = BETA[s2];
-#pragma unroll
-                for (int k8 = 0; k8 < 8; ++k8) {
+#pragma unroll 1
+                for (int k8 = 0; k8 < 8; ++k8) {  // each thread reads back its own values
                     const int r2 = (tid >> 6) + 8 * k8;
-                    AM[r2 * AP + s2] = (s2 < r2) ? sa[k8] * bs : 0.f;
+                    AM[r2 * AP + s2] = (s2 < r2) ? SA[r2 * 64 + s2] * bs : 0.f;
                     if (!failed)
                         *reinterpret_cast<uint16_t*>(blob + BLOB_TP + OpTPh::off(64 + r2, s2)) =
-                            tc::f16_bits((s2 <= r2) ? sp[k8] * bs : 0.f);
+                            tc::f16_bits((s2 <= r2) ? SPV[r2 * 64 + s2] * bs : 0.f);
                 }
             } else {   // thread (lane ln, quarter ch) reads columns [16 ch, 16 ch + 16)
                 float v[16];
