@@ -420,13 +420,15 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     const int* map_cu = seq_cached ? s_cu : cu;
     uint64_t* bar_tma = reinterpret_cast<uint64_t*>(sm + PS_BAR);  // one per raw buffer
     uint64_t* bar_mma = bar_tma + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PS_BAR + 24);
+    uint64_t* bar_mma2 = bar_tma + 3;  // the wide path's second A/P product (its own issuer)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PS_BAR + 32);
     const uint32_t s_opx = tc::smem_u32(sm + PS_OPX), s_y = tc::smem_u32(sm + PS_Y);
 
     if (tid == 0) {
         tc::mbar_init(bar_tma, 1);
         tc::mbar_init(bar_tma + 1, 1);
         tc::mbar_init(bar_mma, 1);
+        tc::mbar_init(bar_mma2, 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&maps.q);
         tc::prefetch_tmap(&maps.k);
@@ -440,7 +442,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     // Per-buffer state is kept as bit masks (bit b): an array indexed by the
     // buffer would live in local memory, whose lines the small L1 left by the
     // shared-memory carve-out does not keep -- an L2 round trip per access.
-    uint32_t ph_mma = 0, ph_tma = 0;
+    uint32_t ph_mma = 0, ph_mma2 = 0, ph_tma = 0;
     bool failed = false;
 
     auto wait_mma = [&]() {
@@ -755,15 +757,27 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 // Two 32-token column blocks (every g of the chunk is >= -kWideGMin).
                 build_xy_wide();
                 sync_for_mma();
+                // the two blocks' products are independent: two threads of two
+                // warps issue them side by side (a single issuing thread spends
+                // about 45 cycles per instruction), each with its own barrier
                 if (tid == 0) {
                     tc::tc_fence_after();
                     issue_mma<OpX, OpY32, 16>(tmem + TC_AP, s_opx, s_y, tc::idesc_tf32(128, 32));
+                    tc::mma_commit(bar_mma);
+                } else if (tid == 32) {
+                    tc::tc_fence_after();
                     issue_mma<OpX1, OpY32, 16>(tmem + TC_AP + 32, tc::smem_u32(x1buf),
                                                s_y + OpY32::bytes(128), tc::idesc_tf32(128, 32));
-                    tc::mma_commit(bar_mma);
+                    tc::mma_commit(bar_mma2);
                 }
                 release_pending();
                 wait_mma();
+                if (!tc::mbar_wait(bar_mma2, ph_mma2)) {
+                    atomicOr(&g_tc_status, STATUS_TIMEOUT);
+                    failed = true;
+                }
+                ph_mma2 ^= 1;
+                tc::tc_fence_after();
                 fetch_next();  // the compact X_1 in the other buffer has been read
                 p3_store();
             } else if (steep) {
