@@ -58,7 +58,9 @@ kda_status validate_prefill(const char* fn, const float* state, const void* q, c
 // Tensor-core prefill for BF16 inputs (prefill_tc.cu): its
 // workspace size for `rows` token rows, and the launch (arguments validated by
 // kda_prefill).
-size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads);
+// Workspace of the tensor-core prefill; FP32 inputs add the FP16 copies of
+// q, k and v the kernels read.
+size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads, bool f32_in = false);
 // Forget-gate inputs of kda_prefill_gated: g and beta are then the raw gate
 // projection g_raw and the raw b_proj output, turned into the core's g and
 // beta inside the prepare kernel.
@@ -84,7 +86,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
                              const void* g, const void* beta, float* o, int t, int t_pad,
                              int heads, long long stride, const int* cu, int n_seqs,
                              void* workspace, cudaStream_t s, const PrefillGate* gate = nullptr,
-                             const PrefillNorm* norm = nullptr);
+                             const PrefillNorm* norm = nullptr, bool f32_in = false);
 
 // decode_k's row walk (decode.cu) for kda_prefill's short FP32 sequences:
 // n_seqs sequences of krows token rows, sequence n starting at row

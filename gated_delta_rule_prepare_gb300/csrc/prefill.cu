@@ -216,13 +216,15 @@ bool simt_pinned() {
 }
 
 // True when this call runs on the tensor-core kernels (which need a
-// workspace): every BF16 call unless the SIMT kernel is pinned.  Those kernels
-// step through the sequence 64 tokens at a time whatever the chunk width: the
-// chunked form gives the same result for any width (the recurrence it
-// reorganises), up to rounding, so the width is the kernels' choice.
+// workspace): every call unless the SIMT kernel is pinned (FP32 inputs are
+// rounded to FP16 copies in the workspace first).  Those kernels step through
+// the sequence 64 tokens at a time whatever the chunk width: the chunked form
+// gives the same result for any width (the recurrence it reorganises), up to
+// rounding, so the width is the kernels' choice.
 bool uses_tensor_cores(int chunk, int in_dtype) {
     (void)chunk;
-    return in_dtype == KDA_BF16 && !simt_pinned();
+    (void)in_dtype;
+    return !simt_pinned();
 }
 
 template <typename TIn>
@@ -241,11 +243,11 @@ kda_status launch(float* state, const void* q, const void* k, const void* v, con
                                    (const float*)g, (const float*)beta, o, n_seqs, t, t_pad,
                                    heads, s);
     }
-    // BF16 inputs with chunk 64 take the tensor-core kernels unless the caller
-    // pins the SIMT kernel (KDA_PREFILL_IMPL=simt, for comparisons).
+    // Everything else takes the tensor-core kernels unless the caller pins
+    // the SIMT kernel (KDA_PREFILL_IMPL=simt, for comparisons).
     if (uses_tensor_cores(chunk, sizeof(TIn) == 2 ? KDA_BF16 : KDA_F32))
         return launch_prefill_tc(state, q, k, v, g, beta, o, t, t_pad, heads, stride, cu, n_seqs,
-                                 workspace, s);
+                                 workspace, s, nullptr, nullptr, sizeof(TIn) == 4);
     const size_t smem = sizeof(ChunkSmem);
     cudaError_t e = cudaFuncSetAttribute(prefill_simt_kernel<TIn>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -278,7 +280,7 @@ extern "C" size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk
                                              int head_dim, int in_dtype) {
     if (rows < 0 || n_seqs < 1 || heads < 1 || head_dim != D) return 0;
     if (!uses_tensor_cores(chunk, in_dtype)) return 0;
-    return prefill_tc_workspace_bytes(rows, n_seqs, heads);
+    return prefill_tc_workspace_bytes(rows, n_seqs, heads, in_dtype == KDA_F32);
 }
 
 namespace kda {

@@ -50,6 +50,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <type_traits>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -141,7 +142,7 @@ constexpr uint32_t PS_GAM = 2 * RAW_BUF;                     // FP32 Gamma [64][
 constexpr uint32_t PS_OPX = PS_GAM + 64 * KP * 4;            // A operand of the A/P products
 constexpr uint32_t PS_Y = PS_OPX + OpX::bytes(128);          // B operands Y_b
 constexpr uint32_t PS_BETA = PS_Y + OpKH::bytes(64);
-constexpr uint32_t PS_BAR = PS_BETA + 64 * 4;  // bar_tma[2], bar_mma, TMEM base
+constexpr uint32_t PS_BAR = PS_BETA + 64 * 4;  // bar_tma[2], bar_mma[2], TMEM base, bar_g
 // Packed batches of up to SEQ_CACHE sequences keep their chunk map (chunk_off
 // and cu_seqlens, n_seqs + 1 entries each) in shared memory: the item lookup
 // is a binary search, dependent global loads otherwise.
@@ -335,6 +336,23 @@ __device__ __forceinline__ float4 raw4(const unsigned char* tile, int r, int c) 
     return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
                        __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
 }
+// FP16 bits to FP32 (exact).
+__device__ __forceinline__ float h2f(uint16_t h) {
+    float f;
+    asm("cvt.f32.f16 %0, %1;" : "=f"(f) : "h"(h));
+    return f;
+}
+// raw4 for the FP16 tiles of FP32 inputs (converted to FP16 before the call).
+template <bool F16>
+__device__ __forceinline__ float4 in4(const unsigned char* tile, int r, int c) {
+    if constexpr (F16) {
+        const uint2 u = *reinterpret_cast<const uint2*>(tile + raw_off(r, c));
+        return make_float4(h2f((uint16_t)u.x), h2f((uint16_t)(u.x >> 16)), h2f((uint16_t)u.y),
+                           h2f((uint16_t)(u.y >> 16)));
+    } else {
+        return raw4(tile, r, c);
+    }
+}
 
 // A (chunk, head) item of the prepare walk: item = g * heads + h.
 struct PrepItem {
@@ -382,8 +400,11 @@ __device__ __forceinline__ PrepItem prep_item(long long item, int heads, const i
 // The prepare walk of one CTA: items first, first + stride, ...  When `ready`
 // is set, each finished item's flag (ready[item]) is released once its
 // operands are in the workspace.
-template <bool GATED>
-__device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_t* __restrict__ beta,
+// F16: the inputs were FP32: q and k arrive as FP16 tiles, g as an FP32 tile
+// (maps.g) loaded into the Gamma array, which the cumulative sum then
+// overwrites in place, and beta as FP32.
+template <bool GATED, bool F16>
+__device__ __forceinline__ void prepare_role(const PrepMaps& maps, const void* __restrict__ beta,
                                              int t, int t_pad, int heads,
                                              const int* __restrict__ cu, int n_seqs,
                                              unsigned char* __restrict__ ws, long long first,
@@ -422,6 +443,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     uint64_t* bar_mma = bar_tma + 2;
     uint64_t* bar_mma2 = bar_tma + 3;  // the wide path's second A/P product (its own issuer)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + PS_BAR + 32);
+    uint64_t* bar_g = reinterpret_cast<uint64_t*>(sm + PS_BAR + 40);  // FP32 g tile (F16)
     const uint32_t s_opx = tc::smem_u32(sm + PS_OPX), s_y = tc::smem_u32(sm + PS_Y);
 
     if (tid == 0) {
@@ -429,6 +451,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         tc::mbar_init(bar_tma + 1, 1);
         tc::mbar_init(bar_mma, 1);
         tc::mbar_init(bar_mma2, 1);
+        if (F16) tc::mbar_init(bar_g, 1);
         tc::fence_mbar_init();
         tc::prefetch_tmap(&maps.q);
         tc::prefetch_tmap(&maps.k);
@@ -442,7 +465,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     // Per-buffer state is kept as bit masks (bit b): an array indexed by the
     // buffer would live in local memory, whose lines the small L1 left by the
     // shared-memory carve-out does not keep -- an L2 round trip per access.
-    uint32_t ph_mma = 0, ph_mma2 = 0, ph_tma = 0;
+    uint32_t ph_mma = 0, ph_mma2 = 0, ph_tma = 0, ph_g = 0;
     bool failed = false;
 
     auto wait_mma = [&]() {
@@ -464,15 +487,24 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         if (copier && it.valid) {
             unsigned char* dst = sm + b * RAW_BUF;
             tc::fence_async_smem();  // the buffer's previous generic-proxy contents are dead
-            tc::mbar_arrive_expect_tx(bar_tma + b, RAW_BUF);
+            tc::mbar_arrive_expect_tx(bar_tma + b, F16 ? 2 * RAW_TILE : RAW_BUF);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const int x = it.h * D + 64 * half;
                 const uint32_t o2 = half * (RAW_TILE / 2);
                 tc::tma_load_2d(dst + RAW_Q + o2, &maps.q, bar_tma + b, x, it.c0);
                 tc::tma_load_2d(dst + RAW_K + o2, &maps.k, bar_tma + b, x, it.c0);
-                tc::tma_load_2d(dst + RAW_G + o2, &maps.g, bar_tma + b, x, it.c0);
+                if (!F16) tc::tma_load_2d(dst + RAW_G + o2, &maps.g, bar_tma + b, x, it.c0);
             }
+        }
+    };
+    // F16: the FP32 g tile of item `it` ([64][128], dense rows) into the Gamma
+    // array, once the previous item's last Gamma reads are behind a barrier.
+    auto load_g32 = [&](const PrepItem& it) {
+        if (F16 && copier && it.valid) {
+            tc::fence_async_smem();
+            tc::mbar_arrive_expect_tx(bar_g, 64 * D * 4);
+            tc::tma_load_2d(sm + PS_GAM, &maps.g, bar_g, it.h * D, it.c0);
         }
     };
     // beta of item `it` (threads 0..63): the raw BF16 bits, widened only
@@ -480,13 +512,17 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     // tensor's first element where the row is not part of the item) and the
     // mask is kept apart and applied at that point: no operation touches the
     // loaded value, and so waits for it, before then.
+    using BetaRaw = typename std::conditional<F16, float, uint16_t>::type;
+    const BetaRaw* betap = static_cast<const BetaRaw*>(beta);
     auto beta_live = [&](const PrepItem& it) { return tid < C && it.valid && tid < it.L; };
     auto load_beta = [&](const PrepItem& it) {
-        const uint16_t* src = beta_live(it) ? beta + (size_t)(it.c0 + tid) * maps.b_stride + it.h : beta;
+        const BetaRaw* src =
+            beta_live(it) ? betap + (size_t)(it.c0 + tid) * maps.b_stride + it.h : betap;
         return __ldg(src);
     };
-    auto beta_of = [&](uint16_t raw, bool live) {
-        return live ? (GATED ? sigmoid_hw(bf(raw)) : bf(raw)) : 0.f;
+    auto beta_of = [&](BetaRaw raw, bool live) {
+        if constexpr (F16) return live ? raw : 0.f;
+        else return live ? (GATED ? sigmoid_hw(bf(raw)) : bf(raw)) : 0.f;
     };
 
     // The item whose ready flag is still to be released (copier thread): an
@@ -505,7 +541,8 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     long long item = first;
     PrepItem cur = prep_item(item, heads, map_cu, map_off, n_seqs, t, t_pad);
     load_raw(cur, 0);
-    uint16_t beta_cur = load_beta(cur);
+    load_g32(cur);
+    BetaRaw beta_cur = load_beta(cur);
     bool blive_cur = beta_live(cur);
     // gated calls: dt_bias of this thread's channel (tid & 127 in the Gamma
     // phase) and a_log of the item's head, loaded one item ahead
@@ -524,7 +561,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         const long long nitem = item + stride;
         PrepItem nxt = {};
         nxt.valid = false;
-        uint16_t beta_nxt = 0;
+        BetaRaw beta_nxt = 0;
         bool blive_nxt = false;
         float2 gate_nxt = make_float2(0.f, 0.f);
         // The next item is resolved (global loads) while the first A/P product
@@ -541,6 +578,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
         if (!cur.valid) {
             if (tid == 0) atomicOr(&g_tc_status, STATUS_BAD_CU_SEQLENS);
             fetch_next();
+            load_g32(nxt);
         } else {
             const int L = cur.L, h = cur.h;
             const unsigned char* RAWQ = sm + b * RAW_BUF + RAW_Q;
@@ -559,6 +597,13 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 failed = true;
             }
             ph_tma ^= 1u << b;
+            if (F16) {
+                if (!tc::mbar_wait(bar_g, ph_g)) {
+                    atomicOr(&g_tc_status, STATUS_TIMEOUT);
+                    failed = true;
+                }
+                ph_g ^= 1u;
+            }
 
             // ------------------------------------------------------ P1 Gamma
             // Four 16-token quarters per channel, then each quarter adds the
@@ -576,12 +621,16 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                     for (int rr = 0; rr < 16; ++rr)
                         acc[rr] = gate_hw(raw1(RAWG, 16 * qt + rr, i), gate_cur.x, nc, maps.lb);
                 }
+                // F16: the FP32 g tile, dense rows, in the Gamma array; every
+                // thread reads its rows before the barriers below, and writes
+                // Gamma over them only after them
+                const float* G32 = GAM;
                 float run = 0.f, gmin = 0.f;
 #pragma unroll
                 for (int rr = 0; rr < 16; ++rr) {
                     const int r = 16 * qt + rr;
                     float gv = 0.f;
-                    if (r < L) gv = GATED ? acc[rr] : raw1(RAWG, r, i);
+                    if (r < L) gv = GATED ? acc[rr] : (F16 ? G32[r * D + i] : raw1(RAWG, r, i));
                     gmin = fminf(gmin, gv);
                     run = __fadd_rn(run, gv);
                     acc[rr] = run;
@@ -630,7 +679,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                         const int j = qg + (NTP / 64) * jj;
                         const float4 gm = *reinterpret_cast<const float4*>(gmb + 4 * j);
                         const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
-                        float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
+                        float4 kf = in4<F16>(RAWK, r, 4 * j), qf = in4<F16>(RAWQ, r, 4 * j);
                         if (!live) kf = qf = make_float4(0.f, 0.f, 0.f, 0.f);
                         const float f0 = __expf(ga.x - gm.x), f1 = __expf(ga.y - gm.y),
                                     f2 = __expf(ga.z - gm.z), f3 = __expf(ga.w - gm.w);
@@ -670,7 +719,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 for (int jj = 0; jj < P3J; ++jj) {
                     const int j = qg + (NTP / 64) * jj;
                     const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
-                    float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
+                    float4 kf = in4<F16>(RAWK, r, 4 * j), qf = in4<F16>(RAWQ, r, 4 * j);
                     if (!live) kf = qf = make_float4(0.f, 0.f, 0.f, 0.f);
                     qf = make_float4(KDA_Q_SCALE * qf.x, KDA_Q_SCALE * qf.y, KDA_Q_SCALE * qf.z,
                                      KDA_Q_SCALE * qf.w);
@@ -742,7 +791,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                     const float4 gm =
                         *reinterpret_cast<const float4*>(GMID + (gm_row0 + bb) * 128 + 4 * j);
                     const float4 ga = *reinterpret_cast<const float4*>(GAM + s * KP + 4 * j);
-                    float4 kf = raw4(RAWK, s, 4 * j);
+                    float4 kf = in4<F16>(RAWK, s, 4 * j);
                     if (s >= L) kf = make_float4(0.f, 0.f, 0.f, 0.f);
                     st4(sm + PS_Y + bb * ybytes, decltype(op)::off(s & ((1 << bshift) - 1), 4 * j),
                         kf.x * __expf(gm.x - ga.x), kf.y * __expf(gm.y - ga.y),
@@ -800,7 +849,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                         for (int i = 0; i < D; i += 4) {
                             const float4 gr = *reinterpret_cast<const float4*>(GAM + r2 * KP + i);
                             const float4 gs = *reinterpret_cast<const float4*>(GAM + s2 * KP + i);
-                            float4 kr = raw4(RAWK, r2, i), qr = raw4(RAWQ, r2, i), ks = raw4(RAWK, s2, i);
+                            float4 kr = in4<F16>(RAWK, r2, i), qr = in4<F16>(RAWQ, r2, i), ks = in4<F16>(RAWK, s2, i);
                             if (!rlive) kr = qr = make_float4(0.f, 0.f, 0.f, 0.f);
                             if (!slive) ks = make_float4(0.f, 0.f, 0.f, 0.f);
                             const float e0 = __expf(gr.x - gs.x), e1 = __expf(gr.y - gs.y),
@@ -855,7 +904,7 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                     const int j = qg + (NTP / 64) * jj;
                     const float4 ga = *reinterpret_cast<const float4*>(GAM + r * KP + 4 * j);
                     const float4 gl = *reinterpret_cast<const float4*>(GLAST + 4 * j);
-                    float4 kf = raw4(RAWK, r, 4 * j), qf = raw4(RAWQ, r, 4 * j);
+                    float4 kf = in4<F16>(RAWK, r, 4 * j), qf = in4<F16>(RAWQ, r, 4 * j);
                     if (!live) kf = qf = make_float4(0.f, 0.f, 0.f, 0.f);
                     const float f0 = __expf(ga.x), f1 = __expf(ga.y), f2 = __expf(ga.z),
                                 f3 = __expf(ga.w);
@@ -871,12 +920,13 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
                 }
             }
             tc::fence_async_smem();
-            __syncthreads();  // the raw tiles and reference rows are dead from here on
+            __syncthreads();  // the raw tiles, Gamma and the reference rows are dead from here on
             if (copier && !failed) {
                 tc::bulk_store(blob + BLOB_OPX, sm + PS_OPX, OpXh::bytes(128));
                 tc::bulk_store(blob + BLOB_KH, sm + PS_Y, OpKHh::bytes(64));
                 tc::bulk_commit();
             }
+            load_g32(nxt);
 
             // ------------------------------------------------------ P4 read A, P
             if (steep) {
@@ -1080,15 +1130,15 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const uint16_
     }
 }
 
-template <bool GATED>
+template <bool GATED, bool F16>
 __global__ void __launch_bounds__(NTP, 1)
-prepare_kernel(const __grid_constant__ PrepMaps maps, const uint16_t* __restrict__ beta, int t,
+prepare_kernel(const __grid_constant__ PrepMaps maps, const void* __restrict__ beta, int t,
                int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
                unsigned char* __restrict__ ws) {
     pdl_wait();  // the chunk map (and the callers' inputs) are complete
     pdl_release();
-    prepare_role<GATED>(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x,
-                        nullptr, 0);
+    prepare_role<GATED, F16>(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x,
+                             nullptr, 0);
 }
 
 // ------------------------------------------------------------ transposed scan
@@ -1153,7 +1203,8 @@ struct ScanT {
 // loaded by TMA a chunk ahead), and the BF16 result leaves by one TMA tile
 // store; the last chunk's tile is normalised after the loop and written by
 // plain stores.
-template <bool NORM>
+// F16: the value tiles hold FP16 (FP32 inputs, converted before the call).
+template <bool NORM, bool F16>
 __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUtensorMap& omap,
                                             float* __restrict__ state,
                                             float* __restrict__ o, int t, int t_pad, int heads,
@@ -1445,7 +1496,10 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         if (copier && more) load_ops(g + 1, xb ^ 1);
         float vr[16];  // V[16 cg + i][j], read while the product runs
 #pragma unroll
-        for (int i = 0; i < 16; ++i) vr[i] = bf(RAWV[(16 * cg + i) * D + j]);
+        for (int i = 0; i < 16; ++i) {
+            const uint16_t e = RAWV[(16 * cg + i) * D + j];
+            vr[i] = F16 ? h2f(e) : bf(e);
+        }
         wait_bar(bar_mma, ph_mma);
         ph_mma ^= 1;
         tc::tc_fence_after();
@@ -1666,11 +1720,11 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
 // (cooperative launch), so every wait on a flag ends.
 static_assert(ScanT::NT == NTP, "the two roles share the block size");
 static_assert(ScanT::TOTAL <= PS_TOTAL, "the two roles share the shared-memory size");
-template <bool GATED, bool NORM>
+template <bool GATED, bool NORM, bool F16>
 __global__ void __launch_bounds__(NTP, 1)
 prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constant__ CUtensorMap vmap,
                      const __grid_constant__ CUtensorMap omap, const __grid_constant__ NormArgs na,
-                     const uint16_t* __restrict__ beta, float* __restrict__ state,
+                     const void* __restrict__ beta, float* __restrict__ state,
                      float* __restrict__ o, int t, int t_pad, int heads,
                      const int* __restrict__ cu, int n_seqs, unsigned char* __restrict__ ws,
                      unsigned* __restrict__ ready, long long ready_pitch, uint32_t fault) {
@@ -1681,18 +1735,18 @@ prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constan
     const bool inject = fault == FAULT_READY_WAIT;
     const int chains = n_seqs * heads;
     if ((int)blockIdx.x < chains)
-        scan_t_role<NORM>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
-                          (int)blockIdx.x % heads, (int)blockIdx.x / heads, ready, ready_pitch, &na,
-                          inject ? 1u << 12 : 1u << 22);
+        scan_t_role<NORM, F16>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
+                               (int)blockIdx.x % heads, (int)blockIdx.x / heads, ready,
+                               ready_pitch, &na, inject ? 1u << 12 : 1u << 22);
     else
-        prepare_role<GATED>(maps, beta, t, t_pad, heads, cu, n_seqs, ws,
-                            (long long)blockIdx.x - chains, (long long)gridDim.x - chains, ready,
-                            ready_pitch, !inject);
+        prepare_role<GATED, F16>(maps, beta, t, t_pad, heads, cu, n_seqs, ws,
+                                 (long long)blockIdx.x - chains, (long long)gridDim.x - chains,
+                                 ready, ready_pitch, !inject);
 }
 
 // The chains of the two-kernel path: one CTA per (sequence, head), after
 // prepare_kernel has written every chunk's operands.
-template <bool NORM>
+template <bool NORM, bool F16>
 __global__ void __launch_bounds__(NTP, 1)
 scan_t_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
               const __grid_constant__ NormArgs na, float* __restrict__ state, float* __restrict__ o,
@@ -1700,15 +1754,44 @@ scan_t_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ 
               const unsigned char* __restrict__ ws) {
     pdl_wait();  // the prepared operands (and the callers' state) are complete
     pdl_release();
-    scan_t_role<NORM>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
-                      (int)blockIdx.x % heads, (int)blockIdx.x / heads, nullptr, 0, &na);
+    scan_t_role<NORM, F16>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
+                           (int)blockIdx.x % heads, (int)blockIdx.x / heads, nullptr, 0, &na);
 }
 
-// BF16 [rows][cols] with a row pitch of `pitch_elems`; boxes of `box_cols`
-// channels x 64 tokens with the given shared-memory swizzle.
+// BF16 (FP16 with f16) [rows][cols] with a row pitch of `pitch_elems`; boxes
+// of `box_cols` channels x 64 tokens with the given shared-memory swizzle.
 bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint64_t pitch_elems,
-              uint32_t box_cols, CUtensorMapSwizzle swizzle) {
-    return tma_map_bf16(m, base, cols, rows, pitch_elems, box_cols, (uint32_t)C, swizzle);
+              uint32_t box_cols, CUtensorMapSwizzle swizzle, bool f16 = false) {
+    return tma_map_bf16(m, base, cols, rows, pitch_elems, box_cols, (uint32_t)C, swizzle,
+                        f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+}
+
+// FP32 inputs: q, k and v rounded to FP16 (round to nearest even; 11
+// significant bits, the precision of the TF32 and FP16 operands they become)
+// into the workspace, [rows][hd] each and contiguous, for the kernels' 16-bit
+// tiles.  A warp per row; lane l converts channels 8 (l + 32 m) .. + 7.
+// Input rows are 16-byte aligned (checked by the callers).
+constexpr int CVT_THREADS = 256;
+__global__ void __launch_bounds__(CVT_THREADS)
+f32_to_f16_kernel(const float* __restrict__ q, const float* __restrict__ k,
+                  const float* __restrict__ v, long long stride, uint16_t* __restrict__ out,
+                  int rows, int hd) {
+    pdl_wait();
+    pdl_release();
+    const float* src_t = blockIdx.y == 0 ? q : (blockIdx.y == 1 ? k : v);
+    uint16_t* dst_t = out + (size_t)blockIdx.y * rows * hd;
+    const int warps = CVT_THREADS / 32, lane = threadIdx.x & 31;
+    for (int row = blockIdx.x * warps + (int)(threadIdx.x >> 5); row < rows;
+         row += gridDim.x * warps) {
+        const float4* src = reinterpret_cast<const float4*>(src_t + (size_t)row * stride);
+        uint4* dst = reinterpret_cast<uint4*>(dst_t + (size_t)row * hd);
+#pragma unroll 4
+        for (int c8 = lane; c8 < hd / 8; c8 += 32) {
+            const float4 a = __ldcs(src + 2 * c8), b = __ldcs(src + 2 * c8 + 1);
+            dst[c8] = make_uint4(tc::pack_f16x2(a.x, a.y), tc::pack_f16x2(a.z, a.w),
+                                 tc::pack_f16x2(b.x, b.y), tc::pack_f16x2(b.z, b.w));
+        }
+    }
 }
 
 // Ready flags of the fused grid: one 32-bit word per (chunk, head) blob,
@@ -1724,9 +1807,12 @@ size_t ready_words(long long chunks, int heads) {
 
 }  // namespace
 
-size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads) {
+size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads, bool f32_in) {
     const long long chunks = (rows + C - 1) / C + n_seqs;
-    return ready_offset(chunks, n_seqs, heads) + ready_words(chunks, heads) * 4;
+    const size_t base = ready_offset(chunks, n_seqs, heads) + ready_words(chunks, heads) * 4;
+    if (!f32_in) return base;
+    // the FP16 copies of q, k and v, 256-byte aligned after the rest
+    return ((base + 255) & ~(size_t)255) + 3 * (size_t)rows * heads * D * 2;
 }
 
 // Per-SM cost figures measured on GB300 (T = 8192, 32 heads) that choose
@@ -1734,13 +1820,14 @@ size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads) {
 // the transposed scan's chain.
 constexpr double kPrepItemUs = 8.3, kScanTChunkUs = 2.3;
 
-// Launches the tensor-core prefill (BF16 inputs, chunk 64); arguments,
-// including the workspace size, are validated by kda_prefill.
+// Launches the tensor-core prefill (BF16 inputs, or FP32 inputs converted to
+// FP16 tiles first; chunk 64); arguments, including the workspace size, are
+// validated by kda_prefill.
 kda_status launch_prefill_tc(float* state, const void* q, const void* k, const void* v,
                              const void* g, const void* beta, float* o, int t, int t_pad,
                              int heads, long long stride, const int* cu, int n_seqs,
                              void* workspace, cudaStream_t s, const PrefillGate* gate,
-                             const PrefillNorm* norm) {
+                             const PrefillNorm* norm, bool f32_in) {
     const uint64_t rows = cu ? (uint64_t)t : (uint64_t)t_pad * n_seqs;
     const int sms = sm_count();
     if (sms <= 0) {
@@ -1762,6 +1849,10 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         const double per_chunk_two = (double)chains * kPrepItemUs / sms + kScanTChunkUs;
         fused = per_chunk_fused < per_chunk_two;
     }
+    if (f32_in && (gate || norm)) {
+        set_error("kda_prefill: FP32 inputs take neither the fused gate nor the fused norm");
+        return KDA_ERR_UNSUPPORTED;
+    }
     PrepMaps maps;
     CUtensorMap vmap, omap;
     NormArgs na;
@@ -1772,10 +1863,29 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     maps.lb = gate ? gate->lb : 0.f;
     maps.b_stride = gate ? gate->b_stride : heads;
     const uint64_t g_pitch = gate ? (uint64_t)gate->g_stride : hd;
-    if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&maps.g, g, hd, rows, g_pitch, 64, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&vmap, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+    // FP32 inputs: the kernels read FP16 copies of q, k and v (written below,
+    // after the other host steps) and the FP32 g in place
+    const float* q32 = static_cast<const float*>(q);
+    const float* k32 = static_cast<const float*>(k);
+    const float* v32 = static_cast<const float*>(v);
+    const long long stride32 = stride;
+    uint16_t* f16 = nullptr;
+    if (f32_in) {
+        f16 = reinterpret_cast<uint16_t*>(
+            static_cast<unsigned char*>(workspace) +
+            ((prefill_tc_workspace_bytes((long long)rows, n_seqs, heads) + 255) & ~(size_t)255));
+        q = f16;
+        k = f16 + rows * hd;
+        v = f16 + 2 * rows * hd;
+        stride = (long long)hd;
+    }
+    const bool gmap_ok =
+        f32_in ? tma_map_f32(&maps.g, g, hd, rows, hd, D, (uint32_t)C)
+               : make_map(&maps.g, g, hd, rows, g_pitch, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (!make_map(&maps.q, q, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B, f32_in) ||
+        !make_map(&maps.k, k, hd, rows, (uint64_t)stride, 64, CU_TENSOR_MAP_SWIZZLE_128B, f32_in) ||
+        !gmap_ok ||
+        !make_map(&vmap, v, hd, rows, (uint64_t)stride, D, CU_TENSOR_MAP_SWIZZLE_NONE, f32_in) ||
         (norm ? !make_map(&na.gmap, norm->gate, hd, rows, (uint64_t)norm->gate_stride, D,
                           CU_TENSOR_MAP_SWIZZLE_NONE) ||
                     !make_map(&na.nmap, norm->out, hd, rows, (uint64_t)norm->out_stride, D,
@@ -1791,10 +1901,14 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         na.eps = norm->eps;
         memset(&omap, 0, sizeof(omap));
     }
-    auto* prep_k = gate ? prepare_kernel<true> : prepare_kernel<false>;
-    auto* fused_k = norm ? prefill_fused_kernel<false, true>
-                         : (gate ? prefill_fused_kernel<true, false> : prefill_fused_kernel<false, false>);
-    auto* scan_k = norm ? scan_t_kernel<true> : scan_t_kernel<false>;
+    auto* prep_k = f32_in ? prepare_kernel<false, true>
+                          : (gate ? prepare_kernel<true, false> : prepare_kernel<false, false>);
+    auto* fused_k = f32_in ? prefill_fused_kernel<false, false, true>
+                    : norm ? prefill_fused_kernel<false, true, false>
+                           : (gate ? prefill_fused_kernel<true, false, false>
+                                   : prefill_fused_kernel<false, false, false>);
+    auto* scan_k = f32_in ? scan_t_kernel<false, true>
+                          : (norm ? scan_t_kernel<true, false> : scan_t_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute(prep_k,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)PS_TOTAL);
@@ -1812,6 +1926,13 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     const long long chunk_bound = ((long long)rows + C - 1) / C + n_seqs;
     unsigned* ready = reinterpret_cast<unsigned*>(ws + ready_offset(chunk_bound, n_seqs, heads));
     const long long n_ready = fused ? (long long)ready_words(chunk_bound, heads) : 0;
+    if (f32_in) {
+        const long long blocks = std::min<long long>(((long long)rows + 7) / 8, 16LL * sms);
+        launch_pdl(f32_to_f16_kernel, dim3((unsigned)blocks, 3), dim3(CVT_THREADS), 0, s, q32, k32,
+                   v32, stride32, f16, (int)rows, (int)hd);
+        const kda_status cs = launch_result("kda_prefill (FP16 copies)");
+        if (cs != KDA_OK) return cs;
+    }
     launch_pdl(chunk_map_kernel, dim3(1), dim3(MAP_THREADS), 0, s, cu, n_seqs, cu ? 0 : t,
                reinterpret_cast<int*>(ws), ready, n_ready);
     kda_status st = launch_result("kda_prefill (chunk map)");
@@ -1827,7 +1948,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, fused_k, maps, vmap, omap, na, (const uint16_t*)beta,
+        e = cudaLaunchKernelEx(&cfg, fused_k, maps, vmap, omap, na, beta,
                                state, o, t, t_pad, heads, cu, n_seqs, ws, ready,
                                ready_pitch(chunk_bound),
                                fault_injected("ready_wait") ? (uint32_t)FAULT_READY_WAIT : 0u);
@@ -1840,7 +1961,7 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     // never more CTAs than (chunk, head) items.
     const long long items = (((long long)rows + C - 1) / C + n_seqs) * heads;
     const unsigned grid = (unsigned)(items < sms ? items : sms);
-    launch_pdl(prep_k, dim3(grid), dim3(NTP), PS_TOTAL, s, maps, (const uint16_t*)beta, t,
+    launch_pdl(prep_k, dim3(grid), dim3(NTP), PS_TOTAL, s, maps, beta, t,
                t_pad, heads, cu, n_seqs, ws);
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;

@@ -26,19 +26,20 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tma_encode_fn() {
     return fn;
 }
 
-// BF16 [rows][cols] with a row pitch of `pitch_elems` elements, copied in
-// boxes of box_cols x box_rows with the given shared-memory swizzle.  Rows
-// past the end read as zero.
+// BF16 (or, with `type`, another 16-bit type) [rows][cols] with a row pitch
+// of `pitch_elems` elements, copied in boxes of box_cols x box_rows with the
+// given shared-memory swizzle.  Rows past the end read as zero.
 inline bool tma_map_bf16(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
                          uint64_t pitch_elems, uint32_t box_cols, uint32_t box_rows,
-                         CUtensorMapSwizzle swizzle) {
+                         CUtensorMapSwizzle swizzle,
+                         CUtensorMapDataType type = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
     auto fn = tma_encode_fn();
     if (!fn) return false;
     cuuint64_t gdim[2] = {cols, rows};
     cuuint64_t gstride[1] = {pitch_elems * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), gdim, gstride, box,
+    return fn(m, type, 2, const_cast<void*>(base), gdim, gstride, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }

@@ -137,24 +137,28 @@ kda_status kda_decode_k(float* state, const float* q, const float* k, const floa
  * Routing: FP32 inputs in the uniform form with t <= KDA_MAX_K and
  * qkv_row_stride == heads*128 run decode_k's row walk (the pages' dispatch
  * for pieces that do not take the chunked arm: state read once, t token steps,
- * state written once); BF16 inputs run the tensor-core prepare and scan
+ * state written once); every other call runs the tensor-core prepare and scan
  * kernels -- as one cooperative grid (the scan consuming each chunk as soon
  * as another SM has prepared it) when there are few (sequence, head) chains
- * relative to the SMs, e.g. one sequence of 32 heads; FP32 inputs otherwise
- * run the FP32 SIMT chunk kernel.  The environment variable
- * KDA_PREFILL_IMPL=simt pins the SIMT kernel and KDA_PREFILL_IMPL=unfused
- * the two-kernel tensor-core path (for comparisons).
+ * relative to the SMs, e.g. one sequence of 32 heads.  FP32 inputs reach
+ * those kernels through FP16 copies of q, k and v that a conversion kernel
+ * writes into the workspace first; g and beta are read in FP32.  The
+ * environment variable KDA_PREFILL_IMPL=simt pins the FP32 SIMT chunk kernel
+ * (FP32 arithmetic throughout, no workspace) and KDA_PREFILL_IMPL=unfused the
+ * two-kernel tensor-core path (for comparisons).
  * Precision of the tensor-core path: A and P from TF32 operands; the scan's
  * products from FP16 operands with FP32 accumulation; the state, T, the
- * decays and all sums in FP32.  Chunks whose steepest decay is below -10 form
- * A and P on the CUDA cores in FP32 (exact factors for any g).
+ * decays and all sums in FP32.  FP32 inputs: q, k and v rounded to FP16 (11
+ * significant bits, the precision of the TF32 and FP16 operands they feed),
+ * g and beta exact.  Chunks whose steepest decay is below -10 form A and P on
+ * the CUDA cores in FP32 (exact factors for any g).
  * Valid domain of the tensor-core path (the FP16 operands): q and k of unit
  * norm or less (as kda_conv_silu_l2 leaves them), and |v| and the entries of
  * the carried state below about 6e4 (FP16's largest value is 65504; larger
  * values turn into inf); values far below 2^-14 keep an absolute error under
  * 2^-25 but lose relative precision.  Inputs with v and the initial state
- * scaled by 1e-4 and by 1e3 are tested within the 2e-3 tolerance.  The FP32
- * paths (FP32 inputs) have no such limits.
+ * scaled by 1e-4 and by 1e3 are tested within the 2e-3 tolerance, BF16 and
+ * FP32.  The row walk and the SIMT kernel have no such limits.
  *
  *   workspace : device scratch, 16-byte aligned, of at least
  *           kda_prefill_workspace_size(...) bytes (may be NULL when that
@@ -170,12 +174,14 @@ kda_status kda_prefill(float* state, const void* q, const void* k, const void* v
 /* Bytes of device workspace kda_prefill needs for `rows` token rows in total
  * (n_seqs * t_pad in the uniform form, t in the packed form) over n_seqs
  * sequences with the given chunk width and input dtype.  Returns 0 when the
- * call needs none (FP32 inputs run without one) or when an
- * argument is invalid.  The BF16 tensor-core path stores the
- * state-independent operands of every (chunk, head) there: 66,176 bytes
- * per chunk of 64 tokens and head (with one chunk of slack per sequence),
- * plus (n_seqs + 1) * 4 bytes rounded up to 256, plus a 4-byte ready flag
- * per chunk and head rounded up to 256 bytes. */
+ * call needs none (KDA_PREFILL_IMPL=simt pins the SIMT kernel) or when an
+ * argument is invalid.  The tensor-core path stores the state-independent
+ * operands of every (chunk, head) there: 66,176 bytes per chunk of 64 tokens
+ * and head (with one chunk of slack per sequence), plus (n_seqs + 1) * 4
+ * bytes rounded up to 256, plus a 4-byte ready flag per chunk and head
+ * rounded up to 256 bytes; FP32 inputs add, 256-byte aligned after that, the
+ * FP16 copies of q, k and v: 3 * rows * heads * 128 * 2 bytes.  (The row walk
+ * of short FP32 sequences uses none of it.) */
 size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads, int head_dim,
                                   int in_dtype);
 
@@ -383,8 +389,9 @@ kda_status kda_conv_silu_l2_k(float* conv_state, const uint16_t* x, const uint16
  *   refusals of invalid arguments (checked first, with the same statuses).
  *   Refused with KDA_ERR_WORKSPACE when kda_prefill_workspace_size(...) for
  *   the call exceeds KDA_STATIC_WORKSPACE_BYTES: at 32 heads that is 30
- *   chunks of 64 tokens in total (one sequence of up to 1,920 tokens); fewer
- *   heads allow proportionally more.
+ *   chunks of 64 tokens in total (one BF16 sequence of up to 1,920 tokens;
+ *   17 chunks, 1,088 tokens, for FP32 inputs, whose FP16 copies sit there
+ *   too); fewer heads allow proportionally more.
  *   The first call on a device resolves the array's device address for that
  *   device (cudaGetSymbolAddress, with the device current); make that first
  *   call before any stream capture.

@@ -125,7 +125,10 @@ def test_workspace_size_is_queryable(lib):
     big = f(8192, 1, 64, 32, 128, 1)          # BF16, chunk 64: tensor-core path
     # per (chunk, head): FP16 [Ktil; Qtil] 32 KiB, [T; P] 16 KiB, Khat^T 16 KiB, dec 512 B
     assert big >= (8192 // 64) * 32 * (32768 + 16384 + 16384 + 512)
-    assert f(8192, 1, 64, 32, 128, 0) == 0    # FP32 inputs need none
+    # FP32 inputs take the same path after FP16 copies of q, k, v (2 B each)
+    # made in the workspace, 256-byte aligned after the rest
+    f32 = f(8192, 1, 64, 32, 128, 0)
+    assert f32 == ((big + 255) & ~255) + 3 * 8192 * 32 * 128 * 2
     # BF16 inputs take the tensor-core path (64-token steps) at every width
     assert f(8192, 1, 16, 32, 128, 1) == big and f(8192, 1, 128, 32, 128, 1) == big
     assert f(8192, 1, 64, 32, 64, 1) == 0     # invalid head_dim

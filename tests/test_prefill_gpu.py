@@ -43,10 +43,10 @@ def test_tiny_config_matches_oracle(orc):
 @pytest.mark.parametrize("chunk,t", [(16, 77), (32, 100), (64, 200), (64, 64), (64, 1),
                                      (16, 16), (64, 129), (128, 300), (128, 77), (128, 128)])
 def test_prefill_matches_oracle(orc, dtype, chunk, t):
-    """Every chunk width the boundary accepts, whole and ragged last chunks:
-    BF16 inputs on the tensor-core kernels (64-token steps whatever the
-    width), FP32 on the SIMT kernel (chunks of min(chunk, 64)) or, for t <= 8,
-    the row walk."""
+    """Every chunk width the boundary accepts, whole and ragged last chunks,
+    on the tensor-core kernels (64-token steps whatever the width; FP32
+    inputs through their FP16 copies) or, for FP32 with t <= 8, the row
+    walk."""
     K = kda()
     d = wl.prefill(seed=t + chunk, t=t, heads=3, chunk=chunk, dtype=dtype)
     o, S, _ = run_prefill(K, d, t, chunk)
@@ -216,9 +216,13 @@ def test_full_size_prefill_sampled_heads(orc):
         assert rel_err(S[0, h:h + 1], S_ref) < TOL_PREFILL, h
 
 
-def test_chained_prefills_equal_one_prefill():
+@pytest.mark.parametrize("impl,tol", [("simt", 1e-5), ("tc", TOL_PREFILL)])
+def test_chained_prefills_equal_one_prefill(monkeypatch, impl, tol):
     """Two prefill calls carrying the state equal one call over both halves
-    (within rounding: the chunk boundaries differ)."""
+    (within rounding: the chunk boundaries differ), on the FP32 SIMT kernel
+    and on the tensor-core path."""
+    if impl == "simt":
+        monkeypatch.setenv("KDA_PREFILL_IMPL", "simt")
     K = kda()
     d = wl.prefill(seed=9, t=200, heads=2, chunk=64, dtype=torch.float32)
     o_all, S_all, _ = run_prefill(K, d, 200, 64)
@@ -228,8 +232,8 @@ def test_chained_prefills_equal_one_prefill():
     second = {n: d[n][100:] for n in ("q", "k", "v", "g", "beta")}
     second["state"] = S1.cpu()
     o2, S2, _ = run_prefill(K, second, 100, 64)
-    assert rel_err(torch.cat([o1, o2]), o_all.cpu().double().numpy()) < 1e-5
-    assert rel_err(S2, S_all.cpu().double().numpy()) < 1e-5
+    assert rel_err(torch.cat([o1, o2]), o_all.cpu().double().numpy()) < tol
+    assert rel_err(S2, S_all.cpu().double().numpy()) < tol
 
 
 def test_tensor_core_and_simt_kernels_agree(orc, monkeypatch):
