@@ -406,6 +406,22 @@ def run_gpu(args):
         pg_per, _ = time_launches(prefill_gated, 20, stream)
         del pg_in
 
+        # ---------------- the prefill step with FP32 inputs (the step's values
+        # widened): FP16 copies of q, k and v made in the workspace, then the
+        # same prepare and scan kernels
+        f_in = [x_.float() for x_ in (q, k, v, g, beta)]
+        f_ws = torch.empty(K.kda_prefill_workspace_size(T_PREFILL, 1, CHUNK, H, torch.float32),
+                           dtype=torch.uint8, device=dev)
+
+        def prefill_f32():
+            K.kda_prefill(S, *f_in, o, T_PREFILL, CHUNK, workspace=f_ws)
+
+        for _ in range(3):
+            prefill_f32()
+        K.kda_sync_status()
+        pf_per, _ = time_launches(prefill_f32, 20, stream)
+        del f_in, f_ws
+
         # ---------------- front end + core: 16 packed sequences, conv then prefill
         fe = wl.frontend()
         cu = fe["cu_seqlens"].to(dev)
@@ -608,6 +624,12 @@ def run_gpu(args):
             "us_per_call": statistics.mean(pg_per) * 1e3,
             "gate_then_prefill_us": (statistics.mean(gate_per) + ms_step) * 1e3,
         },
+        "prefill_f32": {
+            "workload": "the prefill step (8192 x 32 heads) with FP32 q, k, v, g, beta: FP16 "
+                        "copies of q, k, v, then the tensor-core kernels",
+            "value": T_PREFILL / (statistics.mean(pf_per) / 1e3), "unit": "tokens/s",
+            "us_per_call": statistics.mean(pf_per) * 1e3, "gpu_launches_per_call": 3,
+        },
         "gate": {
             "workload": "forget gate and beta of a prefill-sized problem (8192 x 32 x 128, BF16)",
             "value": GATE_BYTES / (statistics.mean(gate_per) / 1e3) / 1e9, "unit": "GB/s",
@@ -712,6 +734,15 @@ def run_case(args):
         fn = lambda: K.kda_prefill(S, q, k, v, g, beta, o, args.seq_len, CHUNK, workspace=ws)
         nbytes = 4 * args.seq_len * H * D * 2 + args.seq_len * H * 2 + args.seq_len * H * D * 4 \
             + 2 * H * D * D * 4
+    elif args.case == "prefill_f32":
+        d = wl.prefill(t=args.seq_len)
+        q, k, v, g, beta = (d[n].float().to(dev) for n in ("q", "k", "v", "g", "beta"))
+        S = d["state"].to(dev)
+        o = torch.empty((args.seq_len, H, D), device=dev)
+        ws = torch.empty(K.kda_prefill_workspace_size(args.seq_len, 1, CHUNK, H, torch.float32),
+                         dtype=torch.uint8, device=dev)
+        fn = lambda: K.kda_prefill(S, q, k, v, g, beta, o, args.seq_len, CHUNK, workspace=ws)
+        nbytes = 5 * args.seq_len * H * D * 4 + args.seq_len * H * 4 + 2 * H * D * D * 4
     elif args.case == "prefill_o_norm":
         d = wl.prefill(t=args.seq_len)
         q, k, v, g, beta = (d[n].to(dev) for n in ("q", "k", "v", "g", "beta"))
@@ -818,8 +849,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default=None,
-                    choices=["prefill", "prefill_gated", "prefill_o_norm", "decode", "decode_k",
-                             "conv", "gate"],
+                    choices=["prefill", "prefill_f32", "prefill_gated", "prefill_o_norm",
+                             "decode", "decode_k", "conv", "gate"],
                     help="time one kernel alone (for profiler captures)")
     ap.add_argument("--seq-len", type=int, default=T_PREFILL)
     args = ap.parse_args()

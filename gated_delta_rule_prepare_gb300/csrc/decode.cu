@@ -35,19 +35,26 @@ struct TokenSmem {
     float red[kWarps][D];
 };
 
+// One input element widened to FP32: FP32 as is, BF16 (raw bits) exactly.
+__device__ __forceinline__ float ld_in(const float* p) { return __ldg(p); }
+__device__ __forceinline__ float ld_in(const uint16_t* p) {
+    return __uint_as_float(static_cast<uint32_t>(__ldg(p)) << 16);
+}
+
 // Stage one token of one head: threads 0..127 take one channel each.
-__device__ __forceinline__ void stage_token(TokenSmem& sm, const float* __restrict__ q,
-                                            const float* __restrict__ k,
-                                            const float* __restrict__ v,
-                                            const float* __restrict__ g, float beta) {
+template <typename TIn>
+__device__ __forceinline__ void stage_token(TokenSmem& sm, const TIn* __restrict__ q,
+                                            const TIn* __restrict__ k,
+                                            const TIn* __restrict__ v,
+                                            const TIn* __restrict__ g, float beta) {
     const int c = threadIdx.x;
     if (c < D) {
-        const float kc = __ldg(k + c);
-        sm.dec[c] = expf(__ldg(g + c));
+        const float kc = ld_in(k + c);
+        sm.dec[c] = expf(ld_in(g + c));
         sm.kk[c] = kc;
         sm.bk[c] = __fmul_rn(beta, kc);
-        sm.qs[c] = __fmul_rn(KDA_Q_SCALE, __ldg(q + c));
-        sm.v[c] = __ldg(v + c);
+        sm.qs[c] = __fmul_rn(KDA_Q_SCALE, ld_in(q + c));
+        sm.v[c] = ld_in(v + c);
     }
 }
 
@@ -156,10 +163,13 @@ struct SnapList {
     float* p[KDA_MAX_K];
 };
 
+// TIn: float (kda_decode_k, and kda_prefill's short FP32 sequences) or the
+// BF16 bits of kda_prefill's short BF16 sequences, widened exactly.
+template <typename TIn>
 __global__ void __launch_bounds__(kThreads, 2)
-decode_k_kernel(float* __restrict__ state, const float* __restrict__ q,
-                const float* __restrict__ k, const float* __restrict__ v,
-                const float* __restrict__ g, const float* __restrict__ beta,
+decode_k_kernel(float* __restrict__ state, const TIn* __restrict__ q,
+                const TIn* __restrict__ k, const TIn* __restrict__ v,
+                const TIn* __restrict__ g, const TIn* __restrict__ beta,
                 float* __restrict__ o, int heads, int krows, long long seq_rows, SnapList snaps,
                 int n_snap) {
     __shared__ TokenSmem sm;
@@ -171,7 +181,7 @@ decode_k_kernel(float* __restrict__ state, const float* __restrict__ q,
     load_state(s, S);
     for (int t = 0; t < krows; ++t) {
         const size_t row = (n * (size_t)seq_rows + t) * heads + h;
-        stage_token(sm, q + row * D, k + row * D, v + row * D, g + row * D, __ldg(beta + row));
+        stage_token(sm, q + row * D, k + row * D, v + row * D, g + row * D, ld_in(beta + row));
         __syncthreads();
         token_step(s, sm, o + row * D);
         if (t < n_snap) store_state(s, snaps.p[t] + nh * (size_t)(D * D));
@@ -204,12 +214,20 @@ namespace kda {
 
 // The decode_k row walk over n_seqs sequences of krows consecutive token rows,
 // sequences seq_rows rows apart (arguments checked by the caller), no
-// snapshots: kda_prefill's route for short FP32 sequences.
-kda_status launch_row_walk(float* state, const float* q, const float* k, const float* v,
-                           const float* g, const float* beta, float* o, int n_seqs, int krows,
-                           long long seq_rows, int heads, cudaStream_t s) {
-    launch_pdl(decode_k_kernel, dim3(n_seqs * heads), dim3(kThreads), 0, s, state, q, k, v, g,
-               beta, o, heads, krows, seq_rows, SnapList{}, 0);
+// snapshots: kda_prefill's route for short sequences, FP32 (in_bf16 false) or
+// BF16 inputs.
+kda_status launch_row_walk(float* state, const void* q, const void* k, const void* v,
+                           const void* g, const void* beta, float* o, int n_seqs, int krows,
+                           long long seq_rows, int heads, bool in_bf16, cudaStream_t s) {
+    if (in_bf16)
+        launch_pdl(decode_k_kernel<uint16_t>, dim3(n_seqs * heads), dim3(kThreads), 0, s, state,
+                   (const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v,
+                   (const uint16_t*)g, (const uint16_t*)beta, o, heads, krows, seq_rows,
+                   SnapList{}, 0);
+    else
+        launch_pdl(decode_k_kernel<float>, dim3(n_seqs * heads), dim3(kThreads), 0, s, state,
+                   (const float*)q, (const float*)k, (const float*)v, (const float*)g,
+                   (const float*)beta, o, heads, krows, seq_rows, SnapList{}, 0);
     return launch_result("kda_prefill (row walk)");
 }
 
@@ -249,7 +267,7 @@ extern "C" kda_status kda_decode_k(float* state, const float* q, const float* k,
                     "kda_decode_k: snapshot %d aliases the state", t);
         sl.p[t] = snapshots[t];
     }
-    launch_pdl(decode_k_kernel, dim3(n_seqs * heads), dim3(kThreads), 0, as_stream(stream),
+    launch_pdl(decode_k_kernel<float>, dim3(n_seqs * heads), dim3(kThreads), 0, as_stream(stream),
                state, q, k, v, g, beta, o, heads, krows, (long long)krows, sl, n_snap);
     return launch_result("kda_decode_k");
 }

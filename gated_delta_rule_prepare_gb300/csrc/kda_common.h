@@ -91,9 +91,9 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
 // decode_k's row walk (decode.cu) for kda_prefill's short FP32 sequences:
 // n_seqs sequences of krows token rows, sequence n starting at row
 // n * seq_rows of the [rows][heads][128] inputs and output.
-kda_status launch_row_walk(float* state, const float* q, const float* k, const float* v,
-                           const float* g, const float* beta, float* o, int n_seqs, int krows,
-                           long long seq_rows, int heads, cudaStream_t s);
+kda_status launch_row_walk(float* state, const void* q, const void* k, const void* v,
+                           const void* g, const void* beta, float* o, int n_seqs, int krows,
+                           long long seq_rows, int heads, bool in_bf16, cudaStream_t s);
 
 // Programmatic dependent launch.  Kernels launched with launch_pdl() may be
 // scheduled while the previous kernel on the stream drains: pdl_wait() blocks

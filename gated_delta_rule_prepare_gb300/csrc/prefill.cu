@@ -234,15 +234,13 @@ kda_status launch(float* state, const void* q, const void* k, const void* v, con
     // The SIMT kernel holds chunks of at most kCMax tokens on chip; a wider
     // chunk runs as consecutive kCMax-token chunks (the same result).
     chunk = chunk < kCMax ? chunk : kCMax;
-    // Short FP32 sequences (uniform form, heads packed in each token row) take
+    // Short sequences (uniform form, heads packed in each token row) take
     // decode_k's row walk, the pages' dispatch for pieces that do not take the
-    // chunked arm: one state read, t token steps in registers, one state write.
-    if constexpr (sizeof(TIn) == 4) {
-        if (!cu && t <= KDA_MAX_K && stride == (long long)heads * D && !simt_pinned())
-            return launch_row_walk(state, (const float*)q, (const float*)k, (const float*)v,
-                                   (const float*)g, (const float*)beta, o, n_seqs, t, t_pad,
-                                   heads, s);
-    }
+    // chunked arm: one state read, t token steps in registers, one state write
+    // (BF16 inputs widened exactly, FP32 arithmetic).
+    if (!cu && t <= KDA_MAX_K && stride == (long long)heads * D && !simt_pinned())
+        return launch_row_walk(state, q, k, v, g, beta, o, n_seqs, t, t_pad, heads,
+                               sizeof(TIn) == 2, s);
     // Everything else takes the tensor-core kernels unless the caller pins
     // the SIMT kernel (KDA_PREFILL_IMPL=simt, for comparisons).
     if (uses_tensor_cores(chunk, sizeof(TIn) == 2 ? KDA_BF16 : KDA_F32))

@@ -134,10 +134,11 @@ kda_status kda_decode_k(float* state, const float* q, const float* k, const floa
  *           performance choice: the tensor-core kernels step 64 tokens at a
  *           time for every width, the SIMT kernel min(chunk, 64).
  *   in_dtype : KDA_F32 or KDA_BF16 (applies to q, k, v, g, beta)
- * Routing: FP32 inputs in the uniform form with t <= KDA_MAX_K and
+ * Routing: inputs in the uniform form with t <= KDA_MAX_K and
  * qkv_row_stride == heads*128 run decode_k's row walk (the pages' dispatch
- * for pieces that do not take the chunked arm: state read once, t token steps,
- * state written once); every other call runs the tensor-core prepare and scan
+ * for pieces that do not take the chunked arm: state read once, t token steps
+ * in FP32 arithmetic, BF16 inputs widened exactly, state written once); every
+ * other call runs the tensor-core prepare and scan
  * kernels -- as one cooperative grid (the scan consuming each chunk as soon
  * as another SM has prepared it) when there are few (sequence, head) chains
  * relative to the SMs, e.g. one sequence of 32 heads.  FP32 inputs reach

@@ -285,16 +285,18 @@ def test_prefill_mixes_wide_and_narrow_decay_blocks(orc):
     assert rel_err(S[0], S_ref) < TOL_PREFILL
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("t,t_pad", [(1, 1), (5, 8), (8, 8)])
-def test_short_fp32_prefill_takes_the_row_walk(orc, t, t_pad):
-    """FP32 sequences of t <= 8 tokens (uniform form) run decode_k's row walk:
-    oracle parity per sequence, padded rows ignored, and the same bits as an
-    explicit kda_decode_k over the same rows."""
+def test_short_prefill_takes_the_row_walk(orc, dtype, t, t_pad):
+    """Sequences of t <= 8 tokens (uniform form) run decode_k's row walk, BF16
+    inputs widened exactly: oracle parity per sequence at the FP32 tolerance,
+    padded rows ignored, and the same bits as an explicit kda_decode_k over
+    the same (widened) rows."""
     from _util import TOL_DECODE
     K = kda()
     gen = torch.Generator().manual_seed(60 + t)
     N, H = 3, 2
-    d = wl.core_inputs(gen, (N, t_pad), H, torch.float32)
+    d = wl.core_inputs(gen, (N, t_pad), H, dtype)
     S0 = wl.state(gen, (N,), H, 0.02)
     dev = {}
     for n in ("q", "k", "v", "g", "beta"):
@@ -315,6 +317,7 @@ def test_short_fp32_prefill_takes_the_row_walk(orc, t, t_pad):
     if t == t_pad:
         S2 = S0.clone().cuda()
         o2 = torch.empty_like(o)
-        K.kda_decode_k(S2, *(d[n].cuda().contiguous() for n in ("q", "k", "v", "g", "beta")), o2)
+        K.kda_decode_k(S2, *(d[n].float().cuda().contiguous()
+                             for n in ("q", "k", "v", "g", "beta")), o2)
         torch.cuda.synchronize()
         assert torch.equal(S2, S) and torch.equal(o2, o)
