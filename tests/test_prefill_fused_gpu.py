@@ -48,10 +48,10 @@ def oracle_all_heads(orc, d, t):
 @pytest.mark.parametrize("t,g_low", [(1000, -5.0), (777, -0.05), (64, -5.0), (1, -5.0),
                                      (130, -10.0), (130, -15.0), (200, -20.0)])
 def test_fused_grid_matches_oracle(orc, t, g_low):
-    """Every head and output row: whole and ragged chunk counts, one-token and
-    one-chunk sequences, slow decay (the state carries across every chunk),
-    and steep decays: down to -10 the 16-token tensor-core blocks, beyond it
-    the exact per-pair products."""
+    """Every head and output row: whole and ragged chunk counts, one-chunk
+    sequences (one token: the row walk), slow decay (the state carries across
+    every chunk), and steep decays: down to -10 the 16-token tensor-core
+    blocks, beyond it the exact per-pair products."""
     K = kda()
     d = inputs(100 + t, t, g_low)
     o, S = run(K, d, t)
@@ -196,3 +196,28 @@ def test_bounded_ready_wait_runs_out_and_reports(orc, monkeypatch):
     o_ref, S_ref = oracle_all_heads(orc, d, t)
     assert rel_err(o2, o_ref) < TOL_PREFILL
     assert rel_err(S2[0], S_ref) < TOL_PREFILL
+
+
+@pytest.mark.parametrize("impl", ["fused", "unfused"])
+@pytest.mark.parametrize("t", [1, 5, 8])
+def test_short_sequences_on_the_tensor_core_kernels(orc, monkeypatch, impl, t):
+    """Sequences of at most 8 tokens on the tensor-core kernels: q, k, v as
+    slices of one wider buffer (a contiguous short sequence takes the row
+    walk instead).  One ragged chunk of t rows against the oracle."""
+    if impl == "unfused":
+        monkeypatch.setenv("KDA_PREFILL_IMPL", "unfused")
+    K = kda()
+    d = inputs(500 + t, t)
+    hd = H * 128
+    qkv = torch.cat([d[n].reshape(t, hd) for n in ("q", "k", "v")], dim=1).cuda()
+    # as_strided keeps the row stride of a one-row view (a plain view may not)
+    q, k, v = (torch.as_strided(qkv, (t, H, 128), (3 * hd, 128, 1), i * hd) for i in range(3))
+    S = d["state"].clone().cuda()
+    o = torch.empty((t, H, 128), device="cuda")
+    assert q.stride(0) == 3 * hd
+    K.kda_prefill(S, q, k, v, d["g"].cuda(), d["beta"].cuda(), o, t, 64)
+    K.kda_sync_status()
+    o_ref, S_ref = oracle_all_heads(orc, d, t)
+    e_o, e_s = rel_err(o, o_ref), rel_err(S[0], S_ref)
+    assert e_o < TOL_PREFILL and e_s < TOL_PREFILL
+    assert e_s > 1e-6  # the FP16 scan operands' rounding: not the FP32 row walk

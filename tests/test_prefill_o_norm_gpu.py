@@ -72,10 +72,16 @@ def test_prefill_o_norm_matches_oracle(orc, monkeypatch, impl, t):
     S0 = wl.state(gen, (1,), H, 0.02)
     gate, w = norm_inputs(gen, t, H)
     dev = {n: d[n].cuda() for n in d}
-    # this library's FP32 core output, for the epilogue check
+    # this library's FP32 core output, for the epilogue check; q, k, v as
+    # slices of one wider buffer keep this call on the tensor-core kernels for
+    # every t (a short contiguous sequence would take the row walk)
+    hd = H * 128
+    qkv = torch.cat([dev[n].reshape(t, hd) for n in ("q", "k", "v")], dim=1)
+    qs, ks, vs = (torch.as_strided(qkv, (t, H, 128), (3 * hd, 128, 1), i * hd)
+                  for i in range(3))
     S1 = S0.clone().cuda()
     o_gpu = torch.empty((t, H, 128), device="cuda")
-    K.kda_prefill(S1, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], o_gpu, t, 64)
+    K.kda_prefill(S1, qs, ks, vs, dev["g"], dev["beta"], o_gpu, t, 64)
     S2 = S0.clone().cuda()
     out = torch.full((t, H * 128), 7.0, dtype=torch.bfloat16, device="cuda")
     K.kda_prefill_o_norm(S2, dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], gate.cuda(),
