@@ -33,7 +33,23 @@ struct TokenSmem {
     float v[D];
     float u[D];    // v - S^T k (decayed S)
     float red[kWarps][D];
+    // decode_k (FP32 inputs): the next token's raw inputs, copied in by
+    // cp.async while the current token's step runs; channel c's entries are
+    // written and read by thread c alone
+    float nq[D], nk[D], nv[D], ng[D], nb[D];
 };
+
+// 4-byte asynchronous global -> shared copy, and the wait for this thread's
+// outstanding ones.
+__device__ __forceinline__ void cp_async4(float* dst_smem, const float* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst_smem))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
 
 // One input element widened to FP32: FP32 as is, BF16 (raw bits) exactly.
 __device__ __forceinline__ float ld_in(const float* p) { return __ldg(p); }
@@ -177,11 +193,42 @@ decode_k_kernel(float* __restrict__ state, const TIn* __restrict__ q,
     const size_t nh = blockIdx.x;
     const size_t n = nh / heads, h = nh % heads;
     float* S = state + nh * (size_t)(D * D);
+    const int c = threadIdx.x;
+    auto row_of = [&](int t) { return (n * (size_t)seq_rows + t) * heads + h; };
+    // FP32 inputs: token t + 1's inputs travel while token t's step runs (the
+    // first token's with the state), so no step waits on a global load
+    auto prefetch = [&](int t) {
+        if constexpr (sizeof(TIn) == 4) {
+            if (c < D) {
+                const size_t row = row_of(t);
+                cp_async4(sm.nq + c, q + row * D + c);
+                cp_async4(sm.nk + c, k + row * D + c);
+                cp_async4(sm.nv + c, v + row * D + c);
+                cp_async4(sm.ng + c, g + row * D + c);
+                cp_async4(sm.nb + c, beta + row);
+            }
+        }
+    };
+    prefetch(0);
     float4 s[kRows];
     load_state(s, S);
     for (int t = 0; t < krows; ++t) {
-        const size_t row = (n * (size_t)seq_rows + t) * heads + h;
-        stage_token(sm, q + row * D, k + row * D, v + row * D, g + row * D, ld_in(beta + row));
+        const size_t row = row_of(t);
+        if constexpr (sizeof(TIn) == 4) {
+            if (c < D) {  // stage_token's arithmetic, from the copies
+                cp_async_wait_all();
+                const float kc = sm.nk[c];
+                sm.dec[c] = expf(sm.ng[c]);
+                sm.kk[c] = kc;
+                sm.bk[c] = __fmul_rn(sm.nb[c], kc);
+                sm.qs[c] = __fmul_rn(KDA_Q_SCALE, sm.nq[c]);
+                sm.v[c] = sm.nv[c];
+            }
+            if (t + 1 < krows) prefetch(t + 1);  // after this thread's reads of its channel
+        } else {
+            stage_token(sm, q + row * D, k + row * D, v + row * D, g + row * D,
+                        ld_in(beta + row));
+        }
         __syncthreads();
         token_step(s, sm, o + row * D);
         if (t < n_snap) store_state(s, snaps.p[t] + nh * (size_t)(D * D));
