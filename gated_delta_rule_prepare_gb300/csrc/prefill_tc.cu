@@ -403,7 +403,7 @@ __device__ __forceinline__ PrepItem prep_item(long long item, int heads, const i
 // F16: the inputs were FP32: q and k arrive as FP16 tiles, g as an FP32 tile
 // (maps.g) loaded into the Gamma array, which the cumulative sum then
 // overwrites in place, and beta as FP32.
-template <bool GATED, bool F16>
+template <bool GATED, bool F16, bool TWO_KERNEL>
 __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const void* __restrict__ beta,
                                              int t, int t_pad, int heads,
                                              const int* __restrict__ cu, int n_seqs,
@@ -567,6 +567,12 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const void* _
         // The next item is resolved (global loads) while the first A/P product
         // runs, and its raw tiles go to the other buffer, which the previous
         // iteration's closing barrier released.
+        auto resolve_next = [&]() {  // the item, and its beta and gate loads
+            if (nitem < items) nxt = prep_item(nitem, heads, map_cu, map_off, n_seqs, t, t_pad);
+            beta_nxt = load_beta(nxt);
+            blive_nxt = beta_live(nxt);
+            gate_nxt = load_gate(nxt);
+        };
         auto fetch_next = [&]() {
             if (nitem < items) nxt = prep_item(nitem, heads, map_cu, map_off, n_seqs, t, t_pad);
             load_raw(nxt, b ^ 1);
@@ -820,6 +826,10 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const void* _
                     tc::mma_commit(bar_mma2);
                 }
                 release_pending();
+                // Two-kernel path: the next item is resolved while the products
+                // run (in the fused grid that moves no time off its critical
+                // path, the copier's, and measured slower)
+                if constexpr (TWO_KERNEL) resolve_next();
                 wait_mma();
                 if (!tc::mbar_wait(bar_mma2, ph_mma2)) {
                     atomicOr(&g_tc_status, STATUS_TIMEOUT);
@@ -827,7 +837,9 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const void* _
                 }
                 ph_mma2 ^= 1;
                 tc::tc_fence_after();
-                fetch_next();  // the compact X_1 in the other buffer has been read
+                // the compact X_1 in the other buffer has been read
+                if constexpr (TWO_KERNEL) load_raw(nxt, b ^ 1);
+                else fetch_next();
                 p3_store();
             } else if (steep) {
                 // Exact products on the CUDA cores: thread (column s = tid & 63)
@@ -1137,7 +1149,8 @@ prepare_kernel(const __grid_constant__ PrepMaps maps, const void* __restrict__ b
                unsigned char* __restrict__ ws) {
     pdl_wait();  // the chunk map (and the callers' inputs) are complete
     pdl_release();
-    prepare_role<GATED, F16>(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x, gridDim.x,
+    prepare_role<GATED, F16, true>(maps, beta, t, t_pad, heads, cu, n_seqs, ws, blockIdx.x,
+                                   gridDim.x,
                              nullptr, 0);
 }
 
@@ -1204,7 +1217,7 @@ struct ScanT {
 // store; the last chunk's tile is normalised after the loop and written by
 // plain stores.
 // F16: the value tiles hold FP16 (FP32 inputs, converted before the call).
-template <bool NORM, bool F16>
+template <bool NORM, bool F16, bool TWO_KERNEL>
 __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUtensorMap& omap,
                                             float* __restrict__ state,
                                             float* __restrict__ o, int t, int t_pad, int heads,
@@ -1318,7 +1331,12 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         }
         return false;
     };
-    auto load_ops = [&](long long gg, int b) {  // chunk gg's operands into group b, after its flag
+    // chunk gg's operands into group b, after its flag.  Two-kernel path
+    // (every blob written before the scan starts, most of them gone from L2):
+    // with next_too, chunk gg + 1's blob is also pulled into L2, so that its
+    // copies, a chunk later, need not wait on DRAM (in the fused grid the
+    // chains read blobs soon after prepare wrote them, and this measured slower)
+    auto load_ops = [&](long long gg, int b, bool next_too) {
         if (!acquire(gg)) {
             atomicOr(&g_tc_status, STATUS_TIMEOUT);
             *abort_flag = 1;
@@ -1330,6 +1348,9 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         tc::bulk_load(sm + tp_off(b), blob + BLOB_TP, ScanT::BGRP, bar_b + b);
         out_x |= 1u << b;
         out_b |= 1u << b;
+        if constexpr (TWO_KERNEL) {
+            if (next_too) tc::bulk_prefetch_l2(blob + BLOB_BYTES * (size_t)heads, BLOB_BYTES);
+        }
     };
     // Value tiles are double-buffered by chunk parity and requested two chunks
     // ahead, as soon as the X phase has consumed the buffer.
@@ -1339,7 +1360,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         out_v |= 1u << vb;
     };
     if (copier && start < end) {
-        load_ops(g0, 0);
+        load_ops(g0, 0, start + C < end);
         load_v(start, 0);
         if (start + C < end) load_v(start + C, 1);
     }
@@ -1493,7 +1514,7 @@ __device__ __forceinline__ void scan_t_role(const CUtensorMap& vmap, const CUten
         }
         // the next chunk's operands into the other groups, whose last products
         // completed in the previous chunk
-        if (copier && more) load_ops(g + 1, xb ^ 1);
+        if (copier && more) load_ops(g + 1, xb ^ 1, c0 + 2 * C < end);
         float vr[16];  // V[16 cg + i][j], read while the product runs
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -1735,11 +1756,11 @@ prefill_fused_kernel(const __grid_constant__ PrepMaps maps, const __grid_constan
     const bool inject = fault == FAULT_READY_WAIT;
     const int chains = n_seqs * heads;
     if ((int)blockIdx.x < chains)
-        scan_t_role<NORM, F16>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
+        scan_t_role<NORM, F16, false>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
                                (int)blockIdx.x % heads, (int)blockIdx.x / heads, ready,
                                ready_pitch, &na, inject ? 1u << 12 : 1u << 22);
     else
-        prepare_role<GATED, F16>(maps, beta, t, t_pad, heads, cu, n_seqs, ws,
+        prepare_role<GATED, F16, false>(maps, beta, t, t_pad, heads, cu, n_seqs, ws,
                                  (long long)blockIdx.x - chains, (long long)gridDim.x - chains,
                                  ready, ready_pitch, !inject);
 }
@@ -1754,7 +1775,7 @@ scan_t_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ 
               const unsigned char* __restrict__ ws) {
     pdl_wait();  // the prepared operands (and the callers' state) are complete
     pdl_release();
-    scan_t_role<NORM, F16>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
+    scan_t_role<NORM, F16, true>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
                            (int)blockIdx.x % heads, (int)blockIdx.x / heads, nullptr, 0, &na);
 }
 
