@@ -323,6 +323,31 @@ chunk_map_kernel(const int* __restrict__ cu, int n_seqs, int t, int* __restrict_
     if (threadIdx.x == MAP_THREADS - 1) chunk_off[n_seqs] = part[MAP_THREADS - 1];
 }
 
+// The two-kernel path's chain order for a packed batch (one CTA): order[rank]
+// = the sequence with that rank by decreasing chunk count (equal counts by
+// index), so that the scan starts the longest chains first instead of
+// wherever they fall in the batch.  n_seqs <= ORDER_MAX ints of dynamic
+// shared memory.
+constexpr int ORDER_MAX = 1024;
+__global__ void __launch_bounds__(MAP_THREADS)
+chain_order_kernel(const int* __restrict__ cu, int n_seqs, int* __restrict__ order) {
+    extern __shared__ int s_chunks[];
+    pdl_wait();
+    pdl_release();
+    for (int n = threadIdx.x; n < n_seqs; n += MAP_THREADS)
+        s_chunks[n] = (max(0, __ldg(cu + n + 1) - __ldg(cu + n)) + C - 1) / C;
+    __syncthreads();
+    for (int n = threadIdx.x; n < n_seqs; n += MAP_THREADS) {
+        const int cn = s_chunks[n];
+        int rank = 0;  // sequences ahead of n
+        for (int m = 0; m < n_seqs; ++m) {
+            const int cm = s_chunks[m];
+            rank += (cm > cn || (cm == cn && m < n)) ? 1 : 0;
+        }
+        order[rank] = n;
+    }
+}
+
 // Byte offset of channel c of row r inside a raw tile (see above).
 __device__ __forceinline__ uint32_t raw_off(int r, int c) {
     return (uint32_t)((c >> 6) * 8192 + r * 128 + ((((c & 63) >> 3) ^ (r & 7)) << 4) + (c & 7) * 2);
@@ -1772,11 +1797,13 @@ __global__ void __launch_bounds__(NTP, 1)
 scan_t_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ CUtensorMap omap,
               const __grid_constant__ NormArgs na, float* __restrict__ state, float* __restrict__ o,
               int t, int t_pad, int heads, const int* __restrict__ cu, int n_seqs,
-              const unsigned char* __restrict__ ws) {
+              const unsigned char* __restrict__ ws, const int* __restrict__ order) {
     pdl_wait();  // the prepared operands (and the callers' state) are complete
     pdl_release();
+    // a packed batch's chains in chain_order_kernel's order, longest first
+    const int n = order ? __ldg(order + (int)blockIdx.x / heads) : (int)blockIdx.x / heads;
     scan_t_role<NORM, F16, true>(vmap, omap, state, o, t, t_pad, heads, cu, n_seqs, ws,
-                           (int)blockIdx.x % heads, (int)blockIdx.x / heads, nullptr, 0, &na);
+                                 (int)blockIdx.x % heads, n, nullptr, 0, &na);
 }
 
 // BF16 (FP16 with f16) [rows][cols] with a row pitch of `pitch_elems`; boxes
@@ -1828,9 +1855,15 @@ size_t ready_words(long long chunks, int heads) {
 
 }  // namespace
 
+// The chains' launch order (n_seqs int32, padded to 256 B), after the flags.
+size_t order_offset(long long chunks, int n_seqs, int heads) {
+    return ready_offset(chunks, n_seqs, heads) + ready_words(chunks, heads) * 4;
+}
+
 size_t prefill_tc_workspace_bytes(long long rows, int n_seqs, int heads, bool f32_in) {
     const long long chunks = (rows + C - 1) / C + n_seqs;
-    const size_t base = ready_offset(chunks, n_seqs, heads) + ready_words(chunks, heads) * 4;
+    const size_t base =
+        order_offset(chunks, n_seqs, heads) + (((size_t)n_seqs * 4 + 255) & ~(size_t)255);
     if (!f32_in) return base;
     // the FP16 copies of q, k and v, 256-byte aligned after the rest
     return ((base + 255) & ~(size_t)255) + 3 * (size_t)rows * heads * D * 2;
@@ -1978,6 +2011,15 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
         // run the two kernels instead
         (void)cudaGetLastError();
     }
+    // A packed batch's chains start longest first (see chain_order_kernel).
+    int* order = nullptr;
+    if (cu && n_seqs > 1 && n_seqs <= ORDER_MAX) {
+        order = reinterpret_cast<int*>(ws + order_offset(chunk_bound, n_seqs, heads));
+        launch_pdl(chain_order_kernel, dim3(1), dim3(MAP_THREADS), (size_t)n_seqs * 4, s, cu,
+                   n_seqs, order);
+        st = launch_result("kda_prefill (chain order)");
+        if (st != KDA_OK) return st;
+    }
     // Persistent prepare: one CTA per SM (shared memory allows no more),
     // never more CTAs than (chunk, head) items.
     const long long items = (((long long)rows + C - 1) / C + n_seqs) * heads;
@@ -1987,7 +2029,8 @@ kda_status launch_prefill_tc(float* state, const void* q, const void* k, const v
     st = launch_result("kda_prefill (prepare)");
     if (st != KDA_OK) return st;
     launch_pdl(scan_k, dim3((unsigned)chains), dim3(NTP), ScanT::TOTAL, s, vmap, omap, na,
-               state, o, t, t_pad, heads, cu, n_seqs, (const unsigned char*)ws);
+               state, o, t, t_pad, heads, cu, n_seqs, (const unsigned char*)ws,
+               (const int*)order);
     return launch_result("kda_prefill (scan)");
 }
 

@@ -180,7 +180,9 @@ kda_status kda_prefill(float* state, const void* q, const void* k, const void* v
  * operands of every (chunk, head) there: 66,176 bytes per chunk of 64 tokens
  * and head (with one chunk of slack per sequence), plus (n_seqs + 1) * 4
  * bytes rounded up to 256, plus a 4-byte ready flag per chunk and head
- * rounded up to 256 bytes; FP32 inputs add, 256-byte aligned after that, the
+ * rounded up to 256 bytes, plus n_seqs * 4 bytes rounded up to 256 (the order
+ * in which a packed batch's chains start); FP32 inputs add, 256-byte aligned
+ * after that, the
  * FP16 copies of q, k and v: 3 * rows * heads * 128 * 2 bytes.  (The row walk
  * of short FP32 sequences uses none of it.) */
 size_t kda_prefill_workspace_size(int64_t rows, int n_seqs, int chunk, int heads, int head_dim,
