@@ -439,10 +439,10 @@ __device__ __forceinline__ void prepare_role(const PrepMaps& maps, const void* _
     const int tid = threadIdx.x, warp = tid >> 5;
     const int ln = tid & 127, ch = tid >> 7;  // TMEM lane and column quarter
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    // Thread 0 issues the tensor-core products; a thread of another warp
-    // issues the tile loads and bulk stores and releases the ready flags, so
-    // the stores' completion and the release's fences are waited for while
-    // the next item's A/P product runs instead of between two items.
+    // Threads 0 and 32 issue the tensor-core products; a thread of another
+    // warp issues the tile loads and bulk stores and releases the ready
+    // flags, so the stores' completion and the release's fences are waited
+    // for while the next item's A/P products run instead of between two items.
     const bool copier = (tid == 128);
 
     const int* chunk_off = reinterpret_cast<const int*>(ws);
